@@ -1,0 +1,440 @@
+/*
+ * oracle.c -- plain, slow, obviously-correct CPU statement of the DeepSeek-V3.2
+ * sparse-attention indexer hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file: only the test suite, the smoke check and the CPU-baseline leg
+ * of the benchmark use it.  It shares no code, header, table or constant
+ * generator with the CUDA library; the two meet only on the seeded inputs.
+ *
+ * Every function states the definition it follows.  Sources (web pages):
+ *   [GATHER]  vLLM PR #25869 "[Model] Support Deepseek V3.2", code review of
+ *             cp_gather_indexer_k_quant_cache (per-request loop: full blocks,
+ *             then the partial last block; indexer-K block = block_size x
+ *             head_dim fp8 values followed by block_size fp32 scales).
+ *   [FALLBK]  vLLM PR #36250 "[kernel] Fix FP8 paged MQA fallback for CUDA
+ *             graph capture": the paged MQA logits op over context_lens and
+ *             the optional -inf tail (clean_logits, review thread).
+ *   [DSMLA]   vLLM PR #47090 (prhub summary), "key source snippet" of
+ *             _fused_norm_rope_kernel, fp8_ds_mla branch: 656 B entry
+ *             [512 B fp8 NoPE][4 x fp32 tile scales][64 x bf16 RoPE],
+ *             tile_scale = max(amax * (1/448), 1.1754944e-38), fp8 = x / scale.
+ *   [ATOM]    ROCm/ATOM PR #1094 "[Feat] Support DSv3.2 with sglang-ATOM plugin
+ *             and sglang sparse MLA", Technical Details: per-query top-k into a
+ *             2-D index buffer, request-local top-k indices converted to global
+ *             paged-KV indices.
+ *   [SCORE]   The DeepSeek-V3.2 lightning-indexer score:
+ *             logit[t,s] = k_scale[s] * sum_h w[t,h] * ReLU(q[t,h,:] . k[s,:]);
+ *             indexer K quantised per token, scale = amax / 448.
+ *   [OCP]     OCP 8-bit floating point specification, E4M3: bias 7, no
+ *             infinities, S.1111.111 is NaN, largest finite 448.
+ *
+ * Readings of points the pages leave open (each also listed in the design notes):
+ *   - fp8 rounding is round-to-nearest-even, saturating to +-448.
+ *   - indexer K: scale = amax / 448 (IEEE f32 division), floored at FLT_MIN so
+ *     that an all-zero token yields zero codes; codes = enc(x / scale) with an
+ *     IEEE f32 division.
+ *   - a negative slot_mapping entry means "skip this token".
+ *   - decode row (b, j) of next_n sees L = context_lens[b] - next_n + 1 + j keys.
+ *   - logits are computed exactly (every e4m3 product is a multiple of 2^-18 and
+ *     |q.k| < 2^25, so a double sum is exact and order-free), weighted in double,
+ *     then rounded once to f32.
+ *   - top-k: order by (value desc, index asc), -0.0 equals +0.0, take
+ *     min(k, L), emit in ascending index order, pad with -1; remap
+ *     g = block_table[b, s / bs] * bs + s % bs, -1 stays -1.
+ *
+ * Build: gcc -O3 -fopenmp -fPIC -shared (no -ffast-math).
+ */
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------- */
+/* OCP FP8 E4M3 codec [OCP]                                                   */
+/* ------------------------------------------------------------------------- */
+
+/* Exact value of an E4M3 code.  Normal: 2^(e-7) * (1 + m/8), e in 1..15;
+ * subnormal: 2^-6 * (m/8); S.1111.111 is NaN. */
+double oracle_e4m3_decode(uint8_t c)
+{
+    int s = (c >> 7) & 1;
+    int e = (c >> 3) & 0xF;
+    int m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* Non-negative finite codes 0x00..0x7E in increasing value order (the code
+ * order is the value order for a fixed sign). */
+static double g_pos_values[127];
+static int g_codec_ready = 0;
+
+static void codec_init(void)
+{
+    if (g_codec_ready) return;
+    for (int c = 0; c < 127; ++c) g_pos_values[c] = oracle_e4m3_decode((uint8_t)c);
+    g_codec_ready = 1;
+}
+
+/* Round-to-nearest, ties to the even code (mantissa LSB 0); magnitudes at or
+ * beyond 448 saturate to 448; NaN maps to the NaN code. */
+uint8_t oracle_e4m3_encode(float x)
+{
+    codec_init();
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    /* largest code lo with value <= a (value(0) = 0 <= a always) */
+    int lo = 0, hi = 126;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) / 2;
+        if (g_pos_values[mid] <= a) lo = mid; else hi = mid - 1;
+    }
+    int c;
+    if (g_pos_values[lo] == a) {
+        c = lo;
+    } else {
+        /* lo < 126 here because a < 448 = value(126) */
+        double below = a - g_pos_values[lo];      /* exact: see header */
+        double above = g_pos_values[lo + 1] - a;  /* exact */
+        if (below < above) c = lo;
+        else if (above < below) c = lo + 1;
+        else c = (lo % 2 == 0) ? lo : lo + 1;
+    }
+    return (uint8_t)(sign | c);
+}
+
+static float bf16_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Indexer K quantise + paged cache write [GATHER layout] [SCORE scale]       */
+/* ------------------------------------------------------------------------- */
+
+/* cache: uint8 [num_blocks, block_size * (head_dim + 4)].  Token at slot
+ * (blk, off): fp8 values at blk*B + off*head_dim, fp32 scale at
+ * blk*B + block_size*head_dim + 4*off.  Returns 0, or -1 on a slot past the
+ * pool. */
+int oracle_quant_write_k(const uint16_t* k_bf16, int64_t n, int head_dim,
+                         const int64_t* slot_mapping, uint8_t* cache,
+                         int64_t num_blocks, int block_size)
+{
+    codec_init();
+    const int64_t block_bytes = (int64_t)block_size * (head_dim + 4);
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int64_t t = 0; t < n; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        int64_t blk = slot / block_size;
+        int64_t off = slot % block_size;
+        if (blk >= num_blocks) { bad = 1; continue; }
+        const uint16_t* src = k_bf16 + t * head_dim;
+        float amax = 0.0f;
+        for (int i = 0; i < head_dim; ++i) {
+            float a = fabsf(bf16_to_f32(src[i]));
+            if (a > amax) amax = a;
+        }
+        float scale = amax / 448.0f;
+        if (!(scale >= FLT_MIN)) scale = FLT_MIN;
+        uint8_t* base = cache + blk * block_bytes;
+        for (int i = 0; i < head_dim; ++i) {
+            float x = bf16_to_f32(src[i]);
+            float y = x / scale;
+            base[off * head_dim + i] = oracle_e4m3_encode(y);
+        }
+        memcpy(base + (int64_t)block_size * head_dim + 4 * off, &scale, 4);
+    }
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Paged gather into contiguous K [GATHER]                                    */
+/* ------------------------------------------------------------------------- */
+
+/* For each request b with s = cu[b+1]-cu[b] > 0: copy its full blocks, then
+ * the first `remaining` rows of its last block, into out_k[cu[b]:] (fp8 rows of
+ * head_dim bytes) and out_scale[cu[b]:] (fp32).  Empty requests are skipped;
+ * rows past cu[batch] are not touched. */
+int oracle_gather_k(const uint8_t* cache, int64_t num_blocks, int block_size,
+                    int head_dim, const int32_t* block_table, int64_t bt_stride,
+                    const int32_t* cu_seq_lens, int batch, uint8_t* out_k,
+                    float* out_scale)
+{
+    const int64_t block_bytes = (int64_t)block_size * (head_dim + 4);
+    const int64_t val_bytes = (int64_t)block_size * head_dim;
+    for (int b = 0; b < batch; ++b) {
+        int64_t s = (int64_t)cu_seq_lens[b + 1] - cu_seq_lens[b];
+        if (s <= 0) continue;
+        int64_t start = cu_seq_lens[b];
+        int64_t tot = (s + block_size - 1) / block_size;
+        const int32_t* blocks = block_table + (int64_t)b * bt_stride;
+        int64_t num_full = s / block_size;
+        for (int64_t i = 0; i < num_full; ++i) {
+            int64_t blk = blocks[i];
+            if (blk < 0 || blk >= num_blocks) return -1;
+            const uint8_t* src = cache + blk * block_bytes;
+            memcpy(out_k + (start + i * block_size) * head_dim, src, (size_t)val_bytes);
+            memcpy(out_scale + start + i * block_size, src + val_bytes, (size_t)block_size * 4);
+        }
+        int64_t remaining = s - num_full * block_size;
+        if (remaining > 0) {
+            int64_t blk = blocks[tot - 1];
+            if (blk < 0 || blk >= num_blocks) return -1;
+            const uint8_t* src = cache + blk * block_bytes;
+            int64_t dst = start + num_full * block_size;
+            memcpy(out_k + dst * head_dim, src, (size_t)(remaining * head_dim));
+            memcpy(out_scale + dst, src + val_bytes, (size_t)(remaining * 4));
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* MQA logits [SCORE] [FALLBK]                                                */
+/* ------------------------------------------------------------------------- */
+
+/* One score: k_scale * sum_h w_h * max(q_h . k, 0); the dot products are
+ * exact in double, the head sum is taken in double in head order. */
+static float score_one(const double* qd /*[heads*head_dim]*/, const float* w,
+                       const double* kd /*[head_dim]*/, float kscale, int heads,
+                       int head_dim)
+{
+    double acc = 0.0;
+    for (int h = 0; h < heads; ++h) {
+        const double* qh = qd + (int64_t)h * head_dim;
+        double d = 0.0;
+        for (int i = 0; i < head_dim; ++i) d += qh[i] * kd[i];
+        if (d > 0.0) acc += (double)w[h] * d;
+    }
+    return (float)((double)kscale * acc);
+}
+
+static void decode_row(const uint8_t* src, double* dst, int64_t n, const double* table)
+{
+    for (int64_t i = 0; i < n; ++i) dst[i] = table[src[i]];
+}
+
+static void build_table(double* table)
+{
+    for (int c = 0; c < 256; ++c) table[c] = oracle_e4m3_decode((uint8_t)c);
+}
+
+/* Decode (paged) logits.  Row r = b*next_n + j sees
+ * L = context_lens[b] - next_n + 1 + j keys (clamped to [0, ld]); key s lives
+ * in block block_table[b, s/bs] at offset s%bs.  logits is [nrows_out, ld];
+ * out row i is logical row rows[i] (or i when rows is NULL).  Entries in
+ * [L, ld) are -inf when clean is non-zero, else untouched. */
+int oracle_paged_mqa_logits(const uint8_t* q, const float* w, const uint8_t* cache,
+                            int64_t num_blocks, int block_size,
+                            const int32_t* context_lens, const int32_t* block_table,
+                            int64_t bt_stride, int batch, int next_n, int heads,
+                            int head_dim, float* logits, int64_t ld, int clean,
+                            const int64_t* rows, int64_t nrows)
+{
+    double table[256];
+    build_table(table);
+    const int64_t block_bytes = (int64_t)block_size * (head_dim + 4);
+    const int64_t total_rows = (int64_t)batch * next_n;
+    const int64_t nout = rows ? nrows : total_rows;
+    const int64_t qrow = (int64_t)heads * head_dim;
+    int bad = 0;
+    if (head_dim > 512) return -2;
+    double* qd = (double*)malloc(sizeof(double) * qrow);
+    if (!qd) return -2;
+    for (int64_t i = 0; i < nout; ++i) {
+        int64_t r = rows ? rows[i] : i;
+        if (r < 0 || r >= total_rows) { bad = 1; continue; }
+        int64_t b = r / next_n, j = r % next_n;
+        int64_t L = (int64_t)context_lens[b] - next_n + 1 + j;
+        if (L < 0) L = 0;
+        if (L > ld) { bad = 1; L = ld; }
+        decode_row(q + r * qrow, qd, qrow, table);
+        const float* wr = w + r * heads;
+        float* out = logits + i * ld;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+        for (int64_t s = 0; s < L; ++s) {
+            int64_t blk = block_table[b * bt_stride + s / block_size];
+            if (blk < 0 || blk >= num_blocks) { bad = 1; continue; }
+            int64_t off = s % block_size;
+            const uint8_t* base = cache + blk * block_bytes;
+            double kd[512];
+            decode_row(base + off * head_dim, kd, head_dim, table);
+            float ks;
+            memcpy(&ks, base + (int64_t)block_size * head_dim + 4 * off, 4);
+            out[s] = score_one(qd, wr, kd, ks, heads, head_dim);
+        }
+        if (clean)
+            for (int64_t s = L; s < ld; ++s) out[s] = -INFINITY;
+    }
+    free(qd);
+    return bad ? -1 : 0;
+}
+
+/* Prefill (contiguous K) logits.  Row t sees keys [ks[t], ke[t]); column j of
+ * the row is key ks[t] + j.  Same output convention as above. */
+int oracle_mqa_logits(const uint8_t* q, const float* w, const uint8_t* k,
+                      const float* k_scale, const int32_t* ks, const int32_t* ke,
+                      int64_t tq, int64_t tk, int heads, int head_dim, float* logits,
+                      int64_t ld, int clean, const int64_t* rows, int64_t nrows)
+{
+    double table[256];
+    build_table(table);
+    const int64_t nout = rows ? nrows : tq;
+    const int64_t qrow = (int64_t)heads * head_dim;
+    int bad = 0;
+    if (head_dim > 512) return -2;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t i = 0; i < nout; ++i) {
+        int64_t t = rows ? rows[i] : i;
+        if (t < 0 || t >= tq) { bad = 1; continue; }
+        int64_t s0 = ks[t], s1 = ke[t];
+        if (s0 < 0 || s1 > tk) { bad = 1; continue; }
+        int64_t n = s1 - s0;
+        if (n < 0) n = 0;
+        if (n > ld) { bad = 1; n = ld; }
+        double* qd = (double*)malloc(sizeof(double) * qrow);
+        double kd[512];
+        if (!qd) { bad = 1; continue; }
+        decode_row(q + t * qrow, qd, qrow, table);
+        float* out = logits + i * ld;
+        for (int64_t j = 0; j < n; ++j) {
+            decode_row(k + (s0 + j) * head_dim, kd, head_dim, table);
+            out[j] = score_one(qd, w + t * heads, kd, k_scale[s0 + j], heads, head_dim);
+        }
+        if (clean)
+            for (int64_t j = n; j < ld; ++j) out[j] = -INFINITY;
+        free(qd);
+    }
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Top-k selection + global remap [ATOM]                                      */
+/* ------------------------------------------------------------------------- */
+
+typedef struct { float v; int32_t i; } vi_t;
+
+/* (value descending, index ascending); C float compare treats -0.0 == +0.0 */
+static int cmp_value_desc(const void* pa, const void* pb)
+{
+    const vi_t* a = (const vi_t*)pa;
+    const vi_t* b = (const vi_t*)pb;
+    if (a->v > b->v) return -1;
+    if (a->v < b->v) return 1;
+    return (a->i > b->i) - (a->i < b->i);
+}
+
+static int cmp_int_asc(const void* pa, const void* pb)
+{
+    int32_t a = *(const int32_t*)pa, b = *(const int32_t*)pb;
+    return (a > b) - (a < b);
+}
+
+/* Row r (length L = row_len[r], request row_req[r]): pick the min(k, L)
+ * columns with the largest logits (ties to the lower index), write them in
+ * ascending index order, pad with -1, and map each to its global paged slot. */
+int oracle_topk_to_global(const float* logits, int64_t ld, int64_t rows,
+                          const int32_t* row_len, const int32_t* row_req,
+                          const int32_t* block_table, int64_t bt_stride,
+                          int block_size, int k, int32_t* out_local,
+                          int32_t* out_global)
+{
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t L = row_len[r];
+        if (L < 0) L = 0;
+        if (L > ld) { bad = 1; L = ld; }
+        vi_t* buf = (vi_t*)malloc(sizeof(vi_t) * (L > 0 ? L : 1));
+        int32_t* sel = (int32_t*)malloc(sizeof(int32_t) * (k > 0 ? k : 1));
+        if (!buf || !sel) { bad = 1; free(buf); free(sel); continue; }
+        for (int64_t s = 0; s < L; ++s) { buf[s].v = logits[r * ld + s]; buf[s].i = (int32_t)s; }
+        qsort(buf, (size_t)L, sizeof(vi_t), cmp_value_desc);
+        int64_t m = L < k ? L : k;
+        for (int64_t i = 0; i < m; ++i) sel[i] = buf[i].i;
+        qsort(sel, (size_t)m, sizeof(int32_t), cmp_int_asc);
+        int64_t b = row_req[r];
+        for (int64_t i = 0; i < k; ++i) {
+            int32_t s = i < m ? sel[i] : -1;
+            int32_t g = -1;
+            if (s >= 0) {
+                int64_t blk = block_table[b * bt_stride + s / block_size];
+                g = (int32_t)(blk * block_size + s % block_size);
+            }
+            if (out_local) out_local[r * k + i] = s;
+            out_global[r * k + i] = g;
+        }
+        free(buf);
+        free(sel);
+    }
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* fp8_ds_mla cache write [DSMLA]                                             */
+/* ------------------------------------------------------------------------- */
+
+/* Entry at blk*block_stride + off*entry_stride (bytes):
+ *   [0,512)   fp8 NoPE, 4 tiles of 128, each coded with its own scale
+ *   [512,528) the 4 fp32 tile scales
+ *   [528,656) the 64 bf16 RoPE values, bit for bit. */
+int oracle_dsmla_quant_write(const uint16_t* nope, const uint16_t* rope, int64_t n,
+                             const int64_t* slot_mapping, uint8_t* cache,
+                             int64_t num_blocks, int block_size,
+                             int64_t block_stride, int64_t entry_stride)
+{
+    codec_init();
+    const float inv448 = (float)(1.0 / 448.0);
+    const float floor_scale = 1.1754944e-38f;
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int64_t t = 0; t < n; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        int64_t blk = slot / block_size, off = slot % block_size;
+        if (blk >= num_blocks) { bad = 1; continue; }
+        uint8_t* e = cache + blk * block_stride + off * entry_stride;
+        for (int tile = 0; tile < 4; ++tile) {
+            const uint16_t* src = nope + t * 512 + tile * 128;
+            float amax = 0.0f;
+            for (int i = 0; i < 128; ++i) {
+                float a = fabsf(bf16_to_f32(src[i]));
+                if (a > amax) amax = a;
+            }
+            float sc = amax * inv448;
+            if (!(sc >= floor_scale)) sc = floor_scale;
+            for (int i = 0; i < 128; ++i)
+                e[tile * 128 + i] = oracle_e4m3_encode(bf16_to_f32(src[i]) / sc);
+            memcpy(e + 512 + 4 * tile, &sc, 4);
+        }
+        memcpy(e + 528, rope + t * 64, 128);
+    }
+    return bad ? -1 : 0;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
