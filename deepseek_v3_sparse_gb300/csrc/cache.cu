@@ -1,0 +1,244 @@
+// cache.cu -- the three bandwidth kernels around the indexer cache:
+//   ix_quant_write_k   indexer-K quantise + paged write
+//   ix_gather_k        ragged paged gather into contiguous K
+//   dsmla_quant_write  the 656-byte fp8_ds_mla entry write
+//
+// All three are pure streaming kernels (16-byte vector loads, grid sized to a
+// multiple of the SM count); their bound is HBM bandwidth.
+#include <float.h>
+
+#include "common.cuh"
+
+namespace dsix {
+namespace {
+
+constexpr int kHeadDim = 128;
+constexpr int kBlockSize = 64;
+constexpr int kBlockBytes = kBlockSize * (kHeadDim + 4);  // 8448
+constexpr int kScaleOffset = kBlockSize * kHeadDim;      // 8192
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&x)[8]) {
+    x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x);
+    x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+    x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z);
+    x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+}
+
+__device__ __forceinline__ float amax8(const float (&x)[8]) {
+    float a = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(x[i]));
+    return a;
+}
+
+// x[i] / scale, correctly rounded, then e4m3 (RNE, satfinite); 8 codes packed
+// little-endian into two words.
+__device__ __forceinline__ uint2 quant8(const float (&x)[8], float scale) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        w[i] = cvt_e4m3x2(__fdiv_rn(x[2 * i], scale), __fdiv_rn(x[2 * i + 1], scale));
+    return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+}
+
+// ---------------------------------------------------------------------------
+// ix_quant_write_k: one 16-lane half-warp per token, 8 bf16 (16 B) per lane.
+// Loop trip counts are uniform per warp so the width-16 shuffles always see
+// all 32 lanes.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) quant_write_k_kernel(const uint4* __restrict__ k, int64_t n,
+                                                            const int64_t* __restrict__ slots,
+                                                            uint8_t* __restrict__ cache,
+                                                            int64_t num_blocks, int* status) {
+    const int lane = threadIdx.x & 31;
+    const int sub = lane & 15;
+    const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t wi = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+         2 * wi < n; wi += warps) {
+        const int64_t tok = 2 * wi + (lane >> 4);
+        const bool valid = tok < n;
+        float x[8];
+        int64_t slot = -1;
+        if (valid) {
+            slot = __ldg(slots + tok);
+            unpack8(__ldg(k + tok * (kHeadDim / 8) + sub), x);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = 0.f;
+        }
+        float amax = amax8(x);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o, 16));
+        const float scale = fmaxf(__fdiv_rn(amax, 448.0f), FLT_MIN);
+        const uint2 codes = quant8(x, scale);
+        if (valid && slot >= 0) {
+            const int64_t blk = slot / kBlockSize;
+            const int off = static_cast<int>(slot % kBlockSize);
+            if (blk >= num_blocks) {
+                if (sub == 0) flag(status, IX_DEV_BAD_SLOT);
+            } else {
+                uint8_t* base = cache + blk * kBlockBytes;
+                *reinterpret_cast<uint2*>(base + off * kHeadDim + sub * 8) = codes;
+                if (sub == 0) *reinterpret_cast<float*>(base + kScaleOffset + 4 * off) = scale;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// ix_gather_k: 8 lanes per token (8 x 16 B = one 128-byte row), token ->
+// request by binary search over cu_seq_lens (staged in shared memory).
+// ---------------------------------------------------------------------------
+constexpr int kGatherSmemCu = 4096;
+
+__global__ void __launch_bounds__(256) gather_k_kernel(const uint8_t* __restrict__ cache,
+                                                       int64_t num_blocks,
+                                                       const int32_t* __restrict__ bt,
+                                                       int64_t bt_stride,
+                                                       const int32_t* __restrict__ cu, int batch,
+                                                       uint8_t* __restrict__ out_k,
+                                                       float* __restrict__ out_scale,
+                                                       int64_t capacity, int* status) {
+    __shared__ int32_t s_cu[kGatherSmemCu];
+    const bool staged = batch + 1 <= kGatherSmemCu;
+    if (staged)
+        for (int i = threadIdx.x; i <= batch; i += blockDim.x) s_cu[i] = __ldg(cu + i);
+    __syncthreads();
+    const int32_t* c = staged ? s_cu : cu;
+    const int64_t total = c[batch];
+    if (blockIdx.x == 0 && threadIdx.x == 0 && total > capacity) flag(status, IX_DEV_BAD_RANGE);
+    const int64_t limit = total < capacity ? total : capacity;
+    const int sub = threadIdx.x & 7;
+    const int64_t groups = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 3;
+    for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3; t < limit;
+         t += groups) {
+        // largest b in [0, batch) with cu[b] <= t (this skips empty requests)
+        int lo = 0, hi = batch - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (c[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        const int64_t i = t - c[lo];
+        const int64_t blk = __ldg(bt + lo * bt_stride + i / kBlockSize);
+        if (blk < 0 || blk >= num_blocks) {
+            if (sub == 0) flag(status, IX_DEV_BAD_BLOCK);
+            continue;
+        }
+        const uint8_t* src = cache + blk * kBlockBytes;
+        const int off = static_cast<int>(i % kBlockSize);
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + off * kHeadDim) + sub);
+        reinterpret_cast<uint4*>(out_k + t * kHeadDim)[sub] = v;
+        if (sub == 0) out_scale[t] = __ldg(reinterpret_cast<const float*>(src + kScaleOffset) + off);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dsmla_quant_write: two warps per token; a warp covers 2 tiles of 128 NoPE
+// values (16 lanes x 8 values per tile).
+// ---------------------------------------------------------------------------
+constexpr float kInv448 = 0x1.24924ap-9f;      // f32(1/448)
+constexpr float kScaleFloor = 1.1754944e-38f;  // rounds to FLT_MIN as an f32
+
+__global__ void __launch_bounds__(256) dsmla_write_kernel(const uint4* __restrict__ nope,
+                                                          const uint4* __restrict__ rope, int64_t n,
+                                                          const int64_t* __restrict__ slots,
+                                                          uint8_t* __restrict__ cache,
+                                                          int64_t num_blocks, int block_size,
+                                                          int64_t block_stride, int64_t entry_stride,
+                                                          int* status) {
+    const int lane = threadIdx.x & 31;
+    const int sub = lane & 15;
+    const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t wi = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; wi < 2 * n;
+         wi += warps) {
+        const int64_t tok = wi >> 1;
+        const int half = static_cast<int>(wi & 1);
+        const int tile = 2 * half + (lane >> 4);
+        const int64_t slot = __ldg(slots + tok);
+        if (slot < 0) continue;  // uniform across the warp
+        const int64_t blk = slot / block_size;
+        if (blk >= num_blocks) {
+            if (lane == 0 && half == 0) flag(status, IX_DEV_BAD_SLOT);
+            continue;
+        }
+        uint8_t* e = cache + blk * block_stride + (slot % block_size) * entry_stride;
+        float x[8];
+        unpack8(__ldg(nope + tok * 64 + tile * 16 + sub), x);
+        float amax = amax8(x);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o, 16));
+        const float sc = fmaxf(amax * kInv448, kScaleFloor);
+        *reinterpret_cast<uint2*>(e + tile * 128 + sub * 8) = quant8(x, sc);
+        if (sub == 0) *reinterpret_cast<float*>(e + 512 + 4 * tile) = sc;
+        if (half == 0 && lane < 8)
+            reinterpret_cast<uint4*>(e + 528)[lane] = __ldg(rope + tok * 8 + lane);
+    }
+}
+
+int grid_for(int64_t work_items, int items_per_block) {
+    const int sms = num_sms();
+    int64_t blocks = (work_items + items_per_block - 1) / items_per_block;
+    const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 148) * 16;
+    if (blocks > cap) blocks = cap;
+    return static_cast<int>(blocks < 1 ? 1 : blocks);
+}
+
+}  // namespace
+}  // namespace dsix
+
+using namespace dsix;
+
+extern "C" int ix_quant_write_k(const void* k_bf16, int64_t n, int head_dim,
+                                const int64_t* slot_mapping, uint8_t* cache, int64_t num_blocks,
+                                int block_size, ix_stream_t stream) {
+    if (n < 0 || num_blocks < 0) return IX_ERR_SHAPE;
+    if (head_dim != kHeadDim || block_size != kBlockSize) return IX_ERR_UNSUPPORTED;
+    if (n == 0) return IX_OK;
+    if (!k_bf16 || !slot_mapping || !cache) return IX_ERR_NULL;
+    if (!aligned16(k_bf16) || !aligned16(cache) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7))
+        return IX_ERR_ALIGN;
+    int* st = status_ptr();
+    if (!st) return IX_ERR_CUDA;
+    quant_write_k_kernel<<<grid_for(n, 16), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(k_bf16), n, slot_mapping, cache, num_blocks, st);
+    return launch_status();
+}
+
+extern "C" int ix_gather_k(const uint8_t* cache, int64_t num_blocks, int block_size, int head_dim,
+                           const int32_t* block_table, int64_t bt_stride,
+                           const int32_t* cu_seq_lens, int batch, uint8_t* out_k, float* out_scale,
+                           int64_t out_capacity, ix_stream_t stream) {
+    if (num_blocks < 0 || batch < 0 || out_capacity < 0 || bt_stride < 0) return IX_ERR_SHAPE;
+    if (head_dim != kHeadDim || block_size != kBlockSize) return IX_ERR_UNSUPPORTED;
+    if (batch == 0 || out_capacity == 0) return IX_OK;
+    if (!cache || !block_table || !cu_seq_lens || !out_k || !out_scale) return IX_ERR_NULL;
+    if (!aligned16(cache) || !aligned16(out_k) || (reinterpret_cast<uintptr_t>(out_scale) & 3))
+        return IX_ERR_ALIGN;
+    int* st = status_ptr();
+    if (!st) return IX_ERR_CUDA;
+    gather_k_kernel<<<grid_for(out_capacity, 32), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        cache, num_blocks, block_table, bt_stride, cu_seq_lens, batch, out_k, out_scale,
+        out_capacity, st);
+    return launch_status();
+}
+
+extern "C" int dsmla_quant_write(const void* nope_bf16, const void* rope_bf16, int64_t n,
+                                 const int64_t* slot_mapping, uint8_t* cache, int64_t num_blocks,
+                                 int block_size, int64_t block_stride_bytes,
+                                 int64_t entry_stride_bytes, ix_stream_t stream) {
+    if (n < 0 || num_blocks < 0 || block_size <= 0 || block_stride_bytes <= 0 ||
+        entry_stride_bytes < 656)
+        return IX_ERR_SHAPE;
+    if (n == 0) return IX_OK;
+    if (!nope_bf16 || !rope_bf16 || !slot_mapping || !cache) return IX_ERR_NULL;
+    if (!aligned16(nope_bf16) || !aligned16(rope_bf16) || !aligned16(cache) ||
+        (block_stride_bytes & 15) || (entry_stride_bytes & 15) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7))
+        return IX_ERR_ALIGN;
+    int* st = status_ptr();
+    if (!st) return IX_ERR_CUDA;
+    dsmla_write_kernel<<<grid_for(2 * n, 8), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(nope_bf16), static_cast<const uint4*>(rope_bf16), n, slot_mapping,
+        cache, num_blocks, block_size, block_stride_bytes, entry_stride_bytes, st);
+    return launch_status();
+}

@@ -1,0 +1,214 @@
+/*
+ * dsix.h -- C ABI of the GB300 (sm_103a) DeepSeek-V3.2 sparse-attention
+ * indexer hot path: indexer-K quantise/write, paged gather, FP8 MQA logits
+ * (paged decode and contiguous prefill), per-row top-k with remap to global
+ * paged-KV slots, and the fp8_ds_mla cache write.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every pointer argument is a DEVICE pointer owned by the caller, unless a
+ *   comment says otherwise.  The library never allocates, frees or retains
+ *   caller memory.
+ * - Every call is asynchronous on `stream` (a cudaStream_t; 0 = legacy default
+ *   stream).  No entry point synchronises, reads device memory on the host, or
+ *   allocates, so every call can be captured into a CUDA graph (the host-sync
+ *   failure that vLLM PR #36250 "[kernel] Fix FP8 paged MQA fallback for CUDA
+ *   graph capture" fixes cannot occur here).  The first call of each entry
+ *   point on a device sets kernel attributes; make it before any capture.
+ * - Return value: IX_OK (0) or a negative IX_ERR_* code.  Argument errors are
+ *   detected on the host before anything is launched; IX_ERR_CUDA reports a
+ *   launch failure from the CUDA runtime.
+ * - Values the host cannot see (block-table entries, lengths) are checked on
+ *   the device: a kernel that meets one that is out of range skips the access
+ *   and ORs a bit into a per-device status word, which ix_device_status()
+ *   returns (synchronously) and clears.
+ * - Supported shapes: head_dim 128, 64 heads, block_size 64 (the DeepSeek-V3.2
+ *   indexer), next_n 1..2.  Anything else returns IX_ERR_UNSUPPORTED.
+ * - fp8 means OCP E4M3 (bias 7, largest finite 448); conversions round to
+ *   nearest even and saturate.
+ *
+ * Indexer-K paged cache layout (vLLM PR #25869 "[Model] Support Deepseek
+ * V3.2", code review of cp_gather_indexer_k_quant_cache): uint8
+ * [num_blocks][block_size*(head_dim+4)]; a block holds block_size x head_dim
+ * fp8 values token by token, then block_size fp32 scales (4 bytes each).  At
+ * 64 x 128 a block is 8448 bytes: token j's values at [128j, 128j+128), its
+ * scale at 8192 + 4j.  The cache base must be 16-byte aligned.
+ */
+#ifndef DSIX_H
+#define DSIX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* ix_stream_t;
+
+enum {
+    IX_OK = 0,
+    IX_ERR_NULL = -1,         /* a required pointer is NULL */
+    IX_ERR_SHAPE = -2,        /* a size or stride is negative or inconsistent */
+    IX_ERR_UNSUPPORTED = -3,  /* head_dim / heads / block_size / next_n / k / ld not supported */
+    IX_ERR_ALIGN = -4,        /* a base pointer or stride breaks the stated alignment */
+    IX_ERR_WORKSPACE = -5,    /* reserved */
+    IX_ERR_CUDA = -6,         /* the CUDA runtime rejected a launch or a query */
+    IX_ERR_DEVICE_CHECK = -7  /* returned by ix_device_status when a device check fired */
+};
+
+/* Bits of the device status word (see ix_device_status). */
+enum {
+    IX_DEV_BAD_SLOT = 1,        /* slot_mapping entry past the block pool: token skipped */
+    IX_DEV_BAD_BLOCK = 2,       /* block_table entry outside [0, num_blocks): access skipped */
+    IX_DEV_ROW_TOO_LONG = 4,    /* a visible row is longer than ld: columns >= ld dropped */
+    IX_DEV_BAD_RANGE = 8,       /* ks/ke outside [0, tk], or cu_seq_lens past out_capacity */
+    IX_DEV_TIMEOUT = 16         /* a pipeline wait gave up (never expected) */
+};
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* ix_status_string(int status);
+
+/*
+ * Reads and clears the calling device's status word.  SYNCHRONOUS: it waits
+ * for all work on the device.  Diagnostic only -- never call it on the hot
+ * path or during stream capture.  *status_out (may be NULL) receives the
+ * IX_DEV_* bits; returns IX_OK if no bit was set, IX_ERR_DEVICE_CHECK if one
+ * was, IX_ERR_CUDA on a runtime error.
+ */
+int ix_device_status(int* status_out);
+
+/*
+ * ix_quant_write_k -- quantise new indexer keys and write them into the paged
+ * cache.  For every token t with slot = slot_mapping[t] >= 0:
+ *   amax  = max_i |k[t,i]|                       (bf16 values, exact in f32)
+ *   scale = max(amax / 448, FLT_MIN)             (IEEE f32 division)
+ *   v[i]  = fp8(k[t,i] / scale)                  (IEEE f32 division, RNE, satfinite)
+ * written to block slot/block_size, row slot%block_size of the layout above.
+ * Tokens with a negative slot are skipped.  This is the DeepSeek-V3.2 indexer
+ * K quantisation, into the layout that vLLM PR #25869's
+ * cp_gather_indexer_k_quant_cache review reads back.
+ *   k_bf16        bf16 [n, head_dim], row-major, 16-byte aligned
+ *   slot_mapping  int64 [n]
+ *   cache         uint8 [num_blocks, block_size*(head_dim+4)], 16-byte aligned
+ */
+int ix_quant_write_k(const void* k_bf16, int64_t n, int head_dim,
+                     const int64_t* slot_mapping, uint8_t* cache,
+                     int64_t num_blocks, int block_size, ix_stream_t stream);
+
+/*
+ * ix_gather_k -- copy ragged paged indexer K into contiguous buffers (vLLM PR
+ * #25869, code review of cp_gather_indexer_k_quant_cache).  For each request b
+ * with s = cu_seq_lens[b+1] - cu_seq_lens[b] > 0 and each i < s:
+ *   out_k[cu_seq_lens[b] + i, :]   = values of row i%bs of block block_table[b, i/bs]
+ *   out_scale[cu_seq_lens[b] + i]  = that row's fp32 scale
+ * i.e. all full blocks, then the first s%bs rows of the last block.  Rows at or
+ * past cu_seq_lens[batch] are not written.
+ *   block_table   int32 [batch, bt_stride]
+ *   cu_seq_lens   int32 [batch+1], non-decreasing, cu_seq_lens[0] = 0
+ *   out_k         fp8 (uint8) [out_capacity, head_dim], 16-byte aligned
+ *   out_scale     fp32 [out_capacity]
+ *   out_capacity  host-side upper bound on cu_seq_lens[batch]; rows at or past
+ *                 it are never written (IX_DEV_BAD_RANGE if that drops any)
+ */
+int ix_gather_k(const uint8_t* cache, int64_t num_blocks, int block_size, int head_dim,
+                const int32_t* block_table, int64_t bt_stride,
+                const int32_t* cu_seq_lens, int batch, uint8_t* out_k,
+                float* out_scale, int64_t out_capacity, ix_stream_t stream);
+
+/*
+ * ix_paged_mqa_logits -- decode indexer logits over the paged cache (the op
+ * that vLLM PR #36250's fp8_paged_mqa_logits fallback computes).  Row
+ * r = b*next_n + j (j < next_n) sees L = context_lens[b] - next_n + 1 + j keys;
+ * for s < L:
+ *   logits[r, s] = k_scale[s] * sum_h w[r, h] * ReLU(sum_d q[b, j, h, d] * k[s, d])
+ * with k and k_scale read through block_table[b, s/64].  FP8 x FP8 products,
+ * FP32 accumulation (tcgen05 tensor cores).  With clean_logits != 0 the
+ * entries [L, ld) are set to -inf; with 0 they are left untouched (the
+ * clean_logits=False mode discussed in the same PR's review).
+ *   q_fp8         uint8 (e4m3) [batch, next_n, heads, head_dim], 16-byte aligned
+ *   w             fp32 [batch*next_n, heads], 16-byte aligned
+ *   context_lens  int32 [batch]
+ *   block_table   int32 [batch, bt_stride]
+ *   logits        fp32 [batch*next_n, ld]; ld >= every L, ld % 4 == 0
+ */
+int ix_paged_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t* cache,
+                        int64_t num_blocks, int block_size,
+                        const int32_t* context_lens, const int32_t* block_table,
+                        int64_t bt_stride, int batch, int next_n, int heads,
+                        int head_dim, float* logits, int64_t ld, int clean_logits,
+                        ix_stream_t stream);
+
+/*
+ * ix_mqa_logits -- prefill indexer logits over contiguous K (the dense
+ * contraction that follows the gather of vLLM PR #25869).  Row t sees keys
+ * [ks[t], ke[t]); for j < ke[t] - ks[t]:
+ *   logits[t, j] = k_scale[ks[t]+j] * sum_h w[t, h] * ReLU(q[t, h, :] . k[ks[t]+j, :])
+ * Column j is the request-local key index when ks[t] is the request's first
+ * gathered row.  clean_logits as above, for [ke[t]-ks[t], ld).
+ *   q_fp8    uint8 (e4m3) [tq, heads, head_dim], 16-byte aligned
+ *   w        fp32 [tq, heads], 16-byte aligned
+ *   k_fp8    uint8 (e4m3) [tk, head_dim], 16-byte aligned
+ *   k_scale  fp32 [tk], 16-byte aligned
+ *   ks, ke   int32 [tq], 0 <= ks <= ke <= tk
+ *   logits   fp32 [tq, ld]; ld >= every ke - ks, ld % 4 == 0
+ */
+int ix_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t* k_fp8,
+                  const float* k_scale, const int32_t* ks, const int32_t* ke,
+                  int64_t tq, int64_t tk, int heads, int head_dim, float* logits,
+                  int64_t ld, int clean_logits, ix_stream_t stream);
+
+/*
+ * ix_topk_to_global -- per-row top-k of the indexer logits and remap of each
+ * selected request-local index to its global paged-KV slot (ROCm/ATOM PR #1094
+ * "[Feat] Support DSv3.2 with sglang-ATOM plugin and sglang sparse MLA",
+ * Technical Details: a 2-D top-k index buffer; request-local top-k indices
+ * converted to global paged KV indices).  Row r, L = row_len[r] (clamped to
+ * [0, ld]), b = row_req[r]:
+ *   select the min(k, L) columns s < L with the largest logits[r, s]; equal
+ *   values go to the lower index; -0.0 equals +0.0;
+ *   out_local[r, :]  = the selected s in ascending order, then -1 up to k
+ *   out_global[r, i] = block_table[b, s/block_size]*block_size + s%block_size,
+ *                      or -1 where out_local is -1
+ * Logits at or past L are never read.  NaN logits give an unspecified
+ * selection.
+ *   logits      fp32 [rows, ld], 16-byte aligned, ld % 4 == 0
+ *   row_len, row_req  int32 [rows]
+ *   block_table int32 [*, bt_stride]
+ *   out_local   int32 [rows, k] or NULL
+ *   out_global  int32 [rows, k]
+ * Supports ld <= 262144 (longer rows return IX_ERR_UNSUPPORTED) and k >= 1.
+ */
+int ix_topk_to_global(const float* logits, int64_t ld, int64_t rows,
+                      const int32_t* row_len, const int32_t* row_req,
+                      const int32_t* block_table, int64_t bt_stride, int block_size,
+                      int k, int32_t* out_local, int32_t* out_global,
+                      ix_stream_t stream);
+
+/*
+ * dsmla_quant_write -- the fp8_ds_mla cache write (vLLM PR #47090, prhub
+ * summary, key source snippet of _fused_norm_rope_kernel, fp8_ds_mla branch).
+ * For every token t with slot = slot_mapping[t] >= 0, at byte
+ * (slot/block_size)*block_stride_bytes + (slot%block_size)*entry_stride_bytes:
+ *   bytes [0,512)    fp8 NoPE: for tile c of 128 values,
+ *                    sc_c = max(amax_c * f32(1/448), 1.1754944e-38) (f32 multiply),
+ *                    v = fp8(x / sc_c) (IEEE f32 division, RNE, satfinite)
+ *   bytes [512,528)  sc_0..sc_3 as fp32
+ *   bytes [528,656)  the 64 bf16 RoPE values, copied bit for bit
+ * Tokens with a negative slot are skipped.  The RoPE values arrive already
+ * rotated (normalisation and rotation are the caller's).
+ *   nope_bf16  bf16 [n, 512], 16-byte aligned;  rope_bf16  bf16 [n, 64], 16-byte aligned
+ *   cache      uint8, 16-byte aligned; block_stride_bytes and entry_stride_bytes
+ *              multiples of 16, entry_stride_bytes >= 656
+ */
+int dsmla_quant_write(const void* nope_bf16, const void* rope_bf16, int64_t n,
+                      const int64_t* slot_mapping, uint8_t* cache, int64_t num_blocks,
+                      int block_size, int64_t block_stride_bytes,
+                      int64_t entry_stride_bytes, ix_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSIX_H */
