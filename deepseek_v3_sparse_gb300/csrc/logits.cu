@@ -1,0 +1,782 @@
+// logits.cu -- FP8 MQA indexer logits on the 5th-generation tensor cores.
+//
+//   ix_paged_mqa_logits  decode: keys streamed from the paged indexer-K cache
+//   ix_mqa_logits        prefill: keys from contiguous (gathered) K
+//
+// Score (DeepSeek-V3.2 lightning indexer):
+//   logit[row, s] = k_scale[s] * sum_h w[row, h] * ReLU(q[row, h, :] . k[s, :])
+//
+// Design (one persistent CTA per SM, warp-specialised):
+//   * MMA orientation: keys on M (128 per tile), (query row, head) on N.  TMEM
+//     lane m then holds every head score of key m, so the weighted ReLU head
+//     sum is a per-thread loop with no shuffles.
+//       decode : N = 64 * next_n (the next_n rows of one request), 1 MMA job per tile
+//       prefill: 8 query rows per group, two jobs of N = 256 (rows 0-3, 4-7) per tile
+//     One job = 4 x tcgen05.mma.kind::f8f6f4 (K = 128 = 4 x 32), FP32 accumulators
+//     in TMEM (512 columns: 4 slots of 128 for decode, 2 of 256 for prefill).
+//   * Warp 0 is the TMA producer: K tiles (128 B rows, 128-byte swizzle; a paged
+//     tile is two 64-key blocks, each one 3-D TMA box), the tile's fp32 key
+//     scales, and per group the Q operand (TMA) and head weights (bulk copy).
+//   * Warp 1 (one elected lane) issues the MMAs and commits to mbarriers.
+//   * Warps 2-9 are two epilogue warpgroups that alternate jobs: tcgen05.ld of
+//     the accumulators, ReLU, head-weighted sum, key scale, masked store.
+//   * Work = the flattened list of (group, key-tile) units over all groups,
+//     split evenly across CTAs on the device from context_lens / ks,ke (no host
+//     sync, graph-capturable).  Each role walks the same unit sequence.
+//   * Every wait is bounded (mbar_wait): on a timeout the CTA raises an abort
+//     flag, all roles leave their loops, in-flight copies and MMAs are drained
+//     with bounded waits, TMEM is freed, and IX_DEV_TIMEOUT is recorded.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+
+namespace dsix {
+namespace {
+
+constexpr int kHeads = 64;
+constexpr int kDim = 128;
+constexpr int kBlk = 64;
+constexpr int kTile = 128;       // keys per tile (MMA M)
+constexpr int kTileBytes = kTile * kDim;
+constexpr int kThreads = 320;    // 10 warps
+constexpr int kProducerWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kFirstEpiWarp = 2;
+constexpr int kScaleRing = 16;   // key-scale ring entries (one per tile in flight)
+constexpr int kScaleBox = 132;   // floats per entry (128 + 4 for an aligned start)
+constexpr int kSmemGroups = 2048;
+constexpr int kTmemCols = 512;
+constexpr uint64_t kDrainLimitNs = 100000000ull;  // 100 ms
+
+template <bool kPaged>
+struct Cfg;
+
+template <>
+struct Cfg<true> {  // decode over the paged cache
+    static constexpr int kStages = 8;
+    static constexpr int kQBytes = 2 * kHeads * kDim;  // next_n <= 2
+    static constexpr int kWFloats = 2 * kHeads;
+    static constexpr int kSlots = 4;
+    static constexpr int kSlotCols = 128;
+    static constexpr int kHalves = 1;
+    static constexpr int kScEmptyCount = 4;
+};
+
+template <>
+struct Cfg<false> {  // prefill over contiguous K
+    static constexpr int kRows = 8;
+    static constexpr int kStages = 4;
+    static constexpr int kQBytes = kRows * kHeads * kDim;  // 64 KB
+    static constexpr int kWFloats = kRows * kHeads;
+    static constexpr int kSlots = 2;
+    static constexpr int kSlotCols = 256;
+    static constexpr int kHalves = 2;
+    static constexpr int kScEmptyCount = 8;
+};
+
+template <bool P>
+struct Smem {
+    using C = Cfg<P>;
+    static constexpr int kQ = 0;                                     // 2 Q buffers
+    static constexpr int kK = kQ + 2 * C::kQBytes;                   // K stages
+    static constexpr int kSc = kK + C::kStages * kTileBytes;         // key-scale ring
+    static constexpr int kW = kSc + kScaleRing * kScaleBox * 4;      // 2 head-weight buffers
+    static constexpr int kTiles = kW + 2 * C::kWFloats * 4;          // tiles per group
+    static constexpr int kBar = kTiles + kSmemGroups * 4;
+    static constexpr int kNumBars = 2 * C::kStages + 4 + 2 * C::kSlots + 2 * kScaleRing + 1;
+    static constexpr int kMisc = kBar + kNumBars * 8;
+    static constexpr int kScan = kMisc + 64;
+    static constexpr int kTotal = kScan + 64 * 4;
+    static constexpr int kAlloc = kTotal + 1024;  // slack for 1024-byte alignment
+    static_assert(kAlloc <= 232448, "shared memory budget");
+    static_assert(kSc % 16 == 0 && kW % 16 == 0 && kBar % 8 == 0, "alignment");
+};
+
+struct LogitsArgs {
+    const float* w;
+    float* logits;
+    int64_t ld;
+    int num_groups;
+    int* status;
+    // decode
+    const int32_t* context_lens;
+    const int32_t* bt;
+    int64_t bt_stride;
+    int next_n;
+    int64_t num_blocks;
+    // prefill
+    const int32_t* ks;
+    const int32_t* ke;
+    int64_t tq;
+    int64_t tk;
+};
+
+// ---------------------------------------------------------------------------
+// per-row visible ranges (clamped; report=true records why)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int decode_row_len(const LogitsArgs& a, int ctx, int j, bool report) {
+    int64_t L = static_cast<int64_t>(ctx) - a.next_n + 1 + j;
+    if (L < 0) L = 0;
+    if (L > a.ld) {
+        if (report) flag(a.status, IX_DEV_ROW_TOO_LONG);
+        L = a.ld;
+    }
+    return static_cast<int>(L);
+}
+
+__device__ __forceinline__ void prefill_row_range(const LogitsArgs& a, int64_t r, int& s0, int& s1,
+                                                  bool report) {
+    int64_t x0 = __ldg(a.ks + r), x1 = __ldg(a.ke + r);
+    if (x0 < 0 || x1 > a.tk || x1 < x0) {
+        if (report) flag(a.status, IX_DEV_BAD_RANGE);
+        x0 = x0 < 0 ? 0 : x0;
+        x1 = x1 > a.tk ? a.tk : x1;
+        if (x1 < x0) x1 = x0;
+    }
+    if (x1 - x0 > a.ld) {
+        if (report) flag(a.status, IX_DEV_ROW_TOO_LONG);
+        x1 = x0 + a.ld;
+    }
+    s0 = static_cast<int>(x0);
+    s1 = static_cast<int>(x1);
+}
+
+// Key range [kbeg, kend) that a group's rows need.
+template <bool P>
+__device__ __forceinline__ void group_range(const LogitsArgs& a, int g, int& kbeg, int& kend,
+                                            bool report) {
+    if constexpr (P) {
+        kbeg = 0;
+        kend = decode_row_len(a, __ldg(a.context_lens + g), a.next_n - 1, report);
+    } else {
+        kbeg = 0x7fffffff;
+        kend = 0;
+        const int64_t r0 = static_cast<int64_t>(g) * Cfg<false>::kRows;
+#pragma unroll
+        for (int i = 0; i < Cfg<false>::kRows; ++i) {
+            if (r0 + i >= a.tq) break;
+            int s0, s1;
+            prefill_row_range(a, r0 + i, s0, s1, report);
+            if (s1 > s0) {
+                kbeg = min(kbeg, s0);
+                kend = max(kend, s1);
+            }
+        }
+        if (kend == 0) kbeg = 0;
+    }
+}
+
+template <bool P>
+__device__ __forceinline__ int group_tiles(const LogitsArgs& a, int g, bool report) {
+    int kb, ke;
+    group_range<P>(a, g, kb, ke, report);
+    return ke > kb ? (ke - kb + kTile - 1) / kTile : 0;
+}
+
+// Block-wide exclusive scan of one int per thread; *total receives the sum.
+__device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scratch[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        constexpr int nw = kThreads / 32;
+        int s = lane < nw ? scratch[lane] : 0;
+        int inc = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        if (lane < nw) scratch[32 + lane] = inc - s;
+        if (lane == nw - 1) scratch[63] = inc;
+    }
+    __syncthreads();
+    const int r = scratch[32 + warp] + x - v;
+    *total = scratch[63];
+    __syncthreads();
+    return r;
+}
+
+// Walks the flattened (group, tile) units of this CTA.
+template <bool P>
+struct Cursor {
+    int g, t, ntiles, left;
+    __device__ __forceinline__ int tiles_of(const LogitsArgs& a, const int* s_tiles, int gg) const {
+        return gg < kSmemGroups ? s_tiles[gg] : group_tiles<P>(a, gg, false);
+    }
+    // Returns true when the next unit starts a new group.
+    __device__ __forceinline__ bool advance(const LogitsArgs& a, const int* s_tiles) {
+        ++t;
+        --left;
+        if (left > 0 && t == ntiles) {
+            do {
+                ++g;
+                ntiles = tiles_of(a, s_tiles, g);
+            } while (ntiles == 0);
+            t = 0;
+            return true;
+        }
+        return false;
+    }
+};
+
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, status);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Wait that ignores the abort flag (drains in-flight work on the way out).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* status) {
+    volatile int never = 0;
+    mbar_wait(bar, parity, &never, status, kDrainLimitNs);
+}
+
+template <bool P>
+__global__ void __launch_bounds__(kThreads, 1)
+    logits_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmS,
+                  const __grid_constant__ CUtensorMap tmQ, const LogitsArgs a) {
+    using C = Cfg<P>;
+    using S = Smem<P>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+    uint8_t* sQ = sm + S::kQ;
+    uint8_t* sK = sm + S::kK;
+    float* sSc = reinterpret_cast<float*>(sm + S::kSc);
+    float* sW = reinterpret_cast<float*>(sm + S::kW);
+    int* s_tiles = reinterpret_cast<int*>(sm + S::kTiles);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S::kBar);
+    uint64_t* empty = full + C::kStages;
+    uint64_t* qw_full = empty + C::kStages;
+    uint64_t* qw_empty = qw_full + 2;
+    uint64_t* acc_full = qw_empty + 2;
+    uint64_t* acc_empty = acc_full + C::kSlots;
+    uint64_t* sc_full = acc_empty + C::kSlots;
+    uint64_t* sc_empty = sc_full + kScaleRing;
+    uint64_t* mma_done = sc_empty + kScaleRing;
+    int* misc = reinterpret_cast<int*>(sm + S::kMisc);  // tmem base, abort, g0, t0, units
+    int* scan = reinterpret_cast<int*>(sm + S::kScan);
+    volatile int* abort_flag = misc + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kStages; ++i) {
+            mbar_init(full + i, 1);
+            mbar_init(empty + i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(qw_full + i, 1);
+            mbar_init(qw_empty + i, 8);
+        }
+        for (int i = 0; i < C::kSlots; ++i) {
+            mbar_init(acc_full + i, 1);
+            mbar_init(acc_empty + i, 4);
+        }
+        for (int i = 0; i < kScaleRing; ++i) {
+            mbar_init(sc_full + i, 1);
+            mbar_init(sc_empty + i, C::kScEmptyCount);
+        }
+        mbar_init(mma_done, 1);
+        fence_barrier_init();
+        misc[1] = 0;
+        misc[4] = 0;
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmS);
+        prefetch_tmap(&tmQ);
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(reinterpret_cast<uint32_t*>(misc), kTmemCols);
+        tmem_relinquish();
+    }
+
+    // ---- schedule: split the flattened unit list evenly across CTAs ----
+    const int G = a.num_groups;
+    int local = 0;
+    for (int g = threadIdx.x; g < G; g += kThreads) {
+        const int n = group_tiles<P>(a, g, blockIdx.x == 0);
+        if (g < kSmemGroups) s_tiles[g] = n;
+        local += n;
+    }
+    int U;
+    block_excl_scan(local, scan, &U);
+    const int64_t u0 = static_cast<int64_t>(blockIdx.x) * U / gridDim.x;
+    const int64_t u1 = static_cast<int64_t>(blockIdx.x + 1) * U / gridDim.x;
+    if (u1 > u0) {
+        int running = 0;
+        for (int base = 0; base < G && running <= u0; base += kThreads) {
+            const int g = base + threadIdx.x;
+            const int n = g < G ? (g < kSmemGroups ? s_tiles[g] : group_tiles<P>(a, g, false)) : 0;
+            int chunk;
+            const int excl = block_excl_scan(n, scan, &chunk) + running;
+            if (n > 0 && excl <= u0 && u0 < excl + n) {
+                misc[2] = g;
+                misc[3] = static_cast<int>(u0 - excl);
+                misc[4] = static_cast<int>(u1 - u0);
+            }
+            running += chunk;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = static_cast<uint32_t>(misc[0]);
+    const int units = misc[4];
+
+    if (units > 0) {
+        Cursor<P> cur;
+        cur.g = misc[2];
+        cur.t = misc[3];
+        cur.left = units;
+        cur.ntiles = cur.tiles_of(a, s_tiles, cur.g);
+
+        if (warp == kProducerWarp) {
+            // ------------------------------------------------------------ producer
+            int it = 0, qi = 0;
+            int kbeg = 0, kend = 0;
+            int bt_base = -1, bt_val = -1;
+            bool new_group = true;
+            while (cur.left > 0) {
+                const int g = cur.g;
+                if (new_group) {
+                    group_range<P>(a, g, kbeg, kend, false);
+                    bt_base = -1;
+                    const int qb = qi & 1;
+                    if (!wait_warp(qw_empty + qb, ((qi >> 1) & 1) ^ 1, abort_flag, a.status)) break;
+                    if (lane == 0) {
+                        uint8_t* qdst = sQ + qb * C::kQBytes;
+                        float* wdst = sW + qb * C::kWFloats;
+                        if constexpr (P) {
+                            const uint32_t wbytes = a.next_n * kHeads * 4;
+                            mbar_arrive_expect_tx(qw_full + qb, a.next_n * kHeads * kDim + wbytes);
+                            tma_load_2d(qdst, &tmQ, qw_full + qb, 0, g * a.next_n * kHeads);
+                            bulk_load(wdst, a.w + static_cast<int64_t>(g) * a.next_n * kHeads, wbytes,
+                                      qw_full + qb);
+                        } else {
+                            const int64_t r0 = static_cast<int64_t>(g) * C::kRows;
+                            const int nrows = static_cast<int>(a.tq - r0 < C::kRows ? a.tq - r0 : C::kRows);
+                            const uint32_t wbytes = nrows * kHeads * 4;
+                            mbar_arrive_expect_tx(qw_full + qb, C::kQBytes + wbytes);
+                            const int qrow = static_cast<int>(r0 * kHeads);
+                            tma_load_2d(qdst, &tmQ, qw_full + qb, 0, qrow);
+                            tma_load_2d(qdst + C::kQBytes / 2, &tmQ, qw_full + qb, 0, qrow + 256);
+                            bulk_load(wdst, a.w + r0 * kHeads, wbytes, qw_full + qb);
+                        }
+                    }
+                    ++qi;
+                }
+                const int stage = it % C::kStages;
+                const int sci = it % kScaleRing;
+                if (!wait_warp(empty + stage, ((it / C::kStages) & 1) ^ 1, abort_flag, a.status)) break;
+                if (!wait_warp(sc_empty + sci, ((it / kScaleRing) & 1) ^ 1, abort_flag, a.status)) break;
+                uint8_t* kdst = sK + stage * kTileBytes;
+                float* sdst = sSc + sci * kScaleBox;
+                if constexpr (P) {
+                    if (bt_base < 0 || cur.t - bt_base >= 16) {
+                        bt_base = cur.t;
+                        const int bi = 2 * cur.t + lane;
+                        bt_val = -1;
+                        if (bi * kBlk < kend) {
+                            bt_val = __ldg(a.bt + static_cast<int64_t>(g) * a.bt_stride + bi);
+                            if (bt_val < 0 || bt_val >= a.num_blocks) {
+                                flag(a.status, IX_DEV_BAD_BLOCK);
+                                bt_val = static_cast<int>(a.num_blocks);  // out of the map: zero fill
+                            }
+                        }
+                    }
+                    const int blk0 = __shfl_sync(0xffffffffu, bt_val, 2 * (cur.t - bt_base));
+                    const int blk1 = __shfl_sync(0xffffffffu, bt_val, 2 * (cur.t - bt_base) + 1);
+                    const bool two = (2 * cur.t + 1) * kBlk < kend;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(full + stage, two ? kTileBytes : kTileBytes / 2);
+                        tma_load_3d(kdst, &tmK, full + stage, 0, 0, blk0);
+                        if (two) tma_load_3d(kdst + kTileBytes / 2, &tmK, full + stage, 0, 0, blk1);
+                        mbar_arrive_expect_tx(sc_full + sci, two ? 512 : 256);
+                        tma_load_2d(sdst, &tmS, sc_full + sci, 0, blk0);
+                        if (two) tma_load_2d(sdst + kBlk, &tmS, sc_full + sci, 0, blk1);
+                    }
+                } else {
+                    const int start = kbeg + cur.t * kTile;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(full + stage, kTileBytes);
+                        tma_load_2d(kdst, &tmK, full + stage, 0, start);
+                        mbar_arrive_expect_tx(sc_full + sci, kScaleBox * 4);
+                        tma_load_1d(sdst, &tmS, sc_full + sci, start & ~3);
+                    }
+                }
+                ++it;
+                new_group = cur.advance(a, s_tiles);
+            }
+            // drain: the last copies issued into each buffer must land before exit
+            if (lane == 0) {
+                for (int i = max(0, it - C::kStages); i < it; ++i)
+                    drain_wait(full + i % C::kStages, (i / C::kStages) & 1, a.status);
+                for (int i = max(0, it - kScaleRing); i < it; ++i)
+                    drain_wait(sc_full + i % kScaleRing, (i / kScaleRing) & 1, a.status);
+                for (int i = max(0, qi - 2); i < qi; ++i)
+                    drain_wait(qw_full + (i & 1), (i >> 1) & 1, a.status);
+            }
+        } else if (warp == kMmaWarp) {
+            // ------------------------------------------------------------ MMA issuer
+            if (lane == 0) {
+                int it = 0, qi = 0, job = 0;
+                uint32_t qaddr = 0;
+                bool issued = false, new_group = true;
+                const uint32_t idesc = P ? idesc_e4m3_f32(kTile, kHeads * a.next_n)
+                                         : idesc_e4m3_f32(kTile, 256);
+                while (cur.left > 0) {
+                    if (new_group) {
+                        const int qb = qi & 1;
+                        if (!mbar_wait(qw_full + qb, (qi >> 1) & 1, abort_flag, a.status)) break;
+                        qaddr = smem_u32(sQ + qb * C::kQBytes);
+                        ++qi;
+                    }
+                    const int stage = it % C::kStages;
+                    if (!mbar_wait(full + stage, (it / C::kStages) & 1, abort_flag, a.status)) break;
+                    tc_fence_after();
+                    const uint32_t aaddr = smem_u32(sK + stage * kTileBytes);
+                    bool ok = true;
+#pragma unroll
+                    for (int h = 0; h < C::kHalves; ++h) {
+                        const int slot = job % C::kSlots;
+                        if (!mbar_wait(acc_empty + slot, ((job / C::kSlots) & 1) ^ 1, abort_flag,
+                                       a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d = tmem_base + slot * C::kSlotCols;
+                        const uint32_t baddr = qaddr + h * (C::kQBytes / 2);
+#pragma unroll
+                        for (int kk = 0; kk < kDim / 32; ++kk)
+                            mma_e4m3(d, sdesc_k_sw128(aaddr + 32 * kk), sdesc_k_sw128(baddr + 32 * kk),
+                                     idesc, kk > 0);
+                        mma_commit(acc_full + slot);
+                        issued = true;
+                        ++job;
+                    }
+                    if (!ok) break;
+                    mma_commit(empty + stage);
+                    ++it;
+                    new_group = cur.advance(a, s_tiles);
+                }
+                if (issued) {
+                    mma_commit(mma_done);
+                    drain_wait(mma_done, 0, a.status);
+                }
+            }
+        } else {
+            // ------------------------------------------------------------ epilogue
+            const int wg = (warp - kFirstEpiWarp) >> 2;
+            const int quad = warp & 3;
+            const int m = quad * 32 + lane;  // tile row = TMEM lane
+            const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+            int it = 0, qi = 0, job = 0;
+            int kbeg = 0, kend = 0;
+            int rlen[2] = {0, 0};      // decode: visible length per row
+            int rs0[4], rs1[4];        // prefill: [ks, ke) of this warpgroup's rows
+            bool new_group = true, have_group = false;
+            while (cur.left > 0) {
+                const int g = cur.g;
+                if (new_group) {
+                    if (have_group) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(qw_empty + ((qi - 1) & 1));
+                    }
+                    if (!wait_warp(qw_full + (qi & 1), (qi >> 1) & 1, abort_flag, a.status)) break;
+                    ++qi;
+                    have_group = true;
+                    group_range<P>(a, g, kbeg, kend, false);
+                    if constexpr (P) {
+                        const int ctx = __ldg(a.context_lens + g);
+                        for (int j = 0; j < a.next_n; ++j) rlen[j] = decode_row_len(a, ctx, j, false);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int64_t r = static_cast<int64_t>(g) * C::kRows + wg * 4 + i;
+                            rs0[i] = 0;
+                            rs1[i] = 0;
+                            if (r < a.tq) prefill_row_range(a, r, rs0[i], rs1[i], false);
+                        }
+                    }
+                }
+                const float* wbuf = sW + ((qi - 1) & 1) * C::kWFloats;
+                bool ok = true;
+#pragma unroll
+                for (int h = 0; h < C::kHalves; ++h, ++job) {
+                    if ((job & 1) != wg) continue;
+                    const int slot = job % C::kSlots;
+                    const int sci = it % kScaleRing;
+                    if (!wait_warp(sc_full + sci, (it / kScaleRing) & 1, abort_flag, a.status) ||
+                        !wait_warp(acc_full + slot, (job / C::kSlots) & 1, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int s = kbeg + cur.t * kTile + m;  // key index
+                    const float ksc = sSc[sci * kScaleBox + (P ? 0 : (s - m) & 3) + m];
+                    const uint32_t tbase = lane_addr + slot * C::kSlotCols;
+                    const int nrows = P ? a.next_n : 4;
+                    for (int i = 0; i < nrows; ++i) {
+                        uint32_t v0[32], v1[32];
+                        tmem_ld32(tbase + i * kHeads, v0);
+                        tmem_ld32(tbase + i * kHeads + 32, v1);
+                        tmem_wait_ld();
+                        const float4* w4 = reinterpret_cast<const float4*>(
+                            wbuf + (P ? i : wg * 4 + i) * kHeads);
+                        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const float4 wa = w4[c];
+                            acc0 = fmaf(wa.x, fmaxf(__uint_as_float(v0[4 * c + 0]), 0.f), acc0);
+                            acc1 = fmaf(wa.y, fmaxf(__uint_as_float(v0[4 * c + 1]), 0.f), acc1);
+                            acc0 = fmaf(wa.z, fmaxf(__uint_as_float(v0[4 * c + 2]), 0.f), acc0);
+                            acc1 = fmaf(wa.w, fmaxf(__uint_as_float(v0[4 * c + 3]), 0.f), acc1);
+                            const float4 wb = w4[8 + c];
+                            acc0 = fmaf(wb.x, fmaxf(__uint_as_float(v1[4 * c + 0]), 0.f), acc0);
+                            acc1 = fmaf(wb.y, fmaxf(__uint_as_float(v1[4 * c + 1]), 0.f), acc1);
+                            acc0 = fmaf(wb.z, fmaxf(__uint_as_float(v1[4 * c + 2]), 0.f), acc0);
+                            acc1 = fmaf(wb.w, fmaxf(__uint_as_float(v1[4 * c + 3]), 0.f), acc1);
+                        }
+                        const float logit = (acc0 + acc1) * ksc;
+                        if constexpr (P) {
+                            if (s < rlen[i])
+                                a.logits[(static_cast<int64_t>(g) * a.next_n + i) * a.ld + s] = logit;
+                        } else {
+                            if (s >= rs0[i] && s < rs1[i]) {
+                                const int64_t r = static_cast<int64_t>(g) * C::kRows + wg * 4 + i;
+                                a.logits[r * a.ld + (s - rs0[i])] = logit;
+                            }
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(acc_empty + slot);
+                        mbar_arrive(sc_empty + sci);
+                    }
+                }
+                if (!ok) break;
+                ++it;
+                new_group = cur.advance(a, s_tiles);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// -inf for [visible end, ld) of every row.
+template <bool P>
+__global__ void __launch_bounds__(256) fill_tail_kernel(const LogitsArgs a, int64_t rows) {
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        int64_t start;
+        if constexpr (P) {
+            const int b = static_cast<int>(r / a.next_n), j = static_cast<int>(r % a.next_n);
+            start = decode_row_len(a, __ldg(a.context_lens + b), j, false);
+        } else {
+            int s0, s1;
+            prefill_row_range(a, r, s0, s1, false);
+            start = s1 - s0;
+        }
+        float* row = a.logits + r * a.ld;
+        for (int64_t c = start + threadIdx.x; c < a.ld; c += blockDim.x) row[c] = -INFINITY;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
+              const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+              CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t d[3], s[2];
+    cuuint32_t b[3], e[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+    }
+    for (int i = 0; i + 1 < rank; ++i) s[i] = strides[i];
+    return fn(m, dt, rank, const_cast<void*>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool P>
+int launch(const CUtensorMap& tmK, const CUtensorMap& tmS, const CUtensorMap& tmQ,
+           const LogitsArgs& a, int64_t rows, int clean, cudaStream_t stream) {
+    static std::mutex mu;
+    static std::vector<char> ready;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return IX_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= static_cast<int>(ready.size())) ready.resize(dev + 1, 0);
+        if (!ready[dev]) {
+            if (cudaFuncSetAttribute(logits_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Smem<P>::kAlloc) != cudaSuccess)
+                return IX_ERR_CUDA;
+            ready[dev] = 1;
+        }
+    }
+    const int sms = num_sms();
+    if (sms <= 0) return IX_ERR_CUDA;
+    if (a.num_groups > 0) {
+        logits_kernel<P><<<sms, kThreads, Smem<P>::kAlloc, stream>>>(tmK, tmS, tmQ, a);
+        if (launch_status() != IX_OK) return IX_ERR_CUDA;
+    }
+    if (clean && rows > 0) {
+        const int64_t grid = rows < static_cast<int64_t>(sms) * 8 ? rows : static_cast<int64_t>(sms) * 8;
+        fill_tail_kernel<P><<<static_cast<int>(grid), 256, 0, stream>>>(a, rows);
+        if (launch_status() != IX_OK) return IX_ERR_CUDA;
+    }
+    return IX_OK;
+}
+
+}  // namespace
+}  // namespace dsix
+
+using namespace dsix;
+
+extern "C" int ix_paged_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t* cache,
+                                   int64_t num_blocks, int block_size,
+                                   const int32_t* context_lens, const int32_t* block_table,
+                                   int64_t bt_stride, int batch, int next_n, int heads,
+                                   int head_dim, float* logits, int64_t ld, int clean_logits,
+                                   ix_stream_t stream) {
+    if (batch < 0 || num_blocks < 0 || ld < 0 || bt_stride < 0) return IX_ERR_SHAPE;
+    if (heads != kHeads || head_dim != kDim || block_size != kBlk || next_n < 1 || next_n > 2)
+        return IX_ERR_UNSUPPORTED;
+    if (batch == 0 || ld == 0) return IX_OK;
+    if (ld % 4 != 0 || ld > (1ll << 30)) return IX_ERR_UNSUPPORTED;
+    if (num_blocks < 1 || bt_stride < 1) return IX_ERR_SHAPE;
+    if (!q_fp8 || !w || !cache || !context_lens || !block_table || !logits) return IX_ERR_NULL;
+    if (!aligned16(q_fp8) || !aligned16(w) || !aligned16(cache) || !aligned16(logits))
+        return IX_ERR_ALIGN;
+    int* st = status_ptr();
+    if (!st) return IX_ERR_CUDA;
+    CUtensorMap tmK, tmS, tmQ;
+    {
+        const uint64_t dims[3] = {kDim, kBlk, static_cast<uint64_t>(num_blocks)};
+        const uint64_t strides[2] = {kDim, kBlk * (kDim + 4)};
+        const uint32_t box[3] = {kDim, kBlk, 1};
+        if (!make_map(&tmK, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, cache, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+            return IX_ERR_CUDA;
+    }
+    {
+        const uint64_t dims[2] = {kBlk, static_cast<uint64_t>(num_blocks)};
+        const uint64_t strides[1] = {kBlk * (kDim + 4)};
+        const uint32_t box[2] = {kBlk, 1};
+        if (!make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, cache + kBlk * kDim, dims, strides,
+                      box, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return IX_ERR_CUDA;
+    }
+    {
+        const uint64_t dims[2] = {kDim, static_cast<uint64_t>(batch) * next_n * kHeads};
+        const uint64_t strides[1] = {kDim};
+        const uint32_t box[2] = {kDim, static_cast<uint32_t>(next_n * kHeads)};
+        if (!make_map(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q_fp8, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+            return IX_ERR_CUDA;
+    }
+    LogitsArgs a{};
+    a.w = w;
+    a.logits = logits;
+    a.ld = ld;
+    a.num_groups = batch;
+    a.status = st;
+    a.context_lens = context_lens;
+    a.bt = block_table;
+    a.bt_stride = bt_stride;
+    a.next_n = next_n;
+    a.num_blocks = num_blocks;
+    return launch<true>(tmK, tmS, tmQ, a, static_cast<int64_t>(batch) * next_n, clean_logits,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int ix_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t* k_fp8,
+                             const float* k_scale, const int32_t* ks, const int32_t* ke, int64_t tq,
+                             int64_t tk, int heads, int head_dim, float* logits, int64_t ld,
+                             int clean_logits, ix_stream_t stream) {
+    if (tq < 0 || tk < 0 || ld < 0) return IX_ERR_SHAPE;
+    if (heads != kHeads || head_dim != kDim) return IX_ERR_UNSUPPORTED;
+    if (tq == 0 || ld == 0) return IX_OK;
+    if (ld % 4 != 0 || ld > (1ll << 30) || tk >= (1ll << 31) || tq * kHeads >= (1ll << 31))
+        return IX_ERR_UNSUPPORTED;
+    if (!q_fp8 || !w || !ks || !ke || !logits) return IX_ERR_NULL;
+    if (tk > 0 && (!k_fp8 || !k_scale)) return IX_ERR_NULL;
+    if (!aligned16(q_fp8) || !aligned16(w) || !aligned16(logits) ||
+        (tk > 0 && (!aligned16(k_fp8) || !aligned16(k_scale))))
+        return IX_ERR_ALIGN;
+    int* st = status_ptr();
+    if (!st) return IX_ERR_CUDA;
+    LogitsArgs a{};
+    a.w = w;
+    a.logits = logits;
+    a.ld = ld;
+    a.num_groups = tk > 0 ? static_cast<int>((tq + Cfg<false>::kRows - 1) / Cfg<false>::kRows) : 0;
+    a.status = st;
+    a.ks = ks;
+    a.ke = ke;
+    a.tq = tq;
+    a.tk = tk;
+    CUtensorMap tmK{}, tmS{}, tmQ{};
+    if (tk > 0) {
+        {
+            const uint64_t dims[2] = {kDim, static_cast<uint64_t>(tk)};
+            const uint64_t strides[1] = {kDim};
+            const uint32_t box[2] = {kDim, kTile};
+            if (!make_map(&tmK, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k_fp8, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+                return IX_ERR_CUDA;
+        }
+        {
+            const uint64_t dims[1] = {static_cast<uint64_t>(tk)};
+            const uint32_t box[1] = {kScaleBox};
+            if (!make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, k_scale, dims, nullptr, box,
+                          CU_TENSOR_MAP_SWIZZLE_NONE))
+                return IX_ERR_CUDA;
+        }
+        {
+            const uint64_t dims[2] = {kDim, static_cast<uint64_t>(tq) * kHeads};
+            const uint64_t strides[1] = {kDim};
+            const uint32_t box[2] = {kDim, 256};
+            if (!make_map(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q_fp8, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+                return IX_ERR_CUDA;
+        }
+    }
+    return launch<false>(tmK, tmS, tmQ, a, tq, clean_logits, reinterpret_cast<cudaStream_t>(stream));
+}
