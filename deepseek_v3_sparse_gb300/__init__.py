@@ -1,0 +1,204 @@
+"""Python binding of libdsix (include/dsix.h): the GB300 DeepSeek-V3.2
+sparse-attention indexer hot path.
+
+Argument marshalling only: each function checks dtypes/devices of its torch
+tensors, passes their device pointers and sizes to the C entry point of the
+same name, and raises ``DsixError`` on a non-zero status.  Every step of the
+path runs in the library's CUDA kernels; there is no fallback of any kind --
+if ``libdsix.so`` is missing or fails to load, every call raises.
+
+Outputs are caller-allocated tensors (the library allocates nothing).  Calls
+are asynchronous on ``stream`` (default: torch's current stream) and never
+synchronise, so a sequence of them can be captured in a CUDA graph.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "DsixError", "load", "ix_status_string", "ix_device_status", "ix_quant_write_k",
+    "ix_gather_k", "ix_paged_mqa_logits", "ix_mqa_logits", "ix_topk_to_global",
+    "dsmla_quant_write", "LIB_PATH", "HEADS", "HEAD_DIM", "BLOCK_SIZE",
+]
+
+HEADS = 64
+HEAD_DIM = 128
+BLOCK_SIZE = 64
+INDEXER_BLOCK_BYTES = BLOCK_SIZE * (HEAD_DIM + 4)
+DSMLA_ENTRY_BYTES = 656
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdsix.so")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class DsixError(RuntimeError):
+    pass
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int
+
+_SIGNATURES = {
+    "ix_status_string": ([_I32], ctypes.c_char_p),
+    "ix_device_status": ([_P], _I32),
+    "ix_quant_write_k": ([_P, _I64, _I32, _P, _P, _I64, _I32, _P], _I32),
+    "ix_gather_k": ([_P, _I64, _I32, _I32, _P, _I64, _P, _I32, _P, _P, _I64, _P], _I32),
+    "ix_paged_mqa_logits": ([_P, _P, _P, _I64, _I32, _P, _P, _I64, _I32, _I32, _I32, _I32, _P,
+                             _I64, _I32, _P], _I32),
+    "ix_mqa_logits": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64, _I32, _P], _I32),
+    "ix_topk_to_global": ([_P, _I64, _I64, _P, _P, _P, _I64, _I32, _I32, _P, _P, _P], _I32),
+    "dsmla_quant_write": ([_P, _P, _I64, _P, _P, _I64, _I32, _I64, _I64, _P], _I32),
+}
+
+
+def load(path: Optional[str] = None):
+    """Load libdsix.so (built by ``deepseek_v3_sparse_gb300.build``); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise DsixError(f"{p} is missing: build it with `python -m deepseek_v3_sparse_gb300.build` "
+                            "(there is no non-CUDA fallback)")
+        lib = ctypes.CDLL(p)
+        for name, (args, res) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def ix_status_string(status: int) -> str:
+    return load().ix_status_string(int(status)).decode()
+
+
+def _check(rc: int, name: str):
+    if rc != 0:
+        raise DsixError(f"{name}: {ix_status_string(rc)} ({rc})")
+
+
+def ix_device_status() -> int:
+    """Synchronously read and clear the device status word (IX_DEV_* bits)."""
+    v = ctypes.c_int(0)
+    rc = load().ix_device_status(ctypes.byref(v))
+    if rc not in (0, -7):
+        _check(rc, "ix_device_status")
+    return int(v.value)
+
+
+def _dev(t: torch.Tensor, name: str, dtypes) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise DsixError(f"{name}: must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise DsixError(f"{name}: must be contiguous")
+    return t.data_ptr()
+
+
+def _opt(t, name, dtypes):
+    return None if t is None else _dev(t, name, dtypes)
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+_U8 = (torch.uint8, torch.float8_e4m3fn)
+_BF16 = (torch.bfloat16,)
+_F32 = (torch.float32,)
+_I32T = (torch.int32,)
+_I64T = (torch.int64,)
+
+
+def ix_quant_write_k(k_bf16: torch.Tensor, slot_mapping: torch.Tensor, cache: torch.Tensor,
+                     block_size: int = BLOCK_SIZE, stream=None) -> None:
+    """k_bf16 [n, 128] bf16; slot_mapping [n] int64; cache uint8 [num_blocks, 8448]."""
+    n, d = k_bf16.shape
+    rc = load().ix_quant_write_k(_dev(k_bf16, "k_bf16", _BF16), n, d,
+                                 _dev(slot_mapping, "slot_mapping", _I64T),
+                                 _dev(cache, "cache", (torch.uint8,)), cache.shape[0], block_size,
+                                 _stream(stream))
+    _check(rc, "ix_quant_write_k")
+
+
+def ix_gather_k(cache: torch.Tensor, block_table: torch.Tensor, cu_seq_lens: torch.Tensor,
+                out_k: torch.Tensor, out_scale: torch.Tensor, block_size: int = BLOCK_SIZE,
+                head_dim: int = HEAD_DIM, stream=None) -> None:
+    """block_table [B, stride] int32; cu_seq_lens [B+1] int32; out_k [cap, 128] fp8/u8;
+    out_scale [cap] f32."""
+    rc = load().ix_gather_k(_dev(cache, "cache", (torch.uint8,)), cache.shape[0], block_size,
+                            head_dim, _dev(block_table, "block_table", _I32T), block_table.stride(0),
+                            _dev(cu_seq_lens, "cu_seq_lens", _I32T), cu_seq_lens.numel() - 1,
+                            _dev(out_k, "out_k", _U8), _dev(out_scale, "out_scale", _F32),
+                            out_k.shape[0], _stream(stream))
+    _check(rc, "ix_gather_k")
+
+
+def ix_paged_mqa_logits(q_fp8: torch.Tensor, w: torch.Tensor, cache: torch.Tensor,
+                        context_lens: torch.Tensor, block_table: torch.Tensor,
+                        logits: torch.Tensor, clean_logits: bool = False,
+                        block_size: int = BLOCK_SIZE, stream=None) -> None:
+    """q_fp8 [B, next_n, 64, 128] e4m3 (or its uint8 bits); w [B*next_n, 64] f32;
+    logits [B*next_n, ld] f32 (written in place)."""
+    B, next_n, H, D = q_fp8.shape
+    rc = load().ix_paged_mqa_logits(
+        _dev(q_fp8, "q_fp8", _U8), _dev(w, "w", _F32), _dev(cache, "cache", (torch.uint8,)),
+        cache.shape[0], block_size, _dev(context_lens, "context_lens", _I32T),
+        _dev(block_table, "block_table", _I32T), block_table.stride(0), B, next_n, H, D,
+        _dev(logits, "logits", _F32), logits.shape[1], int(bool(clean_logits)), _stream(stream))
+    _check(rc, "ix_paged_mqa_logits")
+
+
+def ix_mqa_logits(q_fp8: torch.Tensor, w: torch.Tensor, k_fp8: torch.Tensor,
+                  k_scale: torch.Tensor, ks: torch.Tensor, ke: torch.Tensor,
+                  logits: torch.Tensor, clean_logits: bool = False, stream=None) -> None:
+    """q_fp8 [Tq, 64, 128]; w [Tq, 64]; k_fp8 [Tk, 128]; k_scale [Tk]; ks/ke [Tq] int32;
+    logits [Tq, ld] f32."""
+    tq, H, D = q_fp8.shape
+    rc = load().ix_mqa_logits(
+        _dev(q_fp8, "q_fp8", _U8), _dev(w, "w", _F32), _dev(k_fp8, "k_fp8", _U8),
+        _dev(k_scale, "k_scale", _F32), _dev(ks, "ks", _I32T), _dev(ke, "ke", _I32T), tq,
+        k_fp8.shape[0], H, D, _dev(logits, "logits", _F32), logits.shape[1],
+        int(bool(clean_logits)), _stream(stream))
+    _check(rc, "ix_mqa_logits")
+
+
+def ix_topk_to_global(logits: torch.Tensor, row_len: torch.Tensor, row_req: torch.Tensor,
+                      block_table: torch.Tensor, k: int, out_global: torch.Tensor,
+                      out_local: Optional[torch.Tensor] = None, block_size: int = BLOCK_SIZE,
+                      stream=None) -> None:
+    """logits [R, ld] f32; row_len/row_req [R] int32; out_global/out_local [R, k] int32."""
+    R, ld = logits.shape
+    rc = load().ix_topk_to_global(
+        _dev(logits, "logits", _F32), ld, R, _dev(row_len, "row_len", _I32T),
+        _dev(row_req, "row_req", _I32T), _dev(block_table, "block_table", _I32T),
+        block_table.stride(0), block_size, int(k), _opt(out_local, "out_local", _I32T),
+        _dev(out_global, "out_global", _I32T), _stream(stream))
+    _check(rc, "ix_topk_to_global")
+
+
+def dsmla_quant_write(nope_bf16: torch.Tensor, rope_bf16: torch.Tensor,
+                      slot_mapping: torch.Tensor, cache: torch.Tensor, stream=None) -> None:
+    """nope [n, 512] bf16; rope [n, 64] bf16; cache uint8 [num_blocks, block_size, 656+]."""
+    nb, bs, entry = cache.shape
+    rc = load().dsmla_quant_write(
+        _dev(nope_bf16, "nope_bf16", _BF16), _dev(rope_bf16, "rope_bf16", _BF16),
+        nope_bf16.shape[0], _dev(slot_mapping, "slot_mapping", _I64T),
+        _dev(cache, "cache", (torch.uint8,)), nb, bs, cache.stride(0), cache.stride(1),
+        _stream(stream))
+    _check(rc, "dsmla_quant_write")

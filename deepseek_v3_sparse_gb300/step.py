@@ -1,0 +1,144 @@
+"""One indexer step on one GPU: the six C-ABI calls chained over device-resident
+buffers.
+
+Order of a step (the new tokens' caches are written before anything reads them):
+  1. ix_quant_write_k     new tokens' indexer K -> paged indexer-K cache
+  2. dsmla_quant_write    new tokens' NoPE/RoPE -> fp8_ds_mla cache
+  3. ix_gather_k          prefill requests' paged K -> contiguous K + scales
+  4. ix_mqa_logits        prefill rows' logits over the gathered K
+  5. ix_paged_mqa_logits  decode rows' logits over the paged cache
+  6. ix_topk_to_global    top-k + remap, once for the decode rows and once for the
+                          prefill rows (they live in logits buffers of different ld)
+
+All buffers are allocated once here (torch, on the device); ``run`` allocates
+nothing and never synchronises, so it can be captured in a CUDA graph.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import (BLOCK_SIZE, DSMLA_ENTRY_BYTES, HEAD_DIM, HEADS, INDEXER_BLOCK_BYTES,
+               dsmla_quant_write, ix_gather_k, ix_mqa_logits, ix_paged_mqa_logits,
+               ix_quant_write_k, ix_topk_to_global)
+
+
+def round_up(x: int, m: int) -> int:
+    return (x + m - 1) // m * m
+
+
+@dataclass
+class DecodePart:
+    context_lens: torch.Tensor   # int32 [B]
+    q: torch.Tensor              # uint8/e4m3 [B, next_n, 64, 128]
+    w: torch.Tensor              # f32 [B*next_n, 64]
+    row_len: torch.Tensor        # int32 [B*next_n]
+    row_req: torch.Tensor        # int32 [B*next_n] (rows of block_table)
+    ld: int                      # logits row stride (>= longest row, multiple of 4)
+
+
+@dataclass
+class PrefillPart:
+    req: list                    # request ids (rows of block_table)
+    cu_seq_lens: torch.Tensor    # int32 [C+1] over the requests' whole contexts
+    ks: torch.Tensor             # int32 [T]
+    ke: torch.Tensor             # int32 [T]
+    row_len: torch.Tensor        # int32 [T]
+    row_req: torch.Tensor        # int32 [T]
+    q: torch.Tensor              # uint8/e4m3 [T, 64, 128]
+    w: torch.Tensor              # f32 [T, 64]
+    gathered: int                # cu_seq_lens[-1] (host copy, sizes the gather buffers)
+    ld: int
+
+
+class IndexerStep:
+    def __init__(self, *, num_blocks: int, block_table: torch.Tensor, topk: int,
+                 new_k: torch.Tensor, new_slot: torch.Tensor,
+                 decode: Optional[DecodePart] = None, prefill: Optional[PrefillPart] = None,
+                 nope: Optional[torch.Tensor] = None, rope: Optional[torch.Tensor] = None,
+                 clean_logits: bool = False, with_local: bool = False):
+        dev = block_table.device
+        self.num_blocks = num_blocks
+        self.block_table = block_table
+        self.topk = topk
+        self.new_k = new_k
+        self.new_slot = new_slot
+        self.decode = decode
+        self.prefill = prefill
+        self.nope = nope
+        self.rope = rope
+        self.clean = clean_logits
+        self.cache = torch.zeros(num_blocks, INDEXER_BLOCK_BYTES, dtype=torch.uint8, device=dev)
+        self.dsmla_cache = None
+        if nope is not None:
+            self.dsmla_cache = torch.zeros(num_blocks, BLOCK_SIZE, DSMLA_ENTRY_BYTES,
+                                           dtype=torch.uint8, device=dev)
+        i32 = dict(dtype=torch.int32, device=dev)
+        if decode is not None:
+            R = decode.w.shape[0]
+            self.dec_logits = torch.empty(R, decode.ld, dtype=torch.float32, device=dev)
+            self.dec_global = torch.empty(R, topk, **i32)
+            self.dec_local = torch.empty(R, topk, **i32) if with_local else None
+        if prefill is not None:
+            T = prefill.w.shape[0]
+            self.k_fp8 = torch.empty(max(prefill.gathered, 1), HEAD_DIM, dtype=torch.uint8,
+                                     device=dev)
+            self.k_scale = torch.empty(max(prefill.gathered, 1), dtype=torch.float32, device=dev)
+            self.pf_bt = block_table[prefill.req]
+            self.pf_logits = torch.empty(T, prefill.ld, dtype=torch.float32, device=dev)
+            self.pf_global = torch.empty(T, topk, **i32)
+            self.pf_local = torch.empty(T, topk, **i32) if with_local else None
+
+    def write_history(self, k_bf16: torch.Tensor, slots: torch.Tensor, chunk: int = 1 << 20):
+        """Fill the indexer-K cache with already-cached positions (set-up, not a step)."""
+        for i in range(0, k_bf16.shape[0], chunk):
+            ix_quant_write_k(k_bf16[i:i + chunk], slots[i:i + chunk], self.cache)
+
+    def kernels_per_step(self) -> int:
+        n = 1 + (self.nope is not None)
+        if self.prefill is not None:
+            n += 3 + (1 if self.clean else 0)
+        if self.decode is not None:
+            n += 2 + (1 if self.clean else 0)
+        return n
+
+    def run(self, stream=None, events=None):
+        """One step.  ``events``: optional dict name -> (start, end) CUDA events
+        recorded around the logits launches on ``stream``."""
+        s = stream
+        ix_quant_write_k(self.new_k, self.new_slot, self.cache, stream=s)
+        if self.nope is not None:
+            dsmla_quant_write(self.nope, self.rope, self.new_slot, self.dsmla_cache, stream=s)
+        if self.prefill is not None:
+            p = self.prefill
+            ix_gather_k(self.cache, self.pf_bt, p.cu_seq_lens, self.k_fp8, self.k_scale, stream=s)
+            if events and "mqa_logits" in events:
+                events["mqa_logits"][0].record(s)
+            ix_mqa_logits(p.q, p.w, self.k_fp8, self.k_scale, p.ks, p.ke, self.pf_logits,
+                          clean_logits=self.clean, stream=s)
+            if events and "mqa_logits" in events:
+                events["mqa_logits"][1].record(s)
+        if self.decode is not None:
+            d = self.decode
+            if events and "paged_mqa_logits" in events:
+                events["paged_mqa_logits"][0].record(s)
+            ix_paged_mqa_logits(d.q, d.w, self.cache, d.context_lens, self.block_table,
+                                self.dec_logits, clean_logits=self.clean, stream=s)
+            if events and "paged_mqa_logits" in events:
+                events["paged_mqa_logits"][1].record(s)
+            if events and "topk_decode" in events:
+                events["topk_decode"][0].record(s)
+            ix_topk_to_global(self.dec_logits, d.row_len, d.row_req, self.block_table, self.topk,
+                              self.dec_global, self.dec_local, stream=s)
+            if events and "topk_decode" in events:
+                events["topk_decode"][1].record(s)
+        if self.prefill is not None:
+            p = self.prefill
+            if events and "topk_prefill" in events:
+                events["topk_prefill"][0].record(s)
+            ix_topk_to_global(self.pf_logits, p.row_len, p.row_req, self.block_table, self.topk,
+                              self.pf_global, self.pf_local, stream=s)
+            if events and "topk_prefill" in events:
+                events["topk_prefill"][1].record(s)

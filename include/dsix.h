@@ -44,6 +44,13 @@
 extern "C" {
 #endif
 
+/* Exported from the shared library; every other symbol stays hidden. */
+#if defined(__GNUC__)
+#define IX_API __attribute__((visibility("default")))
+#else
+#define IX_API
+#endif
+
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st* ix_stream_t;
 
@@ -68,7 +75,7 @@ enum {
 };
 
 /* Human-readable name of a status code (static string, never NULL). */
-const char* ix_status_string(int status);
+IX_API const char* ix_status_string(int status);
 
 /*
  * Reads and clears the calling device's status word.  SYNCHRONOUS: it waits
@@ -77,7 +84,7 @@ const char* ix_status_string(int status);
  * IX_DEV_* bits; returns IX_OK if no bit was set, IX_ERR_DEVICE_CHECK if one
  * was, IX_ERR_CUDA on a runtime error.
  */
-int ix_device_status(int* status_out);
+IX_API int ix_device_status(int* status_out);
 
 /*
  * ix_quant_write_k -- quantise new indexer keys and write them into the paged
@@ -93,7 +100,7 @@ int ix_device_status(int* status_out);
  *   slot_mapping  int64 [n]
  *   cache         uint8 [num_blocks, block_size*(head_dim+4)], 16-byte aligned
  */
-int ix_quant_write_k(const void* k_bf16, int64_t n, int head_dim,
+IX_API int ix_quant_write_k(const void* k_bf16, int64_t n, int head_dim,
                      const int64_t* slot_mapping, uint8_t* cache,
                      int64_t num_blocks, int block_size, ix_stream_t stream);
 
@@ -112,7 +119,7 @@ int ix_quant_write_k(const void* k_bf16, int64_t n, int head_dim,
  *   out_capacity  host-side upper bound on cu_seq_lens[batch]; rows at or past
  *                 it are never written (IX_DEV_BAD_RANGE if that drops any)
  */
-int ix_gather_k(const uint8_t* cache, int64_t num_blocks, int block_size, int head_dim,
+IX_API int ix_gather_k(const uint8_t* cache, int64_t num_blocks, int block_size, int head_dim,
                 const int32_t* block_table, int64_t bt_stride,
                 const int32_t* cu_seq_lens, int batch, uint8_t* out_k,
                 float* out_scale, int64_t out_capacity, ix_stream_t stream);
@@ -133,7 +140,7 @@ int ix_gather_k(const uint8_t* cache, int64_t num_blocks, int block_size, int he
  *   block_table   int32 [batch, bt_stride]
  *   logits        fp32 [batch*next_n, ld]; ld >= every L, ld % 4 == 0
  */
-int ix_paged_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t* cache,
+IX_API int ix_paged_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t* cache,
                         int64_t num_blocks, int block_size,
                         const int32_t* context_lens, const int32_t* block_table,
                         int64_t bt_stride, int batch, int next_n, int heads,
@@ -154,7 +161,7 @@ int ix_paged_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t* cac
  *   ks, ke   int32 [tq], 0 <= ks <= ke <= tk
  *   logits   fp32 [tq, ld]; ld >= every ke - ks, ld % 4 == 0
  */
-int ix_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t* k_fp8,
+IX_API int ix_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t* k_fp8,
                   const float* k_scale, const int32_t* ks, const int32_t* ke,
                   int64_t tq, int64_t tk, int heads, int head_dim, float* logits,
                   int64_t ld, int clean_logits, ix_stream_t stream);
@@ -180,7 +187,7 @@ int ix_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t* k_fp8,
  *   out_global  int32 [rows, k]
  * Supports ld <= 262144 (longer rows return IX_ERR_UNSUPPORTED) and k >= 1.
  */
-int ix_topk_to_global(const float* logits, int64_t ld, int64_t rows,
+IX_API int ix_topk_to_global(const float* logits, int64_t ld, int64_t rows,
                       const int32_t* row_len, const int32_t* row_req,
                       const int32_t* block_table, int64_t bt_stride, int block_size,
                       int k, int32_t* out_local, int32_t* out_global,
@@ -202,7 +209,7 @@ int ix_topk_to_global(const float* logits, int64_t ld, int64_t rows,
  *   cache      uint8, 16-byte aligned; block_stride_bytes and entry_stride_bytes
  *              multiples of 16, entry_stride_bytes >= 656
  */
-int dsmla_quant_write(const void* nope_bf16, const void* rope_bf16, int64_t n,
+IX_API int dsmla_quant_write(const void* nope_bf16, const void* rope_bf16, int64_t n,
                       const int64_t* slot_mapping, uint8_t* cache, int64_t num_blocks,
                       int block_size, int64_t block_stride_bytes,
                       int64_t entry_stride_bytes, ix_stream_t stream);

@@ -1,0 +1,136 @@
+"""The C ABI library (CPU only: no kernel is launched).
+
+* libdsix.so builds for sm_103a and loads;
+* it exports exactly the functions include/dsix.h declares;
+* every host-side argument check returns its status code before anything
+  touches the GPU.
+"""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsix.h")
+
+IX_OK, IX_ERR_NULL, IX_ERR_SHAPE, IX_ERR_UNSUPPORTED, IX_ERR_ALIGN = 0, -1, -2, -3, -4
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and
+                                not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="nvcc not available")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from deepseek_v3_sparse_gb300 import build
+    import deepseek_v3_sparse_gb300 as dsix
+    build.build()
+    return dsix.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"IX_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)))
+
+
+def test_exports_match_header(lib):
+    names = _declared()
+    assert len(names) == 8
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True,
+                         text=True, check=True).stdout
+    exported = sorted(l.split()[-1] for l in out.splitlines()
+                      if l.split()[-2:-1] == ["T"] and not l.split()[-1].startswith("_"))
+    assert exported == names
+
+
+def test_status_strings(lib):
+    import deepseek_v3_sparse_gb300 as dsix
+    for code in range(0, -8, -1):
+        s = dsix.ix_status_string(code)
+        assert s and "unknown" not in s
+    assert "unknown" in dsix.ix_status_string(-99)
+
+
+P = ctypes.c_void_p
+A16 = P(0x10000)      # aligned fake device address (never dereferenced by the checks)
+A1 = P(0x10001)       # misaligned
+
+
+def test_quant_write_k_host_checks(lib):
+    f = lib.ix_quant_write_k
+    assert f(A16, 4, 64, A16, A16, 8, 64, None) == IX_ERR_UNSUPPORTED
+    assert f(A16, 4, 128, A16, A16, 8, 32, None) == IX_ERR_UNSUPPORTED
+    assert f(A16, -1, 128, A16, A16, 8, 64, None) == IX_ERR_SHAPE
+    assert f(None, 4, 128, A16, A16, 8, 64, None) == IX_ERR_NULL
+    assert f(A1, 4, 128, A16, A16, 8, 64, None) == IX_ERR_ALIGN
+    assert f(None, 0, 128, None, None, 8, 64, None) == IX_OK   # empty: nothing to do
+
+
+def test_gather_host_checks(lib):
+    f = lib.ix_gather_k
+    assert f(A16, 8, 64, 64, A16, 4, A16, 2, A16, A16, 100, None) == IX_ERR_UNSUPPORTED
+    assert f(A16, 8, 64, 128, A16, 4, A16, -1, A16, A16, 100, None) == IX_ERR_SHAPE
+    assert f(A16, 8, 64, 128, None, 4, A16, 2, A16, A16, 100, None) == IX_ERR_NULL
+    assert f(A16, 8, 64, 128, A16, 4, A16, 2, A1, A16, 100, None) == IX_ERR_ALIGN
+    assert f(A16, 8, 64, 128, A16, 4, A16, 0, A16, A16, 100, None) == IX_OK
+
+
+def test_paged_logits_host_checks(lib):
+    f = lib.ix_paged_mqa_logits
+    args = lambda **kw: [kw.get("q", A16), A16, A16, kw.get("nb", 8), kw.get("bs", 64), A16, A16,
+                         4, kw.get("batch", 2), kw.get("next_n", 1), kw.get("heads", 64),
+                         kw.get("dim", 128), kw.get("logits", A16), kw.get("ld", 64), 0, None]
+    assert f(*args(heads=32)) == IX_ERR_UNSUPPORTED
+    assert f(*args(next_n=3)) == IX_ERR_UNSUPPORTED
+    assert f(*args(bs=16)) == IX_ERR_UNSUPPORTED
+    assert f(*args(ld=66)) == IX_ERR_UNSUPPORTED
+    assert f(*args(batch=-1)) == IX_ERR_SHAPE
+    assert f(*args(nb=0)) == IX_ERR_SHAPE
+    assert f(*args(q=None)) == IX_ERR_NULL
+    assert f(*args(logits=A1)) == IX_ERR_ALIGN
+    assert f(*args(batch=0)) == IX_OK
+
+
+def test_mqa_logits_host_checks(lib):
+    f = lib.ix_mqa_logits
+    args = lambda **kw: [kw.get("q", A16), A16, kw.get("k", A16), A16, A16, A16, kw.get("tq", 16),
+                         kw.get("tk", 16), kw.get("heads", 64), 128, A16, kw.get("ld", 16), 0, None]
+    assert f(*args(heads=16)) == IX_ERR_UNSUPPORTED
+    assert f(*args(ld=18)) == IX_ERR_UNSUPPORTED
+    assert f(*args(tq=-2)) == IX_ERR_SHAPE
+    assert f(*args(k=None)) == IX_ERR_NULL
+    assert f(*args(q=A1)) == IX_ERR_ALIGN
+    assert f(*args(tq=0)) == IX_OK
+
+
+def test_topk_host_checks(lib):
+    f = lib.ix_topk_to_global
+    args = lambda **kw: [kw.get("lg", A16), kw.get("ld", 64), kw.get("rows", 4), A16, A16, A16, 8,
+                         64, kw.get("k", 16), None, kw.get("out", A16), None]
+    assert f(*args(k=0)) == IX_ERR_UNSUPPORTED
+    assert f(*args(ld=62)) == IX_ERR_UNSUPPORTED
+    assert f(*args(ld=8 * 32768 + 4)) == IX_ERR_UNSUPPORTED
+    assert f(*args(rows=-1)) == IX_ERR_SHAPE
+    assert f(*args(out=None)) == IX_ERR_NULL
+    assert f(*args(lg=A1)) == IX_ERR_ALIGN
+    assert f(*args(rows=0)) == IX_OK
+
+
+def test_dsmla_host_checks(lib):
+    f = lib.dsmla_quant_write
+    assert f(A16, A16, 4, A16, A16, 8, 64, 64 * 656, 600, None) == IX_ERR_SHAPE
+    assert f(A16, A16, 4, A16, A16, 8, 64, 64 * 656, 660, None) == IX_ERR_ALIGN
+    assert f(A16, A16, 4, A16, A1, 8, 64, 64 * 656, 656, None) == IX_ERR_ALIGN
+    assert f(None, A16, 4, A16, A16, 8, 64, 64 * 656, 656, None) == IX_ERR_NULL
+    assert f(None, None, 0, None, None, 8, 64, 64 * 656, 656, None) == IX_OK
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import deepseek_v3_sparse_gb300 as dsix
+    with pytest.raises(dsix.DsixError):
+        dsix.load(str(tmp_path / "missing.so"))
