@@ -212,18 +212,21 @@ template <bool P>
 struct Cursor {
     int g, t, ntiles, left;
     __device__ __forceinline__ int tiles_of(const LogitsArgs& a, const int* s_tiles, int gg) const {
+        if (gg >= a.num_groups) return 0;
         return gg < kSmemGroups ? s_tiles[gg] : group_tiles<P>(a, gg, false);
     }
-    // Returns true when the next unit starts a new group.
+    // Returns true when the next unit starts a new group.  Never walks past
+    // the last group: if the unit count and the groups disagree, it stops.
     __device__ __forceinline__ bool advance(const LogitsArgs& a, const int* s_tiles) {
         ++t;
         --left;
-        if (left > 0 && t == ntiles) {
+        if (left > 0 && t >= ntiles) {
             do {
                 ++g;
                 ntiles = tiles_of(a, s_tiles, g);
-            } while (ntiles == 0);
+            } while (ntiles == 0 && g < a.num_groups);
             t = 0;
+            if (g >= a.num_groups) left = 0;
             return true;
         }
         return false;

@@ -1,0 +1,103 @@
+"""GPU parity: top-k + remap.
+
+* On the oracle's own f32 logits the GPU result must match the oracle exactly
+  (local and global indices, ties to the lower index, -0.0 == +0.0, padding).
+* Row lengths cover every cluster split (1/2/4/8 CTAs per row), short rows,
+  L = k, L = k + 1, L = 0, and 131072-key rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests._helpers import require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dsix():
+    require_gpu()
+    import __graft_entry__
+    __graft_entry__.build()
+    import deepseek_v3_sparse_gb300 as m
+    m.ix_device_status()
+    return m
+
+
+def _run(dsix, logits, row_len, row_req, bt, k, bs=64):
+    R, ld = logits.shape
+    dl = torch.from_numpy(logits).cuda()
+    loc = torch.full((R, k), -5, dtype=torch.int32, device="cuda")
+    glb = torch.full((R, k), -5, dtype=torch.int32, device="cuda")
+    dsix.ix_topk_to_global(dl, torch.from_numpy(row_len).cuda(), torch.from_numpy(row_req).cuda(),
+                           torch.from_numpy(bt).cuda(), k, glb, loc, block_size=bs)
+    return loc.cpu().numpy(), glb.cpu().numpy()
+
+
+def _table(R, ld, bs, seed):
+    nblk = -(-ld // bs)
+    return np.random.default_rng(seed).permutation(R * nblk).reshape(R, nblk).astype(np.int32)
+
+
+def _exact(dsix, logits, row_len, k, bs=64, seed=0):
+    R, ld = logits.shape
+    bt = _table(R, ld, bs, seed)
+    row_req = np.arange(R, dtype=np.int32)[::-1].copy()
+    loc, glb = _run(dsix, logits, row_len, row_req, bt, k, bs)
+    rl, rg = oracle.topk_to_global(logits, row_len, row_req, bt, bs, k)
+    bad = np.nonzero((loc != rl).any(axis=1) | (glb != rg).any(axis=1))[0]
+    assert bad.size == 0, f"rows {bad[:5]} differ"
+
+
+@pytest.mark.parametrize("ld,R", [(64, 5), (4096, 40), (8192, 300), (20000, 8), (131072, 4)])
+def test_exact_on_oracle_like_logits(dsix, ld, R):
+    rng = np.random.default_rng(ld)
+    logits = (rng.standard_normal((R, ld)) * 3).astype(np.float32)
+    logits[:, ::5] = np.round(logits[:, ::5] * 4) / 4   # many exact ties
+    logits[0, :ld // 2] = 0.0
+    logits[0, 1::3] = -0.0
+    k = 2048 if ld > 64 else 16
+    row_len = rng.integers(0, ld + 1, R).astype(np.int32)
+    row_len[0] = ld
+    row_len[1 % R] = min(k, ld)
+    if R > 2:
+        row_len[2] = min(k + 1, ld)
+    if R > 3:
+        row_len[3] = 0
+    _exact(dsix, logits, row_len, k)
+
+
+@pytest.mark.parametrize("k", [1, 7, 64, 2048, 5000])
+def test_exact_various_k(dsix, k):
+    rng = np.random.default_rng(k)
+    R, ld = 12, 12000
+    logits = rng.integers(-50, 50, size=(R, ld)).astype(np.float32)  # heavy ties
+    row_len = rng.integers(k, ld + 1, R).astype(np.int32)
+    _exact(dsix, logits, row_len, k, seed=k)
+
+
+def test_exact_all_equal_and_extremes(dsix):
+    R, ld, k = 4, 9000, 2048
+    logits = np.zeros((R, ld), np.float32)
+    logits[1] = -np.inf
+    logits[2] = np.finfo(np.float32).max
+    logits[2, ::2] = -np.finfo(np.float32).max
+    logits[3] = np.linspace(-1, 1, ld, dtype=np.float32)[::-1]
+    _exact(dsix, logits, np.full(R, ld, np.int32), k)
+
+
+def test_never_reads_past_row_len(dsix):
+    # NaNs after L must not influence the result
+    R, ld, k = 3, 8192, 100
+    rng = np.random.default_rng(1)
+    logits = rng.standard_normal((R, ld)).astype(np.float32)
+    row_len = np.array([5000, 150, 8000], np.int32)
+    clean = logits.copy()
+    for r in range(R):
+        logits[r, row_len[r]:] = np.nan
+    bt = _table(R, ld, 64, 2)
+    rq = np.arange(R, dtype=np.int32)
+    loc, glb = _run(dsix, logits, row_len, rq, bt, k)
+    rl, rg = oracle.topk_to_global(clean, row_len, rq, bt, 64, k)
+    assert np.array_equal(loc, rl) and np.array_equal(glb, rg)
