@@ -47,7 +47,8 @@ constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kFirstEpiWarp = 2;
 constexpr int kScaleRing = 16;   // key-scale ring entries (one per tile in flight)
-constexpr int kScaleBox = 132;   // floats per entry (128 + 4 for an aligned start)
+constexpr int kScaleBox = 132;   // floats loaded per entry (128 + 4 for an aligned start)
+constexpr int kScaleStride = 160;  // floats between entries: TMA destinations need 128-byte alignment
 constexpr int kSmemGroups = 2048;
 constexpr int kTmemCols = 512;
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 100 ms
@@ -84,7 +85,7 @@ struct Smem {
     static constexpr int kQ = 0;                                     // 2 Q buffers
     static constexpr int kK = kQ + 2 * C::kQBytes;                   // K stages
     static constexpr int kSc = kK + C::kStages * kTileBytes;         // key-scale ring
-    static constexpr int kW = kSc + kScaleRing * kScaleBox * 4;      // 2 head-weight buffers
+    static constexpr int kW = kSc + kScaleRing * kScaleStride * 4;   // 2 head-weight buffers
     static constexpr int kTiles = kW + 2 * C::kWFloats * 4;          // tiles per group
     static constexpr int kBar = kTiles + kSmemGroups * 4;
     static constexpr int kNumBars = 2 * C::kStages + 4 + 2 * C::kSlots + 2 * kScaleRing + 1;
@@ -93,7 +94,8 @@ struct Smem {
     static constexpr int kTotal = kScan + 64 * 4;
     static constexpr int kAlloc = kTotal + 1024;  // slack for 1024-byte alignment
     static_assert(kAlloc <= 232448, "shared memory budget");
-    static_assert(kSc % 16 == 0 && kW % 16 == 0 && kBar % 8 == 0, "alignment");
+    static_assert(kSc % 128 == 0 && (kScaleStride * 4) % 128 == 0, "TMA destinations: 128 B");
+    static_assert(kW % 16 == 0 && kBar % 8 == 0, "alignment");
 };
 
 struct LogitsArgs {
@@ -384,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_warp(empty + stage, ((it / C::kStages) & 1) ^ 1, abort_flag, a.status)) break;
                 if (!wait_warp(sc_empty + sci, ((it / kScaleRing) & 1) ^ 1, abort_flag, a.status)) break;
                 uint8_t* kdst = sK + stage * kTileBytes;
-                float* sdst = sSc + sci * kScaleBox;
+                float* sdst = sSc + sci * kScaleStride;
                 if constexpr (P) {
                     if (bt_base < 0 || cur.t - bt_base >= 16) {
                         bt_base = cur.t;
@@ -528,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const int s = kbeg + cur.t * kTile + m;  // key index
-                    const float ksc = sSc[sci * kScaleBox + (P ? 0 : (s - m) & 3) + m];
+                    const float ksc = sSc[sci * kScaleStride + (P ? 0 : (s - m) & 3) + m];
                     const uint32_t tbase = lane_addr + slot * C::kSlotCols;
                     const int nrows = P ? a.next_n : 4;
                     for (int i = 0; i < nrows; ++i) {

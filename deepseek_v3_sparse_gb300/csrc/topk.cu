@@ -264,7 +264,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const bool keep = fg[j] || (fe[j] && be < k_rem);
-                if (keep) emit(a, r, b, bg + min(be, k_rem), lo + i0 + j);
+                const int pos = bg + min(be, k_rem);
+                if (keep && pos < a.k) emit(a, r, b, pos, lo + i0 + j);
                 bg += fg[j];
                 be += fe[j];
             }

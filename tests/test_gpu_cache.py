@@ -155,9 +155,10 @@ def test_dsmla_bit_exact(dsix, n, entry, extra):
         b, o = divmod(int(slots[t]), bs)
         ref[b * block_bytes + o * entry:b * block_bytes + o * entry + 656] = dense[b, o]
     import deepseek_v3_sparse_gb300 as m
-    rc = m.load().dsmla_quant_write(nope.cuda().data_ptr(), rope.cuda().data_ptr(), n,
-                                    torch.from_numpy(slots).cuda().data_ptr(), base.data_ptr(),
-                                    nb, bs, block_bytes, entry, None)
+    d_nope, d_rope, d_slots = nope.cuda(), rope.cuda(), torch.from_numpy(slots).cuda()
+    rc = m.load().dsmla_quant_write(d_nope.data_ptr(), d_rope.data_ptr(), n, d_slots.data_ptr(),
+                                    base.data_ptr(), nb, bs, block_bytes, entry,
+                                    torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert rc == 0
     got = base.cpu().numpy()

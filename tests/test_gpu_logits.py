@@ -25,6 +25,7 @@ def dsix():
 
 def _decode_gpu(dsix, wl, clean, ld=None, sentinel=123.0):
     step = make_step(wl, "cuda", clean=clean)
+    dsix.ix_quant_write_k(step.new_k, step.new_slot, step.cache)  # the step's new tokens
     d = step.decode
     ld = ld or d.ld
     logits = torch.full((d.w.shape[0], ld), sentinel, dtype=torch.float32, device="cuda")
