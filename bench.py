@@ -1,0 +1,416 @@
+"""Benchmark of the DeepSeek-V3.2 sparse-attention indexer hot path on GB300.
+
+One step = the whole hot path over one batch of the long-context mixed
+workload (16 decode requests at context 131072 + 4 prefill chunks of 2048
+query tokens on 8192-token contexts; top_k 2048):
+  indexer-K quant-write and fp8_ds_mla write of the 8208 new tokens, paged
+  gather of the prefill contexts, prefill FP8 logits (tcgen05), decode FP8
+  logits over the paged cache (tcgen05), top-k + remap of all 8208 rows.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+value = query tokens (decode + prefill rows) per second over all ranks.
+Multi-GPU runs are independent replicas (one process per GPU, no collective on
+the data path; barrier + max-over-ranks timing only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "indexer decode query-tokens/s and prefill TFLOP/s; HBM GB/s & FP8 roofline fraction"
+UNIT = "query-tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DECODE_BYTES_PER_KEY = 132        # 128 fp8 values + one fp32 scale
+PREFILL_FLOP_PER_PAIR = 2 * 64 * 128
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = str(device_index)
+        try:  # nvidia-smi numbering can differ from CUDA's; the UUID cannot
+            u = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.dev = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            pass
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def workload_config(wl):
+    return {"workload": wl.name, "decode_requests": wl.n_decode,
+            "decode_context": int(wl.context_lens.max()) if wl.n_decode else 0,
+            "next_n": wl.next_n, "prefill_chunks": len(wl.prefill_req),
+            "prefill_chunk_len": wl.chunk_len[0] if wl.chunk_len else 0,
+            "prefill_context": int(wl.req_ctx[wl.prefill_req[0]]) if wl.prefill_req else 0,
+            "top_k": wl.topk, "block_size": wl.block_size, "heads": wl.heads,
+            "head_dim": wl.head_dim, "new_tokens": int(wl.is_new.sum()),
+            "l2": "no flush: inputs larger than L2 (about 0.6 GB touched per step)"}
+
+
+def algorithmic(wl):
+    dec_keys = int(wl.decode_rows()[0].astype(np.int64).sum()) if wl.n_decode else 0
+    if wl.n_decode and wl.next_n > 1:  # keys are read once per request
+        dec_keys = int(wl.context_lens.astype(np.int64).sum())
+    pairs = int(wl.prefill_rows()[2].astype(np.int64).sum()) if wl.prefill_req else 0
+    return dec_keys, pairs
+
+
+def gpu_arm(args, world, rank, local):
+    import deepseek_v3_sparse_gb300 as dsix
+    from deepseek_v3_sparse_gb300 import build as libbuild
+    import workloads as W
+    from workloads.device import make_step
+
+    libbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = W.mixed_long(seed=rank)
+    step = make_step(wl, dev)
+    stream = torch.cuda.current_stream(dev)
+    names = ["mqa_logits", "paged_mqa_logits", "topk_decode", "topk_prefill"]
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    if dsix.ix_device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)] for n in names}
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for i in range(args.steps):
+            step.run(events={n: ev[n][i] for n in names})
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    elapsed_ms = t0.elapsed_time(t1)
+    kern_ms = {n: float(np.mean([a.elapsed_time(b) for a, b in ev[n]])) for n in names}
+    clk = clocks.summary()
+    status = dsix.ix_device_status()
+
+    # ---- end to end through the public API: pinned host inputs in, indices out
+    e2e_steps = min(args.steps, 50)
+    host_in = {
+        "new_k": (wl.new_k.pin_memory(), step.new_k),
+        "new_slot": (torch.from_numpy(wl.new_slot.copy()).pin_memory(), step.new_slot),
+        "q_dec": (wl.q_decode.pin_memory(), step.decode.q),
+        "w_dec": (wl.w_decode.pin_memory(), step.decode.w),
+        "ctx": (torch.from_numpy(wl.context_lens.copy()).pin_memory(), step.decode.context_lens),
+        "q_pf": (wl.q_prefill.pin_memory(), step.prefill.q),
+        "w_pf": (wl.w_prefill.pin_memory(), step.prefill.w),
+        "nope": (wl.nope_bf16.pin_memory(), step.nope),
+        "rope": (wl.rope_bf16.pin_memory(), step.rope),
+        "bt": (torch.from_numpy(wl.block_table.copy()).pin_memory(), step.block_table),
+    }
+    host_out = [(step.dec_global, torch.empty(step.dec_global.shape, dtype=torch.int32).pin_memory()),
+                (step.pf_global, torch.empty(step.pf_global.shape, dtype=torch.int32).pin_memory())]
+    h2d = sum(h.numel() * h.element_size() for h, _ in host_in.values())
+    d2h = sum(h.numel() * h.element_size() for _, h in host_out)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for h, d in host_in.values():
+            d.copy_(h, non_blocking=True)
+        step.run()
+        for d, h in host_out:
+            h.copy_(d, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall_e2e = time.perf_counter() - w0
+    barrier(world)
+    e2e_ms = max(e0.elapsed_time(e1), wall_e2e * 1e3)
+
+    dec_keys, pairs = algorithmic(wl)
+    rows = int(wl.n_decode * wl.next_n + wl.n_prefill_rows)
+    return dict(wl=wl, step=step, elapsed_ms=elapsed_ms, kern_ms=kern_ms, clocks=clk,
+                status=status, e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h,
+                dec_keys=dec_keys, pairs=pairs, rows=rows)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg / reference arm)
+# ---------------------------------------------------------------------------
+class OracleSampler:
+    """The oracle timed on bounded samples of the workload.  Set-up (the cache
+    of already-cached positions) is done once; each sample times a slice of a
+    decode row and whole prefill rows (logits + top-k), rotating over rows;
+    per-key / per-pair costs extrapolate to one whole step."""
+
+    def __init__(self, wl):
+        import oracle
+        import workloads as W
+        self.W, self.o, self.wl = W, oracle, wl
+        oracle.build()
+        self.cache = np.zeros((wl.num_blocks, 64 * 132), np.uint8)
+        hist = ~wl.is_new
+        oracle.quant_write_k(W.bf16_bits(wl.k_bf16[torch.from_numpy(hist)]), wl.slot[hist],
+                             self.cache, 64)
+        t = time.perf_counter()  # whole-step cache writes and gather, timed once
+        oracle.quant_write_k(W.bf16_bits(wl.new_k), wl.new_slot, self.cache, 64)
+        dcache = np.zeros((wl.num_blocks, 64, 656), np.uint8)
+        oracle.dsmla_quant_write(W.bf16_bits(wl.nope_bf16), W.bf16_bits(wl.rope_bf16),
+                                 wl.new_slot, dcache, 64)
+        cu = wl.prefill_gather()
+        self.kf = np.zeros((int(cu[-1]), 128), np.uint8)
+        self.ksc = np.zeros(int(cu[-1]), np.float32)
+        oracle.gather_k(self.cache, 64, 128, wl.prefill_block_table(), cu, self.kf, self.ksc)
+        self.t_fixed = time.perf_counter() - t
+        del dcache
+        self.ks, self.ke, self.rl, self.rq = wl.prefill_rows()
+        self.full_keys = int(wl.context_lens.astype(np.int64).sum())
+        self.full_pairs = int(self.rl.astype(np.int64).sum())
+        self.keys = self.pairs = 0
+        self.t_keys = self.t_pairs = 0.0
+        self.n = 0
+
+    def sample(self, dec_keys: int = 2048, pf_rows: int = 0):
+        wl, o, W = self.wl, self.o, self.W
+        pf_rows = pf_rows or o.num_threads()  # one row per thread: rows run in parallel
+        ctx = wl.context_lens.copy()
+        ctx[0] = dec_keys
+        t = time.perf_counter()
+        lg = o.paged_mqa_logits(W.u8(wl.q_decode), wl.w_decode.numpy(), self.cache, 64, ctx,
+                                wl.block_table, ld=dec_keys, clean=False, rows=[0])
+        o.topk_to_global(lg, np.array([dec_keys], np.int32), np.zeros(1, np.int32),
+                         wl.block_table, 64, wl.topk)
+        self.t_keys += time.perf_counter() - t
+        self.keys += dec_keys
+        T = len(self.ks)
+        rows = np.array([(int((self.n + j) * 0.6180339887 * T)) % T for j in range(pf_rows)],
+                        dtype=np.int64)
+        self.n += pf_rows
+        t = time.perf_counter()
+        plg = o.mqa_logits(W.u8(wl.q_prefill), wl.w_prefill.numpy(), self.kf, self.ksc, self.ks,
+                           self.ke, ld=int(self.rl[rows].max()), clean=False, rows=rows)
+        o.topk_to_global(plg, self.rl[rows], self.rq[rows], wl.block_table, 64, wl.topk)
+        self.t_pairs += time.perf_counter() - t
+        self.pairs += int(self.rl[rows].astype(np.int64).sum())
+
+    def step_seconds(self) -> float:
+        return (self.t_fixed + self.t_keys / self.keys * self.full_keys
+                + self.t_pairs / self.pairs * self.full_pairs)
+
+    def describe(self) -> str:
+        return (f"oracle on the host cores: new-token cache writes, fp8_ds_mla write and gather "
+                f"timed whole; decode logits+top-k over {self.keys} keys and prefill logits+top-k "
+                f"over {self.n} rows ({self.pairs} pairs) spread over the chunks, extrapolated "
+                f"per key / per pair to one step ({self.full_keys} decode keys, "
+                f"{self.full_pairs} prefill pairs)")
+
+
+def reference_arm(args, world, rank):
+    import oracle
+    import workloads as W
+    if rank != 0:
+        return
+    wl = W.mixed_long(seed=0)
+    rows = int(wl.n_decode * wl.next_n + wl.n_prefill_rows)
+    s = OracleSampler(wl)
+    for _ in range(args.warmup):
+        s.sample()
+    s.keys = s.pairs = 0
+    s.t_keys = s.t_pairs = 0.0
+    w0 = time.perf_counter()
+    for _ in range(args.steps):
+        s.sample()
+    wall = time.perf_counter() - w0
+    est = s.step_seconds()
+    value = rows / est
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": est * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 (exact fp8 products, double head sum)",
+            "data": "synthetic (seeded; no dataset, no weights)",
+            "config": workload_config(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": s.describe()},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "wall_s": wall}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="dsix", choices=["dsix", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        reference_arm(args, world, rank)
+        return
+    r = gpu_arm(args, world, rank, local)
+    elapsed = max_over_ranks(r["elapsed_ms"], world)
+    e2e_ms = max_over_ranks(r["e2e_ms"], world)
+    if rank != 0:
+        return
+    wl, step = r["wl"], r["step"]
+    pk, pk_kind = peaks()
+    fp8_peak = 2.0 * pk["bf16_tflops"]
+    value = world * r["rows"] * args.steps / (elapsed / 1e3)
+    km = r["kern_ms"]
+    pf_tflops = r["pairs"] * PREFILL_FLOP_PER_PAIR / (km["mqa_logits"] / 1e3) / 1e12
+    dec_gbs = r["dec_keys"] * DECODE_BYTES_PER_KEY / (km["paged_mqa_logits"] / 1e3) / 1e9
+    kernels = {
+        "mqa_logits": {"ms": km["mqa_logits"], "achieved": pf_tflops, "unit": "TFLOP/s",
+                       "peak": fp8_peak, "frac": pf_tflops / fp8_peak,
+                       "per_unit": f"{PREFILL_FLOP_PER_PAIR} flop per visible (query, key) pair",
+                       "units": r["pairs"]},
+        "paged_mqa_logits": {"ms": km["paged_mqa_logits"], "achieved": dec_gbs, "unit": "GB/s",
+                             "peak": pk["hbm_gbs"], "frac": dec_gbs / pk["hbm_gbs"],
+                             "frac_of_8tbs": dec_gbs / 8000.0,
+                             "per_unit": f"{DECODE_BYTES_PER_KEY} B per key",
+                             "units": r["dec_keys"]},
+        "topk_decode": {"ms": km["topk_decode"]},
+        "topk_prefill": {"ms": km["topk_prefill"]},
+    }
+    dominant = max(("mqa_logits", "paged_mqa_logits"), key=lambda n: km[n])
+    kd = kernels[dominant]
+    roofline = {"bound": "tensor" if dominant == "mqa_logits" else "hbm",
+                "kernel": dominant, "achieved": kd["achieved"], "peak": kd["peak"],
+                "unit": kd["unit"], "frac": kd["frac"], "traffic": None,
+                "peak_kind": (f"{pk_kind}: fp8 = 2 x cuBLAS bf16 burst {pk['bf16_tflops']} TFLOP/s"
+                              if dominant == "mqa_logits" else f"{pk_kind} copy bandwidth")}
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8_e4m3 x fp8_e4m3 -> f32 (logits); u8/bf16 cache writes",
+            "data": "synthetic (seeded; random-init inputs of the indexer shapes; no dataset)",
+            "config": {**workload_config(wl), "parallelism": f"replicas x{world}"},
+            "roofline": roofline, "kernels": kernels,
+            "prefill_tflops": pf_tflops, "decode_hbm_gbs": dec_gbs,
+            "e2e": {"value": world * r["rows"] * r["e2e_steps"] / (e2e_ms / 1e3), "unit": UNIT,
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": step.kernels_per_step() * args.steps,
+            "clocks": r["clocks"], "device_status": r["status"]}
+    if not args.no_cpu_baseline:
+        import oracle
+        s = OracleSampler(wl)
+        w0 = time.perf_counter()
+        while time.perf_counter() - w0 < 12.0 or s.n < 8:
+            s.sample(dec_keys=8192)
+        line["cpu_baseline"] = {"value": r["rows"] / s.step_seconds(), "unit": UNIT,
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": s.describe(),
+                                "sample_seconds": time.perf_counter() - w0 + s.t_fixed}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
