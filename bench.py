@@ -131,7 +131,8 @@ class ClockSampler:
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].strip().lower() == "active"})
         return {"sm_mhz": float(np.median(sm)) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
                 "samples": len(rows)}
@@ -168,10 +169,14 @@ def gpu_arm(args, world, rank, local):
     libbuild.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = W.mixed_long(seed=rank)
+    wl = W.NAMED[args.workload](seed=rank)
     step = make_step(wl, dev)
     stream = torch.cuda.current_stream(dev)
-    names = ["mqa_logits", "paged_mqa_logits", "topk_decode", "topk_prefill"]
+    names = []
+    if wl.prefill_req:
+        names += ["mqa_logits", "topk_prefill"]
+    if wl.n_decode:
+        names += ["paged_mqa_logits", "topk_decode"]
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
@@ -200,17 +205,24 @@ def gpu_arm(args, world, rank, local):
     host_in = {
         "new_k": (wl.new_k.pin_memory(), step.new_k),
         "new_slot": (torch.from_numpy(wl.new_slot.copy()).pin_memory(), step.new_slot),
-        "q_dec": (wl.q_decode.pin_memory(), step.decode.q),
-        "w_dec": (wl.w_decode.pin_memory(), step.decode.w),
-        "ctx": (torch.from_numpy(wl.context_lens.copy()).pin_memory(), step.decode.context_lens),
-        "q_pf": (wl.q_prefill.pin_memory(), step.prefill.q),
-        "w_pf": (wl.w_prefill.pin_memory(), step.prefill.w),
-        "nope": (wl.nope_bf16.pin_memory(), step.nope),
-        "rope": (wl.rope_bf16.pin_memory(), step.rope),
         "bt": (torch.from_numpy(wl.block_table.copy()).pin_memory(), step.block_table),
     }
-    host_out = [(step.dec_global, torch.empty(step.dec_global.shape, dtype=torch.int32).pin_memory()),
-                (step.pf_global, torch.empty(step.pf_global.shape, dtype=torch.int32).pin_memory())]
+    host_out = []
+    if wl.n_decode:
+        host_in["q_dec"] = (wl.q_decode.pin_memory(), step.decode.q)
+        host_in["w_dec"] = (wl.w_decode.pin_memory(), step.decode.w)
+        host_in["ctx"] = (torch.from_numpy(wl.context_lens.copy()).pin_memory(),
+                          step.decode.context_lens)
+        host_out.append((step.dec_global, torch.empty(step.dec_global.shape,
+                                                      dtype=torch.int32).pin_memory()))
+    if wl.prefill_req:
+        host_in["q_pf"] = (wl.q_prefill.pin_memory(), step.prefill.q)
+        host_in["w_pf"] = (wl.w_prefill.pin_memory(), step.prefill.w)
+        host_out.append((step.pf_global, torch.empty(step.pf_global.shape,
+                                                     dtype=torch.int32).pin_memory()))
+    if wl.nope_bf16 is not None:
+        host_in["nope"] = (wl.nope_bf16.pin_memory(), step.nope)
+        host_in["rope"] = (wl.rope_bf16.pin_memory(), step.rope)
     h2d = sum(h.numel() * h.element_size() for h, _ in host_in.values())
     d2h = sum(h.numel() * h.element_size() for _, h in host_out)
     barrier(world)
@@ -348,6 +360,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="dsix", choices=["dsix", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="mixed_long",
+                    help="named workload; the benchmark line is mixed_long, the others are "
+                         "for profiling single kernels")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -365,22 +380,25 @@ def main():
     fp8_peak = 2.0 * pk["bf16_tflops"]
     value = world * r["rows"] * args.steps / (elapsed / 1e3)
     km = r["kern_ms"]
-    pf_tflops = r["pairs"] * PREFILL_FLOP_PER_PAIR / (km["mqa_logits"] / 1e3) / 1e12
-    dec_gbs = r["dec_keys"] * DECODE_BYTES_PER_KEY / (km["paged_mqa_logits"] / 1e3) / 1e9
-    kernels = {
-        "mqa_logits": {"ms": km["mqa_logits"], "achieved": pf_tflops, "unit": "TFLOP/s",
-                       "peak": fp8_peak, "frac": pf_tflops / fp8_peak,
-                       "per_unit": f"{PREFILL_FLOP_PER_PAIR} flop per visible (query, key) pair",
-                       "units": r["pairs"]},
-        "paged_mqa_logits": {"ms": km["paged_mqa_logits"], "achieved": dec_gbs, "unit": "GB/s",
-                             "peak": pk["hbm_gbs"], "frac": dec_gbs / pk["hbm_gbs"],
-                             "frac_of_8tbs": dec_gbs / 8000.0,
-                             "per_unit": f"{DECODE_BYTES_PER_KEY} B per key",
-                             "units": r["dec_keys"]},
-        "topk_decode": {"ms": km["topk_decode"]},
-        "topk_prefill": {"ms": km["topk_prefill"]},
-    }
-    dominant = max(("mqa_logits", "paged_mqa_logits"), key=lambda n: km[n])
+    pf_tflops = (r["pairs"] * PREFILL_FLOP_PER_PAIR / (km["mqa_logits"] / 1e3) / 1e12
+                 if "mqa_logits" in km else None)
+    dec_gbs = (r["dec_keys"] * DECODE_BYTES_PER_KEY / (km["paged_mqa_logits"] / 1e3) / 1e9
+               if "paged_mqa_logits" in km else None)
+    kernels = {}
+    if "mqa_logits" in km:
+        kernels["mqa_logits"] = {
+            "ms": km["mqa_logits"], "achieved": pf_tflops, "unit": "TFLOP/s", "peak": fp8_peak,
+            "frac": pf_tflops / fp8_peak, "units": r["pairs"],
+            "per_unit": f"{PREFILL_FLOP_PER_PAIR} flop per visible (query, key) pair"}
+    if "paged_mqa_logits" in km:
+        kernels["paged_mqa_logits"] = {
+            "ms": km["paged_mqa_logits"], "achieved": dec_gbs, "unit": "GB/s",
+            "peak": pk["hbm_gbs"], "frac": dec_gbs / pk["hbm_gbs"], "frac_of_8tbs": dec_gbs / 8000.0,
+            "per_unit": f"{DECODE_BYTES_PER_KEY} B per key", "units": r["dec_keys"]}
+    for n in ("topk_decode", "topk_prefill"):
+        if n in km:
+            kernels[n] = {"ms": km[n]}
+    dominant = max((n for n in ("mqa_logits", "paged_mqa_logits") if n in km), key=lambda n: km[n])
     kd = kernels[dominant]
     roofline = {"bound": "tensor" if dominant == "mqa_logits" else "hbm",
                 "kernel": dominant, "achieved": kd["achieved"], "peak": kd["peak"],
