@@ -247,7 +247,39 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
     mbar_wait(bar, parity, &never, status, kDrainLimitNs);
 }
 
-template <bool P>
+// Head-weighted ReLU sums for this thread's key over R query rows: TMEM
+// columns [tbase + 64 r, +64) hold row r's 64 head scores, w[64 r + h] the
+// row's head weights.  The load of 32-column chunk c+1 overlaps the
+// arithmetic on chunk c; four accumulation chains per row.
+template <int R>
+__device__ __forceinline__ void head_sums(uint32_t tbase, const float* w, float (&out)[R]) {
+    uint32_t buf[2][32];
+    float acc[R][4];
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.f;
+    tmem_ld32(tbase, buf[0]);
+    tmem_wait_ld(buf[0]);
+#pragma unroll
+    for (int c = 0; c < 2 * R; ++c) {
+        if (c + 1 < 2 * R) tmem_ld32(tbase + (c + 1) * 32, buf[(c + 1) & 1]);
+        const int r = c >> 1;
+        const float4* w4 = reinterpret_cast<const float4*>(w + r * kHeads + (c & 1) * 32);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 ww = w4[q];
+            const uint32_t* v = buf[c & 1] + 4 * q;
+            acc[r][0] = fmaf(ww.x, fmaxf(__uint_as_float(v[0]), 0.f), acc[r][0]);
+            acc[r][1] = fmaf(ww.y, fmaxf(__uint_as_float(v[1]), 0.f), acc[r][1]);
+            acc[r][2] = fmaf(ww.z, fmaxf(__uint_as_float(v[2]), 0.f), acc[r][2]);
+            acc[r][3] = fmaf(ww.w, fmaxf(__uint_as_float(v[3]), 0.f), acc[r][3]);
+        }
+        if (c + 1 < 2 * R) tmem_wait_ld(buf[(c + 1) & 1]);
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) out[r] = (acc[r][0] + acc[r][1]) + (acc[r][2] + acc[r][3]);
+}
+
+template <bool P, int NN>
 __global__ void __launch_bounds__(kThreads, 1)
     logits_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmS,
                   const __grid_constant__ CUtensorMap tmQ, const LogitsArgs a) {
@@ -483,14 +515,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else {
             // ------------------------------------------------------------ epilogue
+            constexpr int kRowsPerJob = P ? NN : 4;
             const int wg = (warp - kFirstEpiWarp) >> 2;
             const int quad = warp & 3;
             const int m = quad * 32 + lane;  // tile row = TMEM lane
             const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
             int it = 0, qi = 0, job = 0;
             int kbeg = 0, kend = 0;
-            int rlen[2] = {0, 0};      // decode: visible length per row
-            int rs0[4], rs1[4];        // prefill: [ks, ke) of this warpgroup's rows
+            int rs0[kRowsPerJob], rs1[kRowsPerJob];  // visible key range of each row of a job
             bool new_group = true, have_group = false;
             while (cur.left > 0) {
                 const int g = cur.g;
@@ -505,10 +537,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     group_range<P>(a, g, kbeg, kend, false);
                     if constexpr (P) {
                         const int ctx = __ldg(a.context_lens + g);
-                        for (int j = 0; j < a.next_n; ++j) rlen[j] = decode_row_len(a, ctx, j, false);
+#pragma unroll
+                        for (int j = 0; j < kRowsPerJob; ++j) {
+                            rs0[j] = 0;
+                            rs1[j] = decode_row_len(a, ctx, j, false);
+                        }
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
+                        for (int i = 0; i < kRowsPerJob; ++i) {
                             const int64_t r = static_cast<int64_t>(g) * C::kRows + wg * 4 + i;
                             rs0[i] = 0;
                             rs1[i] = 0;
@@ -516,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                const float* wbuf = sW + ((qi - 1) & 1) * C::kWFloats;
+                const float* wbuf = sW + ((qi - 1) & 1) * C::kWFloats + (P ? 0 : wg * 4 * kHeads);
                 bool ok = true;
 #pragma unroll
                 for (int h = 0; h < C::kHalves; ++h, ++job) {
@@ -531,45 +567,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const int s = kbeg + cur.t * kTile + m;  // key index
                     const float ksc = sSc[sci * kScaleStride + (P ? 0 : (s - m) & 3) + m];
-                    const uint32_t tbase = lane_addr + slot * C::kSlotCols;
-                    const int nrows = P ? a.next_n : 4;
-                    for (int i = 0; i < nrows; ++i) {
-                        uint32_t v0[32], v1[32];
-                        tmem_ld32(tbase + i * kHeads, v0);
-                        tmem_ld32(tbase + i * kHeads + 32, v1);
-                        tmem_wait_ld();
-                        const float4* w4 = reinterpret_cast<const float4*>(
-                            wbuf + (P ? i : wg * 4 + i) * kHeads);
-                        float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const float4 wa = w4[c];
-                            acc0 = fmaf(wa.x, fmaxf(__uint_as_float(v0[4 * c + 0]), 0.f), acc0);
-                            acc1 = fmaf(wa.y, fmaxf(__uint_as_float(v0[4 * c + 1]), 0.f), acc1);
-                            acc0 = fmaf(wa.z, fmaxf(__uint_as_float(v0[4 * c + 2]), 0.f), acc0);
-                            acc1 = fmaf(wa.w, fmaxf(__uint_as_float(v0[4 * c + 3]), 0.f), acc1);
-                            const float4 wb = w4[8 + c];
-                            acc0 = fmaf(wb.x, fmaxf(__uint_as_float(v1[4 * c + 0]), 0.f), acc0);
-                            acc1 = fmaf(wb.y, fmaxf(__uint_as_float(v1[4 * c + 1]), 0.f), acc1);
-                            acc0 = fmaf(wb.z, fmaxf(__uint_as_float(v1[4 * c + 2]), 0.f), acc0);
-                            acc1 = fmaf(wb.w, fmaxf(__uint_as_float(v1[4 * c + 3]), 0.f), acc1);
-                        }
-                        const float logit = (acc0 + acc1) * ksc;
-                        if constexpr (P) {
-                            if (s < rlen[i])
-                                a.logits[(static_cast<int64_t>(g) * a.next_n + i) * a.ld + s] = logit;
-                        } else {
-                            if (s >= rs0[i] && s < rs1[i]) {
-                                const int64_t r = static_cast<int64_t>(g) * C::kRows + wg * 4 + i;
-                                a.logits[r * a.ld + (s - rs0[i])] = logit;
-                            }
-                        }
-                    }
+                    float sums[kRowsPerJob];
+                    head_sums<kRowsPerJob>(lane_addr + slot * C::kSlotCols, wbuf, sums);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
                         mbar_arrive(acc_empty + slot);
                         mbar_arrive(sc_empty + sci);
+                    }
+#pragma unroll
+                    for (int i = 0; i < kRowsPerJob; ++i) {
+                        if (s >= rs0[i] && s < rs1[i]) {
+                            int64_t r;
+                            if constexpr (P) r = static_cast<int64_t>(g) * NN + i;
+                            else r = static_cast<int64_t>(g) * C::kRows + wg * 4 + i;
+                            a.logits[r * a.ld + (s - rs0[i])] = sums[i] * ksc;
+                        }
                     }
                 }
                 if (!ok) break;
@@ -638,7 +651,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool P>
+template <bool P, int NN>
 int launch(const CUtensorMap& tmK, const CUtensorMap& tmS, const CUtensorMap& tmQ,
            const LogitsArgs& a, int64_t rows, int clean, cudaStream_t stream) {
     static std::mutex mu;
@@ -649,7 +662,7 @@ int launch(const CUtensorMap& tmK, const CUtensorMap& tmS, const CUtensorMap& tm
         std::lock_guard<std::mutex> lock(mu);
         if (dev >= static_cast<int>(ready.size())) ready.resize(dev + 1, 0);
         if (!ready[dev]) {
-            if (cudaFuncSetAttribute(logits_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(logits_kernel<P, NN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      Smem<P>::kAlloc) != cudaSuccess)
                 return IX_ERR_CUDA;
             ready[dev] = 1;
@@ -658,7 +671,7 @@ int launch(const CUtensorMap& tmK, const CUtensorMap& tmS, const CUtensorMap& tm
     const int sms = num_sms();
     if (sms <= 0) return IX_ERR_CUDA;
     if (a.num_groups > 0) {
-        logits_kernel<P><<<sms, kThreads, Smem<P>::kAlloc, stream>>>(tmK, tmS, tmQ, a);
+        logits_kernel<P, NN><<<sms, kThreads, Smem<P>::kAlloc, stream>>>(tmK, tmS, tmQ, a);
         if (launch_status() != IX_OK) return IX_ERR_CUDA;
     }
     if (clean && rows > 0) {
@@ -727,8 +740,10 @@ extern "C" int ix_paged_mqa_logits(const uint8_t* q_fp8, const float* w, const u
     a.bt_stride = bt_stride;
     a.next_n = next_n;
     a.num_blocks = num_blocks;
-    return launch<true>(tmK, tmS, tmQ, a, static_cast<int64_t>(batch) * next_n, clean_logits,
-                        reinterpret_cast<cudaStream_t>(stream));
+    const int64_t rows = static_cast<int64_t>(batch) * next_n;
+    cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+    return next_n == 1 ? launch<true, 1>(tmK, tmS, tmQ, a, rows, clean_logits, st_)
+                       : launch<true, 2>(tmK, tmS, tmQ, a, rows, clean_logits, st_);
 }
 
 extern "C" int ix_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t* k_fp8,
@@ -783,5 +798,6 @@ extern "C" int ix_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t
                 return IX_ERR_CUDA;
         }
     }
-    return launch<false>(tmK, tmS, tmQ, a, tq, clean_logits, reinterpret_cast<cudaStream_t>(stream));
+    return launch<false, 1>(tmK, tmS, tmQ, a, tq, clean_logits,
+                            reinterpret_cast<cudaStream_t>(stream));
 }
