@@ -11,15 +11,18 @@
 //     lane m then holds every head score of key m, so the weighted ReLU head
 //     sum is a per-thread loop with no shuffles.
 //       decode : N = 64 * next_n (the next_n rows of one request), 1 MMA job per tile
-//       prefill: 8 query rows per group, two jobs of N = 256 (rows 0-3, 4-7) per tile
+//       prefill: 8 query rows per group, four jobs of N = 128 (2 rows each) per tile
 //     One job = 4 x tcgen05.mma.kind::f8f6f4 (K = 128 = 4 x 32), FP32 accumulators
-//     in TMEM (512 columns: 4 slots of 128 for decode, 2 of 256 for prefill).
+//     in TMEM: 4 slots of 128 columns, so the MMA can run up to 4 jobs ahead of
+//     the epilogue.
 //   * Warp 0 is the TMA producer: K tiles (128 B rows, 128-byte swizzle; a paged
 //     tile is two 64-key blocks, each one 3-D TMA box), the tile's fp32 key
 //     scales, and per group the Q operand (TMA) and head weights (bulk copy).
 //   * Warp 1 (one elected lane) issues the MMAs and commits to mbarriers.
-//   * Warps 2-9 are two epilogue warpgroups that alternate jobs: tcgen05.ld of
-//     the accumulators, ReLU, head-weighted sum, key scale, masked store.
+//   * Warps 2-17 are four epilogue warpgroups; job j (TMEM slot j % 4) belongs
+//     to warpgroup j % 4: tcgen05.ld of the accumulators, ReLU, head-weighted
+//     sum (packed f32x2 FMA; half of the ReLUs as a saturating multiply on the
+//     FMA pipe, half as FMNMX on the ALU pipe), key scale, masked store.
 //   * Work = the flattened list of (group, key-tile) units over all groups,
 //     split evenly across CTAs on the device from context_lens / ks,ke (no host
 //     sync, graph-capturable).  Each role walks the same unit sequence.
@@ -42,7 +45,8 @@ constexpr int kDim = 128;
 constexpr int kBlk = 64;
 constexpr int kTile = 128;       // keys per tile (MMA M)
 constexpr int kTileBytes = kTile * kDim;
-constexpr int kThreads = 320;    // 10 warps
+constexpr int kEpiGroups = 4;
+constexpr int kThreads = 64 + kEpiGroups * 128;  // producer + MMA warps + 4 warpgroups
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kFirstEpiWarp = 2;
@@ -63,8 +67,7 @@ struct Cfg<true> {  // decode over the paged cache
     static constexpr int kWFloats = 2 * kHeads;
     static constexpr int kSlots = 4;
     static constexpr int kSlotCols = 128;
-    static constexpr int kHalves = 1;
-    static constexpr int kScEmptyCount = 4;
+    static constexpr int kJobsPerTile = 1;
 };
 
 template <>
@@ -73,10 +76,10 @@ struct Cfg<false> {  // prefill over contiguous K
     static constexpr int kStages = 4;
     static constexpr int kQBytes = kRows * kHeads * kDim;  // 64 KB
     static constexpr int kWFloats = kRows * kHeads;
-    static constexpr int kSlots = 2;
-    static constexpr int kSlotCols = 256;
-    static constexpr int kHalves = 2;
-    static constexpr int kScEmptyCount = 8;
+    static constexpr int kSlots = 4;
+    static constexpr int kSlotCols = 128;
+    static constexpr int kJobsPerTile = 4;   // job q covers rows 2q, 2q + 1
+    static constexpr int kJobRows = 2;
 };
 
 template <bool P>
@@ -247,16 +250,44 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
     mbar_wait(bar, parity, &never, status, kDrainLimitNs);
 }
 
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// max(s, 0) * 2^-25 in one saturating multiply on the FMA pipe.  Exact: the
+// product is a power-of-two scaling, and |s| < 2^25 for any score of e4m3
+// operands (|q . k| <= 128 * 448^2), so saturation at 1 never clips a score.
+__device__ __forceinline__ float relu_scaled(float s) {
+    float r;
+    asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(r) : "f"(s), "f"(0x1p-25f));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 // Head-weighted ReLU sums for this thread's key over R query rows: TMEM
 // columns [tbase + 64 r, +64) hold row r's 64 head scores, w[64 r + h] the
 // row's head weights.  The load of 32-column chunk c+1 overlaps the
-// arithmetic on chunk c; four accumulation chains per row.
+// arithmetic on chunk c.  Heads are taken in pairs: the even head's ReLU is an
+// FMNMX (ALU pipe), the odd head's a saturating multiply by 2^-25 (FMA pipe),
+// and one packed f32x2 FMA accumulates both; the odd-head lane is rescaled by
+// 2^25 (exactly) at the end.
 template <int R>
 __device__ __forceinline__ void head_sums(uint32_t tbase, const float* w, float (&out)[R]) {
     uint32_t buf[2][32];
-    float acc[R][4];
+    uint64_t acc[R][2];
 #pragma unroll
-    for (int r = 0; r < R; ++r) acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.f;
+    for (int r = 0; r < R; ++r) acc[r][0] = acc[r][1] = 0ull;
     tmem_ld32(tbase, buf[0]);
     tmem_wait_ld(buf[0]);
 #pragma unroll
@@ -268,15 +299,22 @@ __device__ __forceinline__ void head_sums(uint32_t tbase, const float* w, float 
         for (int q = 0; q < 8; ++q) {
             const float4 ww = w4[q];
             const uint32_t* v = buf[c & 1] + 4 * q;
-            acc[r][0] = fmaf(ww.x, fmaxf(__uint_as_float(v[0]), 0.f), acc[r][0]);
-            acc[r][1] = fmaf(ww.y, fmaxf(__uint_as_float(v[1]), 0.f), acc[r][1]);
-            acc[r][2] = fmaf(ww.z, fmaxf(__uint_as_float(v[2]), 0.f), acc[r][2]);
-            acc[r][3] = fmaf(ww.w, fmaxf(__uint_as_float(v[3]), 0.f), acc[r][3]);
+            const uint64_t t01 =
+                pack2(fmaxf(__uint_as_float(v[0]), 0.f), relu_scaled(__uint_as_float(v[1])));
+            const uint64_t t23 =
+                pack2(fmaxf(__uint_as_float(v[2]), 0.f), relu_scaled(__uint_as_float(v[3])));
+            acc[r][0] = fma2(pack2(ww.x, ww.y), t01, acc[r][0]);
+            acc[r][1] = fma2(pack2(ww.z, ww.w), t23, acc[r][1]);
         }
         if (c + 1 < 2 * R) tmem_wait_ld(buf[(c + 1) & 1]);
     }
 #pragma unroll
-    for (int r = 0; r < R; ++r) out[r] = (acc[r][0] + acc[r][1]) + (acc[r][2] + acc[r][3]);
+    for (int r = 0; r < R; ++r) {
+        float e0, o0, e1, o1;
+        unpack2(acc[r][0], e0, o0);
+        unpack2(acc[r][1], e1, o1);
+        out[r] = (e0 + e1) + (o0 + o1) * 0x1p25f;
+    }
 }
 
 template <bool P, int NN>
@@ -315,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(qw_full + i, 1);
-            mbar_init(qw_empty + i, 8);
+            mbar_init(qw_empty + i, 4 * kEpiGroups);
         }
         for (int i = 0; i < C::kSlots; ++i) {
             mbar_init(acc_full + i, 1);
@@ -323,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kScaleRing; ++i) {
             mbar_init(sc_full + i, 1);
-            mbar_init(sc_empty + i, C::kScEmptyCount);
+            mbar_init(sc_empty + i, 4 * C::kJobsPerTile);
         }
         mbar_init(mma_done, 1);
         fence_barrier_init();
@@ -470,8 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int it = 0, qi = 0, job = 0;
                 uint32_t qaddr = 0;
                 bool issued = false, new_group = true;
-                const uint32_t idesc = P ? idesc_e4m3_f32(kTile, kHeads * a.next_n)
-                                         : idesc_e4m3_f32(kTile, 256);
+                const uint32_t idesc = P ? idesc_e4m3_f32(kTile, kHeads * NN)
+                                         : idesc_e4m3_f32(kTile, kHeads * 2);
                 while (cur.left > 0) {
                     if (new_group) {
                         const int qb = qi & 1;
@@ -485,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t aaddr = smem_u32(sK + stage * kTileBytes);
                     bool ok = true;
 #pragma unroll
-                    for (int h = 0; h < C::kHalves; ++h) {
+                    for (int h = 0; h < C::kJobsPerTile; ++h) {
                         const int slot = job % C::kSlots;
                         if (!mbar_wait(acc_empty + slot, ((job / C::kSlots) & 1) ^ 1, abort_flag,
                                        a.status)) {
@@ -494,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tc_fence_after();
                         const uint32_t d = tmem_base + slot * C::kSlotCols;
-                        const uint32_t baddr = qaddr + h * (C::kQBytes / 2);
+                        const uint32_t baddr = qaddr + h * (2 * kHeads * kDim);
 #pragma unroll
                         for (int kk = 0; kk < kDim / 32; ++kk)
                             mma_e4m3(d, sdesc_k_sw128(aaddr + 32 * kk), sdesc_k_sw128(baddr + 32 * kk),
@@ -515,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else {
             // ------------------------------------------------------------ epilogue
-            constexpr int kRowsPerJob = P ? NN : 4;
+            constexpr int kRowsPerJob = P ? NN : 2;
             const int wg = (warp - kFirstEpiWarp) >> 2;
             const int quad = warp & 3;
             const int m = quad * 32 + lane;  // tile row = TMEM lane
@@ -545,18 +583,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
 #pragma unroll
                         for (int i = 0; i < kRowsPerJob; ++i) {
-                            const int64_t r = static_cast<int64_t>(g) * C::kRows + wg * 4 + i;
+                            const int64_t r = static_cast<int64_t>(g) * C::kRows + wg * 2 + i;
                             rs0[i] = 0;
                             rs1[i] = 0;
                             if (r < a.tq) prefill_row_range(a, r, rs0[i], rs1[i], false);
                         }
                     }
                 }
-                const float* wbuf = sW + ((qi - 1) & 1) * C::kWFloats + (P ? 0 : wg * 4 * kHeads);
+                const float* wbuf = sW + ((qi - 1) & 1) * C::kWFloats + (P ? 0 : wg * 2 * kHeads);
                 bool ok = true;
 #pragma unroll
-                for (int h = 0; h < C::kHalves; ++h, ++job) {
-                    if ((job & 1) != wg) continue;
+                for (int h = 0; h < C::kJobsPerTile; ++h, ++job) {
+                    if ((job & 3) != wg) continue;
                     const int slot = job % C::kSlots;
                     const int sci = it % kScaleRing;
                     if (!wait_warp(sc_full + sci, (it / kScaleRing) & 1, abort_flag, a.status) ||
@@ -580,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (s >= rs0[i] && s < rs1[i]) {
                             int64_t r;
                             if constexpr (P) r = static_cast<int64_t>(g) * NN + i;
-                            else r = static_cast<int64_t>(g) * C::kRows + wg * 4 + i;
+                            else r = static_cast<int64_t>(g) * C::kRows + wg * 2 + i;
                             a.logits[r * a.ld + (s - rs0[i])] = sums[i] * ksc;
                         }
                     }
