@@ -79,19 +79,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// A wait that gives up.  Spins on the barrier phase; returns false when the
-// CTA-wide abort flag is raised by another role, or after `limit_ns` of wall
-// time, in which case it raises the abort flag itself and records
-// IX_DEV_TIMEOUT.  Pipelines use it for every wait so that a logic error can
-// never hang the GPU.
+// try_wait with a suspend-time hint: a thread whose phase is not complete is
+// suspended by the hardware until the phase completes or about `hint_ns`
+// passes, so waiting warps do not take issue slots from working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// A wait that gives up.  Sleeps on the barrier phase (suspend-time hint of
+// 1 ms per try); returns false when the CTA-wide abort flag is raised by
+// another role, or after `limit_ns` of wall time, in which case it raises the
+// abort flag itself and records IX_DEV_TIMEOUT.  Pipelines use it for every
+// wait so that a logic error can never hang the GPU.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint32_t kSleepHintNs = 1000000u;       // 1 ms
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* status, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             *abort_flag = 1;
