@@ -10,17 +10,20 @@
 //   * MMA orientation: keys on M (128 per tile), (query row, head) on N.  TMEM
 //     lane m then holds every head score of key m, so the weighted ReLU head
 //     sum is a per-thread loop with no shuffles.
-//       decode : N = 64 * next_n (the next_n rows of one request), 1 MMA job per tile
-//       prefill: 8 query rows per group, four jobs of N = 128 (2 rows each) per tile
-//     One job = 4 x tcgen05.mma.kind::f8f6f4 (K = 128 = 4 x 32), FP32 accumulators
-//     in TMEM: 4 slots of 128 columns, so the MMA can run up to 4 jobs ahead of
-//     the epilogue.
+//       decode : N = 64 * next_n (the next_n rows of one request), 1 MMA job per
+//                tile; TMEM holds 4 job slots of 128 columns
+//       prefill: 8 query rows per group, two jobs of N = 256 (4 rows each) per
+//                tile; TMEM holds 2 job slots of 256 columns.  N = 256 keeps the
+//                single MMA-issuing thread at full tensor rate even while 16
+//                epilogue warps compete for its SMSP's issue slots.
+//     One job = 4 x tcgen05.mma.kind::f8f6f4 (K = 128 = 4 x 32), FP32 accumulators.
 //   * Warp 0 is the TMA producer: K tiles (128 B rows, 128-byte swizzle; a paged
 //     tile is two 64-key blocks, each one 3-D TMA box), the tile's fp32 key
 //     scales, and per group the Q operand (TMA) and head weights (bulk copy).
 //   * Warp 1 (one elected lane) issues the MMAs and commits to mbarriers.
-//   * Warps 2-17 are four epilogue warpgroups; job j (TMEM slot j % 4) belongs
-//     to warpgroup j % 4: tcgen05.ld of the accumulators, ReLU, head-weighted
+//   * Warps 2-17 are four epilogue warpgroups (decode: job j belongs to
+//     warpgroup j % 4; prefill: warpgroup w always takes rows 2w, 2w+1 of every
+//     group, i.e. half of the job in slot w / 2): tcgen05.ld of the accumulators, ReLU, head-weighted
 //     sum (packed f32x2 FMA; half of the ReLUs as a saturating multiply on the
 //     FMA pipe, half as FMNMX on the ALU pipe), key scale, masked store.
 //   * Work = the flattened list of (group, key-tile) units over all groups,
@@ -68,6 +71,7 @@ struct Cfg<true> {  // decode over the paged cache
     static constexpr int kSlots = 4;
     static constexpr int kSlotCols = 128;
     static constexpr int kJobsPerTile = 1;
+    static constexpr int kGroupsPerJob = 1;  // epilogue warpgroups sharing one job
 };
 
 template <>
@@ -76,10 +80,10 @@ struct Cfg<false> {  // prefill over contiguous K
     static constexpr int kStages = 4;
     static constexpr int kQBytes = kRows * kHeads * kDim;  // 64 KB
     static constexpr int kWFloats = kRows * kHeads;
-    static constexpr int kSlots = 4;
-    static constexpr int kSlotCols = 128;
-    static constexpr int kJobsPerTile = 4;   // job q covers rows 2q, 2q + 1
-    static constexpr int kJobRows = 2;
+    static constexpr int kSlots = 2;
+    static constexpr int kSlotCols = 256;
+    static constexpr int kJobsPerTile = 2;   // job h covers rows 4h .. 4h + 3
+    static constexpr int kGroupsPerJob = 2;  // warpgroup w takes rows 2w, 2w + 1
 };
 
 template <bool P>
@@ -357,11 +361,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < C::kSlots; ++i) {
             mbar_init(acc_full + i, 1);
-            mbar_init(acc_empty + i, 4);
+            mbar_init(acc_empty + i, 4 * C::kGroupsPerJob);
         }
         for (int i = 0; i < kScaleRing; ++i) {
             mbar_init(sc_full + i, 1);
-            mbar_init(sc_empty + i, 4 * C::kJobsPerTile);
+            mbar_init(sc_empty + i, 4 * C::kJobsPerTile * C::kGroupsPerJob);  // every reader warp
         }
         mbar_init(mma_done, 1);
         fence_barrier_init();
@@ -506,21 +510,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ------------------------------------------------------------ MMA issuer
             if (lane == 0) {
                 int it = 0, qi = 0, job = 0;
-                uint32_t qaddr = 0;
+                uint64_t qdesc = 0;
                 bool issued = false, new_group = true;
-                const uint32_t idesc = P ? idesc_e4m3_f32(kTile, kHeads * NN)
-                                         : idesc_e4m3_f32(kTile, kHeads * 2);
+                constexpr int kJobN = P ? kHeads * NN : kHeads * 4;
+                constexpr uint32_t idesc = idesc_e4m3_f32(kTile, kJobN);
+                // descriptors advance by (bytes >> 4) in the start-address field
+                const uint64_t a_desc0 = sdesc_k_sw128(smem_u32(sK));
                 while (cur.left > 0) {
                     if (new_group) {
                         const int qb = qi & 1;
                         if (!mbar_wait(qw_full + qb, (qi >> 1) & 1, abort_flag, a.status)) break;
-                        qaddr = smem_u32(sQ + qb * C::kQBytes);
+                        qdesc = sdesc_k_sw128(smem_u32(sQ + qb * C::kQBytes));
                         ++qi;
                     }
                     const int stage = it % C::kStages;
                     if (!mbar_wait(full + stage, (it / C::kStages) & 1, abort_flag, a.status)) break;
                     tc_fence_after();
-                    const uint32_t aaddr = smem_u32(sK + stage * kTileBytes);
+                    const uint64_t adesc = a_desc0 + static_cast<uint64_t>(stage * (kTileBytes >> 4));
                     bool ok = true;
 #pragma unroll
                     for (int h = 0; h < C::kJobsPerTile; ++h) {
@@ -532,11 +538,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tc_fence_after();
                         const uint32_t d = tmem_base + slot * C::kSlotCols;
-                        const uint32_t baddr = qaddr + h * (2 * kHeads * kDim);
+                        const uint64_t bdesc = qdesc + static_cast<uint64_t>(h * ((kJobN * kDim) >> 4));
 #pragma unroll
                         for (int kk = 0; kk < kDim / 32; ++kk)
-                            mma_e4m3(d, sdesc_k_sw128(aaddr + 32 * kk), sdesc_k_sw128(baddr + 32 * kk),
-                                     idesc, kk > 0);
+                            mma_e4m3(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, kk > 0);
                         mma_commit(acc_full + slot);
                         issued = true;
                         ++job;
@@ -594,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = true;
 #pragma unroll
                 for (int h = 0; h < C::kJobsPerTile; ++h, ++job) {
-                    if ((job & 3) != wg) continue;
+                    if (P ? ((job & 3) != wg) : ((job & 1) != (wg >> 1))) continue;
                     const int slot = job % C::kSlots;
                     const int sci = it % kScaleRing;
                     if (!wait_warp(sc_full + sci, (it / kScaleRing) & 1, abort_flag, a.status) ||
@@ -606,7 +611,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int s = kbeg + cur.t * kTile + m;  // key index
                     const float ksc = sSc[sci * kScaleStride + (P ? 0 : (s - m) & 3) + m];
                     float sums[kRowsPerJob];
-                    head_sums<kRowsPerJob>(lane_addr + slot * C::kSlotCols, wbuf, sums);
+                    head_sums<kRowsPerJob>(lane_addr + slot * C::kSlotCols + (P ? 0 : (wg & 1) * 128),
+                                           wbuf, sums);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
