@@ -33,6 +33,7 @@ constexpr int kMaxCluster = 8;
 constexpr int kMaxPer = 64;
 constexpr int kSliceCap = kThreads * kMaxPer;  // keys per CTA
 constexpr int kBins = 2048;
+constexpr int kStage = 4096;  // selected indices staged in shared memory before the write-out
 
 struct TopkArgs {
     const float* logits;
@@ -43,6 +44,7 @@ struct TopkArgs {
     const int32_t* bt;
     int64_t bt_stride;
     int block_size;
+    int bs_shift;  // log2(block_size) when it is a power of two, else -1
     int k;
     int32_t* out_local;
     int32_t* out_global;
@@ -58,8 +60,16 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 __device__ __forceinline__ void emit(const TopkArgs& a, int64_t r, int b, int pos, int s) {
     int32_t g = -1;
     if (s >= 0) {
-        const int64_t blk = __ldg(a.bt + static_cast<int64_t>(b) * a.bt_stride + s / a.block_size);
-        g = static_cast<int32_t>(blk * a.block_size + s % a.block_size);
+        int q, rem;
+        if (a.bs_shift >= 0) {
+            q = s >> a.bs_shift;
+            rem = s & (a.block_size - 1);
+        } else {
+            q = s / a.block_size;
+            rem = s % a.block_size;
+        }
+        const int64_t blk = __ldg(a.bt + static_cast<int64_t>(b) * a.bt_stride + q);
+        g = static_cast<int32_t>(blk * a.block_size + rem);
     }
     if (a.out_local) a.out_local[r * a.k + pos] = s;
     a.out_global[r * a.k + pos] = g;
@@ -139,6 +149,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
     __shared__ int counts[2 * kMaxCluster];  // rank 0 only
     __shared__ int res[4];                   // digit, count above, count in bin
     __shared__ uint32_t scratch[72];
+    __shared__ int stage[kStage];            // this CTA's kept indices, in output order
 
     for (int i = tid; i < kBins; i += kThreads) {
         hist[i] = 0;
@@ -232,6 +243,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
         uint32_t tot;
         const uint32_t ex = scan_excl((gt << 16) | eq, scratch, &tot);  // fields < 2^16 per CTA
         int bg = static_cast<int>(ex >> 16), be = static_cast<int>(ex & 0xFFFFu);
+        int carry_gt = 0, carry_eq = 0;
         if (C > 1) {
             if (tid == 0) {
                 counts0[2 * rank] = static_cast<int>(tot >> 16);
@@ -239,20 +251,34 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
             }
             cluster.sync();
             for (int j = 0; j < rank; ++j) {
-                bg += counts0[2 * j];
-                be += counts0[2 * j + 1];
+                carry_gt += counts0[2 * j];
+                carry_eq += counts0[2 * j + 1];
             }
+            bg += carry_gt;
+            be += carry_eq;
         }
+        // this CTA's kept keys occupy output positions [cstart, cend)
+        const int cstart = carry_gt + min(carry_eq, k_rem);
+        const int cend = min(a.k, carry_gt + static_cast<int>(tot >> 16) +
+                                      min(carry_eq + static_cast<int>(tot & 0xFFFFu), k_rem));
+        const bool staged = cend - cstart <= kStage;
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
             if (j < nv) {
                 const uint32_t v = key[j] >> shift;
                 const bool g = v > prefix, e = v == prefix;
                 const int pos = bg + min(be, k_rem);
-                if ((g || (e && be < k_rem)) && pos < a.k) emit(a, r, b, pos, lo + mine + j);
+                if ((g || (e && be < k_rem)) && pos < a.k) {
+                    if (staged) stage[pos - cstart] = lo + mine + j;
+                    else emit(a, r, b, pos, lo + mine + j);
+                }
                 bg += g;
                 be += e;
             }
+        }
+        if (staged) {  // coalesced write-out with the remap
+            __syncthreads();
+            for (int i = tid; i < cend - cstart; i += kThreads) emit(a, r, b, cstart + i, stage[i]);
         }
         // res, scratch and counts are rewritten only after barriers that every
         // thread of the cluster reaches after its reads above
@@ -316,6 +342,7 @@ extern "C" int ix_topk_to_global(const float* logits, int64_t ld, int64_t rows,
     a.bt = block_table;
     a.bt_stride = bt_stride;
     a.block_size = block_size;
+    a.bs_shift = (block_size & (block_size - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(block_size)) : -1;
     a.k = k;
     a.out_local = out_local;
     a.out_global = out_global;
