@@ -118,6 +118,7 @@ struct LogitsArgs {
     int next_n;
     int64_t num_blocks;
     // prefill
+    const float* k_scale;
     const int32_t* ks;
     const int32_t* ke;
     int64_t tq;
@@ -248,10 +249,11 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, ok);
 }
 
-// Wait that ignores the abort flag (drains in-flight work on the way out).
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* status) {
-    volatile int never = 0;
-    mbar_wait(bar, parity, &never, status, kDrainLimitNs);
+// Wait that ignores the abort flag (drains in-flight work on the way out);
+// `never` points at a shared-memory word that stays 0.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, volatile int* never,
+                                           int* status) {
+    mbar_wait(bar, parity, never, status, kDrainLimitNs);
 }
 
 __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
@@ -371,6 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_barrier_init();
         misc[1] = 0;
         misc[4] = 0;
+        misc[5] = 0;  // never raised: the abort flag seen by drain waits
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmS);
         prefetch_tmap(&tmQ);
@@ -458,7 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int stage = it % C::kStages;
                 const int sci = it % kScaleRing;
                 if (!wait_warp(empty + stage, ((it / C::kStages) & 1) ^ 1, abort_flag, a.status)) break;
-                if (!wait_warp(sc_empty + sci, ((it / kScaleRing) & 1) ^ 1, abort_flag, a.status)) break;
+                if (P && !wait_warp(sc_empty + sci, ((it / kScaleRing) & 1) ^ 1, abort_flag, a.status))
+                    break;
                 uint8_t* kdst = sK + stage * kTileBytes;
                 float* sdst = sSc + sci * kScaleStride;
                 if constexpr (P) {
@@ -490,8 +494,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) {
                         mbar_arrive_expect_tx(full + stage, kTileBytes);
                         tma_load_2d(kdst, &tmK, full + stage, 0, start);
-                        mbar_arrive_expect_tx(sc_full + sci, kScaleBox * 4);
-                        tma_load_1d(sdst, &tmS, sc_full + sci, start & ~3);
                     }
                 }
                 ++it;
@@ -500,11 +502,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // drain: the last copies issued into each buffer must land before exit
             if (lane == 0) {
                 for (int i = max(0, it - C::kStages); i < it; ++i)
-                    drain_wait(full + i % C::kStages, (i / C::kStages) & 1, a.status);
-                for (int i = max(0, it - kScaleRing); i < it; ++i)
-                    drain_wait(sc_full + i % kScaleRing, (i / kScaleRing) & 1, a.status);
+                    drain_wait(full + i % C::kStages, (i / C::kStages) & 1, misc + 5, a.status);
+                if (P)
+                    for (int i = max(0, it - kScaleRing); i < it; ++i)
+                        drain_wait(sc_full + i % kScaleRing, (i / kScaleRing) & 1, misc + 5, a.status);
                 for (int i = max(0, qi - 2); i < qi; ++i)
-                    drain_wait(qw_full + (i & 1), (i >> 1) & 1, a.status);
+                    drain_wait(qw_full + (i & 1), (i >> 1) & 1, misc + 5, a.status);
             }
         } else if (warp == kMmaWarp) {
             // ------------------------------------------------------------ MMA issuer
@@ -553,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (issued) {
                     mma_commit(mma_done);
-                    drain_wait(mma_done, 0, a.status);
+                    drain_wait(mma_done, 0, misc + 5, a.status);
                 }
             }
         } else {
@@ -602,14 +605,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (P ? ((job & 3) != wg) : ((job & 1) != (wg >> 1))) continue;
                     const int slot = job % C::kSlots;
                     const int sci = it % kScaleRing;
-                    if (!wait_warp(sc_full + sci, (it / kScaleRing) & 1, abort_flag, a.status) ||
-                        !wait_warp(acc_full + slot, (job / C::kSlots) & 1, abort_flag, a.status)) {
+                    const int s = kbeg + cur.t * kTile + m;  // key index
+                    float ksc;
+                    if constexpr (P) {
+                        if (!wait_warp(sc_full + sci, (it / kScaleRing) & 1, abort_flag, a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        ksc = sSc[sci * kScaleStride + m];
+                    } else {
+                        // contiguous K: the scale comes straight from L2, issued before the wait
+                        ksc = __ldg(a.k_scale + min(static_cast<int64_t>(s), a.tk - 1));
+                    }
+                    if (!wait_warp(acc_full + slot, (job / C::kSlots) & 1, abort_flag, a.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const int s = kbeg + cur.t * kTile + m;  // key index
-                    const float ksc = sSc[sci * kScaleStride + (P ? 0 : (s - m) & 3) + m];
                     float sums[kRowsPerJob];
                     head_sums<kRowsPerJob>(lane_addr + slot * C::kSlotCols + (P ? 0 : (wg & 1) * 128),
                                            wbuf, sums);
@@ -617,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) {
                         mbar_arrive(acc_empty + slot);
-                        mbar_arrive(sc_empty + sci);
+                        if (P) mbar_arrive(sc_empty + sci);
                     }
 #pragma unroll
                     for (int i = 0; i < kRowsPerJob; ++i) {
@@ -812,6 +824,7 @@ extern "C" int ix_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t
     a.ld = ld;
     a.num_groups = tk > 0 ? static_cast<int>((tq + Cfg<false>::kRows - 1) / Cfg<false>::kRows) : 0;
     a.status = st;
+    a.k_scale = k_scale;
     a.ks = ks;
     a.ke = ke;
     a.tq = tq;

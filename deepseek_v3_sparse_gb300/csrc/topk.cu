@@ -137,8 +137,10 @@ __device__ __forceinline__ void warp_pick(int* h, int nb, int k_rem, int* out) {
     for (int i = 0; i < per; ++i) h[base + ((i + lane) & (per - 1))] = 0;
 }
 
+// Short slices keep several CTAs per SM resident to hide the per-row phase latency.
 template <int PER>
-__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
+__global__ void __launch_bounds__(kThreads, PER <= 8 ? 3 : (PER <= 16 ? 2 : 1))
+    topk_kernel(const TopkArgs a) {
     cg::cluster_group cluster = cg::this_cluster();
     const int C = static_cast<int>(cluster.num_blocks());
     const int rank = static_cast<int>(cluster.block_rank());
@@ -289,6 +291,20 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkArgs a) {
 
 template <int PER>
 int launch_per(const TopkArgs& a, int C, int64_t clusters, cudaStream_t stream) {
+    static std::mutex mu;
+    static std::vector<char> ready;
+    {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return IX_ERR_CUDA;
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= static_cast<int>(ready.size())) ready.resize(dev + 1, 0);
+        if (!ready[dev]) {
+            if (cudaFuncSetAttribute(topk_kernel<PER>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+                return IX_ERR_CUDA;
+            ready[dev] = 1;
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * C));
     cfg.blockDim = dim3(kThreads);
@@ -347,7 +363,7 @@ extern "C" int ix_topk_to_global(const float* logits, int64_t ld, int64_t rows,
     a.out_local = out_local;
     a.out_global = out_global;
     a.slice = ld > 0 ? slice_of(C) : 4;
-    const int64_t max_clusters = static_cast<int64_t>(sms) * 2 / C;
+    const int64_t max_clusters = static_cast<int64_t>(sms) * 3 / C;
     const int64_t clusters = rows < max_clusters ? rows : max_clusters;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int per_needed = (a.slice + kThreads - 1) / kThreads;
