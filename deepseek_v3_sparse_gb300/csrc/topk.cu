@@ -15,6 +15,12 @@
 // and writes it into every CTA of the cluster.  Two barriers per pass.  The
 // ordered compaction needs one block scan (and, for C > 1, each CTA's count of
 // kept keys before its slice, exchanged the same way).  No global scratch.
+//
+// Short rows (ld <= 16384) with many rows: one WARP per row instead (no block
+// barriers; up to 64 rows in flight per SM).  The warp re-reads its row from
+// L2 once per pass with coalesced 128-byte loads, counts digits in a
+// warp-private shared-memory histogram of packed 16-bit counters, and writes
+// the ordered result with ballot/popc positions (coalesced stores).
 #include <cooperative_groups.h>
 
 #include <mutex>
@@ -289,6 +295,119 @@ __global__ void __launch_bounds__(kThreads, PER <= 8 ? 3 : (PER <= 16 ? 2 : 1))
     cluster.sync();  // no CTA leaves while another may still touch its shared memory
 }
 
+
+// ---------------------------------------------------------------------------
+// Short rows: one warp per row.
+// ---------------------------------------------------------------------------
+constexpr int kRowWarps = 8;          // warps (rows in flight) per CTA
+constexpr int kRowsMaxLd = 16384;     // packed 16-bit counters hold any count of such a row
+
+__device__ __forceinline__ void hist16_add(uint32_t* h, uint32_t digit) {
+    atomicAdd(h + (digit >> 1), 1u << ((digit & 1u) * 16u));
+}
+
+// One warp: find the digit (scanning from the top) that holds the k_rem-th
+// largest key among the packed 16-bit counts h[0, nb); zero h.  Lane 0 owns
+// the top range of nb/32 bins; words are read with a lane rotation.
+__device__ __forceinline__ void warp_pick16(uint32_t* h, int nb, int k_rem, int& digit,
+                                            int& above, int& cnt) {
+    const int lane = threadIdx.x & 31;
+    const int per = nb >> 5;        // bins per lane (64 or 32)
+    const int wper = per >> 1;      // words per lane
+    const int wbase = (nb - per * (lane + 1)) >> 1;
+    int sum = 0;
+    for (int i = 0; i < wper; ++i) {
+        const uint32_t x = h[wbase + ((i + lane) & (wper - 1))];
+        sum += static_cast<int>((x & 0xFFFFu) + (x >> 16));
+    }
+    int x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    const int ab = x - sum;  // keys in the bins above this lane's range
+    const bool mine = ab < k_rem && ab + sum >= k_rem;
+    int d = 0, a2 = 0, c2 = 0;
+    if (mine) {
+        int acc = ab;
+        for (int i = per - 1; i >= 0; --i) {
+            const int bin = 2 * wbase + i;
+            const int c = static_cast<int>((h[bin >> 1] >> ((bin & 1) * 16)) & 0xFFFFu);
+            if (acc + c >= k_rem) {
+                d = bin;
+                a2 = acc;
+                c2 = c;
+                break;
+            }
+            acc += c;
+        }
+    }
+    const unsigned who = __ballot_sync(0xffffffffu, mine);
+    const int src = who ? __ffs(who) - 1 : 0;
+    digit = __shfl_sync(0xffffffffu, d, src);
+    above = __shfl_sync(0xffffffffu, a2, src);
+    cnt = __shfl_sync(0xffffffffu, c2, src);
+    __syncwarp();
+    for (int i = 0; i < wper; ++i) h[wbase + ((i + lane) & (wper - 1))] = 0u;
+    __syncwarp();
+}
+
+__global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const TopkArgs a) {
+    __shared__ uint32_t hist_all[kRowWarps][kBins / 2];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    uint32_t* h = hist_all[w];
+    for (int i = lane; i < kBins / 2; i += 32) h[i] = 0u;
+    __syncwarp();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * kRowWarps + w; r < a.rows;
+         r += static_cast<int64_t>(gridDim.x) * kRowWarps) {
+        int64_t L64 = __ldg(a.row_len + r);
+        L64 = L64 < 0 ? 0 : (L64 > a.ld ? a.ld : L64);
+        const int L = static_cast<int>(L64);
+        const int b = __ldg(a.row_req + r);
+        if (L <= a.k) {
+            for (int i = lane; i < a.k; i += 32) emit(a, r, b, i, i < L ? i : -1);
+            continue;
+        }
+        const float* row = a.logits + r * a.ld;
+        uint32_t prefix = 0;
+        int shift = 32, k_rem = a.k;
+        bool done = false;
+        for (int p = 0; p < 3 && !done; ++p) {
+            const int nbits = p < 2 ? 11 : 10;
+            const int nb = 1 << nbits;
+            const int sh = shift - nbits;
+            for (int i = lane; i < L; i += 32) {
+                const uint32_t u = order_key(__ldg(row + i));
+                if (p == 0 || (u >> shift) == prefix) hist16_add(h, (u >> sh) & (nb - 1));
+            }
+            __syncwarp();
+            int digit, above, cnt;
+            warp_pick16(h, nb, k_rem, digit, above, cnt);
+            k_rem -= above;
+            prefix = (shift == 32 ? 0u : (prefix << nbits)) | static_cast<uint32_t>(digit);
+            shift = sh;
+            done = (cnt == k_rem);
+        }
+        // ordered compaction: keys above the threshold, then the first k_rem equal to it
+        int ngt = 0, neq = 0;
+        for (int base = 0; base < L; base += 32) {
+            const int i = base + lane;
+            const bool valid = i < L;
+            const uint32_t v = valid ? (order_key(__ldg(row + i)) >> shift) : 0u;
+            const bool g = valid && v > prefix, e = valid && v == prefix;
+            const unsigned mg = __ballot_sync(0xffffffffu, g), me = __ballot_sync(0xffffffffu, e);
+            const int eb = neq + __popc(me & lt);
+            const int pos = ngt + __popc(mg & lt) + min(eb, k_rem);
+            if ((g || (e && eb < k_rem)) && pos < a.k) emit(a, r, b, pos, i);
+            ngt += __popc(mg);
+            neq += __popc(me);
+            if (ngt + min(neq, k_rem) >= a.k) break;  // warp-uniform: all k written
+        }
+    }
+}
+
 template <int PER>
 int launch_per(const TopkArgs& a, int C, int64_t clusters, cudaStream_t stream) {
     static std::mutex mu;
@@ -366,6 +485,12 @@ extern "C" int ix_topk_to_global(const float* logits, int64_t ld, int64_t rows,
     const int64_t max_clusters = static_cast<int64_t>(sms) * 3 / C;
     const int64_t clusters = rows < max_clusters ? rows : max_clusters;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (ld <= kRowsMaxLd && rows >= 2 * static_cast<int64_t>(sms)) {
+        const int64_t want = (rows + kRowWarps - 1) / kRowWarps;
+        const int64_t cap = static_cast<int64_t>(sms) * 8;
+        topk_rows_kernel<<<static_cast<unsigned>(want < cap ? want : cap), kRowWarps * 32, 0, s>>>(a);
+        return launch_status();
+    }
     const int per_needed = (a.slice + kThreads - 1) / kThreads;
     if (per_needed <= 4) return launch_per<4>(a, C, clusters, s);
     if (per_needed <= 8) return launch_per<8>(a, C, clusters, s);

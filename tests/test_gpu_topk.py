@@ -50,7 +50,9 @@ def _exact(dsix, logits, row_len, k, bs=64, seed=0):
     assert bad.size == 0, f"rows {bad[:5]} differ"
 
 
-@pytest.mark.parametrize("ld,R", [(64, 5), (4096, 40), (8192, 300), (20000, 8), (131072, 4)])
+# (R >= 2 x SMs with ld <= 16384 runs one warp per row; the others run the cluster kernel)
+@pytest.mark.parametrize("ld,R", [(64, 5), (4096, 40), (8192, 300), (20000, 8), (131072, 4),
+                                  (64, 400), (8192, 640), (16384, 320)])
 def test_exact_on_oracle_like_logits(dsix, ld, R):
     rng = np.random.default_rng(ld)
     logits = (rng.standard_normal((R, ld)) * 3).astype(np.float32)
@@ -68,10 +70,11 @@ def test_exact_on_oracle_like_logits(dsix, ld, R):
     _exact(dsix, logits, row_len, k)
 
 
+@pytest.mark.parametrize("R", [12, 400])
 @pytest.mark.parametrize("k", [1, 7, 64, 2048, 5000])
-def test_exact_various_k(dsix, k):
+def test_exact_various_k(dsix, k, R):
     rng = np.random.default_rng(k)
-    R, ld = 12, 12000
+    ld = 12000
     logits = rng.integers(-50, 50, size=(R, ld)).astype(np.float32)  # heavy ties
     row_len = rng.integers(k, ld + 1, R).astype(np.int32)
     _exact(dsix, logits, row_len, k, seed=k)
@@ -87,12 +90,13 @@ def test_exact_all_equal_and_extremes(dsix):
     _exact(dsix, logits, np.full(R, ld, np.int32), k)
 
 
-def test_never_reads_past_row_len(dsix):
+@pytest.mark.parametrize("R", [3, 400])
+def test_never_reads_past_row_len(dsix, R):
     # NaNs after L must not influence the result
-    R, ld, k = 3, 8192, 100
+    ld, k = 8192, 100
     rng = np.random.default_rng(1)
     logits = rng.standard_normal((R, ld)).astype(np.float32)
-    row_len = np.array([5000, 150, 8000], np.int32)
+    row_len = np.resize(np.array([5000, 150, 8000], np.int32), R)
     clean = logits.copy()
     for r in range(R):
         logits[r, row_len[r]:] = np.nan
