@@ -301,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, PER <= 8 ? 3 : (PER <= 16 ? 2 : 1))
 // ---------------------------------------------------------------------------
 constexpr int kRowWarps = 8;          // warps (rows in flight) per CTA
 constexpr int kRowsMaxLd = 16384;     // packed 16-bit counters hold any count of such a row
+constexpr int kRowUnroll = 8;         // independent loads in flight per lane
 
 __device__ __forceinline__ void hist16_add(uint32_t* h, uint32_t digit) {
     atomicAdd(h + (digit >> 1), 1u << ((digit & 1u) * 16u));
@@ -378,9 +379,19 @@ __global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const TopkArg
             const int nbits = p < 2 ? 11 : 10;
             const int nb = 1 << nbits;
             const int sh = shift - nbits;
-            for (int i = lane; i < L; i += 32) {
-                const uint32_t u = order_key(__ldg(row + i));
-                if (p == 0 || (u >> shift) == prefix) hist16_add(h, (u >> sh) & (nb - 1));
+            for (int i0 = lane; i0 < L; i0 += 32 * kRowUnroll) {
+                float x[kRowUnroll];
+#pragma unroll
+                for (int j = 0; j < kRowUnroll; ++j) {
+                    const int i = i0 + 32 * j;
+                    x[j] = i < L ? __ldg(row + i) : 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < kRowUnroll; ++j) {
+                    const uint32_t u = order_key(x[j]);
+                    if (i0 + 32 * j < L && (p == 0 || (u >> shift) == prefix))
+                        hist16_add(h, (u >> sh) & (nb - 1));
+                }
             }
             __syncwarp();
             int digit, above, cnt;
@@ -392,18 +403,26 @@ __global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const TopkArg
         }
         // ordered compaction: keys above the threshold, then the first k_rem equal to it
         int ngt = 0, neq = 0;
-        for (int base = 0; base < L; base += 32) {
-            const int i = base + lane;
-            const bool valid = i < L;
-            const uint32_t v = valid ? (order_key(__ldg(row + i)) >> shift) : 0u;
-            const bool g = valid && v > prefix, e = valid && v == prefix;
-            const unsigned mg = __ballot_sync(0xffffffffu, g), me = __ballot_sync(0xffffffffu, e);
-            const int eb = neq + __popc(me & lt);
-            const int pos = ngt + __popc(mg & lt) + min(eb, k_rem);
-            if ((g || (e && eb < k_rem)) && pos < a.k) emit(a, r, b, pos, i);
-            ngt += __popc(mg);
-            neq += __popc(me);
-            if (ngt + min(neq, k_rem) >= a.k) break;  // warp-uniform: all k written
+        for (int b0 = 0; b0 < L && ngt + min(neq, k_rem) < a.k; b0 += 32 * kRowUnroll) {
+            float x[kRowUnroll];
+#pragma unroll
+            for (int j = 0; j < kRowUnroll; ++j) {
+                const int i = b0 + 32 * j + lane;
+                x[j] = i < L ? __ldg(row + i) : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < kRowUnroll; ++j) {
+                const int i = b0 + 32 * j + lane;
+                const bool valid = i < L;
+                const uint32_t v = order_key(x[j]) >> shift;
+                const bool g = valid && v > prefix, e = valid && v == prefix;
+                const unsigned mg = __ballot_sync(0xffffffffu, g), me = __ballot_sync(0xffffffffu, e);
+                const int eb = neq + __popc(me & lt);
+                const int pos = ngt + __popc(mg & lt) + min(eb, k_rem);
+                if ((g || (e && eb < k_rem)) && pos < a.k) emit(a, r, b, pos, i);
+                ngt += __popc(mg);
+                neq += __popc(me);
+            }
         }
     }
 }
