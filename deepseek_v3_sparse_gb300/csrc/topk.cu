@@ -269,16 +269,19 @@ __global__ void __launch_bounds__(kThreads, PER <= 8 ? 3 : (PER <= 16 ? 2 : 1))
         const int cstart = carry_gt + min(carry_eq, k_rem);
         const int cend = min(a.k, carry_gt + static_cast<int>(tot >> 16) +
                                       min(carry_eq + static_cast<int>(tot & 0xFFFFu), k_rem));
-        const bool staged = cend - cstart <= kStage;
+        const bool staged = cstart >= 0 && cend - cstart <= kStage;
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
             if (j < nv) {
                 const uint32_t v = key[j] >> shift;
                 const bool g = v > prefix, e = v == prefix;
                 const int pos = bg + min(be, k_rem);
-                if ((g || (e && be < k_rem)) && pos < a.k) {
-                    if (staged) stage[pos - cstart] = lo + mine + j;
-                    else emit(a, r, b, pos, lo + mine + j);
+                if ((g || (e && be < k_rem)) && pos >= 0 && pos < a.k) {
+                    if (staged) {
+                        if (pos >= cstart && pos - cstart < kStage) stage[pos - cstart] = lo + mine + j;
+                    } else {
+                        emit(a, r, b, pos, lo + mine + j);
+                    }
                 }
                 bg += g;
                 be += e;
@@ -286,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, PER <= 8 ? 3 : (PER <= 16 ? 2 : 1))
         }
         if (staged) {  // coalesced write-out with the remap
             __syncthreads();
-            for (int i = tid; i < cend - cstart; i += kThreads) emit(a, r, b, cstart + i, stage[i]);
+            for (int i = tid; i < cend - cstart; i += kThreads) emit(a, r, b, cstart + i, stage[i]);  // cstart >= 0, cend <= k
         }
         // res, scratch and counts are rewritten only after barriers that every
         // thread of the cluster reaches after its reads above
@@ -379,7 +382,9 @@ __global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const TopkArg
             const int nbits = p < 2 ? 11 : 10;
             const int nb = 1 << nbits;
             const int sh = shift - nbits;
-            for (int i0 = lane; i0 < L; i0 += 32 * kRowUnroll) {
+            // warp-uniform trip count: the collectives below need every lane
+            for (int b0 = 0; b0 < L; b0 += 32 * kRowUnroll) {
+                const int i0 = b0 + lane;
                 float x[kRowUnroll];
 #pragma unroll
                 for (int j = 0; j < kRowUnroll; ++j) {
@@ -428,7 +433,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const TopkArg
                 const unsigned mg = __ballot_sync(0xffffffffu, g), me = __ballot_sync(0xffffffffu, e);
                 const int eb = neq + __popc(me & lt);
                 const int pos = ngt + __popc(mg & lt) + min(eb, k_rem);
-                if ((g || (e && eb < k_rem)) && pos < a.k) emit(a, r, b, pos, i);
+                if ((g || (e && eb < k_rem)) && pos >= 0 && pos < a.k) emit(a, r, b, pos, i);
                 ngt += __popc(mg);
                 neq += __popc(me);
             }
