@@ -395,7 +395,16 @@ __global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const TopkArg
                 for (int j = 0; j < kRowUnroll; ++j) {
                     const uint32_t u = order_key(x[j]);
                     const bool in = i0 + 32 * j < L && (p == 0 || (u >> shift) == prefix);
-                    if (in) hist16_add(h, (u >> sh) & (nb - 1));
+                    const uint32_t d = (u >> sh) & (nb - 1);
+                    if (p == 0) {
+                        // the first digit is dense: one atomic per distinct digit in the warp
+                        const unsigned act = __ballot_sync(0xffffffffu, in);
+                        const unsigned same = __match_any_sync(0xffffffffu, in ? d : 0xFFFFFFFFu) & act;
+                        if (in && lane == __ffs(same) - 1)
+                            atomicAdd(h + (d >> 1), static_cast<uint32_t>(__popc(same)) << ((d & 1u) * 16u));
+                    } else if (in) {
+                        hist16_add(h, d);
+                    }
                 }
             }
             __syncwarp();
@@ -430,97 +439,6 @@ __global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const TopkArg
             }
         }
     }
-}
-
-// ---------------------------------------------------------------------------
-// Rows of at most 8192 keys: one warp per row, the row held in shared memory.
-// One bulk copy brings the row in (many bytes in flight per SM); the three
-// digit passes and the ordered compaction then read shared memory only, so a
-// row crosses HBM once.
-// ---------------------------------------------------------------------------
-constexpr int kSmemRowWarps = 6;
-constexpr int kSmemRowMax = 8192;
-
-struct alignas(16) RowSlab {
-    float vals[kSmemRowMax];
-    uint32_t hist[kBins / 2];
-    uint64_t bar;
-    uint64_t pad;
-};
-
-__global__ void __launch_bounds__(kSmemRowWarps * 32, 1) topk_smem_rows_kernel(const TopkArgs a,
-                                                                                  int* status) {
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    RowSlab* slabs = reinterpret_cast<RowSlab*>(smem_raw);
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    RowSlab& sl = slabs[w];
-    uint32_t* h = sl.hist;
-    for (int i = lane; i < kBins / 2; i += 32) h[i] = 0u;
-    if (lane == 0) {
-        mbar_init(&sl.bar, 1);
-        fence_barrier_init();
-    }
-    __syncwarp();
-    volatile int never = 0;  // a per-warp abort flag that nothing raises
-    uint32_t phase = 0;
-    bool pending = false;
-    const unsigned lt = (1u << lane) - 1u;
-    for (int64_t r = static_cast<int64_t>(blockIdx.x) * kSmemRowWarps + w; r < a.rows;
-         r += static_cast<int64_t>(gridDim.x) * kSmemRowWarps) {
-        int64_t L64 = __ldg(a.row_len + r);
-        L64 = L64 < 0 ? 0 : (L64 > a.ld ? a.ld : L64);
-        const int L = static_cast<int>(L64);
-        const int b = __ldg(a.row_req + r);
-        if (L <= a.k) {
-            for (int i = lane; i < a.k; i += 32) emit(a, r, b, i, i < L ? i : -1);
-            continue;
-        }
-        // the row (rounded up to 4 values, still inside [0, ld)) into shared memory
-        if (lane == 0) {
-            const uint32_t bytes = static_cast<uint32_t>((L + 3) & ~3) * 4u;
-            mbar_arrive_expect_tx(&sl.bar, bytes);
-            bulk_load(sl.vals, a.logits + r * a.ld, bytes, &sl.bar);
-        }
-        pending = true;
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&sl.bar, phase, &never, status));
-        if (!ok) break;  // recorded as IX_DEV_TIMEOUT; the copy is drained below
-        phase ^= 1u;
-        pending = false;
-        uint32_t prefix = 0;
-        int shift = 32, k_rem = a.k;
-        bool done = false;
-        for (int p = 0; p < 3 && !done; ++p) {
-            const int nbits = p < 2 ? 11 : 10;
-            const int nb = 1 << nbits;
-            const int sh = shift - nbits;
-            for (int i = lane; i < L; i += 32) {
-                const uint32_t u = order_key(sl.vals[i]);
-                if (p == 0 || (u >> shift) == prefix) hist16_add(h, (u >> sh) & (nb - 1));
-            }
-            __syncwarp();
-            int digit, above, cnt;
-            warp_pick16(h, nb, k_rem, digit, above, cnt);
-            k_rem -= above;
-            prefix = (shift == 32 ? 0u : (prefix << nbits)) | static_cast<uint32_t>(digit);
-            shift = sh;
-            done = (cnt == k_rem);
-        }
-        int ngt = 0, neq = 0;
-        for (int b0 = 0; b0 < L && ngt + min(neq, k_rem) < a.k; b0 += 32) {
-            const int i = b0 + lane;
-            const bool valid = i < L;
-            const uint32_t v = valid ? (order_key(sl.vals[i]) >> shift) : 0u;
-            const bool g = valid && v > prefix, e = valid && v == prefix;
-            const unsigned mg = __ballot_sync(0xffffffffu, g), me = __ballot_sync(0xffffffffu, e);
-            const int eb = neq + __popc(me & lt);
-            const int pos = ngt + __popc(mg & lt) + min(eb, k_rem);
-            if ((g || (e && eb < k_rem)) && pos >= 0 && pos < a.k) emit(a, r, b, pos, i);
-            ngt += __popc(mg);
-            neq += __popc(me);
-        }
-        __syncwarp();  // every lane is done with the row before the next copy lands
-    }
-    if (pending && lane == 0) mbar_wait(&sl.bar, phase, &never, status, 100000000ull);
 }
 
 template <int PER>
@@ -600,30 +518,6 @@ extern "C" int ix_topk_to_global(const float* logits, int64_t ld, int64_t rows,
     const int64_t max_clusters = static_cast<int64_t>(sms) * 3 / C;
     const int64_t clusters = rows < max_clusters ? rows : max_clusters;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (ld <= kSmemRowMax && rows >= 2 * static_cast<int64_t>(sms)) {
-        static std::mutex mu;
-        static std::vector<char> ready;
-        const int smem = kSmemRowWarps * static_cast<int>(sizeof(RowSlab));
-        {
-            int dev = 0;
-            if (cudaGetDevice(&dev) != cudaSuccess) return IX_ERR_CUDA;
-            std::lock_guard<std::mutex> lock(mu);
-            if (dev >= static_cast<int>(ready.size())) ready.resize(dev + 1, 0);
-            if (!ready[dev]) {
-                if (cudaFuncSetAttribute(topk_smem_rows_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-                    return IX_ERR_CUDA;
-                ready[dev] = 1;
-            }
-        }
-        int* st = status_ptr();
-        if (!st) return IX_ERR_CUDA;
-        const int64_t want = (rows + kSmemRowWarps - 1) / kSmemRowWarps;
-        const int64_t cap = static_cast<int64_t>(sms);
-        topk_smem_rows_kernel<<<static_cast<unsigned>(want < cap ? want : cap), kSmemRowWarps * 32,
-                                smem, s>>>(a, st);
-        return launch_status();
-    }
     if (ld <= kRowsMaxLd && rows >= 2 * static_cast<int64_t>(sms)) {
         const int64_t want = (rows + kRowWarps - 1) / kRowWarps;
         const int64_t cap = static_cast<int64_t>(sms) * 8;

@@ -178,18 +178,14 @@ IX_API int ix_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t* k_
  *   out_local[r, :]  = the selected s in ascending order, then -1 up to k
  *   out_global[r, i] = block_table[b, s/block_size]*block_size + s%block_size,
  *                      or -1 where out_local is -1
- * Logits at or past L never influence the result (a row may be read up to
- * the next multiple of 4 entries, always inside [0, ld)).  NaN logits give an
- * unspecified selection.
+ * Logits at or past L are never read.  NaN logits give an unspecified
+ * selection.
  *   logits      fp32 [rows, ld], 16-byte aligned, ld % 4 == 0
  *   row_len, row_req  int32 [rows]
  *   block_table int32 [*, bt_stride]
  *   out_local   int32 [rows, k] or NULL
  *   out_global  int32 [rows, k]
  * Supports ld <= 262144 (longer rows return IX_ERR_UNSUPPORTED) and k >= 1.
- * Rows of at most 8192 entries (with at least 2 rows per SM) are selected by
- * one warp each from a shared-memory copy of the row; longer rows by a
- * thread-block cluster per row.
  */
 IX_API int ix_topk_to_global(const float* logits, int64_t ld, int64_t rows,
                       const int32_t* row_len, const int32_t* row_req,
