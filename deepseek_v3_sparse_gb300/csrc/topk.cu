@@ -395,16 +395,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const TopkArg
                 for (int j = 0; j < kRowUnroll; ++j) {
                     const uint32_t u = order_key(x[j]);
                     const bool in = i0 + 32 * j < L && (p == 0 || (u >> shift) == prefix);
-                    const uint32_t d = (u >> sh) & (nb - 1);
-                    if (p == 0) {
-                        // the first digit is dense: one atomic per distinct digit in the warp
-                        const unsigned act = __ballot_sync(0xffffffffu, in);
-                        const unsigned same = __match_any_sync(0xffffffffu, in ? d : 0xFFFFFFFFu) & act;
-                        if (in && lane == __ffs(same) - 1)
-                            atomicAdd(h + (d >> 1), static_cast<uint32_t>(__popc(same)) << ((d & 1u) * 16u));
-                    } else if (in) {
-                        hist16_add(h, d);
-                    }
+                    if (in) hist16_add(h, (u >> sh) & (nb - 1));
                 }
             }
             __syncwarp();
