@@ -304,7 +304,8 @@ __global__ void __launch_bounds__(kThreads, PER <= 8 ? 3 : (PER <= 16 ? 2 : 1))
 // ---------------------------------------------------------------------------
 constexpr int kRowWarps = 8;          // warps (rows in flight) per CTA
 constexpr int kRowsMaxLd = 16384;     // packed 16-bit counters hold any count of such a row
-constexpr int kRowUnroll = 8;         // independent loads in flight per lane
+constexpr int kRowUnroll = 16;        // independent loads in flight per lane
+constexpr int kRowBtMax = 256;        // block-table entries staged per warp (16384 keys at bs 64)
 
 __device__ __forceinline__ void hist16_add(uint32_t* h, uint32_t digit) {
     atomicAdd(h + (digit >> 1), 1u << ((digit & 1u) * 16u));
@@ -357,10 +358,31 @@ __device__ __forceinline__ void warp_pick16(uint32_t* h, int nb, int k_rem, int&
     __syncwarp();
 }
 
+// Global slot of request-local index s from a block-table row staged in shared memory.
+__device__ __forceinline__ void emit_staged(const TopkArgs& a, int64_t r, const int32_t* btrow,
+                                            int pos, int s) {
+    int32_t g = -1;
+    if (s >= 0) {
+        int q, rem;
+        if (a.bs_shift >= 0) {
+            q = s >> a.bs_shift;
+            rem = s & (a.block_size - 1);
+        } else {
+            q = s / a.block_size;
+            rem = s % a.block_size;
+        }
+        g = static_cast<int32_t>(static_cast<int64_t>(btrow[q]) * a.block_size + rem);
+    }
+    if (a.out_local) a.out_local[r * a.k + pos] = s;
+    a.out_global[r * a.k + pos] = g;
+}
+
 __global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const TopkArgs a) {
     __shared__ uint32_t hist_all[kRowWarps][kBins / 2];
+    __shared__ int32_t bt_all[kRowWarps][kRowBtMax];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     uint32_t* h = hist_all[w];
+    int32_t* btrow = bt_all[w];
     for (int i = lane; i < kBins / 2; i += 32) h[i] = 0u;
     __syncwarp();
     const unsigned lt = (1u << lane) - 1u;
@@ -375,6 +397,15 @@ __global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const TopkArg
             continue;
         }
         const float* row = a.logits + r * a.ld;
+        // the request's block-table entries for [0, L), read once (coalesced)
+        const int nblk = (L + a.block_size - 1) / a.block_size;
+        const bool bt_staged = nblk <= kRowBtMax;
+        __syncwarp();  // the previous row's lanes are done with btrow
+        if (bt_staged) {
+            const int32_t* src = a.bt + static_cast<int64_t>(b) * a.bt_stride;
+            for (int i = lane; i < nblk; i += 32) btrow[i] = __ldg(src + i);
+        }
+        __syncwarp();
         uint32_t prefix = 0;
         int shift = 32, k_rem = a.k;
         bool done = false;
@@ -424,7 +455,10 @@ __global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const TopkArg
                 const unsigned mg = __ballot_sync(0xffffffffu, g), me = __ballot_sync(0xffffffffu, e);
                 const int eb = neq + __popc(me & lt);
                 const int pos = ngt + __popc(mg & lt) + min(eb, k_rem);
-                if ((g || (e && eb < k_rem)) && pos >= 0 && pos < a.k) emit(a, r, b, pos, i);
+                if ((g || (e && eb < k_rem)) && pos >= 0 && pos < a.k) {
+                if (bt_staged) emit_staged(a, r, btrow, pos, i);
+                else emit(a, r, b, pos, i);
+            }
                 ngt += __popc(mg);
                 neq += __popc(me);
             }
@@ -510,8 +544,22 @@ extern "C" int ix_topk_to_global(const float* logits, int64_t ld, int64_t rows,
     const int64_t clusters = rows < max_clusters ? rows : max_clusters;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (ld <= kRowsMaxLd && rows >= 2 * static_cast<int64_t>(sms)) {
+        static std::mutex mu;
+        static std::vector<char> ready;
+        {
+            int dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess) return IX_ERR_CUDA;
+            std::lock_guard<std::mutex> lock(mu);
+            if (dev >= static_cast<int>(ready.size())) ready.resize(dev + 1, 0);
+            if (!ready[dev]) {
+                if (cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+                    return IX_ERR_CUDA;
+                ready[dev] = 1;
+            }
+        }
         const int64_t want = (rows + kRowWarps - 1) / kRowWarps;
-        const int64_t cap = static_cast<int64_t>(sms) * 8;
+        const int64_t cap = static_cast<int64_t>(sms) * 6;
         topk_rows_kernel<<<static_cast<unsigned>(want < cap ? want : cap), kRowWarps * 32, 0, s>>>(a);
         return launch_status();
     }
