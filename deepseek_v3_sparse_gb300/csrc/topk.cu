@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const TopkArg
             const int nbits = p < 2 ? 11 : 10;
             const int nb = 1 << nbits;
             const int sh = shift - nbits;
-            // warp-uniform trip count: the collectives below need every lane
+            // warp-uniform trip count (the compaction's collectives need every lane)
             for (int b0 = 0; b0 < L; b0 += 32 * kRowUnroll) {
                 const int i0 = b0 + lane;
                 float x[kRowUnroll];
@@ -438,30 +438,59 @@ __global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const TopkArg
             done = (cnt == k_rem);
         }
         // ordered compaction: keys above the threshold, then the first k_rem equal to it
+        // ordered compaction; loads of the next 16 values per lane are in flight
+        // while the current ones are placed (row and outputs never alias)
+        const float* __restrict__ rrow = row;
+        int32_t* __restrict__ og = a.out_global + r * a.k;
+        int32_t* __restrict__ ol = a.out_local ? a.out_local + r * a.k : nullptr;
         int ngt = 0, neq = 0;
+        float x[kRowUnroll];
+#pragma unroll
+        for (int j = 0; j < kRowUnroll; ++j) {
+            const int i = 32 * j + lane;
+            x[j] = i < L ? __ldg(rrow + i) : 0.f;
+        }
         for (int b0 = 0; b0 < L && ngt + min(neq, k_rem) < a.k; b0 += 32 * kRowUnroll) {
-            float x[kRowUnroll];
+            float y[kRowUnroll];
 #pragma unroll
             for (int j = 0; j < kRowUnroll; ++j) {
-                const int i = b0 + 32 * j + lane;
-                x[j] = i < L ? __ldg(row + i) : 0.f;
+                const int i = b0 + 32 * (kRowUnroll + j) + lane;
+                y[j] = i < L ? __ldg(rrow + i) : 0.f;
             }
+            unsigned mg[kRowUnroll], me[kRowUnroll];
 #pragma unroll
             for (int j = 0; j < kRowUnroll; ++j) {
-                const int i = b0 + 32 * j + lane;
-                const bool valid = i < L;
+                const bool valid = b0 + 32 * j + lane < L;
                 const uint32_t v = order_key(x[j]) >> shift;
-                const bool g = valid && v > prefix, e = valid && v == prefix;
-                const unsigned mg = __ballot_sync(0xffffffffu, g), me = __ballot_sync(0xffffffffu, e);
-                const int eb = neq + __popc(me & lt);
-                const int pos = ngt + __popc(mg & lt) + min(eb, k_rem);
+                mg[j] = __ballot_sync(0xffffffffu, valid && v > prefix);
+                me[j] = __ballot_sync(0xffffffffu, valid && v == prefix);
+            }
+#pragma unroll
+            for (int j = 0; j < kRowUnroll; ++j) {
+                const int i = b0 + 32 * j + lane;
+                const bool g = (mg[j] >> lane) & 1u, e = (me[j] >> lane) & 1u;
+                const int eb = neq + __popc(me[j] & lt);
+                const int pos = ngt + __popc(mg[j] & lt) + min(eb, k_rem);
                 if ((g || (e && eb < k_rem)) && pos >= 0 && pos < a.k) {
-                if (bt_staged) emit_staged(a, r, btrow, pos, i);
-                else emit(a, r, b, pos, i);
+                    int32_t gs;
+                    if (bt_staged) {
+                        const int q = a.bs_shift >= 0 ? (i >> a.bs_shift) : i / a.block_size;
+                        const int rem = a.bs_shift >= 0 ? (i & (a.block_size - 1)) : i % a.block_size;
+                        gs = static_cast<int32_t>(static_cast<int64_t>(btrow[q]) * a.block_size + rem);
+                    } else {
+                        const int q = i / a.block_size;
+                        gs = static_cast<int32_t>(
+                            static_cast<int64_t>(__ldg(a.bt + static_cast<int64_t>(b) * a.bt_stride + q)) *
+                                a.block_size + i % a.block_size);
+                    }
+                    og[pos] = gs;
+                    if (ol) ol[pos] = i;
+                }
+                ngt += __popc(mg[j]);
+                neq += __popc(me[j]);
             }
-                ngt += __popc(mg);
-                neq += __popc(me);
-            }
+#pragma unroll
+            for (int j = 0; j < kRowUnroll; ++j) x[j] = y[j];
         }
     }
 }
