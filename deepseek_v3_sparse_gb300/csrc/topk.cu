@@ -300,198 +300,257 @@ __global__ void __launch_bounds__(kThreads, PER <= 8 ? 3 : (PER <= 16 ? 2 : 1))
 
 
 // ---------------------------------------------------------------------------
-// Short rows: one warp per row.
+// Short rows (ld <= 16384, many rows): one 256-thread CTA per row, no cluster.
+// Keys live in registers (PER consecutive keys per thread), so the row crosses
+// HBM once; each pass is a shared-memory histogram, then a block-wide digit
+// pick (up to 8 bins per thread, one block scan).  The request's block-table
+// row is staged in shared memory for the remap.
 // ---------------------------------------------------------------------------
-constexpr int kRowWarps = 8;          // warps (rows in flight) per CTA
-constexpr int kRowsMaxLd = 16384;     // packed 16-bit counters hold any count of such a row
-constexpr int kRowUnroll = 16;        // independent loads in flight per lane
-constexpr int kRowBtMax = 256;        // block-table entries staged per warp (16384 keys at bs 64)
+constexpr int kBlkThreads = 256;
+constexpr int kBlkWarps = kBlkThreads / 32;
+constexpr int kBlkMaxLd = 16384;
+constexpr int kBlkBt = 256;  // block-table entries staged (16384 keys at block size 64)
 
-__device__ __forceinline__ void hist16_add(uint32_t* h, uint32_t digit) {
-    atomicAdd(h + (digit >> 1), 1u << ((digit & 1u) * 16u));
-}
-
-// One warp: find the digit (scanning from the top) that holds the k_rem-th
-// largest key among the packed 16-bit counts h[0, nb); zero h.  Lane 0 owns
-// the top range of nb/32 bins; words are read with a lane rotation.
-__device__ __forceinline__ void warp_pick16(uint32_t* h, int nb, int k_rem, int& digit,
-                                            int& above, int& cnt) {
-    const int lane = threadIdx.x & 31;
-    const int per = nb >> 5;        // bins per lane (64 or 32)
-    const int wper = per >> 1;      // words per lane
-    const int wbase = (nb - per * (lane + 1)) >> 1;
-    int sum = 0;
-    for (int i = 0; i < wper; ++i) {
-        const uint32_t x = h[wbase + ((i + lane) & (wper - 1))];
-        sum += static_cast<int>((x & 0xFFFFu) + (x >> 16));
-    }
-    int x = sum;
+__device__ __forceinline__ uint32_t blk_scan_excl(uint32_t v, uint32_t* scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
-    const int ab = x - sum;  // keys in the bins above this lane's range
-    const bool mine = ab < k_rem && ab + sum >= k_rem;
-    int d = 0, a2 = 0, c2 = 0;
-    if (mine) {
-        int acc = ab;
-        for (int i = per - 1; i >= 0; --i) {
-            const int bin = 2 * wbase + i;
-            const int c = static_cast<int>((h[bin >> 1] >> ((bin & 1) * 16)) & 0xFFFFu);
-            if (acc + c >= k_rem) {
-                d = bin;
-                a2 = acc;
-                c2 = c;
-                break;
-            }
-            acc += c;
-        }
-    }
-    const unsigned who = __ballot_sync(0xffffffffu, mine);
-    const int src = who ? __ffs(who) - 1 : 0;
-    digit = __shfl_sync(0xffffffffu, d, src);
-    above = __shfl_sync(0xffffffffu, a2, src);
-    cnt = __shfl_sync(0xffffffffu, c2, src);
-    __syncwarp();
-    for (int i = 0; i < wper; ++i) h[wbase + ((i + lane) & (wper - 1))] = 0u;
-    __syncwarp();
+    if (lane == 31) scratch[warp] = x;
+    __syncthreads();
+    uint32_t before = 0;
+#pragma unroll
+    for (int i = 0; i < kBlkWarps; ++i) before += i < warp ? scratch[i] : 0u;
+    return before + x - v;
 }
 
-// Global slot of request-local index s from a block-table row staged in shared memory.
-__device__ __forceinline__ void emit_staged(const TopkArgs& a, int64_t r, const int32_t* btrow,
-                                            int pos, int s) {
-    int32_t g = -1;
-    if (s >= 0) {
-        int q, rem;
-        if (a.bs_shift >= 0) {
-            q = s >> a.bs_shift;
-            rem = s & (a.block_size - 1);
-        } else {
-            q = s / a.block_size;
-            rem = s % a.block_size;
-        }
-        g = static_cast<int32_t>(static_cast<int64_t>(btrow[q]) * a.block_size + rem);
-    }
-    if (a.out_local) a.out_local[r * a.k + pos] = s;
-    a.out_global[r * a.k + pos] = g;
+constexpr int kBlkStage = 2048;  // largest k whose winners are staged in shared memory
+
+// Remap of local key index s (< row length) through the request's block-table
+// row, read from shared memory when it was staged there.
+__device__ __forceinline__ int32_t remap_row(const TopkArgs& a, const int32_t* btrow, bool bt_staged, int b, int s) {
+    if (bt_staged && a.bs_shift >= 0)
+        return static_cast<int32_t>(static_cast<int64_t>(btrow[s >> a.bs_shift]) * a.block_size +
+                                    (s & (a.block_size - 1)));
+    const int64_t blk = __ldg(a.bt + static_cast<int64_t>(b) * a.bt_stride + s / a.block_size);
+    return static_cast<int32_t>(blk * a.block_size + s % a.block_size);
 }
 
-__global__ void __launch_bounds__(kRowWarps * 32) topk_rows_kernel(const TopkArgs a) {
-    __shared__ uint32_t hist_all[kRowWarps][kBins / 2];
-    __shared__ int32_t bt_all[kRowWarps][kRowBtMax];
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    uint32_t* h = hist_all[w];
-    int32_t* btrow = bt_all[w];
-    for (int i = lane; i < kBins / 2; i += 32) h[i] = 0u;
-    __syncwarp();
-    const unsigned lt = (1u << lane) - 1u;
-    for (int64_t r = static_cast<int64_t>(blockIdx.x) * kRowWarps + w; r < a.rows;
-         r += static_cast<int64_t>(gridDim.x) * kRowWarps) {
+template <int PER>
+struct BlkMask;  // one bit per key slot of a thread
+template <>
+struct BlkMask<32> {
+    using T = uint32_t;
+};
+template <>
+struct BlkMask<64> {
+    using T = unsigned long long;
+};
+__device__ __forceinline__ int mask_popc(uint32_t m) { return __popc(m); }
+__device__ __forceinline__ int mask_popc(unsigned long long m) { return __popcll(m); }
+__device__ __forceinline__ int mask_low(uint32_t m) { return __ffs(m) - 1; }
+__device__ __forceinline__ int mask_low(unsigned long long m) { return __ffsll(m) - 1; }
+
+// Slots past the row end hold key 0 and stay out of every histogram.  Key 0 is
+// below the key of every finite value and those slots come after every real
+// key in index order, so even when the threshold bin starts at 0 they are past
+// the k_rem equal keys that are taken.
+template <int PER>
+__global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 3 : 2) topk_block_kernel(const TopkArgs a) {
+    using mask_t = typename BlkMask<PER>::T;
+    __shared__ int hist[kBins];
+    __shared__ int32_t btrow[kBlkBt];
+    __shared__ uint32_t scratch[2][kBlkWarps];
+    __shared__ uint32_t mm[2][kBlkWarps];
+    __shared__ int res[4];
+    __shared__ int32_t stage[kBlkStage];
+    const int tid = threadIdx.x;
+    for (int i = tid; i < kBins; i += kBlkThreads) hist[i] = 0;
+    __syncthreads();
+    int sc = 0;  // alternates the scan scratch so back-to-back scans need no extra barrier
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
         int64_t L64 = __ldg(a.row_len + r);
         L64 = L64 < 0 ? 0 : (L64 > a.ld ? a.ld : L64);
         const int L = static_cast<int>(L64);
         const int b = __ldg(a.row_req + r);
         if (L <= a.k) {
-            for (int i = lane; i < a.k; i += 32) emit(a, r, b, i, i < L ? i : -1);
+            for (int i = tid; i < a.k; i += kBlkThreads) emit(a, r, b, i, i < L ? i : -1);
             continue;
         }
-        const float* row = a.logits + r * a.ld;
-        // the request's block-table entries for [0, L), read once (coalesced)
         const int nblk = (L + a.block_size - 1) / a.block_size;
-        const bool bt_staged = nblk <= kRowBtMax;
-        __syncwarp();  // the previous row's lanes are done with btrow
-        if (bt_staged) {
-            const int32_t* src = a.bt + static_cast<int64_t>(b) * a.bt_stride;
-            for (int i = lane; i < nblk; i += 32) btrow[i] = __ldg(src + i);
+        const bool bt_staged = nblk <= kBlkBt;
+        if (bt_staged)
+            for (int i = tid; i < nblk; i += kBlkThreads)
+                btrow[i] = __ldg(a.bt + static_cast<int64_t>(b) * a.bt_stride + i);
+        const int mine = tid * PER;
+        const int nv = max(0, min(PER, L - mine));
+        const float* src = a.logits + r * a.ld + mine;  // 16-byte aligned
+        uint32_t key[PER];
+        uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll
+        for (int j = 0; j < PER; j += 4) {
+            if (j + 4 <= nv) {
+                const float4 v = __ldg(reinterpret_cast<const float4*>(src + j));
+                key[j] = order_key(v.x);
+                key[j + 1] = order_key(v.y);
+                key[j + 2] = order_key(v.z);
+                key[j + 3] = order_key(v.w);
+                kmin = min(kmin, min(min(key[j], key[j + 1]), min(key[j + 2], key[j + 3])));
+                kmax = max(kmax, max(max(key[j], key[j + 1]), max(key[j + 2], key[j + 3])));
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    key[j + q] = 0u;
+                    if (j + q < nv) {
+                        key[j + q] = order_key(__ldg(src + j + q));
+                        kmin = min(kmin, key[j + q]);
+                        kmax = max(kmax, key[j + q]);
+                    }
+                }
+            }
         }
-        __syncwarp();
-        uint32_t prefix = 0;
-        int shift = 32, k_rem = a.k;
-        bool done = false;
-        for (int p = 0; p < 3 && !done; ++p) {
-            const int nbits = p < 2 ? 11 : 10;
+        // Bits every key of the row shares need no histogram.  A row of logits
+        // often spans one or two binades, so a first digit taken from the sign
+        // and exponent would send nearly every key to a few bins and serialise
+        // the shared-memory atomics; the digits start below the common prefix.
+        kmin = __reduce_min_sync(0xffffffffu, kmin);
+        kmax = __reduce_max_sync(0xffffffffu, kmax);
+        if ((tid & 31) == 0) {
+            mm[0][tid >> 5] = kmin;
+            mm[1][tid >> 5] = kmax;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kBlkWarps; ++i) {
+            kmin = min(kmin, mm[0][i]);
+            kmax = max(kmax, mm[1][i]);
+        }
+        int shift = 32 - __clz(kmin ^ kmax);  // bits below the common prefix; 0 when all keys are equal
+        uint32_t prefix = shift >= 32 ? 0u : (kmin >> shift);
+        int k_rem = a.k;
+        bool done = shift == 0;
+        for (int p = 0; !done; ++p) {
+            const int nbits = shift < 11 ? shift : 11;
             const int nb = 1 << nbits;
             const int sh = shift - nbits;
-            // warp-uniform trip count (the compaction's collectives need every lane)
-            for (int b0 = 0; b0 < L; b0 += 32 * kRowUnroll) {
-                const int i0 = b0 + lane;
-                float x[kRowUnroll];
+            if (p == 0) {
 #pragma unroll
-                for (int j = 0; j < kRowUnroll; ++j) {
-                    const int i = i0 + 32 * j;
-                    x[j] = i < L ? __ldg(row + i) : 0.f;
+                for (int j = 0; j < PER; j += 4) {
+                    if (j + 4 <= nv) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) atomicAdd(hist + ((key[j + q] >> sh) & (nb - 1)), 1);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (j + q < nv) atomicAdd(hist + ((key[j + q] >> sh) & (nb - 1)), 1);
+                    }
                 }
+            } else {
+                // few keys are left in the bin: a warp with none of them skips the atomic
 #pragma unroll
-                for (int j = 0; j < kRowUnroll; ++j) {
-                    const uint32_t u = order_key(x[j]);
-                    const bool in = i0 + 32 * j < L && (p == 0 || (u >> shift) == prefix);
-                    if (in) hist16_add(h, (u >> sh) & (nb - 1));
+                for (int j = 0; j < PER; ++j) {
+                    const bool m = j < nv && (key[j] >> shift) == prefix;
+                    if (__any_sync(0xffffffffu, m)) {
+                        if (m) atomicAdd(hist + ((key[j] >> sh) & (nb - 1)), 1);
+                    }
                 }
             }
-            __syncwarp();
-            int digit, above, cnt;
-            warp_pick16(h, nb, k_rem, digit, above, cnt);
-            k_rem -= above;
-            prefix = (shift == 32 ? 0u : (prefix << nbits)) | static_cast<uint32_t>(digit);
+            __syncthreads();
+            // Block-wide pick: thread t owns max(nb / 256, 1) consecutive bins
+            // counted from the top (thread 0 the highest); with fewer than 256
+            // bins the threads past nb own none.
+            const int per = nb >= kBlkThreads ? nb / kBlkThreads : 1;
+            const int base = nb - per * (tid + 1);
+            int c[8];
+            int sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                c[i] = (i < per && base + i >= 0) ? hist[base + i] : 0;
+                sum += c[i];
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i < per && base + i >= 0) hist[base + i] = 0;  // owner-only: no other thread reads these bins
+            const int above = static_cast<int>(blk_scan_excl(static_cast<uint32_t>(sum), scratch[sc]));
+            sc ^= 1;
+            if (above < k_rem && above + sum >= k_rem) {
+                int acc = above;
+#pragma unroll
+                for (int i = 7; i >= 0; --i) {
+                    const int cnt = c[i];
+                    if (i < per && base + i >= 0 && acc + cnt >= k_rem) {
+                        res[0] = base + i;
+                        res[1] = acc;
+                        res[2] = cnt;
+                        break;
+                    }
+                    acc += cnt;
+                }
+            }
+            __syncthreads();
+            k_rem -= res[1];
+            prefix = (shift >= 32 ? 0u : (prefix << nbits)) | static_cast<uint32_t>(res[0]);
             shift = sh;
-            done = (cnt == k_rem);
+            done = shift == 0 || res[2] == k_rem;
         }
-        // ordered compaction: keys above the threshold, then the first k_rem equal to it
-        // ordered compaction; loads of the next 16 values per lane are in flight
-        // while the current ones are placed (row and outputs never alias)
-        const float* __restrict__ rrow = row;
+        // Keys above the threshold bin are all taken; of the keys in it, the
+        // first k_rem in index order (all of them when the bin holds exactly k_rem).
+        const uint32_t thr_lo = prefix << shift;
+        const uint32_t thr_hi = thr_lo | ((1u << shift) - 1u);
+        mask_t gm = 0, em = 0;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            gm |= key[j] > thr_hi ? (mask_t(1) << j) : mask_t(0);
+            em |= key[j] >= thr_lo ? (mask_t(1) << j) : mask_t(0);
+        }
+        em &= ~gm;
+        const int pg = mask_popc(gm), pe = mask_popc(em);
+        const uint32_t ex = blk_scan_excl((static_cast<uint32_t>(pg) << 16) | static_cast<uint32_t>(pe),
+                                          scratch[sc]);  // both fields stay below 2^16
+        sc ^= 1;
+        const int bg = static_cast<int>(ex >> 16), be = static_cast<int>(ex & 0xFFFFu);
+        const int take = max(0, min(pe, k_rem - be));
+        mask_t sel = gm;
+        if (take == pe) {
+            sel |= em;
+        } else if (take > 0) {
+            mask_t rest = em;
+            for (int i = 0; i < take; ++i) rest &= rest - 1;
+            sel |= em ^ rest;
+        }
+        // The winners of one thread are consecutive positions, so lanes write
+        // far-apart runs; for k <= kBlkStage the local indices are placed in
+        // shared memory first and both outputs leave in coalesced order, with the
+        // remap done only for the k winners.
+        const bool staged = a.k <= kBlkStage;
         int32_t* __restrict__ og = a.out_global + r * a.k;
         int32_t* __restrict__ ol = a.out_local ? a.out_local + r * a.k : nullptr;
-        int ngt = 0, neq = 0;
-        float x[kRowUnroll];
-#pragma unroll
-        for (int j = 0; j < kRowUnroll; ++j) {
-            const int i = 32 * j + lane;
-            x[j] = i < L ? __ldg(rrow + i) : 0.f;
-        }
-        for (int b0 = 0; b0 < L && ngt + min(neq, k_rem) < a.k; b0 += 32 * kRowUnroll) {
-            float y[kRowUnroll];
-#pragma unroll
-            for (int j = 0; j < kRowUnroll; ++j) {
-                const int i = b0 + 32 * (kRowUnroll + j) + lane;
-                y[j] = i < L ? __ldg(rrow + i) : 0.f;
-            }
-            unsigned mg[kRowUnroll], me[kRowUnroll];
-#pragma unroll
-            for (int j = 0; j < kRowUnroll; ++j) {
-                const bool valid = b0 + 32 * j + lane < L;
-                const uint32_t v = order_key(x[j]) >> shift;
-                mg[j] = __ballot_sync(0xffffffffu, valid && v > prefix);
-                me[j] = __ballot_sync(0xffffffffu, valid && v == prefix);
-            }
-#pragma unroll
-            for (int j = 0; j < kRowUnroll; ++j) {
-                const int i = b0 + 32 * j + lane;
-                const bool g = (mg[j] >> lane) & 1u, e = (me[j] >> lane) & 1u;
-                const int eb = neq + __popc(me[j] & lt);
-                const int pos = ngt + __popc(mg[j] & lt) + min(eb, k_rem);
-                if ((g || (e && eb < k_rem)) && pos >= 0 && pos < a.k) {
-                    int32_t gs;
-                    if (bt_staged) {
-                        const int q = a.bs_shift >= 0 ? (i >> a.bs_shift) : i / a.block_size;
-                        const int rem = a.bs_shift >= 0 ? (i & (a.block_size - 1)) : i % a.block_size;
-                        gs = static_cast<int32_t>(static_cast<int64_t>(btrow[q]) * a.block_size + rem);
-                    } else {
-                        const int q = i / a.block_size;
-                        gs = static_cast<int32_t>(
-                            static_cast<int64_t>(__ldg(a.bt + static_cast<int64_t>(b) * a.bt_stride + q)) *
-                                a.block_size + i % a.block_size);
-                    }
-                    og[pos] = gs;
-                    if (ol) ol[pos] = i;
+        int pos = bg + min(be, k_rem);
+        while (sel) {
+            const int s = mine + mask_low(sel);
+            sel &= sel - 1;
+            if (pos >= 0 && pos < a.k) {
+                if (staged) {
+                    stage[pos] = s;
+                } else {
+                    og[pos] = remap_row(a, btrow, bt_staged, b, s);
+                    if (ol) ol[pos] = s;
                 }
-                ngt += __popc(mg[j]);
-                neq += __popc(me[j]);
             }
-#pragma unroll
-            for (int j = 0; j < kRowUnroll; ++j) x[j] = y[j];
+            ++pos;
         }
+        if (staged) {
+            __syncthreads();
+            for (int i = tid; i < a.k; i += kBlkThreads) {
+                const int s = stage[i];
+                og[i] = remap_row(a, btrow, bt_staged, b, s);
+                if (ol) ol[i] = s;
+            }
+        }
+        __syncthreads();  // btrow, mm, res and stage are rewritten by the next row
     }
 }
 
@@ -572,24 +631,13 @@ extern "C" int ix_topk_to_global(const float* logits, int64_t ld, int64_t rows,
     const int64_t max_clusters = static_cast<int64_t>(sms) * 3 / C;
     const int64_t clusters = rows < max_clusters ? rows : max_clusters;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (ld <= kRowsMaxLd && rows >= 2 * static_cast<int64_t>(sms)) {
-        static std::mutex mu;
-        static std::vector<char> ready;
-        {
-            int dev = 0;
-            if (cudaGetDevice(&dev) != cudaSuccess) return IX_ERR_CUDA;
-            std::lock_guard<std::mutex> lock(mu);
-            if (dev >= static_cast<int>(ready.size())) ready.resize(dev + 1, 0);
-            if (!ready[dev]) {
-                if (cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-                    return IX_ERR_CUDA;
-                ready[dev] = 1;
-            }
-        }
-        const int64_t want = (rows + kRowWarps - 1) / kRowWarps;
-        const int64_t cap = static_cast<int64_t>(sms) * 6;
-        topk_rows_kernel<<<static_cast<unsigned>(want < cap ? want : cap), kRowWarps * 32, 0, s>>>(a);
+    if (ld <= kBlkMaxLd && rows >= 2 * static_cast<int64_t>(sms)) {
+        const int64_t cap = static_cast<int64_t>(sms) * 3;
+        const unsigned grid = static_cast<unsigned>(rows < cap ? rows : cap);
+        if (ld <= kBlkThreads * 32)
+            topk_block_kernel<32><<<grid, kBlkThreads, 0, s>>>(a);
+        else
+            topk_block_kernel<64><<<grid, kBlkThreads, 0, s>>>(a);
         return launch_status();
     }
     const int per_needed = (a.slice + kThreads - 1) / kThreads;

@@ -50,7 +50,7 @@ def _exact(dsix, logits, row_len, k, bs=64, seed=0):
     assert bad.size == 0, f"rows {bad[:5]} differ"
 
 
-# (R >= 2 x SMs with ld <= 16384 runs one warp per row; the others run the cluster kernel)
+# (R >= 2 x SMs with ld <= 16384 runs one CTA per row with no cluster; the others run the cluster kernel)
 @pytest.mark.parametrize("ld,R", [(64, 5), (4096, 40), (8192, 300), (20000, 8), (131072, 4),
                                   (64, 400), (8192, 640), (16384, 320)])
 def test_exact_on_oracle_like_logits(dsix, ld, R):
@@ -105,3 +105,38 @@ def test_never_reads_past_row_len(dsix, R):
     loc, glb = _run(dsix, logits, row_len, rq, bt, k)
     rl, rg = oracle.topk_to_global(clean, row_len, rq, bt, 64, k)
     assert np.array_equal(loc, rl) and np.array_equal(glb, rg)
+
+
+@pytest.mark.parametrize("R", [12, 400])
+@pytest.mark.parametrize("kind", ["one_binade", "consecutive_floats", "two_values", "tiny_spread_ties"])
+def test_exact_narrow_ranges(dsix, kind, R):
+    # rows whose keys share many leading bits: the radix digits start below the
+    # common prefix, which must not change the selected set or its order
+    rng = np.random.default_rng(7)
+    ld, k = 8192, 2048
+    if kind == "one_binade":
+        logits = (8 + 8 * rng.random((R, ld))).astype(np.float32)
+    elif kind == "consecutive_floats":
+        base = np.arange(ld, dtype=np.int32) + np.float32(1.0).view(np.int32)
+        logits = np.stack([rng.permutation(base).view(np.float32) for _ in range(R)])
+    elif kind == "two_values":
+        logits = rng.choice(np.array([1.0, np.nextafter(np.float32(1), np.float32(2))], np.float32), (R, ld))
+    else:
+        logits = (np.float32(1000) + rng.integers(0, 20, (R, ld)).astype(np.float32) * np.float32(2 ** -16))
+    logits = logits.astype(np.float32)
+    row_len = rng.integers(k + 1, ld + 1, R).astype(np.int32)
+    row_len[0] = ld
+    _exact(dsix, logits, row_len, k, seed=3)
+
+
+@pytest.mark.parametrize("R", [12, 400])
+def test_exact_all_negative_ragged(dsix, R):
+    # every key below 2^31 (all logits negative): the common prefix and the
+    # threshold bin can start at 0, next to the slots past a ragged row end
+    rng = np.random.default_rng(11)
+    ld, k = 8192, 2048
+    logits = (-np.abs(rng.standard_normal((R, ld))) * 4 - 1).astype(np.float32)
+    logits[1::2] = -rng.integers(1, 4, (R // 2, ld)).astype(np.float32)  # three tied values
+    row_len = rng.integers(k + 1, ld + 1, R).astype(np.int32)
+    row_len[0] = ld
+    _exact(dsix, logits, row_len, k, seed=5)
