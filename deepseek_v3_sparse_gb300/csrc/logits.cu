@@ -15,17 +15,20 @@
 //       prefill: 8 query rows per group, two jobs of N = 256 (4 rows each) per
 //                tile; TMEM holds 2 job slots of 256 columns.  N = 256 keeps the
 //                single MMA-issuing thread at full tensor rate even while 16
-//                epilogue warps compete for its SMSP's issue slots.
+//                epilogue warps compete for its SMSP's issue slots.  All 16
+//                epilogue warps drain one slot while the MMAs fill the other.
 //     One job = 4 x tcgen05.mma.kind::f8f6f4 (K = 128 = 4 x 32), FP32 accumulators.
 //   * Warp 0 is the TMA producer: K tiles (128 B rows, 128-byte swizzle; a paged
 //     tile is two 64-key blocks, each one 3-D TMA box), the tile's fp32 key
 //     scales, and per group the Q operand (TMA) and head weights (bulk copy).
 //   * Warp 1 (one elected lane) issues the MMAs and commits to mbarriers.
 //   * Warps 2-17 are four epilogue warpgroups (decode: job j belongs to
-//     warpgroup j % 4; prefill: warpgroup w always takes rows 2w, 2w+1 of every
-//     group, i.e. half of the job in slot w / 2): tcgen05.ld of the accumulators, ReLU, head-weighted
-//     sum (packed f32x2 FMA; half of the ReLUs as a saturating multiply on the
-//     FMA pipe, half as FMNMX on the ALU pipe), key scale, masked store.
+//     warpgroup j % 4; prefill: warpgroup w takes row w of every job, i.e.
+//     rows w and 4 + w of every group): tcgen05.ld of the accumulators, ReLU,
+//     head-weighted sum (packed f32x2 FMA; half of the ReLUs as a saturating
+//     multiply on the FMA pipe, half as FMNMX on the ALU pipe), key scale,
+//     masked store.  A warp hands its slot back to the MMA warp as soon as its
+//     last TMEM load has landed, before the arithmetic on that chunk.
 //   * Work = the flattened list of (group, key-tile) units over all groups,
 //     split evenly across CTAs on the device from context_lens / ks,ke (no host
 //     sync, graph-capturable).  Each role walks the same unit sequence.
@@ -83,7 +86,8 @@ struct Cfg<false> {  // prefill over contiguous K
     static constexpr int kSlots = 2;
     static constexpr int kSlotCols = 256;
     static constexpr int kJobsPerTile = 2;   // job h covers rows 4h .. 4h + 3
-    static constexpr int kGroupsPerJob = 2;  // warpgroup w takes rows 2w, 2w + 1
+    static constexpr int kGroupsPerJob = 4;  // warpgroup w takes row 4h + w of job h
+    static_assert(kRows == 4 * kJobsPerTile && kGroupsPerJob == kEpiGroups, "one job row per warpgroup");
 };
 
 template <bool P>
@@ -94,7 +98,8 @@ struct Smem {
     static constexpr int kSc = kK + C::kStages * kTileBytes;         // key-scale ring
     static constexpr int kW = kSc + kScaleRing * kScaleStride * 4;   // 2 head-weight buffers
     static constexpr int kTiles = kW + 2 * C::kWFloats * 4;          // tiles per group
-    static constexpr int kBar = kTiles + kSmemGroups * 4;
+    static constexpr int kKbeg = kTiles + kSmemGroups * 4;            // first key of each group
+    static constexpr int kBar = kKbeg + kSmemGroups * 4;
     static constexpr int kNumBars = 2 * C::kStages + 4 + 2 * C::kSlots + 2 * kScaleRing + 1;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kScan = kMisc + 64;
@@ -284,12 +289,13 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
 // Head-weighted ReLU sums for this thread's key over R query rows: TMEM
 // columns [tbase + 64 r, +64) hold row r's 64 head scores, w[64 r + h] the
 // row's head weights.  The load of 32-column chunk c+1 overlaps the
-// arithmetic on chunk c.  Heads are taken in pairs: the even head's ReLU is an
-// FMNMX (ALU pipe), the odd head's a saturating multiply by 2^-25 (FMA pipe),
-// and one packed f32x2 FMA accumulates both; the odd-head lane is rescaled by
-// 2^25 (exactly) at the end.
-template <int R>
-__device__ __forceinline__ void head_sums(uint32_t tbase, const float* w, float (&out)[R]) {
+// arithmetic on chunk c; `release` runs once the last chunk is in registers
+// (the TMEM columns may then be overwritten).  Heads are taken in pairs: the
+// even head's ReLU is an FMNMX (ALU pipe), the odd head's a saturating
+// multiply by 2^-25 (FMA pipe), and one packed f32x2 FMA accumulates both; the
+// odd-head lane is rescaled by 2^25 (exactly) at the end.
+template <int R, class Release>
+__device__ __forceinline__ void head_sums(uint32_t tbase, const float* w, float (&out)[R], Release&& release) {
     uint32_t buf[2][32];
     uint64_t acc[R][2];
 #pragma unroll
@@ -312,7 +318,10 @@ __device__ __forceinline__ void head_sums(uint32_t tbase, const float* w, float 
             acc[r][0] = fma2(pack2(ww.x, ww.y), t01, acc[r][0]);
             acc[r][1] = fma2(pack2(ww.z, ww.w), t23, acc[r][1]);
         }
-        if (c + 1 < 2 * R) tmem_wait_ld(buf[(c + 1) & 1]);
+        if (c + 1 < 2 * R) {
+            tmem_wait_ld(buf[(c + 1) & 1]);
+            if (c + 2 == 2 * R) release();
+        }
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -337,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* sSc = reinterpret_cast<float*>(sm + S::kSc);
     float* sW = reinterpret_cast<float*>(sm + S::kW);
     int* s_tiles = reinterpret_cast<int*>(sm + S::kTiles);
+    int* s_kbeg = reinterpret_cast<int*>(sm + S::kKbeg);
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + S::kBar);
     uint64_t* empty = full + C::kStages;
     uint64_t* qw_full = empty + C::kStages;
@@ -387,8 +397,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = a.num_groups;
     int local = 0;
     for (int g = threadIdx.x; g < G; g += kThreads) {
-        const int n = group_tiles<P>(a, g, blockIdx.x == 0);
-        if (g < kSmemGroups) s_tiles[g] = n;
+        int kb, ke;
+        group_range<P>(a, g, kb, ke, blockIdx.x == 0);
+        const int n = ke > kb ? (ke - kb + kTile - 1) / kTile : 0;
+        if (g < kSmemGroups) {
+            s_tiles[g] = n;
+            s_kbeg[g] = kb;
+        }
         local += n;
     }
     int U;
@@ -415,6 +430,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = static_cast<uint32_t>(misc[0]);
     const int units = misc[4];
+    // key range of a group; prefill groups' first keys were kept in shared
+    // memory by the schedule (their end is not needed past it)
+    auto group_bounds = [&](int gg, int& kb, int& ke) {
+        if (!P && gg < kSmemGroups) {
+            kb = s_kbeg[gg];
+            ke = 0;
+        } else {
+            group_range<P>(a, gg, kb, ke, false);
+        }
+    };
 
     if (units > 0) {
         Cursor<P> cur;
@@ -432,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (cur.left > 0) {
                 const int g = cur.g;
                 if (new_group) {
-                    group_range<P>(a, g, kbeg, kend, false);
+                    group_bounds(g, kbeg, kend);
                     bt_base = -1;
                     const int qb = qi & 1;
                     if (!wait_warp(qw_empty + qb, ((qi >> 1) & 1) ^ 1, abort_flag, a.status)) break;
@@ -561,14 +586,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else {
             // ------------------------------------------------------------ epilogue
-            constexpr int kRowsPerJob = P ? NN : 2;
+            constexpr int kRowsPerJob = P ? NN : 1;              // rows of one job this warp sums
+            constexpr int kWarpRows = P ? NN : C::kJobsPerTile;  // rows of a group this warp stores
             const int wg = (warp - kFirstEpiWarp) >> 2;
             const int quad = warp & 3;
             const int m = quad * 32 + lane;  // tile row = TMEM lane
             const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
             int it = 0, qi = 0, job = 0;
             int kbeg = 0, kend = 0;
-            int rs0[kRowsPerJob], rs1[kRowsPerJob];  // visible key range of each row of a job
+            int rs0[kWarpRows], rs1[kWarpRows];  // visible key range of each row this warp stores
             bool new_group = true, have_group = false;
             while (cur.left > 0) {
                 const int g = cur.g;
@@ -580,42 +606,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!wait_warp(qw_full + (qi & 1), (qi >> 1) & 1, abort_flag, a.status)) break;
                     ++qi;
                     have_group = true;
-                    group_range<P>(a, g, kbeg, kend, false);
+                    group_bounds(g, kbeg, kend);
                     if constexpr (P) {
                         const int ctx = __ldg(a.context_lens + g);
 #pragma unroll
-                        for (int j = 0; j < kRowsPerJob; ++j) {
+                        for (int j = 0; j < kWarpRows; ++j) {
                             rs0[j] = 0;
                             rs1[j] = decode_row_len(a, ctx, j, false);
                         }
                     } else {
 #pragma unroll
-                        for (int i = 0; i < kRowsPerJob; ++i) {
-                            const int64_t r = static_cast<int64_t>(g) * C::kRows + wg * 2 + i;
-                            rs0[i] = 0;
-                            rs1[i] = 0;
-                            if (r < a.tq) prefill_row_range(a, r, rs0[i], rs1[i], false);
+                        for (int h = 0; h < kWarpRows; ++h) {
+                            const int64_t r = static_cast<int64_t>(g) * C::kRows + 4 * h + wg;
+                            rs0[h] = 0;
+                            rs1[h] = 0;
+                            if (r < a.tq) prefill_row_range(a, r, rs0[h], rs1[h], false);
                         }
                     }
                 }
-                const float* wbuf = sW + ((qi - 1) & 1) * C::kWFloats + (P ? 0 : wg * 2 * kHeads);
+                const float* wq = sW + ((qi - 1) & 1) * C::kWFloats;
+                const int s = kbeg + cur.t * kTile + m;  // key index
+                float ksc = 0.f;
+                if constexpr (!P) {
+                    // contiguous K: the scale comes straight from L2, issued before the waits
+                    ksc = __ldg(a.k_scale + min(static_cast<int64_t>(s), a.tk - 1));
+                }
                 bool ok = true;
 #pragma unroll
                 for (int h = 0; h < C::kJobsPerTile; ++h, ++job) {
-                    if (P ? ((job & 3) != wg) : ((job & 1) != (wg >> 1))) continue;
+                    if (P && (job & 3) != wg) continue;
                     const int slot = job % C::kSlots;
                     const int sci = it % kScaleRing;
-                    const int s = kbeg + cur.t * kTile + m;  // key index
-                    float ksc;
                     if constexpr (P) {
                         if (!wait_warp(sc_full + sci, (it / kScaleRing) & 1, abort_flag, a.status)) {
                             ok = false;
                             break;
                         }
                         ksc = sSc[sci * kScaleStride + m];
-                    } else {
-                        // contiguous K: the scale comes straight from L2, issued before the wait
-                        ksc = __ldg(a.k_scale + min(static_cast<int64_t>(s), a.tk - 1));
                     }
                     if (!wait_warp(acc_full + slot, (job / C::kSlots) & 1, abort_flag, a.status)) {
                         ok = false;
@@ -623,22 +650,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     float sums[kRowsPerJob];
-                    head_sums<kRowsPerJob>(lane_addr + slot * C::kSlotCols + (P ? 0 : (wg & 1) * 128),
-                                           wbuf, sums);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(acc_empty + slot);
-                        if (P) mbar_arrive(sc_empty + sci);
-                    }
+                    head_sums<kRowsPerJob>(lane_addr + slot * C::kSlotCols + (P ? 0 : wg * kHeads),
+                                           wq + (P ? 0 : (4 * h + wg) * kHeads), sums, [&] {
+                                               tc_fence_before();
+                                               __syncwarp();
+                                               if (lane == 0) {
+                                                   mbar_arrive(acc_empty + slot);
+                                                   if (P) mbar_arrive(sc_empty + sci);
+                                               }
+                                           });
+                    if constexpr (P) {
 #pragma unroll
-                    for (int i = 0; i < kRowsPerJob; ++i) {
-                        if (s >= rs0[i] && s < rs1[i]) {
-                            int64_t r;
-                            if constexpr (P) r = static_cast<int64_t>(g) * NN + i;
-                            else r = static_cast<int64_t>(g) * C::kRows + wg * 2 + i;
-                            a.logits[r * a.ld + (s - rs0[i])] = sums[i] * ksc;
-                        }
+                        for (int i = 0; i < kRowsPerJob; ++i)
+                            if (s >= rs0[i] && s < rs1[i])
+                                a.logits[(static_cast<int64_t>(g) * NN + i) * a.ld + (s - rs0[i])] = sums[i] * ksc;
+                    } else {
+                        if (s >= rs0[h] && s < rs1[h])
+                            a.logits[(static_cast<int64_t>(g) * C::kRows + 4 * h + wg) * a.ld + (s - rs0[h])] =
+                                sums[0] * ksc;
                     }
                 }
                 if (!ok) break;
