@@ -37,6 +37,47 @@ DECODE_BYTES_PER_KEY = 132        # 128 fp8 values + one fp32 scale
 PREFILL_FLOP_PER_PAIR = 2 * 64 * 128
 
 
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "traffic_mixed_long.txt")
+KERNEL_SOURCES = {
+    "mqa_logits": ("deepseek_v3_sparse_gb300/csrc/logits.cu", "deepseek_v3_sparse_gb300/csrc/common.cuh"),
+    "paged_mqa_logits": ("deepseek_v3_sparse_gb300/csrc/logits.cu", "deepseek_v3_sparse_gb300/csrc/common.cuh"),
+    "topk_decode": ("deepseek_v3_sparse_gb300/csrc/topk.cu", "deepseek_v3_sparse_gb300/csrc/common.cuh"),
+    "topk_prefill": ("deepseek_v3_sparse_gb300/csrc/topk.cu", "deepseek_v3_sparse_gb300/csrc/common.cuh"),
+}
+
+
+def measured_traffic(workload_name):
+    """DRAM bytes per launch from the committed ncu capture, per kernel, for the
+    kernels whose sources still hash to the captured build (others: None)."""
+    import hashlib
+    out = {}
+    if not os.path.exists(TRAFFIC_PROFILE):
+        return out
+    sources, kernels, wl = {}, {}, None
+    with open(TRAFFIC_PROFILE) as f:
+        for line in f:
+            t = line.split()
+            if not t or t[0].startswith("#"):
+                continue
+            if t[0] == "workload":
+                wl = t[1]
+            elif t[0] == "source":
+                sources[t[1]] = t[2]
+            elif t[0] == "kernel":
+                kv = dict(zip(t[2::2], t[3::2]))
+                kernels[t[1]] = int(kv["read"]) + int(kv["write"])
+    if wl != workload_name:
+        return out
+    def current(path):
+        with open(os.path.join(ROOT, path), "rb") as f:
+            return hashlib.sha256(f.read()).hexdigest()
+    for name, nbytes in kernels.items():
+        srcs = KERNEL_SOURCES.get(name, ())
+        if srcs and all(sources.get(src) == current(src) for src in srcs):
+            out[name] = nbytes
+    return out
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -73,6 +114,12 @@ def max_over_ranks(x: float, world: int) -> float:
     t = torch.tensor([x], dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(world: int, rows_per_step: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job rows per second: every rank runs the same per-rank workload
+    (weak scaling), and the elapsed time is the slowest rank's."""
+    return world * rows_per_step * steps / (elapsed_ms / 1e3)
 
 
 # ---------------------------------------------------------------------------
@@ -378,7 +425,7 @@ def main():
     wl, step = r["wl"], r["step"]
     pk, pk_kind = peaks()
     fp8_peak = 2.0 * pk["bf16_tflops"]
-    value = world * r["rows"] * args.steps / (elapsed / 1e3)
+    value = job_throughput(world, r["rows"], args.steps, elapsed)
     km = r["kern_ms"]
     pf_tflops = (r["pairs"] * PREFILL_FLOP_PER_PAIR / (km["mqa_logits"] / 1e3) / 1e12
                  if "mqa_logits" in km else None)
@@ -398,11 +445,15 @@ def main():
     for n in ("topk_decode", "topk_prefill"):
         if n in km:
             kernels[n] = {"ms": km[n]}
+    traffic = measured_traffic(workload_config(wl)["workload"])
+    for n, kd in kernels.items():
+        kd["traffic"] = traffic.get(n)
     dominant = max((n for n in ("mqa_logits", "paged_mqa_logits") if n in km), key=lambda n: km[n])
     kd = kernels[dominant]
     roofline = {"bound": "tensor" if dominant == "mqa_logits" else "hbm",
                 "kernel": dominant, "achieved": kd["achieved"], "peak": kd["peak"],
-                "unit": kd["unit"], "frac": kd["frac"], "traffic": None,
+                "unit": kd["unit"], "frac": kd["frac"], "traffic": kd["traffic"],
+                "traffic_unit": "bytes per launch (ncu dram read + write; null once the kernel changed)",
                 "peak_kind": (f"{pk_kind}: fp8 = 2 x cuBLAS bf16 burst {pk['bf16_tflops']} TFLOP/s"
                               if dominant == "mqa_logits" else f"{pk_kind} copy bandwidth")}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -413,7 +464,7 @@ def main():
             "config": {**workload_config(wl), "parallelism": f"replicas x{world}"},
             "roofline": roofline, "kernels": kernels,
             "prefill_tflops": pf_tflops, "decode_hbm_gbs": dec_gbs,
-            "e2e": {"value": world * r["rows"] * r["e2e_steps"] / (e2e_ms / 1e3), "unit": UNIT,
+            "e2e": {"value": job_throughput(world, r["rows"], r["e2e_steps"], e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
             "gpu_launches": step.kernels_per_step() * args.steps,
             "clocks": r["clocks"], "device_status": r["status"]}
