@@ -109,43 +109,47 @@ __device__ __forceinline__ uint32_t scan_excl(uint32_t v, uint32_t* scratch, uin
     return r;
 }
 
-// One warp: find the bin (scanning from the top) that holds the k_rem-th
-// largest key among the counts h[0, nb), write (digit, count above, count in
-// bin) to out, and zero h.  Lanes own contiguous bin ranges (lane 0 the top
-// one), read with a lane rotation so the reads do not collide on banks.
-__device__ __forceinline__ void warp_pick(int* h, int nb, int k_rem, int* out) {
-    const int lane = threadIdx.x & 31;
-    const int per = nb >> 5;
-    const int base = nb - per * (lane + 1);
+// Block-wide digit pick over histogram h of nb bins (a power of two <= 2048):
+// thread t owns max(nb / kThreads, 1) consecutive bins counted from the top
+// (thread 0 the highest), zeroes them after reading, and the thread whose
+// range holds the k_rem-th key writes {digit, keys above it, keys in it} to out.
+// Ends with a barrier.
+__device__ __forceinline__ void block_pick(int* h, int nb, int k_rem, int* out, uint32_t* scratch) {
+    constexpr int kMaxPer = kBins / kThreads;
+    const int tid = threadIdx.x;
+    const int per = nb >= kThreads ? nb / kThreads : 1;
+    const int base = nb - per * (tid + 1);  // negative: no bin for this thread (nb < kThreads)
+    int c[kMaxPer];
     int sum = 0;
-    for (int i = 0; i < per; ++i) sum += h[base + ((i + lane) & (per - 1))];
-    int x = sum;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+    for (int i = 0; i < kMaxPer; ++i) {
+        c[i] = (i < per && base + i >= 0) ? h[base + i] : 0;
+        sum += c[i];
     }
-    const int above = x - sum;  // keys in the bins above this lane's range
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i)
+        if (i < per && base + i >= 0) h[base + i] = 0;
+    uint32_t tot;
+    const int above = static_cast<int>(scan_excl(static_cast<uint32_t>(sum), scratch, &tot));
     if (above < k_rem && above + sum >= k_rem) {
         int acc = above;
-        for (int i = per - 1; i >= 0; --i) {
-            const int c = h[base + i];
-            if (acc + c >= k_rem) {
+#pragma unroll
+        for (int i = kMaxPer - 1; i >= 0; --i) {
+            if (i < per && base + i >= 0 && acc + c[i] >= k_rem) {
                 out[0] = base + i;
                 out[1] = acc;
-                out[2] = c;
+                out[2] = c[i];
                 break;
             }
-            acc += c;
+            acc += c[i];
         }
     }
-    __syncwarp();
-    for (int i = 0; i < per; ++i) h[base + ((i + lane) & (per - 1))] = 0;
+    __syncthreads();
 }
 
 // Short slices keep several CTAs per SM resident to hide the per-row phase latency.
 template <int PER>
-__global__ void __launch_bounds__(kThreads, PER <= 8 ? 3 : (PER <= 16 ? 2 : 1))
+__global__ void __launch_bounds__(kThreads, PER <= 4 ? 3 : (PER <= 16 ? 2 : 1))
     topk_kernel(const TopkArgs a) {
     cg::cluster_group cluster = cg::this_cluster();
     const int C = static_cast<int>(cluster.num_blocks());
@@ -158,6 +162,8 @@ __global__ void __launch_bounds__(kThreads, PER <= 8 ? 3 : (PER <= 16 ? 2 : 1))
     __shared__ int res[4];                   // digit, count above, count in bin
     __shared__ uint32_t scratch[72];
     __shared__ int stage[kStage];            // this CTA's kept indices, in output order
+    __shared__ uint32_t mmx[2 * (kThreads / 32)];  // per-warp key min / max
+    __shared__ uint32_t cmm[2 * kMaxCluster];      // per-CTA key min / max (rank 0's copy is read)
 
     for (int i = tid; i < kBins; i += kThreads) {
         hist[i] = 0;
@@ -166,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, PER <= 8 ? 3 : (PER <= 16 ? 2 : 1))
     cluster.sync();
     int* merged0 = cluster.map_shared_rank(merged, 0);
     int* counts0 = cluster.map_shared_rank(counts, 0);
+    uint32_t* cmm0 = cluster.map_shared_rank(cmm, 0);
 
     const int64_t cid = blockIdx.x / C;
     const int64_t nclusters = gridDim.x / C;
@@ -185,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, PER <= 8 ? 3 : (PER <= 16 ? 2 : 1))
         const int nv = max(0, min(PER, n - mine));         // valid keys of this thread
         const float* src = a.logits + r * a.ld + lo + mine;  // 16-byte aligned
         uint32_t key[PER];
+        uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
 #pragma unroll
         for (int j = 0; j < PER; j += 4) {
             if (j + 4 <= nv) {
@@ -193,18 +201,57 @@ __global__ void __launch_bounds__(kThreads, PER <= 8 ? 3 : (PER <= 16 ? 2 : 1))
                 key[j + 1] = order_key(v.y);
                 key[j + 2] = order_key(v.z);
                 key[j + 3] = order_key(v.w);
+                kmin = min(kmin, min(min(key[j], key[j + 1]), min(key[j + 2], key[j + 3])));
+                kmax = max(kmax, max(max(key[j], key[j + 1]), max(key[j + 2], key[j + 3])));
             } else {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    key[j + q] = j + q < nv ? order_key(__ldg(src + j + q)) : 0u;
+                for (int q = 0; q < 4; ++q) {
+                    key[j + q] = 0u;
+                    if (j + q < nv) {
+                        key[j + q] = order_key(__ldg(src + j + q));
+                        kmin = min(kmin, key[j + q]);
+                        kmax = max(kmax, key[j + q]);
+                    }
+                }
             }
         }
-
-        uint32_t prefix = 0;
-        int shift = 32, k_rem = a.k;
-        bool done = false;
-        for (int p = 0; p < 3 && !done; ++p) {
-            const int nbits = p < 2 ? 11 : 10;
+        // Bits every key of the row shares need no histogram (a row of logits
+        // often spans one or two binades): the digits start below them.  Key
+        // min / max over the row: warps, then CTAs through rank 0.
+        kmin = __reduce_min_sync(0xffffffffu, kmin);
+        kmax = __reduce_max_sync(0xffffffffu, kmax);
+        if ((tid & 31) == 0) {
+            mmx[2 * warp] = kmin;
+            mmx[2 * warp + 1] = kmax;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            for (int i = 1; i < kThreads / 32; ++i) {
+                kmin = min(kmin, mmx[2 * i]);
+                kmax = max(kmax, mmx[2 * i + 1]);
+            }
+            cmm0[2 * rank] = kmin;
+            cmm0[2 * rank + 1] = kmax;
+        }
+        if (C > 1)
+            cluster.sync();
+        else
+            __syncthreads();
+        kmin = cmm0[0];
+        kmax = cmm0[1];
+#pragma unroll
+        for (int i = 1; i < kMaxCluster; ++i) {  // unrolled: the remote loads go out together
+            if (i < C) {
+                kmin = min(kmin, cmm0[2 * i]);
+                kmax = max(kmax, cmm0[2 * i + 1]);
+            }
+        }
+        int shift = 32 - __clz(kmin ^ kmax);  // bits below the common prefix; 0 when all keys are equal
+        uint32_t prefix = shift >= 32 ? 0u : (kmin >> shift);
+        int k_rem = a.k;
+        bool done = shift == 0;
+        for (int p = 0; !done; ++p) {
+            const int nbits = shift < 11 ? shift : 11;
             const int nb = 1 << nbits;
             const int sh = shift - nbits;
 #pragma unroll
@@ -212,31 +259,30 @@ __global__ void __launch_bounds__(kThreads, PER <= 8 ? 3 : (PER <= 16 ? 2 : 1))
                 if (j < nv && (p == 0 || (key[j] >> shift) == prefix))
                     atomicAdd(hist + ((key[j] >> sh) & (nb - 1)), 1);
             }
-            __syncthreads();
             if (C > 1) {
-                for (int i = tid; i < nb; i += kThreads) {
-                    const int c = hist[i];
-                    if (c) {
-                        atomicAdd(merged0 + i, c);
-                        hist[i] = 0;
-                    }
+                cluster.sync();  // every CTA's histogram of this pass is complete
+                // distributed merge: each bin is summed by one thread of the cluster
+                for (int i = rank * kThreads + tid; i < nb; i += C * kThreads) {
+                    int sum = 0;
+                    for (int j = 0; j < C; ++j) sum += cluster.map_shared_rank(hist, j)[i];
+                    merged0[i] = sum;
                 }
-                cluster.sync();
-                if (rank == 0 && warp == 0) {
-                    warp_pick(merged, nb, k_rem, res);
-                    __syncwarp();
+                cluster.sync();  // merged bins complete; no CTA reads another's histogram now
+                for (int i = tid; i < nb; i += kThreads) hist[i] = 0;
+                if (rank == 0) {
+                    block_pick(merged, nb, k_rem, res, scratch);
                     if (tid < 3)
                         for (int j = 1; j < C; ++j) cluster.map_shared_rank(res, j)[tid] = res[tid];
                 }
                 cluster.sync();
             } else {
-                if (warp == 0) warp_pick(hist, nb, k_rem, res);
                 __syncthreads();
+                block_pick(hist, nb, k_rem, res, scratch);
             }
             k_rem -= res[1];
-            prefix = (shift == 32 ? 0u : (prefix << nbits)) | static_cast<uint32_t>(res[0]);
+            prefix = (shift >= 32 ? 0u : (prefix << nbits)) | static_cast<uint32_t>(res[0]);
             shift = sh;
-            done = (res[2] == k_rem);  // every key of this digit is kept
+            done = shift == 0 || res[2] == k_rem;  // every key of this digit is kept
         }
         // kept: keys with (u >> shift) > prefix, and the first k_rem equal to it
         uint32_t gt = 0, eq = 0;
@@ -359,7 +405,7 @@ __device__ __forceinline__ int mask_low(unsigned long long m) { return __ffsll(m
 // key in index order, so even when the threshold bin starts at 0 they are past
 // the k_rem equal keys that are taken.
 template <int PER>
-__global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 3 : 2) topk_block_kernel(const TopkArgs a) {
+__global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_kernel(const TopkArgs a) {
     using mask_t = typename BlkMask<PER>::T;
     __shared__ int hist[kBins];
     __shared__ int32_t btrow[kBlkBt];
@@ -555,21 +601,26 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 3 : 2) topk_block_ker
 }
 
 template <int PER>
-int launch_per(const TopkArgs& a, int C, int64_t clusters, cudaStream_t stream) {
+int cluster_setup() {  // the carve-out attribute, once per device
     static std::mutex mu;
     static std::vector<char> ready;
-    {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess) return IX_ERR_CUDA;
-        std::lock_guard<std::mutex> lock(mu);
-        if (dev >= static_cast<int>(ready.size())) ready.resize(dev + 1, 0);
-        if (!ready[dev]) {
-            if (cudaFuncSetAttribute(topk_kernel<PER>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-                return IX_ERR_CUDA;
-            ready[dev] = 1;
-        }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return IX_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= static_cast<int>(ready.size())) ready.resize(dev + 1, 0);
+    if (!ready[dev]) {
+        if (cudaFuncSetAttribute(topk_kernel<PER>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+            return IX_ERR_CUDA;
+        ready[dev] = 1;
     }
+    return IX_OK;
+}
+
+template <int PER>
+int launch_per(const TopkArgs& a, int C, int64_t clusters, cudaStream_t stream) {
+    const int st = cluster_setup<PER>();
+    if (st != IX_OK) return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * C));
     cfg.blockDim = dim3(kThreads);
@@ -632,7 +683,8 @@ extern "C" int ix_topk_to_global(const float* logits, int64_t ld, int64_t rows,
     const int64_t clusters = rows < max_clusters ? rows : max_clusters;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (ld <= kBlkMaxLd && rows >= 2 * static_cast<int64_t>(sms)) {
-        const int64_t cap = static_cast<int64_t>(sms) * 3;
+        // resident CTAs per SM: 4 at PER = 32 (registers bounded to 64), 2 at PER = 64
+        const int64_t cap = static_cast<int64_t>(sms) * (ld <= kBlkThreads * 32 ? 4 : 2);
         const unsigned grid = static_cast<unsigned>(rows < cap ? rows : cap);
         if (ld <= kBlkThreads * 32)
             topk_block_kernel<32><<<grid, kBlkThreads, 0, s>>>(a);
