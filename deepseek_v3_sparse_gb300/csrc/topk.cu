@@ -149,7 +149,7 @@ __device__ __forceinline__ void block_pick(int* h, int nb, int k_rem, int* out, 
 
 // Short slices keep several CTAs per SM resident to hide the per-row phase latency.
 template <int PER>
-__global__ void __launch_bounds__(kThreads, PER <= 4 ? 3 : (PER <= 16 ? 2 : 1))
+__global__ void __launch_bounds__(kThreads, PER <= 4 ? 3 : (PER <= 32 ? 2 : 1))
     topk_kernel(const TopkArgs a) {
     cg::cluster_group cluster = cg::this_cluster();
     const int C = static_cast<int>(cluster.num_blocks());
