@@ -356,6 +356,8 @@ constexpr int kBlkThreads = 256;
 constexpr int kBlkWarps = kBlkThreads / 32;
 constexpr int kBlkMaxLd = 16384;
 constexpr int kBlkBt = 256;  // block-table entries staged (16384 keys at block size 64)
+constexpr int kBlkBits = 12;  // radix digit width: 12 + 12 + 8 bits cover a 32-bit key
+constexpr int kBlkBins = 1 << kBlkBits;
 
 __device__ __forceinline__ uint32_t blk_scan_excl(uint32_t v, uint32_t* scratch) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -377,10 +379,10 @@ constexpr int kBlkStage = 2048;  // largest k whose winners are staged in shared
 
 // Remap of local key index s (< row length) through the request's block-table
 // row, read from shared memory when it was staged there.
+// btrow holds the staged entries already multiplied by the block size (low 32
+// bits, the same value the int64 product is narrowed to).
 __device__ __forceinline__ int32_t remap_row(const TopkArgs& a, const int32_t* btrow, bool bt_staged, int b, int s) {
-    if (bt_staged && a.bs_shift >= 0)
-        return static_cast<int32_t>(static_cast<int64_t>(btrow[s >> a.bs_shift]) * a.block_size +
-                                    (s & (a.block_size - 1)));
+    if (bt_staged && a.bs_shift >= 0) return btrow[s >> a.bs_shift] + (s & (a.block_size - 1));
     const int64_t blk = __ldg(a.bt + static_cast<int64_t>(b) * a.bt_stride + s / a.block_size);
     return static_cast<int32_t>(blk * a.block_size + s % a.block_size);
 }
@@ -407,14 +409,14 @@ __device__ __forceinline__ int mask_low(unsigned long long m) { return __ffsll(m
 template <int PER>
 __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_kernel(const TopkArgs a) {
     using mask_t = typename BlkMask<PER>::T;
-    __shared__ int hist[kBins];
+    __shared__ __align__(16) int hist[kBlkBins];
     __shared__ int32_t btrow[kBlkBt];
     __shared__ uint32_t scratch[2][kBlkWarps];
     __shared__ uint32_t mm[2][kBlkWarps];
     __shared__ int res[4];
-    __shared__ int32_t stage[kBlkStage];
+    __shared__ __align__(16) int32_t stage[kBlkStage];
     const int tid = threadIdx.x;
-    for (int i = tid; i < kBins; i += kBlkThreads) hist[i] = 0;
+    for (int i = tid; i < kBlkBins; i += kBlkThreads) hist[i] = 0;
     __syncthreads();
     int sc = 0;  // alternates the scan scratch so back-to-back scans need no extra barrier
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
@@ -428,9 +430,11 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
         }
         const int nblk = (L + a.block_size - 1) / a.block_size;
         const bool bt_staged = nblk <= kBlkBt;
-        if (bt_staged)
+        if (bt_staged && a.bs_shift >= 0)
             for (int i = tid; i < nblk; i += kBlkThreads)
-                btrow[i] = __ldg(a.bt + static_cast<int64_t>(b) * a.bt_stride + i);
+                btrow[i] = static_cast<int32_t>(
+                    static_cast<uint32_t>(__ldg(a.bt + static_cast<int64_t>(b) * a.bt_stride + i)) *
+                    static_cast<uint32_t>(a.block_size));
         const int mine = tid * PER;
         const int nv = max(0, min(PER, L - mine));
         const float* src = a.logits + r * a.ld + mine;  // 16-byte aligned
@@ -479,7 +483,7 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
         int k_rem = a.k;
         bool done = shift == 0;
         for (int p = 0; !done; ++p) {
-            const int nbits = shift < 11 ? shift : 11;
+            const int nbits = shift < kBlkBits ? shift : kBlkBits;
             const int nb = 1 << nbits;
             const int sh = shift - nbits;
             if (p == 0) {
@@ -506,28 +510,30 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
             }
             __syncthreads();
             // Block-wide pick: thread t owns max(nb / 256, 1) consecutive bins
-            // counted from the top (thread 0 the highest); with fewer than 256
-            // bins the threads past nb own none.
+            // counted from the top (thread 0 the highest; with fewer than 256
+            // bins the threads past nb own none).  Owners read their bins with
+            // 16-byte loads; the thread whose range holds the k_rem-th key walks
+            // its bins again, and every owner clears its bins before the barrier
+            // that publishes the digit.
             const int per = nb >= kBlkThreads ? nb / kBlkThreads : 1;
             const int base = nb - per * (tid + 1);
-            int c[8];
             int sum = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                c[i] = (i < per && base + i >= 0) ? hist[base + i] : 0;
-                sum += c[i];
+            if (per >= 4) {
+                const int4* h4 = reinterpret_cast<const int4*>(hist + base);  // base is a multiple of 4
+                for (int i = 0; i < per / 4; ++i) {
+                    const int4 v = h4[i];
+                    sum += (v.x + v.y) + (v.z + v.w);
+                }
+            } else if (base >= 0) {
+                for (int i = 0; i < per; ++i) sum += hist[base + i];
             }
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (i < per && base + i >= 0) hist[base + i] = 0;  // owner-only: no other thread reads these bins
             const int above = static_cast<int>(blk_scan_excl(static_cast<uint32_t>(sum), scratch[sc]));
             sc ^= 1;
             if (above < k_rem && above + sum >= k_rem) {
                 int acc = above;
-#pragma unroll
-                for (int i = 7; i >= 0; --i) {
-                    const int cnt = c[i];
-                    if (i < per && base + i >= 0 && acc + cnt >= k_rem) {
+                for (int i = per - 1; i >= 0; --i) {
+                    const int cnt = hist[base + i];
+                    if (acc + cnt >= k_rem) {
                         res[0] = base + i;
                         res[1] = acc;
                         res[2] = cnt;
@@ -535,6 +541,12 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
                     }
                     acc += cnt;
                 }
+            }
+            if (per >= 4) {
+                int4* h4 = reinterpret_cast<int4*>(hist + base);
+                for (int i = 0; i < per / 4; ++i) h4[i] = make_int4(0, 0, 0, 0);
+            } else if (base >= 0) {
+                for (int i = 0; i < per; ++i) hist[base + i] = 0;
             }
             __syncthreads();
             k_rem -= res[1];
@@ -590,10 +602,24 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
         }
         if (staged) {
             __syncthreads();
-            for (int i = tid; i < a.k; i += kBlkThreads) {
-                const int s = stage[i];
-                og[i] = remap_row(a, btrow, bt_staged, b, s);
-                if (ol) ol[i] = s;
+            // four outputs per thread and step, 16-byte stores when the rows allow
+            const bool vec = (a.k & 3) == 0 &&
+                             ((reinterpret_cast<uintptr_t>(a.out_global) |
+                               reinterpret_cast<uintptr_t>(a.out_local)) & 15u) == 0;
+            if (vec) {
+                for (int i = 4 * tid; i < a.k; i += 4 * kBlkThreads) {
+                    const int4 s4 = *reinterpret_cast<const int4*>(stage + i);
+                    *reinterpret_cast<int4*>(og + i) =
+                        make_int4(remap_row(a, btrow, bt_staged, b, s4.x), remap_row(a, btrow, bt_staged, b, s4.y),
+                                  remap_row(a, btrow, bt_staged, b, s4.z), remap_row(a, btrow, bt_staged, b, s4.w));
+                    if (ol) *reinterpret_cast<int4*>(ol + i) = s4;
+                }
+            } else {
+                for (int i = tid; i < a.k; i += kBlkThreads) {
+                    const int s = stage[i];
+                    og[i] = remap_row(a, btrow, bt_staged, b, s);
+                    if (ol) ol[i] = s;
+                }
             }
         }
         __syncthreads();  // btrow, mm, res and stage are rewritten by the next row

@@ -140,3 +140,14 @@ def test_exact_all_negative_ragged(dsix, R):
     row_len = rng.integers(k + 1, ld + 1, R).astype(np.int32)
     row_len[0] = ld
     _exact(dsix, logits, row_len, k, seed=5)
+
+
+@pytest.mark.parametrize("R", [12, 400])
+@pytest.mark.parametrize("bs", [16, 48])
+def test_exact_other_block_sizes(dsix, bs, R):
+    # the remap for a power-of-two block size other than 64, and for one that is not
+    rng = np.random.default_rng(bs)
+    ld, k = 8192, 2048
+    logits = (rng.standard_normal((R, ld)) * 2).astype(np.float32)
+    row_len = rng.integers(k + 1, ld + 1, R).astype(np.int32)
+    _exact(dsix, logits, row_len, k, bs=bs, seed=bs)
