@@ -19,8 +19,9 @@
 //                epilogue warps drain one slot while the MMAs fill the other.
 //     One job = 4 x tcgen05.mma.kind::f8f6f4 (K = 128 = 4 x 32), FP32 accumulators.
 //   * Warp 0 is the TMA producer: K tiles (128 B rows, 128-byte swizzle; a paged
-//     tile is two 64-key blocks, each one 3-D TMA box), the tile's fp32 key
-//     scales, and per group the Q operand (TMA) and head weights (bulk copy).
+//     tile is two 64-key blocks, each one 3-D TMA box) and per group the Q
+//     operand (TMA) and head weights (bulk copy).  The epilogue reads each key's
+//     fp32 scale itself (decode: from its cache block; prefill: from k_scale).
 //   * Warp 1 (one elected lane) issues the MMAs and commits to mbarriers.
 //   * Warps 2-17 are four epilogue warpgroups (decode: job j belongs to
 //     warpgroup j % 4; prefill: warpgroup w takes row w of every job, i.e.
@@ -56,9 +57,6 @@ constexpr int kThreads = 64 + kEpiGroups * 128;  // producer + MMA warps + 4 war
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kFirstEpiWarp = 2;
-constexpr int kScaleRing = 16;   // key-scale ring entries (one per tile in flight)
-constexpr int kScaleBox = 132;   // floats loaded per entry (128 + 4 for an aligned start)
-constexpr int kScaleStride = 160;  // floats between entries: TMA destinations need 128-byte alignment
 constexpr int kSmemGroups = 2048;
 constexpr int kTmemCols = 512;
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 100 ms
@@ -95,18 +93,17 @@ struct Smem {
     using C = Cfg<P>;
     static constexpr int kQ = 0;                                     // 2 Q buffers
     static constexpr int kK = kQ + 2 * C::kQBytes;                   // K stages
-    static constexpr int kSc = kK + C::kStages * kTileBytes;         // key-scale ring
-    static constexpr int kW = kSc + kScaleRing * kScaleStride * 4;   // 2 head-weight buffers
+    static constexpr int kW = kK + C::kStages * kTileBytes;          // 2 head-weight buffers
     static constexpr int kTiles = kW + 2 * C::kWFloats * 4;          // tiles per group
     static constexpr int kKbeg = kTiles + kSmemGroups * 4;            // first key of each group
     static constexpr int kBar = kKbeg + kSmemGroups * 4;
-    static constexpr int kNumBars = 2 * C::kStages + 4 + 2 * C::kSlots + 2 * kScaleRing + 1;
+    static constexpr int kNumBars = 2 * C::kStages + 4 + 2 * C::kSlots + 1;
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kScan = kMisc + 64;
     static constexpr int kTotal = kScan + 64 * 4;
     static constexpr int kAlloc = kTotal + 1024;  // slack for 1024-byte alignment
     static_assert(kAlloc <= 232448, "shared memory budget");
-    static_assert(kSc % 128 == 0 && (kScaleStride * 4) % 128 == 0, "TMA destinations: 128 B");
+    static_assert(kK % 1024 == 0 && C::kQBytes % 1024 == 0, "128-byte-swizzled TMA tiles: 1024 B");
     static_assert(kW % 16 == 0 && kBar % 8 == 0, "alignment");
 };
 
@@ -119,6 +116,7 @@ struct LogitsArgs {
     // decode
     const int32_t* context_lens;
     const int32_t* bt;
+    const uint8_t* cache;  // the paged cache (key scales are read from it directly)
     int64_t bt_stride;
     int next_n;
     int64_t num_blocks;
@@ -334,8 +332,8 @@ __device__ __forceinline__ void head_sums(uint32_t tbase, const float* w, float 
 
 template <bool P, int NN>
 __global__ void __launch_bounds__(kThreads, 1)
-    logits_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmS,
-                  const __grid_constant__ CUtensorMap tmQ, const LogitsArgs a) {
+    logits_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
+                  const LogitsArgs a) {
     using C = Cfg<P>;
     using S = Smem<P>;
     extern __shared__ uint8_t smem_raw[];
@@ -343,7 +341,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
     uint8_t* sQ = sm + S::kQ;
     uint8_t* sK = sm + S::kK;
-    float* sSc = reinterpret_cast<float*>(sm + S::kSc);
     float* sW = reinterpret_cast<float*>(sm + S::kW);
     int* s_tiles = reinterpret_cast<int*>(sm + S::kTiles);
     int* s_kbeg = reinterpret_cast<int*>(sm + S::kKbeg);
@@ -353,9 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* qw_empty = qw_full + 2;
     uint64_t* acc_full = qw_empty + 2;
     uint64_t* acc_empty = acc_full + C::kSlots;
-    uint64_t* sc_full = acc_empty + C::kSlots;
-    uint64_t* sc_empty = sc_full + kScaleRing;
-    uint64_t* mma_done = sc_empty + kScaleRing;
+    uint64_t* mma_done = acc_empty + C::kSlots;
     int* misc = reinterpret_cast<int*>(sm + S::kMisc);  // tmem base, abort, g0, t0, units
     int* scan = reinterpret_cast<int*>(sm + S::kScan);
     volatile int* abort_flag = misc + 1;
@@ -375,17 +370,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(acc_full + i, 1);
             mbar_init(acc_empty + i, 4 * C::kGroupsPerJob);
         }
-        for (int i = 0; i < kScaleRing; ++i) {
-            mbar_init(sc_full + i, 1);
-            mbar_init(sc_empty + i, 4 * C::kJobsPerTile * C::kGroupsPerJob);  // every reader warp
-        }
         mbar_init(mma_done, 1);
         fence_barrier_init();
         misc[1] = 0;
         misc[4] = 0;
         misc[5] = 0;  // never raised: the abort flag seen by drain waits
         prefetch_tmap(&tmK);
-        prefetch_tmap(&tmS);
         prefetch_tmap(&tmQ);
     }
     if (warp == kMmaWarp) {
@@ -484,12 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++qi;
                 }
                 const int stage = it % C::kStages;
-                const int sci = it % kScaleRing;
                 if (!wait_warp(empty + stage, ((it / C::kStages) & 1) ^ 1, abort_flag, a.status)) break;
-                if (P && !wait_warp(sc_empty + sci, ((it / kScaleRing) & 1) ^ 1, abort_flag, a.status))
-                    break;
                 uint8_t* kdst = sK + stage * kTileBytes;
-                float* sdst = sSc + sci * kScaleStride;
                 if constexpr (P) {
                     if (bt_base < 0 || cur.t - bt_base >= 16) {
                         bt_base = cur.t;
@@ -510,9 +496,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(full + stage, two ? kTileBytes : kTileBytes / 2);
                         tma_load_3d(kdst, &tmK, full + stage, 0, 0, blk0);
                         if (two) tma_load_3d(kdst + kTileBytes / 2, &tmK, full + stage, 0, 0, blk1);
-                        mbar_arrive_expect_tx(sc_full + sci, two ? 512 : 256);
-                        tma_load_2d(sdst, &tmS, sc_full + sci, 0, blk0);
-                        if (two) tma_load_2d(sdst + kBlk, &tmS, sc_full + sci, 0, blk1);
                     }
                 } else {
                     const int start = kbeg + cur.t * kTile;
@@ -528,9 +511,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 for (int i = max(0, it - C::kStages); i < it; ++i)
                     drain_wait(full + i % C::kStages, (i / C::kStages) & 1, misc + 5, a.status);
-                if (P)
-                    for (int i = max(0, it - kScaleRing); i < it; ++i)
-                        drain_wait(sc_full + i % kScaleRing, (i / kScaleRing) & 1, misc + 5, a.status);
                 for (int i = max(0, qi - 2); i < qi; ++i)
                     drain_wait(qw_full + (i & 1), (i >> 1) & 1, misc + 5, a.status);
             }
@@ -636,13 +616,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int h = 0; h < C::kJobsPerTile; ++h, ++job) {
                     if (P && (job & 3) != wg) continue;
                     const int slot = job % C::kSlots;
-                    const int sci = it % kScaleRing;
                     if constexpr (P) {
-                        if (!wait_warp(sc_full + sci, (it / kScaleRing) & 1, abort_flag, a.status)) {
-                            ok = false;
-                            break;
+                        // the key's scale straight from its cache block (a warp's 32 keys
+                        // share one block-table entry), issued before the accumulator wait
+                        // and used only at the store; invalid blocks read as scale 0 like
+                        // the zero-filled tile the producer loads for them
+                        ksc = 0.f;
+                        if (s < kend) {
+                            const int blk = __ldg(a.bt + static_cast<int64_t>(g) * a.bt_stride + (s >> 6));
+                            if (blk >= 0 && blk < a.num_blocks)
+                                ksc = __ldg(reinterpret_cast<const float*>(
+                                                a.cache + static_cast<int64_t>(blk) * (kBlk * (kDim + 4)) +
+                                                kBlk * kDim) +
+                                            (s & (kBlk - 1)));
                         }
-                        ksc = sSc[sci * kScaleStride + m];
                     }
                     if (!wait_warp(acc_full + slot, (job / C::kSlots) & 1, abort_flag, a.status)) {
                         ok = false;
@@ -656,7 +643,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                __syncwarp();
                                                if (lane == 0) {
                                                    mbar_arrive(acc_empty + slot);
-                                                   if (P) mbar_arrive(sc_empty + sci);
                                                }
                                            });
                     if constexpr (P) {
@@ -737,7 +723,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
 }
 
 template <bool P, int NN>
-int launch(const CUtensorMap& tmK, const CUtensorMap& tmS, const CUtensorMap& tmQ,
+int launch(const CUtensorMap& tmK, const CUtensorMap& tmQ,
            const LogitsArgs& a, int64_t rows, int clean, cudaStream_t stream) {
     static std::mutex mu;
     static std::vector<char> ready;
@@ -756,7 +742,7 @@ int launch(const CUtensorMap& tmK, const CUtensorMap& tmS, const CUtensorMap& tm
     const int sms = num_sms();
     if (sms <= 0) return IX_ERR_CUDA;
     if (a.num_groups > 0) {
-        logits_kernel<P, NN><<<sms, kThreads, Smem<P>::kAlloc, stream>>>(tmK, tmS, tmQ, a);
+        logits_kernel<P, NN><<<sms, kThreads, Smem<P>::kAlloc, stream>>>(tmK, tmQ, a);
         if (launch_status() != IX_OK) return IX_ERR_CUDA;
     }
     if (clean && rows > 0) {
@@ -789,21 +775,13 @@ extern "C" int ix_paged_mqa_logits(const uint8_t* q_fp8, const float* w, const u
         return IX_ERR_ALIGN;
     int* st = status_ptr();
     if (!st) return IX_ERR_CUDA;
-    CUtensorMap tmK, tmS, tmQ;
+    CUtensorMap tmK, tmQ;
     {
         const uint64_t dims[3] = {kDim, kBlk, static_cast<uint64_t>(num_blocks)};
         const uint64_t strides[2] = {kDim, kBlk * (kDim + 4)};
         const uint32_t box[3] = {kDim, kBlk, 1};
         if (!make_map(&tmK, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, cache, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_128B))
-            return IX_ERR_CUDA;
-    }
-    {
-        const uint64_t dims[2] = {kBlk, static_cast<uint64_t>(num_blocks)};
-        const uint64_t strides[1] = {kBlk * (kDim + 4)};
-        const uint32_t box[2] = {kBlk, 1};
-        if (!make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, cache + kBlk * kDim, dims, strides,
-                      box, CU_TENSOR_MAP_SWIZZLE_NONE))
             return IX_ERR_CUDA;
     }
     {
@@ -825,10 +803,11 @@ extern "C" int ix_paged_mqa_logits(const uint8_t* q_fp8, const float* w, const u
     a.bt_stride = bt_stride;
     a.next_n = next_n;
     a.num_blocks = num_blocks;
+    a.cache = cache;
     const int64_t rows = static_cast<int64_t>(batch) * next_n;
     cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
-    return next_n == 1 ? launch<true, 1>(tmK, tmS, tmQ, a, rows, clean_logits, st_)
-                       : launch<true, 2>(tmK, tmS, tmQ, a, rows, clean_logits, st_);
+    return next_n == 1 ? launch<true, 1>(tmK, tmQ, a, rows, clean_logits, st_)
+                       : launch<true, 2>(tmK, tmQ, a, rows, clean_logits, st_);
 }
 
 extern "C" int ix_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t* k_fp8,
@@ -858,7 +837,7 @@ extern "C" int ix_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t
     a.ke = ke;
     a.tq = tq;
     a.tk = tk;
-    CUtensorMap tmK{}, tmS{}, tmQ{};
+    CUtensorMap tmK{}, tmQ{};
     if (tk > 0) {
         {
             const uint64_t dims[2] = {kDim, static_cast<uint64_t>(tk)};
@@ -866,13 +845,6 @@ extern "C" int ix_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t
             const uint32_t box[2] = {kDim, kTile};
             if (!make_map(&tmK, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k_fp8, dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_128B))
-                return IX_ERR_CUDA;
-        }
-        {
-            const uint64_t dims[1] = {static_cast<uint64_t>(tk)};
-            const uint32_t box[1] = {kScaleBox};
-            if (!make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, k_scale, dims, nullptr, box,
-                          CU_TENSOR_MAP_SWIZZLE_NONE))
                 return IX_ERR_CUDA;
         }
         {
@@ -884,6 +856,6 @@ extern "C" int ix_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t
                 return IX_ERR_CUDA;
         }
     }
-    return launch<false, 1>(tmK, tmS, tmQ, a, tq, clean_logits,
+    return launch<false, 1>(tmK, tmQ, a, tq, clean_logits,
                             reinterpret_cast<cudaStream_t>(stream));
 }
