@@ -440,9 +440,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (warp == kProducerWarp) {
             // ------------------------------------------------------------ producer
+            // The whole warp walks the loop; one lane, elected once, issues the copies.
+            const bool leader = elect_one();
             int it = 0, qi = 0;
             int kbeg = 0, kend = 0;
-            int bt_base = -1, bt_val = -1;
+            // decode: lane l holds the block-table entry of block 2 * bt_base + l (16
+            // tiles); the next window of the group is loaded one window ahead
+            int bt_base = -1, bt_val = -1, bt_nxt = -1;
+            auto bt_fetch = [&](int gg, int t0) {
+                const int bi = 2 * t0 + lane;
+                return bi * kBlk < kend ? __ldg(a.bt + static_cast<int64_t>(gg) * a.bt_stride + bi) : -1;
+            };
             bool new_group = true;
             while (cur.left > 0) {
                 const int g = cur.g;
@@ -451,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bt_base = -1;
                     const int qb = qi & 1;
                     if (!wait_warp(qw_empty + qb, ((qi >> 1) & 1) ^ 1, abort_flag, a.status)) break;
-                    if (lane == 0) {
+                    if (leader) {
                         uint8_t* qdst = sQ + qb * C::kQBytes;
                         float* wdst = sW + qb * C::kWFloats;
                         if constexpr (P) {
@@ -478,11 +486,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* kdst = sK + stage * kTileBytes;
                 if constexpr (P) {
                     if (bt_base < 0 || cur.t - bt_base >= 16) {
+                        const int raw = (bt_base >= 0 && cur.t == bt_base + 16) ? bt_nxt : bt_fetch(g, cur.t);
                         bt_base = cur.t;
-                        const int bi = 2 * cur.t + lane;
+                        bt_nxt = bt_fetch(g, bt_base + 16);
                         bt_val = -1;
-                        if (bi * kBlk < kend) {
-                            bt_val = __ldg(a.bt + static_cast<int64_t>(g) * a.bt_stride + bi);
+                        if ((2 * bt_base + lane) * kBlk < kend) {
+                            bt_val = raw;
                             if (bt_val < 0 || bt_val >= a.num_blocks) {
                                 flag(a.status, IX_DEV_BAD_BLOCK);
                                 bt_val = static_cast<int>(a.num_blocks);  // out of the map: zero fill
@@ -492,14 +501,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int blk0 = __shfl_sync(0xffffffffu, bt_val, 2 * (cur.t - bt_base));
                     const int blk1 = __shfl_sync(0xffffffffu, bt_val, 2 * (cur.t - bt_base) + 1);
                     const bool two = (2 * cur.t + 1) * kBlk < kend;
-                    if (lane == 0) {
+                    if (leader) {
                         mbar_arrive_expect_tx(full + stage, two ? kTileBytes : kTileBytes / 2);
                         tma_load_3d(kdst, &tmK, full + stage, 0, 0, blk0);
                         if (two) tma_load_3d(kdst + kTileBytes / 2, &tmK, full + stage, 0, 0, blk1);
                     }
                 } else {
                     const int start = kbeg + cur.t * kTile;
-                    if (lane == 0) {
+                    if (leader) {
                         mbar_arrive_expect_tx(full + stage, kTileBytes);
                         tma_load_2d(kdst, &tmK, full + stage, 0, start);
                     }
@@ -516,53 +525,61 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else if (warp == kMmaWarp) {
             // ------------------------------------------------------------ MMA issuer
-            if (lane == 0) {
-                int it = 0, qi = 0, job = 0;
-                uint64_t qdesc = 0;
-                bool issued = false, new_group = true;
-                constexpr int kJobN = P ? kHeads * NN : kHeads * 4;
-                constexpr uint32_t idesc = idesc_e4m3_f32(kTile, kJobN);
-                // descriptors advance by (bytes >> 4) in the start-address field
-                const uint64_t a_desc0 = sdesc_k_sw128(smem_u32(sK));
-                while (cur.left > 0) {
-                    if (new_group) {
-                        const int qb = qi & 1;
-                        if (!mbar_wait(qw_full + qb, (qi >> 1) & 1, abort_flag, a.status)) break;
-                        qdesc = sdesc_k_sw128(smem_u32(sQ + qb * C::kQBytes));
-                        ++qi;
-                    }
-                    const int stage = it % C::kStages;
-                    if (!mbar_wait(full + stage, (it / C::kStages) & 1, abort_flag, a.status)) break;
-                    tc_fence_after();
-                    const uint64_t adesc = a_desc0 + static_cast<uint64_t>(stage * (kTileBytes >> 4));
-                    bool ok = true;
+            // The whole warp walks the loop and waits; one lane, elected once, issues
+            // every MMA and commit (a commit tracks the issuing thread's MMAs), so
+            // every operand stays warp-uniform.
+            const bool leader = elect_one();
+            int it = 0, qi = 0, job = 0;
+            uint64_t qdesc = 0;
+            bool issued = false, new_group = true;
+            constexpr int kJobN = P ? kHeads * NN : kHeads * 4;
+            constexpr uint32_t idesc = idesc_e4m3_f32(kTile, kJobN);
+            // descriptors advance by (bytes >> 4) in the start-address field
+            const uint64_t a_desc0 = sdesc_k_sw128(smem_u32(sK));
+            while (cur.left > 0) {
+                if (new_group) {
+                    const int qb = qi & 1;
+                    if (!wait_warp(qw_full + qb, (qi >> 1) & 1, abort_flag, a.status)) break;
+                    qdesc = sdesc_k_sw128(smem_u32(sQ + qb * C::kQBytes));
+                    ++qi;
+                }
+                const int stage = it % C::kStages;
+                if (!wait_warp(full + stage, (it / C::kStages) & 1, abort_flag, a.status)) break;
+                tc_fence_after();
+                const uint64_t adesc = a_desc0 + static_cast<uint64_t>(stage * (kTileBytes >> 4));
+                bool ok = true;
 #pragma unroll
-                    for (int h = 0; h < C::kJobsPerTile; ++h) {
-                        const int slot = job % C::kSlots;
-                        if (!mbar_wait(acc_empty + slot, ((job / C::kSlots) & 1) ^ 1, abort_flag,
-                                       a.status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t d = tmem_base + slot * C::kSlotCols;
-                        const uint64_t bdesc = qdesc + static_cast<uint64_t>(h * ((kJobN * kDim) >> 4));
+                for (int h = 0; h < C::kJobsPerTile; ++h) {
+                    const int slot = job % C::kSlots;
+                    if (!wait_warp(acc_empty + slot, ((job / C::kSlots) & 1) ^ 1, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + slot * C::kSlotCols;
+                    const uint64_t bdesc = qdesc + static_cast<uint64_t>(h * ((kJobN * kDim) >> 4));
+                    if (leader) {
 #pragma unroll
                         for (int kk = 0; kk < kDim / 32; ++kk)
                             mma_e4m3(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, kk > 0);
                         mma_commit(acc_full + slot);
-                        issued = true;
-                        ++job;
                     }
-                    if (!ok) break;
-                    mma_commit(empty + stage);
-                    ++it;
-                    new_group = cur.advance(a, s_tiles);
+                    __syncwarp();
+                    issued = true;
+                    ++job;
                 }
-                if (issued) {
+                if (!ok) break;
+                if (leader) mma_commit(empty + stage);
+                __syncwarp();
+                ++it;
+                new_group = cur.advance(a, s_tiles);
+            }
+            if (issued) {
+                if (leader) {
                     mma_commit(mma_done);
                     drain_wait(mma_done, 0, misc + 5, a.status);
                 }
+                __syncwarp();
             }
         } else {
             // ------------------------------------------------------------ epilogue
