@@ -284,6 +284,14 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
     return d;
 }
 
+// Final sum of two packed accumulators (even heads plain, odd heads scaled by 2^-25).
+__device__ __forceinline__ float combine_sums(uint64_t acc0, uint64_t acc1) {
+    float e0, o0, e1, o1;
+    unpack2(acc0, e0, o0);
+    unpack2(acc1, e1, o1);
+    return (e0 + e1) + (o0 + o1) * 0x1p25f;
+}
+
 // Head-weighted ReLU sums for this thread's key over R query rows: TMEM
 // columns [tbase + 64 r, +64) hold row r's 64 head scores, w[64 r + h] the
 // row's head weights.  The load of 32-column chunk c+1 overlaps the
@@ -328,6 +336,62 @@ __device__ __forceinline__ void head_sums(uint32_t tbase, const float* w, float 
         unpack2(acc[r][1], e1, o1);
         out[r] = (e0 + e1) + (o0 + o1) * 0x1p25f;
     }
+}
+
+// Prefill head sum of one query row for the 32 keys of a warp's TMEM lane
+// quadrant, read in the 16x256b shape: for each 16-lane half, thread t holds
+// keys t/4 and t/4 + 8 of the half for heads 8j + 2(t%4) + {0, 1}, j = 0..7.  A
+// thread therefore needs only 16 of the row's head weights (w2[j] = the packed
+// pair for repeat j), which stay in registers for a whole group.  Four chunks
+// of 32 columns, (half 0, heads 0-31), (half 0, heads 32-63), (half 1, ...),
+// each in flight while the previous one is summed; `release` runs once the last
+// chunk is in registers.  The four threads t%4 = 0..3 that hold a key's partial
+// sums combine them in a two-step reduce-scatter: thread t returns the total of
+// key (16 ((t%4) >> 1) + 8 ((t%4) & 1) + t/4) of the quadrant.
+template <class Release>
+__device__ __forceinline__ float head_sums_16x256b(uint32_t tbase, const uint64_t (&w2)[8], int tq,
+                                                   Release&& release) {
+    uint32_t buf[2][16];
+    float part[4];  // (half 0, key a), (half 0, key b), (half 1, key a), (half 1, key b)
+    uint64_t acc[2][2];
+    tmem_ld16x256b_x4(tbase, buf[0]);
+    tmem_wait_ld(buf[0]);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int half = c >> 1, cc = c & 1;
+        if (c + 1 < 4) {
+            const int nh = (c + 1) >> 1, ncc = (c + 1) & 1;
+            tmem_ld16x256b_x4(tbase + (static_cast<uint32_t>(16 * nh) << 16) + 32 * ncc, buf[(c + 1) & 1]);
+        }
+        if (cc == 0) acc[0][0] = acc[0][1] = acc[1][0] = acc[1][1] = 0ull;
+        const uint32_t* v = buf[c & 1];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint64_t wp = w2[4 * cc + j];
+            const uint64_t ta = pack2(fmaxf(__uint_as_float(v[4 * j]), 0.f), relu_scaled(__uint_as_float(v[4 * j + 1])));
+            const uint64_t tb =
+                pack2(fmaxf(__uint_as_float(v[4 * j + 2]), 0.f), relu_scaled(__uint_as_float(v[4 * j + 3])));
+            acc[0][j & 1] = fma2(wp, ta, acc[0][j & 1]);
+            acc[1][j & 1] = fma2(wp, tb, acc[1][j & 1]);
+        }
+        if (cc == 1) {
+            part[2 * half] = combine_sums(acc[0][0], acc[0][1]);
+            part[2 * half + 1] = combine_sums(acc[1][0], acc[1][1]);
+        }
+        if (c + 1 < 4) {
+            tmem_wait_ld(buf[(c + 1) & 1]);
+            if (c + 2 == 4) release();
+        }
+    }
+    // reduce-scatter over the 4 threads of a key: first across halves (lane ^ 2),
+    // then across keys a / b (lane ^ 1)
+    const bool hi = (tq & 2) != 0, odd = (tq & 1) != 0;
+    const float s0 = __shfl_xor_sync(0xffffffffu, hi ? part[0] : part[2], 2);
+    const float s1 = __shfl_xor_sync(0xffffffffu, hi ? part[1] : part[3], 2);
+    const float x0 = (hi ? part[2] : part[0]) + s0;
+    const float x1 = (hi ? part[3] : part[1]) + s1;
+    const float r = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
+    return (odd ? x1 : x0) + r;
 }
 
 template <bool P, int NN>
@@ -581,8 +645,75 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             }
+        } else if constexpr (!P) {
+            // ------------------------------------------------------------ prefill epilogue
+            // Warpgroup wg sums rows wg (job 0) and 4 + wg (job 1) of every group; the
+            // accumulators are read in the 16x256b shape (head_sums_16x256b), so each
+            // thread keeps the 16 head weights it needs of each of its two rows in
+            // registers for the whole group.
+            const int wg = (warp - kFirstEpiWarp) >> 2;
+            const int quad = warp & 3;
+            const int tq = lane & 3;
+            const int m = quad * 32 + 16 * (tq >> 1) + 8 * (tq & 1) + (lane >> 2);  // key this thread stores
+            const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+            int qi = 0, job = 0;
+            int kbeg = 0, kend = 0;
+            int rs0[2], rs1[2];  // visible key range of rows wg and 4 + wg
+            uint64_t w2[2][8];   // packed head-weight pairs of those rows
+            bool new_group = true, have_group = false;
+            while (cur.left > 0) {
+                const int g = cur.g;
+                if (new_group) {
+                    if (have_group) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(qw_empty + ((qi - 1) & 1));
+                    }
+                    if (!wait_warp(qw_full + (qi & 1), (qi >> 1) & 1, abort_flag, a.status)) break;
+                    have_group = true;
+                    group_bounds(g, kbeg, kend);
+                    const float* wq = sW + (qi & 1) * C::kWFloats;
+                    ++qi;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int64_t r = static_cast<int64_t>(g) * C::kRows + 4 * h + wg;
+                        rs0[h] = 0;
+                        rs1[h] = 0;
+                        if (r < a.tq) prefill_row_range(a, r, rs0[h], rs1[h], false);
+                        const float* wr = wq + (4 * h + wg) * kHeads + 2 * tq;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float2 wv = *reinterpret_cast<const float2*>(wr + 8 * j);
+                            w2[h][j] = pack2(wv.x, wv.y);
+                        }
+                    }
+                }
+                const int s = kbeg + cur.t * kTile + m;  // key index
+                // the scale comes straight from L2, issued before the waits
+                const float ksc = __ldg(a.k_scale + min(static_cast<int64_t>(s), a.tk - 1));
+                bool ok = true;
+#pragma unroll
+                for (int h = 0; h < C::kJobsPerTile; ++h, ++job) {
+                    const int slot = job % C::kSlots;
+                    if (!wait_warp(acc_full + slot, (job / C::kSlots) & 1, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const float sum =
+                        head_sums_16x256b(lane_addr + slot * C::kSlotCols + wg * kHeads, w2[h], tq, [&] {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(acc_empty + slot);
+                        });
+                    if (s >= rs0[h] && s < rs1[h])
+                        a.logits[(static_cast<int64_t>(g) * C::kRows + 4 * h + wg) * a.ld + (s - rs0[h])] =
+                            sum * ksc;
+                }
+                if (!ok) break;
+                new_group = cur.advance(a, s_tiles);
+            }
         } else {
-            // ------------------------------------------------------------ epilogue
+            // ------------------------------------------------------------ decode epilogue
             constexpr int kRowsPerJob = P ? NN : 1;              // rows of one job this warp sums
             constexpr int kWarpRows = P ? NN : C::kJobsPerTile;  // rows of a group this warp stores
             const int wg = (warp - kFirstEpiWarp) >> 2;
