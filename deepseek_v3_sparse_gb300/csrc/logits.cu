@@ -28,8 +28,17 @@
 //     rows w and 4 + w of every group): tcgen05.ld of the accumulators, ReLU,
 //     head-weighted sum (packed f32x2 FMA; half of the ReLUs as a saturating
 //     multiply on the FMA pipe, half as FMNMX on the ALU pipe), key scale,
-//     masked store.  A warp hands its slot back to the MMA warp as soon as its
-//     last TMEM load has landed, before the arithmetic on that chunk.
+//     masked store.  Prefill reads the accumulators in the 16x256b shape, in
+//     which a thread meets only 16 heads of a row (for two keys), so its head
+//     weights live in registers for the whole group and no shared-memory
+//     traffic competes with the MMA operand reads; a shuffle reduce-scatter
+//     finishes each key.  Decode (32x32b, one key per thread) reads its head
+//     weights from shared memory.  A warp hands its slot back to the MMA warp
+//     as soon as its last TMEM load has landed, before the arithmetic on that
+//     chunk.
+//   * The producer and MMA warps walk their loops converged and issue through
+//     one lane elected once: operands computed by the whole warp stay
+//     warp-uniform, which keeps the issue of a tile's four MMAs near 100 cycles.
 //   * Work = the flattened list of (group, key-tile) units over all groups,
 //     split evenly across CTAs on the device from context_lens / ks,ke (no host
 //     sync, graph-capturable).  Each role walks the same unit sequence.
@@ -714,15 +723,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else {
             // ------------------------------------------------------------ decode epilogue
-            constexpr int kRowsPerJob = P ? NN : 1;              // rows of one job this warp sums
-            constexpr int kWarpRows = P ? NN : C::kJobsPerTile;  // rows of a group this warp stores
+            // Job j (tile j of this CTA) belongs to warpgroup j % 4; each thread sums the
+            // next_n rows of its key.
             const int wg = (warp - kFirstEpiWarp) >> 2;
             const int quad = warp & 3;
             const int m = quad * 32 + lane;  // tile row = TMEM lane
             const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-            int it = 0, qi = 0, job = 0;
+            int qi = 0, job = 0;
             int kbeg = 0, kend = 0;
-            int rs0[kWarpRows], rs1[kWarpRows];  // visible key range of each row this warp stores
+            int rs1[NN];  // visible length of each row of the group
             bool new_group = true, have_group = false;
             while (cur.left > 0) {
                 const int g = cur.g;
@@ -735,77 +744,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++qi;
                     have_group = true;
                     group_bounds(g, kbeg, kend);
-                    if constexpr (P) {
-                        const int ctx = __ldg(a.context_lens + g);
+                    const int ctx = __ldg(a.context_lens + g);
 #pragma unroll
-                        for (int j = 0; j < kWarpRows; ++j) {
-                            rs0[j] = 0;
-                            rs1[j] = decode_row_len(a, ctx, j, false);
-                        }
-                    } else {
-#pragma unroll
-                        for (int h = 0; h < kWarpRows; ++h) {
-                            const int64_t r = static_cast<int64_t>(g) * C::kRows + 4 * h + wg;
-                            rs0[h] = 0;
-                            rs1[h] = 0;
-                            if (r < a.tq) prefill_row_range(a, r, rs0[h], rs1[h], false);
-                        }
-                    }
+                    for (int j = 0; j < NN; ++j) rs1[j] = decode_row_len(a, ctx, j, false);
                 }
                 const float* wq = sW + ((qi - 1) & 1) * C::kWFloats;
                 const int s = kbeg + cur.t * kTile + m;  // key index
-                float ksc = 0.f;
-                if constexpr (!P) {
-                    // contiguous K: the scale comes straight from L2, issued before the waits
-                    ksc = __ldg(a.k_scale + min(static_cast<int64_t>(s), a.tk - 1));
-                }
                 bool ok = true;
-#pragma unroll
-                for (int h = 0; h < C::kJobsPerTile; ++h, ++job) {
-                    if (P && (job & 3) != wg) continue;
+                if ((job & 3) == wg) {
                     const int slot = job % C::kSlots;
-                    if constexpr (P) {
-                        // the key's scale straight from its cache block (a warp's 32 keys
-                        // share one block-table entry), issued before the accumulator wait
-                        // and used only at the store; invalid blocks read as scale 0 like
-                        // the zero-filled tile the producer loads for them
-                        ksc = 0.f;
-                        if (s < kend) {
-                            const int blk = __ldg(a.bt + static_cast<int64_t>(g) * a.bt_stride + (s >> 6));
-                            if (blk >= 0 && blk < a.num_blocks)
-                                ksc = __ldg(reinterpret_cast<const float*>(
-                                                a.cache + static_cast<int64_t>(blk) * (kBlk * (kDim + 4)) +
-                                                kBlk * kDim) +
-                                            (s & (kBlk - 1)));
-                        }
+                    // the key's scale straight from its cache block (a warp's 32 keys share
+                    // one block-table entry), issued before the accumulator wait and used
+                    // only at the store; invalid blocks read as scale 0 like the
+                    // zero-filled tile the producer loads for them
+                    float ksc = 0.f;
+                    if (s < kend) {
+                        const int blk = __ldg(a.bt + static_cast<int64_t>(g) * a.bt_stride + (s >> 6));
+                        if (blk >= 0 && blk < a.num_blocks)
+                            ksc = __ldg(reinterpret_cast<const float*>(
+                                            a.cache + static_cast<int64_t>(blk) * (kBlk * (kDim + 4)) + kBlk * kDim) +
+                                        (s & (kBlk - 1)));
                     }
                     if (!wait_warp(acc_full + slot, (job / C::kSlots) & 1, abort_flag, a.status)) {
                         ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    float sums[kRowsPerJob];
-                    head_sums<kRowsPerJob>(lane_addr + slot * C::kSlotCols + (P ? 0 : wg * kHeads),
-                                           wq + (P ? 0 : (4 * h + wg) * kHeads), sums, [&] {
-                                               tc_fence_before();
-                                               __syncwarp();
-                                               if (lane == 0) {
-                                                   mbar_arrive(acc_empty + slot);
-                                               }
-                                           });
-                    if constexpr (P) {
-#pragma unroll
-                        for (int i = 0; i < kRowsPerJob; ++i)
-                            if (s >= rs0[i] && s < rs1[i])
-                                a.logits[(static_cast<int64_t>(g) * NN + i) * a.ld + (s - rs0[i])] = sums[i] * ksc;
                     } else {
-                        if (s >= rs0[h] && s < rs1[h])
-                            a.logits[(static_cast<int64_t>(g) * C::kRows + 4 * h + wg) * a.ld + (s - rs0[h])] =
-                                sums[0] * ksc;
+                        tc_fence_after();
+                        float sums[NN];
+                        head_sums<NN>(lane_addr + slot * C::kSlotCols, wq, sums, [&] {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(acc_empty + slot);
+                        });
+#pragma unroll
+                        for (int i = 0; i < NN; ++i)
+                            if (s < rs1[i]) a.logits[(static_cast<int64_t>(g) * NN + i) * a.ld + s] = sums[i] * ksc;
                     }
                 }
+                ++job;
                 if (!ok) break;
-                ++it;
                 new_group = cur.advance(a, s_tiles);
             }
         }
