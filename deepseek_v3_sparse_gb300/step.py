@@ -106,39 +106,39 @@ class IndexerStep:
 
     def run(self, stream=None, events=None):
         """One step.  ``events``: optional dict name -> (start, end) CUDA events
-        recorded around the logits launches on ``stream``."""
+        recorded around the logits and top-k launches on ``stream``.
+
+        Order: cache writes, then the decode pair (paged logits streaming the
+        cache, top-k), then the prefill pair (gather, logits, top-k).  The
+        prefill logits leave L2 full of freshly written rows; run right after
+        them, the HBM-bound decode pass would pay for writing those lines back,
+        while the prefill top-k reads them where they are."""
         s = stream
+
+        def timed(name, fn):
+            if events and name in events:
+                events[name][0].record(s)
+            fn()
+            if events and name in events:
+                events[name][1].record(s)
+
         ix_quant_write_k(self.new_k, self.new_slot, self.cache, stream=s)
         if self.nope is not None:
             dsmla_quant_write(self.nope, self.rope, self.new_slot, self.dsmla_cache, stream=s)
+        if self.decode is not None:
+            d = self.decode
+            timed("paged_mqa_logits", lambda: ix_paged_mqa_logits(
+                d.q, d.w, self.cache, d.context_lens, self.block_table, self.dec_logits,
+                clean_logits=self.clean, stream=s))
+            timed("topk_decode", lambda: ix_topk_to_global(
+                self.dec_logits, d.row_len, d.row_req, self.block_table, self.topk,
+                self.dec_global, self.dec_local, stream=s))
         if self.prefill is not None:
             p = self.prefill
             ix_gather_k(self.cache, self.pf_bt, p.cu_seq_lens, self.k_fp8, self.k_scale, stream=s)
-            if events and "mqa_logits" in events:
-                events["mqa_logits"][0].record(s)
-            ix_mqa_logits(p.q, p.w, self.k_fp8, self.k_scale, p.ks, p.ke, self.pf_logits,
-                          clean_logits=self.clean, stream=s)
-            if events and "mqa_logits" in events:
-                events["mqa_logits"][1].record(s)
-        if self.decode is not None:
-            d = self.decode
-            if events and "paged_mqa_logits" in events:
-                events["paged_mqa_logits"][0].record(s)
-            ix_paged_mqa_logits(d.q, d.w, self.cache, d.context_lens, self.block_table,
-                                self.dec_logits, clean_logits=self.clean, stream=s)
-            if events and "paged_mqa_logits" in events:
-                events["paged_mqa_logits"][1].record(s)
-            if events and "topk_decode" in events:
-                events["topk_decode"][0].record(s)
-            ix_topk_to_global(self.dec_logits, d.row_len, d.row_req, self.block_table, self.topk,
-                              self.dec_global, self.dec_local, stream=s)
-            if events and "topk_decode" in events:
-                events["topk_decode"][1].record(s)
-        if self.prefill is not None:
-            p = self.prefill
-            if events and "topk_prefill" in events:
-                events["topk_prefill"][0].record(s)
-            ix_topk_to_global(self.pf_logits, p.row_len, p.row_req, self.block_table, self.topk,
-                              self.pf_global, self.pf_local, stream=s)
-            if events and "topk_prefill" in events:
-                events["topk_prefill"][1].record(s)
+            timed("mqa_logits", lambda: ix_mqa_logits(
+                p.q, p.w, self.k_fp8, self.k_scale, p.ks, p.ke, self.pf_logits,
+                clean_logits=self.clean, stream=s))
+            timed("topk_prefill", lambda: ix_topk_to_global(
+                self.pf_logits, p.row_len, p.row_req, self.block_table, self.topk,
+                self.pf_global, self.pf_local, stream=s))
