@@ -470,10 +470,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         local += n;
     }
     int U;
-    block_excl_scan(local, scan, &U);
+    const int excl0 = block_excl_scan(local, scan, &U);
     const int64_t u0 = static_cast<int64_t>(blockIdx.x) * U / gridDim.x;
     const int64_t u1 = static_cast<int64_t>(blockIdx.x + 1) * U / gridDim.x;
-    if (u1 > u0) {
+    if (G <= kThreads) {
+        // one group per thread: the scan above already placed every group
+        if (u1 > u0 && local > 0 && excl0 <= u0 && u0 < excl0 + local) {
+            misc[2] = threadIdx.x;
+            misc[3] = static_cast<int>(u0 - excl0);
+            misc[4] = static_cast<int>(u1 - u0);
+        }
+    } else if (u1 > u0) {
         int running = 0;
         for (int base = 0; base < G && running <= u0; base += kThreads) {
             const int g = base + threadIdx.x;
