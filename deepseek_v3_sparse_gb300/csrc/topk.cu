@@ -355,9 +355,11 @@ __global__ void __launch_bounds__(kThreads, PER <= 4 ? 3 : (PER <= 32 ? 2 : 1))
 constexpr int kBlkThreads = 256;
 constexpr int kBlkWarps = kBlkThreads / 32;
 constexpr int kBlkMaxLd = 16384;
-constexpr int kBlkBt = 256;  // block-table entries staged (16384 keys at block size 64)
+constexpr int kBlkBt = 256;  // block-table entries staged (16384 keys at block size 64), one per thread
+static_assert(kBlkBt == kBlkThreads, "one staged block-table entry per thread");
 constexpr int kBlkBits = 12;  // radix digit width: 12 + 12 + 8 bits cover a 32-bit key
 constexpr int kBlkBins = 1 << kBlkBits;
+constexpr int kBlkFewKeys = 1024;  // threshold-bin size below which later passes take 10-bit digits
 
 __device__ __forceinline__ uint32_t blk_scan_excl(uint32_t v, uint32_t* scratch) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -419,22 +421,29 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
     for (int i = tid; i < kBlkBins; i += kBlkThreads) hist[i] = 0;
     __syncthreads();
     int sc = 0;  // alternates the scan scratch so back-to-back scans need no extra barrier
+    // A row's length and request are read one row ahead, and its block-table
+    // entries are loaded before the row and stored to shared memory only after
+    // the first barrier, so no global load waits on another at the row start.
+    int64_t len_nx = blockIdx.x < a.rows ? __ldg(a.row_len + blockIdx.x) : 0;
+    int req_nx = blockIdx.x < a.rows ? __ldg(a.row_req + blockIdx.x) : 0;
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
-        int64_t L64 = __ldg(a.row_len + r);
+        int64_t L64 = len_nx;
         L64 = L64 < 0 ? 0 : (L64 > a.ld ? a.ld : L64);
         const int L = static_cast<int>(L64);
-        const int b = __ldg(a.row_req + r);
+        const int b = req_nx;
+        if (r + gridDim.x < a.rows) {
+            len_nx = __ldg(a.row_len + r + gridDim.x);
+            req_nx = __ldg(a.row_req + r + gridDim.x);
+        }
         if (L <= a.k) {
             for (int i = tid; i < a.k; i += kBlkThreads) emit(a, r, b, i, i < L ? i : -1);
             continue;
         }
         const int nblk = (L + a.block_size - 1) / a.block_size;
-        const bool bt_staged = nblk <= kBlkBt;
-        if (bt_staged && a.bs_shift >= 0)
-            for (int i = tid; i < nblk; i += kBlkThreads)
-                btrow[i] = static_cast<int32_t>(
-                    static_cast<uint32_t>(__ldg(a.bt + static_cast<int64_t>(b) * a.bt_stride + i)) *
-                    static_cast<uint32_t>(a.block_size));
+        const bool bt_staged = nblk <= kBlkBt;  // kBlkBt == kBlkThreads: one entry per thread
+        const bool bt_mine = bt_staged && a.bs_shift >= 0 && tid < nblk;
+        uint32_t btv = 0;
+        if (bt_mine) btv = static_cast<uint32_t>(__ldg(a.bt + static_cast<int64_t>(b) * a.bt_stride + tid));
         const int mine = tid * PER;
         const int nv = max(0, min(PER, L - mine));
         const float* src = a.logits + r * a.ld + mine;  // 16-byte aligned
@@ -473,6 +482,7 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
             mm[1][tid >> 5] = kmax;
         }
         __syncthreads();
+        if (bt_mine) btrow[tid] = static_cast<int32_t>(btv * static_cast<uint32_t>(a.block_size));
 #pragma unroll
         for (int i = 0; i < kBlkWarps; ++i) {
             kmin = min(kmin, mm[0][i]);
@@ -483,7 +493,10 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
         int k_rem = a.k;
         bool done = shift == 0;
         for (int p = 0; !done; ++p) {
-            const int nbits = shift < kBlkBits ? shift : kBlkBits;
+            // after the first pass few keys remain in the threshold bin: a 10-bit
+            // digit (four bins per thread in the pick) usually settles them
+            const int width = (p > 0 && res[2] <= kBlkFewKeys) ? 10 : kBlkBits;
+            const int nbits = shift < width ? shift : width;
             const int nb = 1 << nbits;
             const int sh = shift - nbits;
             if (p == 0) {
@@ -531,15 +544,44 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
             sc ^= 1;
             if (above < k_rem && above + sum >= k_rem) {
                 int acc = above;
-                for (int i = per - 1; i >= 0; --i) {
-                    const int cnt = hist[base + i];
-                    if (acc + cnt >= k_rem) {
-                        res[0] = base + i;
-                        res[1] = acc;
-                        res[2] = cnt;
-                        break;
+                if (per >= 4) {  // 16-byte steps from the top bin down
+                    const int4* h4 = reinterpret_cast<const int4*>(hist + base);
+                    for (int i = per / 4 - 1; i >= 0; --i) {
+                        const int4 v = h4[i];
+                        bool found = false;
+                        int bin = 0, cnt_bin = 0, acc_bin = 0;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {  // bins base + 4i + 3 down to base + 4i
+                            const int cnt = q == 0 ? v.w : (q == 1 ? v.z : (q == 2 ? v.y : v.x));
+                            if (!found) {
+                                if (acc + cnt >= k_rem) {
+                                    found = true;
+                                    bin = base + 4 * i + 3 - q;
+                                    cnt_bin = cnt;
+                                    acc_bin = acc;
+                                } else {
+                                    acc += cnt;
+                                }
+                            }
+                        }
+                        if (found) {
+                            res[0] = bin;
+                            res[1] = acc_bin;
+                            res[2] = cnt_bin;
+                            break;
+                        }
                     }
-                    acc += cnt;
+                } else {
+                    for (int i = per - 1; i >= 0; --i) {
+                        const int cnt = hist[base + i];
+                        if (acc + cnt >= k_rem) {
+                            res[0] = base + i;
+                            res[1] = acc;
+                            res[2] = cnt;
+                            break;
+                        }
+                        acc += cnt;
+                    }
                 }
             }
             if (per >= 4) {
