@@ -24,6 +24,10 @@ passage it follows; the definitions are:
   #1094, Technical Details).
 * ``dsmla_quant_write``: the fp8_ds_mla 656-byte entry of vLLM PR #47090's
   _fused_norm_rope_kernel snippet.
+* ``dsmla_norm_rope_write``: the whole step of that kernel for one token, RMSNorm
+  of the NoPE values (sum of squares and reciprocal root in double, scaling in
+  f32), rotation of the interleaved RoPE pairs from a cos/sin table (f32, no
+  fused multiply-add, bf16 nearest-even), then the same 656-byte entry.
 
 Parity pins live in ``tests/test_oracle_*.py`` (marked ``not gpu``).
 """
@@ -78,9 +82,12 @@ def _load():
                                           I32, P, I64]
         lib.oracle_topk_to_global.argtypes = [P, I64, I64, P, P, P, I64, I32, I32, P, P]
         lib.oracle_dsmla_quant_write.argtypes = [P, P, I64, P, P, I64, I32, I64, I64]
+        lib.oracle_dsmla_norm_rope_write.argtypes = [P, P, P, ctypes.c_float, P, P, I64, P, I64, P,
+                                                     I64, I32, I64, I64]
         for name in ("oracle_quant_write_k", "oracle_gather_k", "oracle_paged_mqa_logits",
                      "oracle_mqa_logits", "oracle_topk_to_global",
-                     "oracle_dsmla_quant_write", "oracle_num_threads"):
+                     "oracle_dsmla_quant_write", "oracle_dsmla_norm_rope_write",
+                     "oracle_num_threads"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -221,3 +228,29 @@ def dsmla_quant_write(nope_bf16: np.ndarray, rope_bf16: np.ndarray, slot_mapping
     rc = _load().oracle_dsmla_quant_write(_p(nope), _p(rope), nope.shape[0], _p(sm), _p(cache),
                                           nb, block_size, bs * entry, entry)
     _check(rc, "dsmla_quant_write")
+
+
+def dsmla_norm_rope_write(kv_bf16: np.ndarray, pe_bf16: np.ndarray, gamma_bf16: np.ndarray,
+                          eps: float, positions: np.ndarray, cos_sin: np.ndarray,
+                          slot_mapping: np.ndarray, cache: np.ndarray, block_size: int) -> bool:
+    """RMSNorm + RoPE + fp8_ds_mla entry write, in place.
+
+    kv_bf16 uint16 [n, 512], pe_bf16 uint16 [n, 64], gamma_bf16 uint16 [512]
+    (bf16 bits); positions int64 [n]; cos_sin f32 [max_pos, 64] (cosines, then
+    sines); cache uint8 [num_blocks, block_size, entry_bytes].  Returns False
+    when a slot or a position was out of range (those tokens are skipped)."""
+    kv = _c(kv_bf16, np.uint16)
+    pe = _c(pe_bf16, np.uint16)
+    g = _c(gamma_bf16, np.uint16)
+    pos = _c(positions, np.int64)
+    cs = _c(cos_sin, np.float32)
+    sm = _c(slot_mapping, np.int64)
+    assert kv.ndim == 2 and kv.shape[1] == 512 and pe.shape == (kv.shape[0], 64) and g.shape == (512,)
+    assert cs.ndim == 2 and cs.shape[1] == 64 and pos.shape == sm.shape == (kv.shape[0],)
+    assert cache.flags.c_contiguous and cache.dtype == np.uint8 and cache.ndim == 3
+    nb, bs, entry = cache.shape
+    assert bs == block_size
+    rc = _load().oracle_dsmla_norm_rope_write(_p(kv), _p(pe), _p(g), float(eps), _p(pos), _p(cs),
+                                              cs.shape[0], _p(sm), kv.shape[0], _p(cache), nb,
+                                              block_size, bs * entry, entry)
+    return rc == 0

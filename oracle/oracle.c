@@ -28,6 +28,9 @@
  *             indexer K quantised per token, scale = amax / 448.
  *   [OCP]     OCP 8-bit floating point specification, E4M3: bias 7, no
  *             infinities, S.1111.111 is NaN, largest finite 448.
+ *   [DSMLA] also names the step this branch belongs to: the fused RMSNorm +
+ *             RoPE + cache write of one token (the norm and rotation formulas are
+ *             not printed there; the readings sit with the function).
  *
  * Readings of points the pages leave open (each also listed in the design notes):
  *   - fp8 rounding is round-to-nearest-even, saturating to +-448.
@@ -426,6 +429,103 @@ int oracle_dsmla_quant_write(const uint16_t* nope, const uint16_t* rope, int64_t
             memcpy(e + 512 + 4 * tile, &sc, 4);
         }
         memcpy(e + 528, rope + t * 64, 128);
+    }
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Fused RMSNorm + RoPE + fp8_ds_mla write: the whole per-token step of the    */
+/* page's _fused_norm_rope_kernel, fp8_ds_mla branch [DSMLA]; the norm and the */
+/* rotation follow the readings listed at the top of this function             */
+/* ------------------------------------------------------------------------- */
+
+/* Nearest bf16, ties to the even bf16 (NaN stays a quiet NaN). */
+static uint16_t f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lsb = (u >> 16) & 1u;
+    return (uint16_t)((u + 0x7FFFu + lsb) >> 16);
+}
+
+/* One 128-value NoPE tile of f32 values: sc = max(amax * f32(1/448),
+ * 1.1754944e-38) (f32 multiply), codes = enc(y / sc) (IEEE f32 division). */
+static float code_tile_f32(const float* y, uint8_t* codes)
+{
+    const float inv448 = (float)(1.0 / 448.0);
+    const float floor_scale = 1.1754944e-38f;
+    float amax = 0.0f;
+    for (int i = 0; i < 128; ++i) {
+        float a = fabsf(y[i]);
+        if (a > amax) amax = a;
+    }
+    float sc = amax * inv448;
+    if (!(sc >= floor_scale)) sc = floor_scale;
+    for (int i = 0; i < 128; ++i) codes[i] = oracle_e4m3_encode(y[i] / sc);
+    return sc;
+}
+
+/* Per token t with slot_mapping[t] >= 0 (readings of what the page leaves open):
+ *   RMSNorm of the 512 bf16 NoPE values x with weights g (bf16):
+ *     S = sum_i x_i^2 in double (every square of a bf16 value has at most 16
+ *         significant bits, so the sum is exact for these inputs and does not
+ *         depend on the order of the terms);
+ *     r = (float)(1.0 / sqrt(S / 512.0 + (double)eps)), each double operation
+ *         correctly rounded;
+ *     y_i = (x_i * r) * g_i in f32 (two rounded products, no fused multiply-add).
+ *   The 512 y are coded as the fp8_ds_mla NoPE (4 tiles of 128, as above) and
+ *   the tile scales follow them.
+ *   RoPE, interleaved pairs (the page stores r1, r2 at 2i, 2i+1): for pair i of
+ *   the 64 bf16 values, at position p = positions[t], with c = cos_sin[p*64 + i]
+ *   and s = cos_sin[p*64 + 32 + i] (the cosine half, then the sine half):
+ *     r1 = x0*c - x1*s,  r2 = x0*s + x1*c  in f32 (products rounded, then the
+ *     sum), each stored as bf16, nearest with ties to even.
+ * A slot past the pool or a position outside [0, max_pos) skips the token and
+ * makes the call return -1. */
+int oracle_dsmla_norm_rope_write(const uint16_t* kv, const uint16_t* pe, const uint16_t* gamma,
+                                 float eps, const int64_t* positions, const float* cos_sin,
+                                 int64_t max_pos, const int64_t* slot_mapping, int64_t n,
+                                 uint8_t* cache, int64_t num_blocks, int block_size,
+                                 int64_t block_stride, int64_t entry_stride)
+{
+    codec_init();
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int64_t t = 0; t < n; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        int64_t blk = slot / block_size, off = slot % block_size;
+        int64_t p = positions[t];
+        if (blk >= num_blocks || p < 0 || p >= max_pos) { bad = 1; continue; }
+        uint8_t* e = cache + blk * block_stride + off * entry_stride;
+        const uint16_t* x = kv + t * 512;
+        double S = 0.0;
+        for (int i = 0; i < 512; ++i) {
+            double v = (double)bf16_to_f32(x[i]);
+            S += v * v;
+        }
+        float r = (float)(1.0 / sqrt(S / 512.0 + (double)eps));
+        float y[512];
+        for (int i = 0; i < 512; ++i) {
+            float xr = bf16_to_f32(x[i]) * r;
+            y[i] = xr * bf16_to_f32(gamma[i]);
+        }
+        for (int tile = 0; tile < 4; ++tile) {
+            float sc = code_tile_f32(y + 128 * tile, e + 128 * tile);
+            memcpy(e + 512 + 4 * tile, &sc, 4);
+        }
+        const uint16_t* q = pe + t * 64;
+        const float* cs = cos_sin + p * 64;
+        uint16_t out[64];
+        for (int i = 0; i < 32; ++i) {
+            float x0 = bf16_to_f32(q[2 * i]), x1 = bf16_to_f32(q[2 * i + 1]);
+            float c = cs[i], s = cs[32 + i];
+            float a = x0 * c, b = x1 * s, u = x0 * s, w = x1 * c;
+            out[2 * i] = f32_to_bf16(a - b);
+            out[2 * i + 1] = f32_to_bf16(u + w);
+        }
+        memcpy(e + 528, out, 128);
     }
     return bad ? -1 : 0;
 }
