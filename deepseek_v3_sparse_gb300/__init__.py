@@ -23,7 +23,7 @@ import torch
 __all__ = [
     "DsixError", "load", "ix_status_string", "ix_device_status", "ix_quant_write_k",
     "ix_gather_k", "ix_paged_mqa_logits", "ix_mqa_logits", "ix_topk_to_global",
-    "dsmla_quant_write", "LIB_PATH", "HEADS", "HEAD_DIM", "BLOCK_SIZE",
+    "dsmla_quant_write", "dsmla_norm_rope_write", "LIB_PATH", "HEADS", "HEAD_DIM", "BLOCK_SIZE",
 ]
 
 HEADS = 64
@@ -56,6 +56,8 @@ _SIGNATURES = {
     "ix_mqa_logits": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64, _I32, _P], _I32),
     "ix_topk_to_global": ([_P, _I64, _I64, _P, _P, _P, _I64, _I32, _I32, _P, _P, _P], _I32),
     "dsmla_quant_write": ([_P, _P, _I64, _P, _P, _I64, _I32, _I64, _I64, _P], _I32),
+    "dsmla_norm_rope_write": ([_P, _P, _P, ctypes.c_float, _P, _P, _I64, _P, _I64, _P, _I64, _I32,
+                               _I64, _I64, _P], _I32),
 }
 
 
@@ -202,3 +204,18 @@ def dsmla_quant_write(nope_bf16: torch.Tensor, rope_bf16: torch.Tensor,
         _dev(cache, "cache", (torch.uint8,)), nb, bs, cache.stride(0), cache.stride(1),
         _stream(stream))
     _check(rc, "dsmla_quant_write")
+
+
+def dsmla_norm_rope_write(kv_bf16: torch.Tensor, pe_bf16: torch.Tensor, gamma_bf16: torch.Tensor,
+                          eps: float, positions: torch.Tensor, cos_sin: torch.Tensor,
+                          slot_mapping: torch.Tensor, cache: torch.Tensor, stream=None) -> None:
+    """kv [n, 512] bf16; pe [n, 64] bf16; gamma [512] bf16; positions [n] int64;
+    cos_sin [max_pos, 64] f32; cache uint8 [num_blocks, block_size, 656+]."""
+    nb, bs, entry = cache.shape
+    rc = load().dsmla_norm_rope_write(
+        _dev(kv_bf16, "kv_bf16", _BF16), _dev(pe_bf16, "pe_bf16", _BF16),
+        _dev(gamma_bf16, "gamma_bf16", _BF16), float(eps), _dev(positions, "positions", _I64T),
+        _dev(cos_sin, "cos_sin", _F32), cos_sin.shape[0], _dev(slot_mapping, "slot_mapping", _I64T),
+        kv_bf16.shape[0], _dev(cache, "cache", (torch.uint8,)), nb, bs, cache.stride(0),
+        cache.stride(1), _stream(stream))
+    _check(rc, "dsmla_norm_rope_write")

@@ -1,9 +1,10 @@
-// cache.cu -- the three bandwidth kernels around the indexer cache:
-//   ix_quant_write_k   indexer-K quantise + paged write
-//   ix_gather_k        ragged paged gather into contiguous K
-//   dsmla_quant_write  the 656-byte fp8_ds_mla entry write
+// cache.cu -- the bandwidth kernels around the caches:
+//   ix_quant_write_k       indexer-K quantise + paged write
+//   ix_gather_k            ragged paged gather into contiguous K
+//   dsmla_quant_write      the 656-byte fp8_ds_mla entry write
+//   dsmla_norm_rope_write  RMSNorm + RoPE + that entry write, fused per token
 //
-// All three are pure streaming kernels (16-byte vector loads, grid sized to a
+// All are pure streaming kernels (16-byte vector loads, grid sized to a
 // multiple of the SM count); their bound is HBM bandwidth.
 #include <float.h>
 
@@ -175,6 +176,94 @@ __global__ void __launch_bounds__(256) dsmla_write_kernel(const uint4* __restric
     }
 }
 
+// ---------------------------------------------------------------------------
+// dsmla_norm_rope_write: one warp per token.  Lane l holds NoPE values
+// [16 l, 16 l + 16) (tile l / 8) and RoPE pair l.
+//   RMSNorm: the lanes' sums of squares in double (each square of a bf16 value
+//   is exact) reduce to the exact S; r = f32(1 / sqrt(S / 512 + eps)) in
+//   double; y = (x * r) * g in f32 with round-to-nearest products (no fused
+//   multiply-add), then the ds_mla tile coding.
+//   RoPE: r1 = x0 c - x1 s, r2 = x0 s + x1 c in f32 (products rounded, then
+//   the sum), packed to bf16 with round-to-nearest-even, stored at 2l, 2l + 1.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) dsmla_norm_rope_kernel(
+    const uint4* __restrict__ kv, const uint32_t* __restrict__ pe, const uint4* __restrict__ gamma,
+    float eps, const int64_t* __restrict__ positions, const float* __restrict__ cos_sin,
+    int64_t max_pos, const int64_t* __restrict__ slots, int64_t n, uint8_t* __restrict__ cache,
+    int64_t num_blocks, int block_size, int64_t block_stride, int64_t entry_stride, int* status) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    // this lane's 16 norm weights stay in registers for every token
+    float g[16];
+    {
+        float a[8], b[8];
+        unpack8(__ldg(gamma + 2 * lane), a);
+        unpack8(__ldg(gamma + 2 * lane + 1), b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            g[i] = a[i];
+            g[8 + i] = b[i];
+        }
+    }
+    for (int64_t tok = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; tok < n;
+         tok += warps) {
+        const int64_t slot = __ldg(slots + tok);
+        if (slot < 0) continue;  // uniform across the warp
+        const int64_t blk = slot / block_size;
+        const int64_t pos = __ldg(positions + tok);
+        if (blk >= num_blocks || pos < 0 || pos >= max_pos) {
+            if (lane == 0) flag(status, blk >= num_blocks ? IX_DEV_BAD_SLOT : IX_DEV_BAD_POSITION);
+            continue;
+        }
+        uint8_t* e = cache + blk * block_stride + (slot % block_size) * entry_stride;
+        float x[16];
+        {
+            float a[8], b[8];
+            unpack8(__ldg(kv + tok * 64 + 2 * lane), a);
+            unpack8(__ldg(kv + tok * 64 + 2 * lane + 1), b);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                x[i] = a[i];
+                x[8 + i] = b[i];
+            }
+        }
+        const uint32_t pair = __ldg(pe + tok * 32 + lane);
+        const float c = __ldg(cos_sin + pos * 64 + lane);
+        const float sn = __ldg(cos_sin + pos * 64 + 32 + lane);
+        double ss = 0.0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ss = __dadd_rn(ss, __dmul_rn(static_cast<double>(x[i]), static_cast<double>(x[i])));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss = __dadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+        const float r = __double2float_rn(
+            __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(__dmul_rn(ss, 0x1p-9), static_cast<double>(eps)))));
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            x[i] = __fmul_rn(__fmul_rn(x[i], r), g[i]);
+            amax = fmaxf(amax, fabsf(x[i]));
+        }
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o, 8));
+        const float sc = fmaxf(__fmul_rn(amax, kInv448), kScaleFloor);
+        float lo[8], hi[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            lo[i] = x[i];
+            hi[i] = x[8 + i];
+        }
+        const uint2 c0 = quant8(lo, sc), c1 = quant8(hi, sc);
+        *reinterpret_cast<uint4*>(e + 16 * lane) = make_uint4(c0.x, c0.y, c1.x, c1.y);
+        if ((lane & 7) == 0) *reinterpret_cast<float*>(e + 512 + 4 * (lane >> 3)) = sc;
+        const float x0 = bf16_lo(pair), x1 = bf16_hi(pair);
+        const float r1 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, sn));
+        const float r2 = __fadd_rn(__fmul_rn(x0, sn), __fmul_rn(x1, c));
+        uint32_t packed;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed) : "f"(r2), "f"(r1));  // r1 in the low half
+        reinterpret_cast<uint32_t*>(e + 528)[lane] = packed;
+    }
+}
+
 int grid_for(int64_t work_items, int items_per_block) {
     const int sms = num_sms();
     int64_t blocks = (work_items + items_per_block - 1) / items_per_block;
@@ -240,5 +329,31 @@ extern "C" int dsmla_quant_write(const void* nope_bf16, const void* rope_bf16, i
     dsmla_write_kernel<<<grid_for(2 * n, 8), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint4*>(nope_bf16), static_cast<const uint4*>(rope_bf16), n, slot_mapping,
         cache, num_blocks, block_size, block_stride_bytes, entry_stride_bytes, st);
+    return launch_status();
+}
+
+extern "C" int dsmla_norm_rope_write(const void* kv_bf16, const void* pe_bf16, const void* gamma_bf16,
+                                     float eps, const int64_t* positions, const float* cos_sin,
+                                     int64_t max_pos, const int64_t* slot_mapping, int64_t n,
+                                     uint8_t* cache, int64_t num_blocks, int block_size,
+                                     int64_t block_stride_bytes, int64_t entry_stride_bytes,
+                                     ix_stream_t stream) {
+    if (n < 0 || num_blocks < 0 || block_size <= 0 || block_stride_bytes <= 0 ||
+        entry_stride_bytes < 656 || max_pos < 0)
+        return IX_ERR_SHAPE;
+    if (n == 0) return IX_OK;
+    if (!kv_bf16 || !pe_bf16 || !gamma_bf16 || !positions || !cos_sin || !slot_mapping || !cache)
+        return IX_ERR_NULL;
+    if (!aligned16(kv_bf16) || !aligned16(gamma_bf16) || !aligned16(cache) ||
+        (reinterpret_cast<uintptr_t>(pe_bf16) & 3) || (reinterpret_cast<uintptr_t>(cos_sin) & 3) ||
+        (block_stride_bytes & 15) || (entry_stride_bytes & 15) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7) || (reinterpret_cast<uintptr_t>(positions) & 7))
+        return IX_ERR_ALIGN;
+    int* st = status_ptr();
+    if (!st) return IX_ERR_CUDA;
+    dsmla_norm_rope_kernel<<<grid_for(n, 8), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(kv_bf16), static_cast<const uint32_t*>(pe_bf16),
+        static_cast<const uint4*>(gamma_bf16), eps, positions, cos_sin, max_pos, slot_mapping, n, cache,
+        num_blocks, block_size, block_stride_bytes, entry_stride_bytes, st);
     return launch_status();
 }

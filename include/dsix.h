@@ -71,7 +71,8 @@ enum {
     IX_DEV_BAD_BLOCK = 2,       /* block_table entry outside [0, num_blocks): access skipped */
     IX_DEV_ROW_TOO_LONG = 4,    /* a visible row is longer than ld: columns >= ld dropped */
     IX_DEV_BAD_RANGE = 8,       /* ks/ke outside [0, tk], or cu_seq_lens past out_capacity */
-    IX_DEV_TIMEOUT = 16         /* a pipeline wait gave up (never expected) */
+    IX_DEV_TIMEOUT = 16,        /* a pipeline wait gave up (never expected) */
+    IX_DEV_BAD_POSITION = 32    /* a RoPE position outside [0, max_pos): token skipped */
 };
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -213,6 +214,40 @@ IX_API int dsmla_quant_write(const void* nope_bf16, const void* rope_bf16, int64
                       const int64_t* slot_mapping, uint8_t* cache, int64_t num_blocks,
                       int block_size, int64_t block_stride_bytes,
                       int64_t entry_stride_bytes, ix_stream_t stream);
+
+/*
+ * dsmla_norm_rope_write -- the whole per-token step that the fp8_ds_mla write
+ * above is the last part of (vLLM PR #47090, prhub summary: the fp8_ds_mla
+ * branch of _fused_norm_rope_kernel writes the normalised KV and the rotated
+ * RoPE values).  The page prints neither the norm nor the rotation; this entry
+ * point computes, for every token t with slot = slot_mapping[t] >= 0:
+ *   RMSNorm of the 512 NoPE values x with weights g:
+ *     S = sum x_i^2 (double; exact, since each square of a bf16 value has at
+ *     most 16 significant bits), r = f32(1 / sqrt(S / 512 + eps)) (double
+ *     operations, each correctly rounded), y_i = (x_i * r) * g_i (f32, two
+ *     rounded products);
+ *   the 512 y coded as dsmla_quant_write codes its NoPE values (tiles of 128,
+ *   sc = max(amax * f32(1/448), 1.1754944e-38), v = fp8(y / sc)), the tile
+ *   scales after them;
+ *   RoPE on interleaved pairs: with p = positions[t], for pair i (values 2i,
+ *   2i + 1) c = cos_sin[p*64 + i], s = cos_sin[p*64 + 32 + i],
+ *     r1 = x0*c - x1*s, r2 = x0*s + x1*c (f32: products rounded, then the sum),
+ *   stored as bf16 (nearest, ties to even) at 2i and 2i + 1 of bytes [528,656).
+ * Tokens with a negative slot are skipped; a slot past the pool sets
+ * IX_DEV_BAD_SLOT and a position outside [0, max_pos) sets IX_DEV_BAD_POSITION,
+ * and the token is skipped.
+ *   kv_bf16     bf16 [n, 512], 16-byte aligned (the compressed KV before the norm)
+ *   pe_bf16     bf16 [n, 64], 4-byte aligned (the RoPE part before the rotation)
+ *   gamma_bf16  bf16 [512], 16-byte aligned (the norm weights)
+ *   positions   int64 [n];  cos_sin  f32 [max_pos, 64] (32 cosines, then 32 sines)
+ *   cache, strides: as dsmla_quant_write
+ */
+IX_API int dsmla_norm_rope_write(const void* kv_bf16, const void* pe_bf16, const void* gamma_bf16,
+                      float eps, const int64_t* positions, const float* cos_sin,
+                      int64_t max_pos, const int64_t* slot_mapping, int64_t n,
+                      uint8_t* cache, int64_t num_blocks, int block_size,
+                      int64_t block_stride_bytes, int64_t entry_stride_bytes,
+                      ix_stream_t stream);
 
 #ifdef __cplusplus
 }

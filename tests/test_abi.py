@@ -38,7 +38,7 @@ def _declared():
 
 def test_exports_match_header(lib):
     names = _declared()
-    assert len(names) == 8
+    assert len(names) == 9
     for n in names:
         assert hasattr(lib, n), n
     out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True,
@@ -128,6 +128,23 @@ def test_dsmla_host_checks(lib):
     assert f(A16, A16, 4, A16, A1, 8, 64, 64 * 656, 656, None) == IX_ERR_ALIGN
     assert f(None, A16, 4, A16, A16, 8, 64, 64 * 656, 656, None) == IX_ERR_NULL
     assert f(None, None, 0, None, None, 8, 64, 64 * 656, 656, None) == IX_OK
+
+
+def test_dsmla_norm_rope_host_checks(lib):
+    f = lib.dsmla_norm_rope_write
+    args = lambda **kw: [kw.get("kv", A16), kw.get("pe", A16), kw.get("g", A16), 1e-6,
+                         kw.get("pos", A16), A16, kw.get("max_pos", 16), A16, kw.get("n", 4),
+                         kw.get("cache", A16), 8, 64, 64 * 656, kw.get("entry", 656), None]
+    assert f(*args(entry=600)) == IX_ERR_SHAPE
+    assert f(*args(max_pos=-1)) == IX_ERR_SHAPE
+    assert f(*args(n=-1)) == IX_ERR_SHAPE
+    assert f(*args(entry=660)) == IX_ERR_ALIGN
+    assert f(*args(kv=A1)) == IX_ERR_ALIGN
+    assert f(*args(g=P(0x10004))) == IX_ERR_ALIGN
+    assert f(*args(pos=P(0x10004))) == IX_ERR_ALIGN
+    assert f(*args(pe=None)) == IX_ERR_NULL
+    assert f(*args(cache=None)) == IX_ERR_NULL
+    assert f(*args(kv=None, pe=None, g=None, pos=None, cache=None, n=0)) == IX_OK
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

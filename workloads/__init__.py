@@ -87,6 +87,11 @@ class Workload:
     def hist_k(self) -> torch.Tensor:
         return self.k_bf16[torch.from_numpy(~self.is_new)]
 
+    def new_positions(self) -> np.ndarray:
+        """int64 [n_new]: each new token's position in its request (cached order)."""
+        pos = np.concatenate([np.arange(int(c), dtype=np.int64) for c in self.req_ctx])
+        return pos[self.is_new]
+
     def decode_rows(self):
         """(row_len int32 [B*next_n], row_req int32 [B*next_n]) for decode rows."""
         B, n = self.n_decode, self.next_n
@@ -267,6 +272,20 @@ NAMED = {
 # ---------------------------------------------------------------------------
 # numpy views for the oracle side
 # ---------------------------------------------------------------------------
+
+def norm_rope_params(max_pos: int, seed: int = 0):
+    """Synthetic parameters of the fused RMSNorm + RoPE cache write, from a
+    generator of their own (the draws above are unchanged):
+    norm weights bf16 [512] drawn as 1 + N(0,1)/8, and a rotary table f32
+    [max_pos, 64] holding the cosines (columns 0-31) and sines (32-63) of angles
+    drawn uniformly in [0, 2 pi) -- a valid rotation for every (position, pair),
+    not a particular frequency schedule."""
+    g = torch.Generator(device="cpu").manual_seed(seed + 7919)
+    gamma = _bf16(1 + torch.randn(NOPE_DIM, generator=g) / 8)
+    ang = torch.rand(max_pos, ROPE_DIM // 2, generator=g, dtype=torch.float64) * (2 * math.pi)
+    table = torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32)
+    return gamma, table
+
 
 def bf16_bits(x: torch.Tensor) -> np.ndarray:
     """bfloat16 tensor -> uint16 numpy array of its bit patterns."""
