@@ -25,9 +25,10 @@ passage it follows; the definitions are:
 * ``dsmla_quant_write``: the fp8_ds_mla 656-byte entry of vLLM PR #47090's
   _fused_norm_rope_kernel snippet.
 * ``dsmla_norm_rope_write``: the whole step of that kernel for one token, RMSNorm
-  of the NoPE values (sum of squares and reciprocal root in double, scaling in
-  f32), rotation of the interleaved RoPE pairs from a cos/sin table (f32, no
-  fused multiply-add, bf16 nearest-even), then the same 656-byte entry.
+  of the NoPE values (exact sum of squares in double, mean square plus eps
+  rounded once to f32, reciprocal root and scaling in f32), rotation of the
+  interleaved RoPE pairs from a cos/sin table (f32, no fused multiply-add, bf16
+  nearest-even), then the same 656-byte entry.
 
 Parity pins live in ``tests/test_oracle_*.py`` (marked ``not gpu``).
 """

@@ -471,8 +471,9 @@ static float code_tile_f32(const float* y, uint8_t* codes)
  *     S = sum_i x_i^2 in double (every square of a bf16 value has at most 16
  *         significant bits, so the sum is exact for these inputs and does not
  *         depend on the order of the terms);
- *     r = (float)(1.0 / sqrt(S / 512.0 + (double)eps)), each double operation
- *         correctly rounded;
+ *     t = (float)(S / 512.0 + (double)eps): the mean square plus eps, formed in
+ *         double and rounded once to f32;
+ *     r = 1 / sqrt(t) in f32 (IEEE square root, then IEEE division);
  *     y_i = (x_i * r) * g_i in f32 (two rounded products, no fused multiply-add).
  *   The 512 y are coded as the fp8_ds_mla NoPE (4 tiles of 128, as above) and
  *   the tile scales follow them.
@@ -505,7 +506,8 @@ int oracle_dsmla_norm_rope_write(const uint16_t* kv, const uint16_t* pe, const u
             double v = (double)bf16_to_f32(x[i]);
             S += v * v;
         }
-        float r = (float)(1.0 / sqrt(S / 512.0 + (double)eps));
+        float t32 = (float)(S / 512.0 + (double)eps);
+        float r = 1.0f / sqrtf(t32);
         float y[512];
         for (int i = 0; i < 512; ++i) {
             float xr = bf16_to_f32(x[i]) * r;
