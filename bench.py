@@ -35,6 +35,7 @@ UNIT = "query-tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DECODE_BYTES_PER_KEY = 132        # 128 fp8 values + one fp32 scale
 PREFILL_FLOP_PER_PAIR = 2 * 64 * 128
+NORM_ROPE_BYTES_PER_TOKEN = 1024 + 128 + 8 + 8 + 256 + 656  # fused norm/RoPE ds_mla write
 
 
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "traffic_mixed_long.txt")
@@ -247,6 +248,37 @@ def gpu_arm(args, world, rank, local):
     clk = clocks.summary()
     status = dsix.ix_device_status()
 
+    # ---- the next row beyond the step: fused RMSNorm + RoPE + fp8_ds_mla write of
+    # the step's new tokens at their own positions, timed launch by launch with
+    # L2 flushed between launches (its inputs are far smaller than L2)
+    next_rows = {}
+    if wl.nope_bf16 is not None:
+        pos = wl.new_positions()
+        gamma, table = W.norm_rope_params(int(pos.max()) + 1)
+        nr_in = dict(kv=wl.nope_bf16.to(dev), pe=wl.rope_bf16.to(dev), gamma=gamma.to(dev),
+                     pos=torch.from_numpy(pos).to(dev), table=table.to(dev))
+        nr_cache = torch.zeros(wl.num_blocks, 64, 656, dtype=torch.uint8, device=dev)
+        nr_slots = step.new_slot
+        flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)  # 256 MB > L2
+        nr = lambda: dsix.dsmla_norm_rope_write(nr_in["kv"], nr_in["pe"], nr_in["gamma"], 1e-6,
+                                                nr_in["pos"], nr_in["table"], nr_slots, nr_cache,
+                                                stream=stream)
+        for _ in range(3):
+            nr()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(50)]
+        for a, b in evs:
+            flush.fill_(1.0)
+            a.record(stream)
+            nr()
+            b.record(stream)
+        torch.cuda.synchronize()
+        nr_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+        next_rows["dsmla_norm_rope_write"] = dict(ms=nr_ms, units=int(len(pos)))
+        del flush, nr_cache, nr_in
+        if dsix.ix_device_status() != 0:
+            raise RuntimeError("device status set by the fused norm/rope write")
+
     # ---- end to end through the public API: pinned host inputs in, indices out.
     # Two step instances alternate, so the host-to-device copy of step i+1's
     # inputs and the device-to-host copy of step i-1's indices (each on a copy
@@ -335,7 +367,7 @@ def gpu_arm(args, world, rank, local):
     rows = int(wl.n_decode * wl.next_n + wl.n_prefill_rows)
     return dict(wl=wl, step=step, elapsed_ms=elapsed_ms, kern_ms=kern_ms, clocks=clk,
                 status=status, e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h,
-                dec_keys=dec_keys, pairs=pairs, rows=rows)
+                dec_keys=dec_keys, pairs=pairs, rows=rows, next_rows=next_rows)
 
 
 # ---------------------------------------------------------------------------
@@ -510,6 +542,14 @@ def main():
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
             "gpu_launches": step.kernels_per_step() * args.steps,
             "clocks": r["clocks"], "device_status": r["status"]}
+    for n, d in r["next_rows"].items():  # rows beyond the step, timed on their own
+        gbs = d["units"] * NORM_ROPE_BYTES_PER_TOKEN / (d["ms"] / 1e3) / 1e9
+        line.setdefault("next_rows", {})[n] = {
+            "ms": d["ms"], "achieved": gbs, "unit": "GB/s", "peak": pk["hbm_gbs"],
+            "frac": gbs / pk["hbm_gbs"], "units": d["units"],
+            "per_unit": f"{NORM_ROPE_BYTES_PER_TOKEN} B per token (1024 NoPE + 128 RoPE in, "
+                        "8 position + 8 slot + 256 table row read, 656 entry out)",
+            "l2": "flushed between launches (256 MB write)"}
     if not args.no_cpu_baseline:
         import oracle
         s = OracleSampler(wl)

@@ -179,14 +179,29 @@ __global__ void __launch_bounds__(256) dsmla_write_kernel(const uint4* __restric
 // ---------------------------------------------------------------------------
 // dsmla_norm_rope_write: one warp per token.  Lane l holds NoPE values
 // [16 l, 16 l + 16) (tile l / 8) and RoPE pair l.
-//   RMSNorm: the lanes' sums of squares in double (each square of a bf16 value
-//   is exact) reduce to the exact S; r = f32(1 / sqrt(S / 512 + eps)) in
-//   double; y = (x * r) * g in f32 with round-to-nearest products (no fused
+//   RMSNorm: S = sum x_i^2 is formed exactly in integers (below); t = f32(S / 512
+//   + eps) in double, r = 1 / sqrt(t) in f32 (IEEE square root and division);
+//   y = (x * r) * g in f32 with round-to-nearest products (no fused
 //   multiply-add), then the ds_mla tile coding.
+//   Exact S without the (slow) FP64 pipe: a bf16 value is M * 2^E with M an
+//   8-bit integer, so x^2 = M^2 * 2^(2E) with M^2 < 2^16.  With Emax the
+//   largest E of the token, every square is an integer multiple of 2^L,
+//   L = 2 Emax - 39, as long as E >= Emax - 19; those multiples are below 2^55
+//   and 512 of them sum below 2^64 in a uint64.  The sum is exact, and S =
+//   double(sum) * 2^L is the exact S rounded once to double.  Squares of values
+//   more than 2^19 below the token's largest are cut to their multiple of 2^L
+//   (a change below 2^-38 of the largest square).
 //   RoPE: r1 = x0 c - x1 s, r2 = x0 s + x1 c in f32 (products rounded, then
 //   the sum), packed to bf16 with round-to-nearest-even, stored at 2l, 2l + 1.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) dsmla_norm_rope_kernel(
+// bf16 bits -> (M, E) with |x| = M * 2^E (M = 0 for a zero)
+__device__ __forceinline__ void bf16_split(uint32_t b, uint32_t& m, int& e) {
+    const uint32_t ef = (b >> 7) & 0xFFu, mf = b & 0x7Fu;
+    m = ef ? (128u | mf) : mf;
+    e = ef ? static_cast<int>(ef) - 134 : -133;
+}
+
+__global__ void __launch_bounds__(256, 4) dsmla_norm_rope_kernel(
     const uint4* __restrict__ kv, const uint32_t* __restrict__ pe, const uint4* __restrict__ gamma,
     float eps, const int64_t* __restrict__ positions, const float* __restrict__ cos_sin,
     int64_t max_pos, const int64_t* __restrict__ slots, int64_t n, uint8_t* __restrict__ cache,
@@ -207,10 +222,15 @@ __global__ void __launch_bounds__(256) dsmla_norm_rope_kernel(
     }
     for (int64_t tok = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; tok < n;
          tok += warps) {
+        // every load that depends only on the token goes out first; the
+        // rotary table row follows once the position has arrived
         const int64_t slot = __ldg(slots + tok);
+        const int64_t pos = __ldg(positions + tok);
+        const uint4 kva = __ldg(kv + tok * 64 + 2 * lane);
+        const uint4 kvb = __ldg(kv + tok * 64 + 2 * lane + 1);
+        const uint32_t pair = __ldg(pe + tok * 32 + lane);
         if (slot < 0) continue;  // uniform across the warp
         const int64_t blk = slot / block_size;
-        const int64_t pos = __ldg(positions + tok);
         if (blk >= num_blocks || pos < 0 || pos >= max_pos) {
             if (lane == 0) flag(status, blk >= num_blocks ? IX_DEV_BAD_SLOT : IX_DEV_BAD_POSITION);
             continue;
@@ -219,24 +239,48 @@ __global__ void __launch_bounds__(256) dsmla_norm_rope_kernel(
         float x[16];
         {
             float a[8], b[8];
-            unpack8(__ldg(kv + tok * 64 + 2 * lane), a);
-            unpack8(__ldg(kv + tok * 64 + 2 * lane + 1), b);
+            unpack8(kva, a);
+            unpack8(kvb, b);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 x[i] = a[i];
                 x[8 + i] = b[i];
             }
         }
-        const uint32_t pair = __ldg(pe + tok * 32 + lane);
         const float c = __ldg(cos_sin + pos * 64 + lane);
         const float sn = __ldg(cos_sin + pos * 64 + 32 + lane);
-        double ss = 0.0;
+        // exact sum of squares (see above); (M, E) are recomputed in the second
+        // loop rather than held, to keep the registers for more resident warps
+        int emax = -1000;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) ss = __dadd_rn(ss, __dmul_rn(static_cast<double>(x[i]), static_cast<double>(x[i])));
+        for (int i = 0; i < 16; ++i) {
+            uint32_t m;
+            int ex;
+            bf16_split(__float_as_uint(x[i]) >> 16, m, ex);
+            if (m) emax = max(emax, ex);
+        }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss = __dadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
-        const float r = __double2float_rn(
-            __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(__dmul_rn(ss, 0x1p-9), static_cast<double>(eps)))));
+        for (int o = 16; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+        double S = 0.0;
+        if (emax > -1000) {  // not an all-zero token (uniform across the warp)
+            const int L = 2 * emax - 39;  // every shift below is at most 39
+            unsigned long long acc = 0ull;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                uint32_t m;
+                int ex;
+                bf16_split(__float_as_uint(x[i]) >> 16, m, ex);
+                const unsigned long long sq = static_cast<unsigned long long>(m * m);
+                const int sh = 2 * ex - L;
+                acc += sh >= 0 ? (sq << sh) : (sh > -64 ? (sq >> -sh) : 0ull);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            // 2^L is a normal double for every bf16 exponent (L in [-305, 201])
+            S = __dmul_rn(__ull2double_rn(acc), __longlong_as_double(static_cast<long long>(L + 1023) << 52));
+        }
+        const float t = __double2float_rn(__dadd_rn(__dmul_rn(S, 0x1p-9), static_cast<double>(eps)));
+        const float r = __fdiv_rn(1.0f, __fsqrt_rn(t));
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {

@@ -222,10 +222,11 @@ IX_API int dsmla_quant_write(const void* nope_bf16, const void* rope_bf16, int64
  * RoPE values).  The page prints neither the norm nor the rotation; this entry
  * point computes, for every token t with slot = slot_mapping[t] >= 0:
  *   RMSNorm of the 512 NoPE values x with weights g:
- *     S = sum x_i^2 (double; exact, since each square of a bf16 value has at
- *     most 16 significant bits), r = f32(1 / sqrt(S / 512 + eps)) (double
- *     operations, each correctly rounded), y_i = (x_i * r) * g_i (f32, two
- *     rounded products);
+ *     S = sum x_i^2, exact and rounded once to double (each square of a bf16
+ *     value has at most 16 significant bits; squares more than 2^38 below the
+ *     token's largest are cut to a multiple of 2^-38 of it),
+ *     t = f32(S / 512 + eps), r = 1 / sqrt(t) (f32: IEEE square root, then
+ *     IEEE division), y_i = (x_i * r) * g_i (f32, two rounded products);
  *   the 512 y coded as dsmla_quant_write codes its NoPE values (tiles of 128,
  *   sc = max(amax * f32(1/448), 1.1754944e-38), v = fp8(y / sc)), the tile
  *   scales after them;
