@@ -124,3 +124,20 @@ def test_norm_rope_empty_is_a_no_op(dsix):
                                table.cuda(), torch.empty(0, dtype=torch.int64, device="cuda"), cache)
     torch.cuda.synchronize()
     assert bool((cache == 7).all())
+
+
+@pytest.mark.parametrize("bs,entry,extra", [(16, 656, 0), (48, 672, 16)])
+def test_norm_rope_other_block_sizes_and_edge_positions(dsix, bs, entry, extra):
+    n = 257
+    kv, pe = _inputs(n, bs)
+    gamma, table = W.norm_rope_params(97, seed=bs)
+    rng = np.random.default_rng(bs)
+    pos = rng.integers(0, 97, n).astype(np.int64)
+    pos[:3] = [0, 96, 96]                       # the table's first and last rows
+    nb = -(-n // bs) + 3
+    slots = rng.permutation(nb * bs)[:n].astype(np.int64)
+    slots[7::11] = -1
+    ok, got, ref = _run_both(dsix, kv, pe, gamma, 1e-6, pos, table, slots, nb, bs, entry, extra)
+    assert ok
+    assert np.array_equal(got, ref), np.argwhere(got != ref)[:5]
+    assert dsix.ix_device_status() == 0
