@@ -362,7 +362,7 @@ __device__ __forceinline__ float head_sums_16x256b(uint32_t tbase, const uint64_
                                                    Release&& release) {
     uint32_t buf[2][16];
     float part[4];  // (half 0, key a), (half 0, key b), (half 1, key a), (half 1, key b)
-    uint64_t acc[2][2];
+    uint64_t acc[2];  // keys a and b of the current half: (even heads, odd heads scaled by 2^-25)
     tmem_ld16x256b_x4(tbase, buf[0]);
     tmem_wait_ld(buf[0]);
 #pragma unroll
@@ -372,7 +372,7 @@ __device__ __forceinline__ float head_sums_16x256b(uint32_t tbase, const uint64_
             const int nh = (c + 1) >> 1, ncc = (c + 1) & 1;
             tmem_ld16x256b_x4(tbase + (static_cast<uint32_t>(16 * nh) << 16) + 32 * ncc, buf[(c + 1) & 1]);
         }
-        if (cc == 0) acc[0][0] = acc[0][1] = acc[1][0] = acc[1][1] = 0ull;
+        if (cc == 0) acc[0] = acc[1] = 0ull;
         const uint32_t* v = buf[c & 1];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -380,12 +380,15 @@ __device__ __forceinline__ float head_sums_16x256b(uint32_t tbase, const uint64_
             const uint64_t ta = pack2(fmaxf(__uint_as_float(v[4 * j]), 0.f), relu_scaled(__uint_as_float(v[4 * j + 1])));
             const uint64_t tb =
                 pack2(fmaxf(__uint_as_float(v[4 * j + 2]), 0.f), relu_scaled(__uint_as_float(v[4 * j + 3])));
-            acc[0][j & 1] = fma2(wp, ta, acc[0][j & 1]);
-            acc[1][j & 1] = fma2(wp, tb, acc[1][j & 1]);
+            acc[0] = fma2(wp, ta, acc[0]);
+            acc[1] = fma2(wp, tb, acc[1]);
         }
         if (cc == 1) {
-            part[2 * half] = combine_sums(acc[0][0], acc[0][1]);
-            part[2 * half + 1] = combine_sums(acc[1][0], acc[1][1]);
+            float e, o;
+            unpack2(acc[0], e, o);
+            part[2 * half] = fmaf(o, 0x1p25f, e);
+            unpack2(acc[1], e, o);
+            part[2 * half + 1] = fmaf(o, 0x1p25f, e);
         }
         if (c + 1 < 4) {
             tmem_wait_ld(buf[(c + 1) & 1]);
@@ -675,6 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int qi = 0, job = 0;
             int kbeg = 0, kend = 0;
             int rs0[2], rs1[2];  // visible key range of rows wg and 4 + wg
+            float* orow[2];      // their logits rows
             uint64_t w2[2][8];   // packed head-weight pairs of those rows
             bool new_group = true, have_group = false;
             while (cur.left > 0) {
@@ -695,6 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         rs0[h] = 0;
                         rs1[h] = 0;
                         if (r < a.tq) prefill_row_range(a, r, rs0[h], rs1[h], false);
+                        orow[h] = a.logits + (r < a.tq ? r : 0) * a.ld;
                         const float* wr = wq + (4 * h + wg) * kHeads + 2 * tq;
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
@@ -721,9 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             __syncwarp();
                             if (lane == 0) mbar_arrive(acc_empty + slot);
                         });
-                    if (s >= rs0[h] && s < rs1[h])
-                        a.logits[(static_cast<int64_t>(g) * C::kRows + 4 * h + wg) * a.ld + (s - rs0[h])] =
-                            sum * ksc;
+                    if (s >= rs0[h] && s < rs1[h]) orow[h][s - rs0[h]] = sum * ksc;
                 }
                 if (!ok) break;
                 new_group = cur.advance(a, s_tiles);
