@@ -26,9 +26,9 @@
 //   * Warps 2-17 are four epilogue warpgroups (decode: job j belongs to
 //     warpgroup j % 4; prefill: warpgroup w takes row w of every job, i.e.
 //     rows w and 4 + w of every group): tcgen05.ld of the accumulators, ReLU,
-//     head-weighted sum (packed f32x2 FMA; half of the ReLUs as a saturating
-//     multiply on the FMA pipe, half as FMNMX on the ALU pipe), key scale,
-//     masked store.  Prefill reads the accumulators in the 16x256b shape, in
+//     head-weighted sum (packed f32x2 FMA; the ReLU as a saturating multiply by
+//     2^-25, undone exactly at the end -- decode takes half of the ReLUs as
+//     FMNMX on the ALU pipe instead), key scale, masked store.  Prefill reads the accumulators in the 16x256b shape, in
 //     which a thread meets only 16 heads of a row (for two keys), so its head
 //     weights live in registers for the whole group and no shared-memory
 //     traffic competes with the MMA operand reads; a shuffle reduce-scatter
@@ -293,14 +293,6 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
     return d;
 }
 
-// Final sum of two packed accumulators (even heads plain, odd heads scaled by 2^-25).
-__device__ __forceinline__ float combine_sums(uint64_t acc0, uint64_t acc1) {
-    float e0, o0, e1, o1;
-    unpack2(acc0, e0, o0);
-    unpack2(acc1, e1, o1);
-    return (e0 + e1) + (o0 + o1) * 0x1p25f;
-}
-
 // Head-weighted ReLU sums for this thread's key over R query rows: TMEM
 // columns [tbase + 64 r, +64) hold row r's 64 head scores, w[64 r + h] the
 // row's head weights.  The load of 32-column chunk c+1 overlaps the
@@ -362,7 +354,7 @@ __device__ __forceinline__ float head_sums_16x256b(uint32_t tbase, const uint64_
                                                    Release&& release) {
     uint32_t buf[2][16];
     float part[4];  // (half 0, key a), (half 0, key b), (half 1, key a), (half 1, key b)
-    uint64_t acc[2];  // keys a and b of the current half: (even heads, odd heads scaled by 2^-25)
+    uint64_t acc[2];  // keys a and b of the current half: (even heads, odd heads), both scaled by 2^-25
     tmem_ld16x256b_x4(tbase, buf[0]);
     tmem_wait_ld(buf[0]);
 #pragma unroll
@@ -377,18 +369,20 @@ __device__ __forceinline__ float head_sums_16x256b(uint32_t tbase, const uint64_
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const uint64_t wp = w2[4 * cc + j];
-            const uint64_t ta = pack2(fmaxf(__uint_as_float(v[4 * j]), 0.f), relu_scaled(__uint_as_float(v[4 * j + 1])));
+            // both ReLUs as saturating multiplies by 2^-25 (the FMA pipe measured
+            // faster here than splitting them with FMNMX on the ALU pipe)
+            const uint64_t ta = pack2(relu_scaled(__uint_as_float(v[4 * j])), relu_scaled(__uint_as_float(v[4 * j + 1])));
             const uint64_t tb =
-                pack2(fmaxf(__uint_as_float(v[4 * j + 2]), 0.f), relu_scaled(__uint_as_float(v[4 * j + 3])));
+                pack2(relu_scaled(__uint_as_float(v[4 * j + 2])), relu_scaled(__uint_as_float(v[4 * j + 3])));
             acc[0] = fma2(wp, ta, acc[0]);
             acc[1] = fma2(wp, tb, acc[1]);
         }
-        if (cc == 1) {
+        if (cc == 1) {  // undo the 2^-25 (exact)
             float e, o;
             unpack2(acc[0], e, o);
-            part[2 * half] = fmaf(o, 0x1p25f, e);
+            part[2 * half] = (e + o) * 0x1p25f;
             unpack2(acc[1], e, o);
-            part[2 * half + 1] = fmaf(o, 0x1p25f, e);
+            part[2 * half + 1] = (e + o) * 0x1p25f;
         }
         if (c + 1 < 4) {
             tmem_wait_ld(buf[(c + 1) & 1]);
