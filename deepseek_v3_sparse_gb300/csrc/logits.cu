@@ -377,12 +377,12 @@ __device__ __forceinline__ float head_sums_16x256b(uint32_t tbase, const uint64_
             acc[0] = fma2(wp, ta, acc[0]);
             acc[1] = fma2(wp, tb, acc[1]);
         }
-        if (cc == 1) {  // undo the 2^-25 (exact)
+        if (cc == 1) {  // still scaled by 2^-25; undone once after the reduction
             float e, o;
             unpack2(acc[0], e, o);
-            part[2 * half] = (e + o) * 0x1p25f;
+            part[2 * half] = e + o;
             unpack2(acc[1], e, o);
-            part[2 * half + 1] = (e + o) * 0x1p25f;
+            part[2 * half + 1] = e + o;
         }
         if (c + 1 < 4) {
             tmem_wait_ld(buf[(c + 1) & 1]);
@@ -397,7 +397,7 @@ __device__ __forceinline__ float head_sums_16x256b(uint32_t tbase, const uint64_
     const float x0 = (hi ? part[2] : part[0]) + s0;
     const float x1 = (hi ? part[3] : part[1]) + s1;
     const float r = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
-    return (odd ? x1 : x0) + r;
+    return ((odd ? x1 : x0) + r) * 0x1p25f;  // undo the ReLU's 2^-25 (exact)
 }
 
 template <bool P, int NN>
