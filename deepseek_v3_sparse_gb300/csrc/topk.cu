@@ -58,9 +58,10 @@ struct TopkArgs {
 };
 
 __device__ __forceinline__ uint32_t order_key(float f) {
-    uint32_t b = __float_as_uint(f);
-    if (b == 0x80000000u) b = 0u;  // -0.0 == +0.0
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    // f + 0 turns -0.0 into +0.0 (round to nearest) and leaves every other
+    // value alone; then negative floats flip all bits, others only the sign bit
+    const uint32_t b = __float_as_uint(__fadd_rn(f, 0.0f));
+    return b ^ (static_cast<uint32_t>(static_cast<int32_t>(b) >> 31) | 0x80000000u);
 }
 
 __device__ __forceinline__ void emit(const TopkArgs& a, int64_t r, int b, int pos, int s) {
