@@ -29,6 +29,10 @@ passage it follows; the definitions are:
   rounded once to f32, reciprocal root and scaling in f32), rotation of the
   interleaved RoPE pairs from a cos/sin table (f32, no fused multiply-add, bf16
   nearest-even), then the same 656-byte entry.
+* ``dsmla_sparse_decode``: the consumer of the global top-k indices -- softmax
+  attention of the bf16 query (ql_nope, q_pe) over the dequantised 656-byte
+  entries each token's index row names (fp8 NoPE times its tile scale, bf16
+  RoPE), in double; output and natural-log sum of exponentials per head.
 
 Parity pins live in ``tests/test_oracle_*.py`` (marked ``not gpu``).
 """
@@ -85,7 +89,9 @@ def _load():
         lib.oracle_dsmla_quant_write.argtypes = [P, P, I64, P, P, I64, I32, I64, I64]
         lib.oracle_dsmla_norm_rope_write.argtypes = [P, P, P, ctypes.c_float, P, P, I64, P, I64, P,
                                                      I64, I32, I64, I64]
-        for name in ("oracle_quant_write_k", "oracle_gather_k", "oracle_paged_mqa_logits",
+        lib.oracle_dsmla_sparse_decode.argtypes = [P, P, P, I64, I32, I64, I64, P, I64, I32, I32,
+                                                   ctypes.c_double, P, P]
+        for name in ("oracle_dsmla_sparse_decode", "oracle_quant_write_k", "oracle_gather_k", "oracle_paged_mqa_logits",
                      "oracle_mqa_logits", "oracle_topk_to_global",
                      "oracle_dsmla_quant_write", "oracle_dsmla_norm_rope_write",
                      "oracle_num_threads"):
@@ -255,3 +261,37 @@ def dsmla_norm_rope_write(kv_bf16: np.ndarray, pe_bf16: np.ndarray, gamma_bf16: 
                                               cs.shape[0], _p(sm), kv.shape[0], _p(cache), nb,
                                               block_size, bs * entry, entry)
     return rc == 0
+
+
+def dsmla_sparse_decode(q_nope_bf16: np.ndarray, q_pe_bf16: np.ndarray, cache: np.ndarray,
+                        block_size: int, indices: np.ndarray, sm_scale: float,
+                        block_stride: int = None, entry_stride: int = None):
+    """Sparse MLA decode over the fp8_ds_mla cache.
+
+    q_nope uint16 [T, H, 512], q_pe uint16 [T, H, 64] (bf16 bits); cache uint8,
+    either [num_blocks, block_size, entry_bytes] (dense) or flat bytes with
+    explicit strides; indices int32 [T, topk] global slots (-1: none).
+    Returns (out float64 [T, H, 512], lse float64 [T, H], ok)."""
+    qn = _c(q_nope_bf16, np.uint16)
+    qp = _c(q_pe_bf16, np.uint16)
+    idx = _c(indices, np.int32)
+    assert qn.ndim == 3 and qn.shape[2] == 512 and qp.shape == qn.shape[:2] + (64,)
+    T, H = qn.shape[:2]
+    assert idx.ndim == 2 and idx.shape[0] == T
+    topk = idx.shape[1]
+    cache = np.ascontiguousarray(cache)
+    assert cache.dtype == np.uint8
+    if cache.ndim == 3:
+        nb, bs, entry = cache.shape
+        assert bs == block_size
+        block_stride = bs * entry if block_stride is None else block_stride
+        entry_stride = entry if entry_stride is None else entry_stride
+    else:
+        assert block_stride is not None and entry_stride is not None
+        nb = cache.size // block_stride
+    out = np.empty((T, H, 512), dtype=np.float64)
+    lse = np.empty((T, H), dtype=np.float64)
+    rc = _load().oracle_dsmla_sparse_decode(_p(qn), _p(qp), _p(cache), nb, block_size, block_stride,
+                                            entry_stride, _p(idx), T, H, topk, float(sm_scale),
+                                            _p(out), _p(lse))
+    return out, lse, rc == 0

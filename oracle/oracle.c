@@ -45,6 +45,9 @@
  *   - top-k: order by (value desc, index asc), -0.0 equals +0.0, take
  *     min(k, L), emit in ascending index order, pad with -1; remap
  *     g = block_table[b, s / bs] * bs + s % bs, -1 stays -1.
+ *   - sparse MLA decode: softmax attention of the bf16 query over the
+ *     dequantised entries its global indices name (the reading sits with the
+ *     function).
  *
  * Build: gcc -O3 -fopenmp -fPIC -shared (no -ffast-math).
  */
@@ -528,6 +531,94 @@ int oracle_dsmla_norm_rope_write(const uint16_t* kv, const uint16_t* pe, const u
             out[2 * i + 1] = f32_to_bf16(u + w);
         }
         memcpy(e + 528, out, 128);
+    }
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Sparse MLA decode attention over the fp8_ds_mla cache [DSMLA] [ATOM]       */
+/* ------------------------------------------------------------------------- */
+
+/* The consumer of the global top-k indices: for query token t and head h,
+ * attention over the cache entries its index row names.  [DSMLA] gives the
+ * query as the bf16 pair (ql_nope [512], q_pe [64]) and the 656-byte entry;
+ * [ATOM] gives the per-query 2-D buffer of global paged-KV indices.  Neither
+ * prints the attention itself; the reading is plain scaled-dot-product
+ * attention over the selected entries:
+ *   key j (slot g = indices[t, j] >= 0) at blk = g / bs, off = g % bs:
+ *     k[i] = dec(code[i]) * scale[i / 128]   (i < 512, exact in double)
+ *     k[512 + i] = rope[i]                   (bf16, exact)
+ *     v = k[0 .. 512)                        (the latent is both key and value)
+ *   z_j = sm_scale * (q_nope . k[0..512) + q_pe . k[512..576))
+ *   out[t,h,:] = sum_j exp(z_j - m) v_j / sum_j exp(z_j - m),  m = max_j z_j
+ *   lse[t,h]   = m + log(sum_j exp(z_j - m))   (natural log)
+ * A negative index names no key; a row with no key has out = 0 and
+ * lse = -inf.  An index past the cache is skipped and makes the call return -1.
+ * Everything is in double. */
+int oracle_dsmla_sparse_decode(const uint16_t* q_nope, const uint16_t* q_pe,
+                               const uint8_t* cache, int64_t num_blocks, int block_size,
+                               int64_t block_stride, int64_t entry_stride,
+                               const int32_t* indices, int64_t tokens, int heads, int topk,
+                               double sm_scale, double* out, double* lse)
+{
+    codec_init();
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t t = 0; t < tokens; ++t) {
+        double* kd = (double*)malloc(sizeof(double) * (size_t)(topk > 0 ? topk : 1) * 576);
+        double* z = (double*)malloc(sizeof(double) * (size_t)(topk > 0 ? topk : 1));
+        int* ok = (int*)malloc(sizeof(int) * (size_t)(topk > 0 ? topk : 1));
+        for (int j = 0; j < topk; ++j) {
+            int64_t g = indices[t * topk + j];
+            ok[j] = 0;
+            if (g < 0) continue;
+            if (g / block_size >= num_blocks) { bad = 1; continue; }
+            const uint8_t* e = cache + (g / block_size) * block_stride + (g % block_size) * entry_stride;
+            for (int i = 0; i < 512; ++i) {
+                float sc;
+                memcpy(&sc, e + 512 + 4 * (i / 128), 4);
+                kd[(size_t)j * 576 + i] = oracle_e4m3_decode(e[i]) * (double)sc;
+            }
+            for (int i = 0; i < 64; ++i) {
+                uint16_t r;
+                memcpy(&r, e + 528 + 2 * i, 2);
+                kd[(size_t)j * 576 + 512 + i] = (double)bf16_to_f32(r);
+            }
+            ok[j] = 1;
+        }
+        for (int h = 0; h < heads; ++h) {
+            const uint16_t* qn = q_nope + ((size_t)t * heads + h) * 512;
+            const uint16_t* qp = q_pe + ((size_t)t * heads + h) * 64;
+            double m = -INFINITY;
+            for (int j = 0; j < topk; ++j) {
+                if (!ok[j]) continue;
+                const double* k = kd + (size_t)j * 576;
+                double s = 0.0;
+                for (int i = 0; i < 512; ++i) s += (double)bf16_to_f32(qn[i]) * k[i];
+                for (int i = 0; i < 64; ++i) s += (double)bf16_to_f32(qp[i]) * k[512 + i];
+                z[j] = sm_scale * s;
+                if (z[j] > m) m = z[j];
+            }
+            double* o = out + ((size_t)t * heads + h) * 512;
+            for (int i = 0; i < 512; ++i) o[i] = 0.0;
+            if (m == -INFINITY) {
+                lse[(size_t)t * heads + h] = -INFINITY;
+                continue;
+            }
+            double l = 0.0;
+            for (int j = 0; j < topk; ++j) {
+                if (!ok[j]) continue;
+                const double p = exp(z[j] - m);
+                l += p;
+                const double* v = kd + (size_t)j * 576;
+                for (int i = 0; i < 512; ++i) o[i] += p * v[i];
+            }
+            for (int i = 0; i < 512; ++i) o[i] /= l;
+            lse[(size_t)t * heads + h] = m + log(l);
+        }
+        free(kd);
+        free(z);
+        free(ok);
     }
     return bad ? -1 : 0;
 }
