@@ -36,6 +36,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 DECODE_BYTES_PER_KEY = 132        # 128 fp8 values + one fp32 scale
 PREFILL_FLOP_PER_PAIR = 2 * 64 * 128
 NORM_ROPE_BYTES_PER_TOKEN = 1024 + 128 + 8 + 8 + 256 + 656  # fused norm/RoPE ds_mla write
+SPARSE_DECODE_ENTRY = 656  # bytes of one fp8_ds_mla entry read by the sparse MLA decode
 
 
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "traffic_mixed_long.txt")
@@ -91,6 +92,25 @@ def peaks():
 # ---------------------------------------------------------------------------
 # distributed plumbing (replicas only)
 # ---------------------------------------------------------------------------
+def sparse_decode_line(d, pk):
+    """Bench entry of the sparse MLA decode: tokens/s and both rooflines.
+    Per token (128 heads, topk indices, all valid): 2 * 128 * topk * (576 + 512)
+    flop; bytes = topk * (656 entry + 4 index) + 128 * (576 * 2 query + 512 * 2
+    output + 4 lse)."""
+    T, topk, ms = d["units"], d["topk"], d["ms"]
+    flop = 2.0 * 128 * d["valid"] * (576 + 512)
+    byts = T * (topk * (SPARSE_DECODE_ENTRY + 4) + 128 * (576 * 2 + 512 * 2 + 4))
+    tfs = flop / (ms / 1e3) / 1e12
+    gbs = byts / (ms / 1e3) / 1e9
+    return {"ms": ms, "tokens_per_s": T / (ms / 1e3), "units": T, "topk": topk, "heads": 128,
+            "tensor": {"achieved": tfs, "unit": "TFLOP/s", "peak": pk["bf16_tflops"],
+                       "frac": tfs / pk["bf16_tflops"], "per_unit": "2*128*topk*(576+512) flop per token"},
+            "hbm": {"achieved": gbs, "unit": "GB/s", "peak": pk["hbm_gbs"], "frac": gbs / pk["hbm_gbs"],
+                    "per_unit": "topk*660 + 128*(1152+1024+4) B per token"},
+            "bound": "tensor" if flop / (pk["bf16_tflops"] * 1e12) > byts / (pk["hbm_gbs"] * 1e9) else "hbm",
+            "l2": "flushed between launches (256 MB read)"}
+
+
 def dist_init():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -287,6 +307,41 @@ def gpu_arm(args, world, rank, local):
         del flush, nr_cache, nr_in
         if dsix.ix_device_status() != 0:
             raise RuntimeError("device status set by the fused norm/rope write")
+
+    # ---- the consumer of the decode indices: sparse MLA decode attention of the
+    # decode tokens (128 heads) over top-k entries of the fp8_ds_mla cache, each
+    # token's indices drawn from its own 131072-position context; entries written
+    # by dsmla_quant_write.  Timed like the row above (L2 flushed per launch).
+    if wl.n_decode > 0:
+        T = wl.n_decode * wl.next_n
+        ctx = int(wl.context_lens.max())
+        x = W.sparse_decode_inputs(T, wl.topk, ctx, seed=17)
+        mla_cache = torch.zeros(x.num_blocks, 64, 656, dtype=torch.uint8, device=dev)
+        dsix.dsmla_quant_write(x.nope_bf16.to(dev), x.rope_bf16.to(dev), torch.from_numpy(x.slots).to(dev),
+                               mla_cache, stream=stream)
+        sd = dict(qn=x.q_nope.to(dev), qp=x.q_pe.to(dev), idx=torch.from_numpy(x.indices).to(dev),
+                  out=torch.empty(T, 128, 512, dtype=torch.bfloat16, device=dev),
+                  lse=torch.empty(T, 128, dtype=torch.float32, device=dev),
+                  ws=torch.empty(dsix.dsmla_sparse_decode_workspace_size(T, 128, wl.topk), dtype=torch.uint8,
+                                 device=dev))
+        flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+        sink = torch.empty((), dtype=torch.float32, device=dev)
+        sdc = lambda: dsix.dsmla_sparse_decode(sd["qn"], sd["qp"], mla_cache, sd["idx"], x.sm_scale, sd["out"],
+                                               sd["lse"], sd["ws"], stream=stream)
+        for _ in range(3):
+            sdc()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+        for a, b in evs:
+            torch.sum(flush, 0, out=sink)
+            a.record(stream)
+            sdc()
+            b.record(stream)
+        torch.cuda.synchronize()
+        next_rows["dsmla_sparse_decode"] = dict(ms=float(np.mean([a.elapsed_time(b) for a, b in evs])), units=T,
+                                                topk=wl.topk, valid=int((x.indices >= 0).sum()))
+        del flush, mla_cache, sd
+        if dsix.ix_device_status() != 0:
+            raise RuntimeError("device status set by the sparse MLA decode")
 
     # ---- end to end through the public API: pinned host inputs in, indices out.
     # Two step instances alternate, so the host-to-device copy of step i+1's
@@ -552,6 +607,9 @@ def main():
             "gpu_launches": step.kernels_per_step() * args.steps,
             "clocks": r["clocks"], "device_status": r["status"]}
     for n, d in r["next_rows"].items():  # rows beyond the step, timed on their own
+        if n == "dsmla_sparse_decode":
+            line.setdefault("next_rows", {})[n] = sparse_decode_line(d, pk)
+            continue
         gbs = d["units"] * NORM_ROPE_BYTES_PER_TOKEN / (d["ms"] / 1e3) / 1e9
         line.setdefault("next_rows", {})[n] = {
             "ms": d["ms"], "achieved": gbs, "unit": "GB/s", "peak": pk["hbm_gbs"],

@@ -23,7 +23,8 @@ import torch
 __all__ = [
     "DsixError", "load", "ix_status_string", "ix_device_status", "ix_quant_write_k",
     "ix_gather_k", "ix_paged_mqa_logits", "ix_mqa_logits", "ix_topk_to_global",
-    "dsmla_quant_write", "dsmla_norm_rope_write", "LIB_PATH", "HEADS", "HEAD_DIM", "BLOCK_SIZE",
+    "dsmla_quant_write", "dsmla_norm_rope_write", "dsmla_sparse_decode",
+    "dsmla_sparse_decode_workspace_size", "MLA_HEADS", "LIB_PATH", "HEADS", "HEAD_DIM", "BLOCK_SIZE",
 ]
 
 HEADS = 64
@@ -58,6 +59,9 @@ _SIGNATURES = {
     "dsmla_quant_write": ([_P, _P, _I64, _P, _P, _I64, _I32, _I64, _I64, _P], _I32),
     "dsmla_norm_rope_write": ([_P, _P, _P, ctypes.c_float, _P, _P, _I64, _P, _I64, _P, _I64, _I32,
                                _I64, _I64, _P], _I32),
+    "dsmla_sparse_decode_workspace_size": ([_I64, _I32, _I32], ctypes.c_size_t),
+    "dsmla_sparse_decode": ([_P, _P, _P, _I64, _I32, _I64, _I64, _P, _I64, _I32, _I32, ctypes.c_float,
+                             _P, _P, _P, ctypes.c_size_t, _P], _I32),
 }
 
 
@@ -219,3 +223,30 @@ def dsmla_norm_rope_write(kv_bf16: torch.Tensor, pe_bf16: torch.Tensor, gamma_bf
         kv_bf16.shape[0], _dev(cache, "cache", (torch.uint8,)), nb, bs, cache.stride(0),
         cache.stride(1), _stream(stream))
     _check(rc, "dsmla_norm_rope_write")
+
+
+MLA_HEADS = 128
+
+
+def dsmla_sparse_decode_workspace_size(tokens: int, heads: int, topk: int) -> int:
+    """Bytes of scratch dsmla_sparse_decode needs for this shape."""
+    return int(load().dsmla_sparse_decode_workspace_size(int(tokens), int(heads), int(topk)))
+
+
+def dsmla_sparse_decode(q_nope_bf16: torch.Tensor, q_pe_bf16: torch.Tensor, cache: torch.Tensor,
+                        indices: torch.Tensor, sm_scale: float, out: torch.Tensor, lse: torch.Tensor,
+                        workspace: torch.Tensor, stream=None) -> None:
+    """q_nope [T, 128, 512] bf16; q_pe [T, 128, 64] bf16; cache uint8
+    [num_blocks, block_size, 656+]; indices int32 [T, topk] global slots (-1:
+    none); out [T, 128, 512] bf16 and lse [T, 128] f32 (written); workspace
+    uint8 of at least dsmla_sparse_decode_workspace_size(T, 128, topk) bytes."""
+    nb, bs, entry = cache.shape
+    T, H = q_nope_bf16.shape[:2]
+    topk = indices.shape[1]
+    rc = load().dsmla_sparse_decode(
+        _dev(q_nope_bf16, "q_nope_bf16", _BF16), _dev(q_pe_bf16, "q_pe_bf16", _BF16),
+        _dev(cache, "cache", (torch.uint8,)), nb, bs, cache.stride(0), cache.stride(1),
+        _dev(indices, "indices", (torch.int32,)), T, H, topk, float(sm_scale),
+        _dev(out, "out", _BF16), _dev(lse, "lse", _F32), _dev(workspace, "workspace", (torch.uint8,)),
+        workspace.numel(), _stream(stream))
+    _check(rc, "dsmla_sparse_decode")

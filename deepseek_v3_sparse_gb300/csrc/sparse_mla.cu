@@ -1,0 +1,629 @@
+// sparse_mla.cu -- sparse MLA decode attention over the fp8_ds_mla cache.
+//
+// The consumer of the global top-k indices: for query token t and head h,
+// softmax attention of the bf16 query (ql_nope [512], q_pe [64]) over the
+// 656-byte cache entries named by row t of the index buffer (vLLM PR #47090,
+// prhub summary: the fp8_ds_mla layout and the bf16 query pair; ROCm/ATOM PR
+// #1094, Technical Details: per-query global paged-KV indices).  Entry of slot g:
+//   k[i] = e4m3(code[i]) * scale[i / 128]  (i < 512),  k[512 + i] = rope[i],
+//   v = k[0, 512);  z_j = sm_scale * (q . k_j);
+//   out = sum_j softmax(z)_j v_j,  lse = log sum_j exp(z_j)  (natural log).
+// A negative index names no key; a token with no key gets out = 0, lse = -inf.
+//
+// GPU layout: one CTA per (token, split of 256 indices), 448 threads, one CTA
+// per SM (512 TMEM columns, ~195 KB of shared memory).
+//   warp 0      MMA issuer (one lane elected once) and TMEM owner
+//   warp 1      TMA producer of the query chunks (bf16, 128-byte swizzle)
+//   warps 2-9   dequantisers: fp8 x tile scale -> bf16 operand tiles written
+//               into shared memory in the 128-byte-swizzled K-major layout
+//   warps 10-13 softmax and epilogue, one thread per head (= TMEM lane)
+// Phase 1  S[128 heads x 256 keys] = Q K^T (tcgen05 kind::f16, M 128, N 256)
+//          into TMEM columns [0, 256), over nine 64-dim chunks (eight NoPE
+//          chunks, then the RoPE chunk), two stages.
+// Phase 2  the softmax threads read their row of S twice (max, then
+//          exponentials), write P in bf16 as the A operand of the next product
+//          and keep the row sums.
+// Phase 3  O[128 x 512] = P V into TMEM columns [0, 512) (S has been read by
+//          then): four chunks of 64 keys, V^T tiles [512 dims x 64 keys]
+//          written by the dequantisers, two N = 256 halves per K step.
+// Epilogue O / sum and the split's lse go to the caller's workspace; a second
+//          kernel merges the splits of each (token, head) into bf16 output.
+// Every wait is bounded (IX_DEV_TIMEOUT, then all roles leave; in-flight
+// copies and MMAs are drained before the CTA frees its TMEM and exits).
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+
+namespace dsix {
+namespace {
+
+constexpr int kH = 128;        // heads = MMA M
+constexpr int kNope = 512;
+constexpr int kEntry = 656;    // bytes of one entry: codes, 4 scales, RoPE
+constexpr int kSplit = 256;    // indices per CTA = N of the first product
+constexpr int kChunks = 9;     // 64-dim chunks of the 576-dim dot product
+constexpr int kKeyChunks = kSplit / 64;
+constexpr int kMaxTopk = 65536;
+constexpr int kThreads = 448;
+constexpr int kMmaWarp = 0, kTmaWarp = 1, kDeqWarp0 = 2, kDeqWarps = 8, kSmWarp0 = 10;
+constexpr int kDeqThreads = kDeqWarps * 32;
+static_assert(kSmWarp0 == kDeqWarp0 + kDeqWarps && (kSmWarp0 + 4) * 32 == kThreads,
+              "four softmax warps after the dequantisers cover the 128 TMEM lanes");
+static_assert(kDeqThreads == kSplit, "one dequantiser thread per key of a split");
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s
+
+// shared memory map (offsets from a 1024-byte-aligned base)
+constexpr int kQBytes = kH * 128;                 // one 64-dim query chunk (16 KB)
+constexpr int kKBytes = kSplit * 128;             // one 64-dim key chunk (32 KB)
+constexpr int kStage1 = kQBytes + kKBytes;        // phase-1 stage (48 KB)
+constexpr int kVtBytes = kNope * 128;             // V^T tile: 512 rows x 64 keys (64 KB)
+constexpr int kRegion = 2 * kVtBytes;             // both phase-1 stages, later both V^T stages
+constexpr int kPOff = kRegion;                    // P: 4 tiles of 128 rows x 64 keys
+constexpr int kPAtom = kH * 128;
+constexpr int kOffOff = kPOff + kKeyChunks * kPAtom;  // int64 entry offset per key (-1: none)
+constexpr int kMaskOff = kOffOff + kSplit * 8;        // validity bits of the 256 keys
+constexpr int kBarOff = kMaskOff + 64;
+constexpr int kNumBars = 12;
+constexpr int kMiscOff = kBarOff + kNumBars * 8;      // tmem base, abort flag, never-raised flag
+constexpr int kSmemUsed = kMiscOff + 64;
+constexpr int kSmemAlloc = kSmemUsed + 1024;
+static_assert(2 * kStage1 <= kRegion, "phase-1 stages fit the shared region");
+static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
+
+struct SmlaArgs {
+    const uint8_t* cache;
+    int64_t num_blocks;
+    int64_t block_stride;
+    int64_t entry_stride;
+    const int32_t* indices;
+    int64_t tokens;
+    int block_size;
+    int topk;
+    int splits;
+    float scale_log2;  // sm_scale * log2(e)
+    float* ws_o;       // [tokens * splits * 128, 512]: O / row sum of each split
+    float* ws_lse;     // [tokens * splits * 128]: natural-log sum of exponentials
+    int* status;
+};
+
+// ---------------------------------------------------------------------------
+// small device helpers of this file
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
+}
+
+// Instruction descriptor, kind::f16: A = B = BF16, D = F32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4)                                // D format: F32
+           | (1u << 7) | (1u << 10)                 // A, B format: BF16
+           | (static_cast<uint32_t>(N >> 3) << 17)  // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24); // M / 16
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// bf16x2 of (lo, hi), round to nearest even; lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two e4m3 codes (low byte = first) -> their exact values as f32.
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t two, float& lo, float& hi) {
+    uint32_t h2;
+    asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(h2) : "r"(two));
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
+}
+
+// Four codes (bytes of w, first in the low byte) times one scale -> 4 bf16.
+__device__ __forceinline__ uint2 deq4(uint32_t w, float sc) {
+    float a, b, c, d;
+    e4m3x2_to_f32(w & 0xFFFFu, a, b);
+    e4m3x2_to_f32(w >> 16, c, d);
+    return make_uint2(pack_bf16(a * sc, b * sc), pack_bf16(c * sc, d * sc));
+}
+
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, status);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Wait that ignores the abort flag (drains in-flight work on the way out);
+// `never` points at a shared-memory word that stays 0.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, volatile int* never, int* status) {
+    mbar_wait(bar, parity, never, status, kDrainLimitNs);
+}
+
+// ---------------------------------------------------------------------------
+// main kernel: one CTA per (token, split)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+    smla_decode_kernel(const __grid_constant__ CUtensorMap tmQn, const __grid_constant__ CUtensorMap tmQp,
+                       const SmlaArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    int64_t* koff = reinterpret_cast<int64_t*>(sm + kOffOff);
+    uint32_t* vmask = reinterpret_cast<uint32_t*>(sm + kMaskOff);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBarOff);
+    uint64_t* full1 = bars;       // [2] query chunk landed + key chunk written
+    uint64_t* empty1 = bars + 2;  // [2] the MMAs of a phase-1 stage are done
+    uint64_t* s_full = bars + 4;  // all of S is in TMEM (phase-1 MMAs done)
+    uint64_t* p_full = bars + 5;  // P written, S read (128 softmax threads)
+    uint64_t* full3 = bars + 6;   // [2] V^T chunk written
+    uint64_t* empty3 = bars + 8;  // [2] the MMAs of a V^T stage are done
+    uint64_t* o_full = bars + 10; // O complete in TMEM
+    uint64_t* mma_done = bars + 11;
+    int* misc = reinterpret_cast<int*>(sm + kMiscOff);
+    volatile int* abort_flag = misc + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t = blockIdx.x / a.splits;
+    const int split = static_cast<int>(blockIdx.x % a.splits);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(full1 + i, 1 + kDeqThreads);
+            mbar_init(empty1 + i, 1);
+            mbar_init(full3 + i, kDeqThreads);
+            mbar_init(empty3 + i, 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(p_full, kH);
+        mbar_init(o_full, 1);
+        mbar_init(mma_done, 1);
+        fence_barrier_init();
+        misc[1] = 0;
+        misc[2] = 0;  // never raised: the abort flag seen by drain waits
+    }
+    if (warp == kTmaWarp && lane == 0) {
+        prefetch_tmap(&tmQn);
+        prefetch_tmap(&tmQp);
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(reinterpret_cast<uint32_t*>(misc), kTmemCols);
+        tmem_relinquish();
+    }
+    // this split's indices -> entry byte offsets (-1: no key); each entry is
+    // pulled into L2 now, so the dequantisers' chunk loads hit L2
+    if (threadIdx.x < kSplit) {
+        const int j = split * kSplit + threadIdx.x;
+        int64_t off = -1;
+        if (j < a.topk) {
+            const int64_t g = __ldg(a.indices + t * a.topk + j);
+            if (g >= 0) {
+                const int64_t blk = g / a.block_size;
+                if (blk < a.num_blocks) {
+                    off = blk * a.block_stride + (g - blk * a.block_size) * a.entry_stride;
+                    prefetch_l2(a.cache + off, kEntry);
+                } else {
+                    flag(a.status, IX_DEV_BAD_SLOT);
+                }
+            }
+        }
+        koff[threadIdx.x] = off;
+        const uint32_t bal = __ballot_sync(0xffffffffu, off >= 0);
+        if (lane == 0) vmask[threadIdx.x >> 5] = bal;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = static_cast<uint32_t>(misc[0]);
+
+    if (warp == kTmaWarp) {
+        // ------------------------------------------------------------ query chunks
+        const bool leader = elect_one();
+        int c = 0;
+        for (; c < kChunks; ++c) {
+            const int stage = c & 1, use = c >> 1;
+            if (use > 0 && !wait_warp(empty1 + stage, (use - 1) & 1, abort_flag, a.status)) break;
+            if (leader) {
+                uint8_t* qdst = sm + stage * kStage1;
+                mbar_arrive_expect_tx(full1 + stage, kQBytes);
+                if (c < 8)
+                    tma_load_2d(qdst, &tmQn, full1 + stage, c * 64, static_cast<int>(t * kH));
+                else
+                    tma_load_2d(qdst, &tmQp, full1 + stage, 0, static_cast<int>(t * kH));
+            }
+            __syncwarp();
+        }
+        // drain: the last copies issued must land before the CTA exits
+        if (leader)
+            for (int i = c > 2 ? c - 2 : 0; i < c; ++i) drain_wait(full1 + (i & 1), (i >> 1) & 1, misc + 2, a.status);
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        const bool leader = elect_one();
+        constexpr uint32_t kId = idesc_bf16_f32(kH, 256);
+        bool ok = true, issued = false;
+        for (int c = 0; c < kChunks; ++c) {
+            const int stage = c & 1;
+            if (!wait_warp(full1 + stage, (c >> 1) & 1, abort_flag, a.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (leader) {
+                const uint32_t qa = smem_u32(sm + stage * kStage1), kb = qa + kQBytes;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem_base, sdesc_k_sw128(qa + 32 * kk), sdesc_k_sw128(kb + 32 * kk), kId,
+                             (c | kk) != 0);
+                mma_commit(empty1 + stage);
+            }
+            issued = true;
+            __syncwarp();
+        }
+        if (ok) {
+            if (leader) mma_commit(s_full);
+            __syncwarp();
+            ok = wait_warp(p_full, 0, abort_flag, a.status);
+        }
+        for (int kc = 0; kc < kKeyChunks && ok; ++kc) {
+            const int stage = kc & 1;
+            if (!wait_warp(full3 + stage, (kc >> 1) & 1, abort_flag, a.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (leader) {
+                const uint32_t pa = smem_u32(sm + kPOff + kc * kPAtom), vb = smem_u32(sm + stage * kVtBytes);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t ad = sdesc_k_sw128(pa + 32 * kk);
+                    mma_bf16(tmem_base, ad, sdesc_k_sw128(vb + 32 * kk), kId, (kc | kk) != 0);
+                    mma_bf16(tmem_base + 256, ad, sdesc_k_sw128(vb + kVtBytes / 2 + 32 * kk), kId, (kc | kk) != 0);
+                }
+                mma_commit(empty3 + stage);
+            }
+            __syncwarp();
+        }
+        if (ok) {
+            if (leader) mma_commit(o_full);
+            __syncwarp();
+        }
+        if (issued) {
+            if (leader) {
+                mma_commit(mma_done);
+                drain_wait(mma_done, 0, misc + 2, a.status);
+            }
+            __syncwarp();
+        }
+    } else if (warp < kDeqWarp0 + kDeqWarps) {
+        // ------------------------------------------------------------ dequantisers
+        const int i = threadIdx.x - kDeqWarp0 * 32;
+        bool ok = true;
+        {
+            // phase 1: thread i writes key i's row of each 64-dim chunk
+            const int64_t off = koff[i];
+            const uint8_t* ent = a.cache + (off < 0 ? 0 : off);
+            for (int c = 0; c < kChunks; ++c) {
+                const int stage = c & 1, use = c >> 1;
+                if (use > 0 && !wait_warp(empty1 + stage, (use - 1) & 1, abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
+                uint4 o[8];
+                if (off < 0) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) o[q] = make_uint4(0u, 0u, 0u, 0u);
+                } else if (c < 8) {
+                    const uint4* src = reinterpret_cast<const uint4*>(ent + c * 64);
+                    const float sc = __ldg(reinterpret_cast<const float*>(ent + kNope) + (c >> 1));
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 w = __ldg(src + q);
+                        const uint2 a0 = deq4(w.x, sc), a1 = deq4(w.y, sc), a2 = deq4(w.z, sc), a3 = deq4(w.w, sc);
+                        o[2 * q] = make_uint4(a0.x, a0.y, a1.x, a1.y);
+                        o[2 * q + 1] = make_uint4(a2.x, a2.y, a3.x, a3.y);
+                    }
+                } else {
+                    const uint4* src = reinterpret_cast<const uint4*>(ent + kNope + 16);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) o[q] = __ldg(src + q);
+                }
+                uint8_t* krow = sm + stage * kStage1 + kQBytes + i * 128;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(krow + ((q ^ (i & 7)) << 4)) = o[q];
+                fence_proxy_async();
+                mbar_arrive(full1 + stage);
+            }
+        }
+        // phase 3: V^T tiles; thread i covers 8 keys (g) x 16 dims (e) of a chunk.
+        // The region is reused, so wait until every phase-1 MMA has read it.
+        if (ok) ok = wait_warp(s_full, 0, abort_flag, a.status);
+        const int g = i & 7, e = i >> 3;
+        for (int kc = 0; kc < kKeyChunks && ok; ++kc) {
+            const int stage = kc & 1, use = kc >> 1;
+            if (use > 0 && !wait_warp(empty3 + stage, (use - 1) & 1, abort_flag, a.status)) {
+                ok = false;
+                break;
+            }
+            uint32_t w[8][4];
+            float sc[8];
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const int64_t ko = koff[kc * 64 + g * 8 + kk];
+                if (ko >= 0) {
+                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.cache + ko + e * 16));
+                    w[kk][0] = v.x;
+                    w[kk][1] = v.y;
+                    w[kk][2] = v.z;
+                    w[kk][3] = v.w;
+                    sc[kk] = __ldg(reinterpret_cast<const float*>(a.cache + ko + kNope) + (e >> 3));
+                } else {
+                    w[kk][0] = w[kk][1] = w[kk][2] = w[kk][3] = 0u;
+                    sc[kk] = 0.0f;
+                }
+            }
+            uint8_t* vt = sm + stage * kVtBytes;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const int d = e * 16 + r;
+                const uint32_t sel = static_cast<uint32_t>((r & 3) | ((4 + (r & 3)) << 4));
+                uint32_t ow[4];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    float lo, hi;
+                    e4m3x2_to_f32(__byte_perm(w[2 * p][r >> 2], w[2 * p + 1][r >> 2], sel), lo, hi);
+                    ow[p] = pack_bf16(lo * sc[2 * p], hi * sc[2 * p + 1]);
+                }
+                *reinterpret_cast<uint4*>(vt + d * 128 + ((g ^ (d & 7)) << 4)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            }
+            fence_proxy_async();
+            mbar_arrive(full3 + stage);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int q4 = warp & 3;
+        const int h = q4 * 32 + lane;
+        const uint32_t trow = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16);
+        float m = -INFINITY, mc = 0.0f, l_exact = 0.0f, l_used = 0.0f;
+        bool ok = wait_warp(s_full, 0, abort_flag, a.status);
+        if (ok) {
+            tc_fence_after();
+            for (int cc = 0; cc < kSplit / 32; ++cc) {
+                uint32_t r[32];
+                tmem_ld32(trow + cc * 32, r);
+                tmem_wait_ld(r);
+                const uint32_t vm = vmask[cc];
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    if ((vm >> k) & 1u) m = fmaxf(m, __uint_as_float(r[k]));
+            }
+            // sm_scale > 0, so the max of the scaled scores is the scaled max
+            mc = m == -INFINITY ? 0.0f : m * a.scale_log2;
+            uint8_t* prow = sm + kPOff + h * 128;
+            for (int cc = 0; cc < kSplit / 32; ++cc) {
+                uint32_t r[32];
+                tmem_ld32(trow + cc * 32, r);
+                tmem_wait_ld(r);
+                const uint32_t vm = vmask[cc];
+                uint32_t pk[16];
+#pragma unroll
+                for (int k = 0; k < 32; k += 2) {
+                    const float p0 = ((vm >> k) & 1u) ? exp2f(fmaf(__uint_as_float(r[k]), a.scale_log2, -mc)) : 0.0f;
+                    const float p1 =
+                        ((vm >> (k + 1)) & 1u) ? exp2f(fmaf(__uint_as_float(r[k + 1]), a.scale_log2, -mc)) : 0.0f;
+                    l_exact += p0 + p1;
+                    const uint32_t b = pack_bf16(p0, p1);
+                    l_used += __uint_as_float(b << 16) + __uint_as_float(b & 0xFFFF0000u);
+                    pk[k >> 1] = b;
+                }
+                uint8_t* atom = prow + (cc >> 1) * kPAtom;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = (cc & 1) * 4 + q;
+                    *reinterpret_cast<uint4*>(atom + ((j ^ (h & 7)) << 4)) =
+                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
+            }
+            tc_fence_before();
+            fence_proxy_async();
+            mbar_arrive(p_full);
+            ok = wait_warp(o_full, 0, abort_flag, a.status);
+        }
+        if (ok) {
+            tc_fence_after();
+            const float inv = l_used > 0.0f ? 1.0f / l_used : 0.0f;
+            const int64_t prow_idx = (t * a.splits + split) * kH + h;
+            float* dst = a.ws_o + prow_idx * kNope;
+            for (int cc = 0; cc < kNope / 32; ++cc) {
+                uint32_t r[32];
+                tmem_ld32(trow + cc * 32, r);
+                tmem_wait_ld(r);
+#pragma unroll
+                for (int k = 0; k < 32; k += 4)
+                    *reinterpret_cast<float4*>(dst + cc * 32 + k) =
+                        make_float4(__uint_as_float(r[k]) * inv, __uint_as_float(r[k + 1]) * inv,
+                                    __uint_as_float(r[k + 2]) * inv, __uint_as_float(r[k + 3]) * inv);
+            }
+            a.ws_lse[prow_idx] = m == -INFINITY ? -INFINITY : (mc + log2f(l_exact)) * 0.69314718055994531f;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// split merge: one warp per (token, head); lane l owns dims 4 (l + 32 q) .. +3
+// ---------------------------------------------------------------------------
+constexpr int kCombineWarps = 8;
+
+__global__ void __launch_bounds__(kCombineWarps * 32)
+    smla_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse, int64_t rows,
+                        int splits, uint16_t* __restrict__ out, float* __restrict__ lse) {
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const int64_t t = row / kH;
+    const int h = static_cast<int>(row % kH);
+    float M = -INFINITY;
+    for (int s = 0; s < splits; ++s) M = fmaxf(M, __ldg(ws_lse + (t * splits + s) * kH + h));
+    float4 acc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.0f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < splits; ++s) {
+            const int64_t pr = (t * splits + s) * kH + h;
+            const float ls = __ldg(ws_lse + pr);
+            if (ls == -INFINITY) continue;  // a split without keys (uniform over the warp)
+            const float w = expf(ls - M);
+            L += w;
+            const float4* src = reinterpret_cast<const float4*>(ws_o + pr * kNope);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 v = __ldg(src + lane + 32 * q);
+                acc[q].x = fmaf(w, v.x, acc[q].x);
+                acc[q].y = fmaf(w, v.y, acc[q].y);
+                acc[q].z = fmaf(w, v.z, acc[q].z);
+                acc[q].w = fmaf(w, v.w, acc[q].w);
+            }
+        }
+    }
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    uint2* dst = reinterpret_cast<uint2*>(out + row * kNope);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        dst[lane + 32 * q] = make_uint2(pack_bf16(acc[q].x * inv, acc[q].y * inv), pack_bf16(acc[q].z * inv, acc[q].w * inv));
+    if (lane == 0) lse[row] = M == -INFINITY ? -INFINITY : M + logf(L);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 map over rows of `cols` values (row pitch `cols` * 2 bytes), box of
+// 64 values x 128 rows, 128-byte swizzle: one query chunk lands in the MMA's
+// K-major layout.
+bool make_query_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t d[2] = {cols, rows};
+    cuuint64_t s[1] = {cols * 2};
+    cuuint32_t b[2] = {64, static_cast<cuuint32_t>(kH)};
+    cuuint32_t e[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), d, s, b, e,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int smem_setup() {  // the dynamic shared memory limit, once per device
+    static std::mutex mu;
+    static std::vector<char> ready;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return IX_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= static_cast<int>(ready.size())) ready.resize(dev + 1, 0);
+    if (!ready[dev]) {
+        if (cudaFuncSetAttribute(smla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
+            cudaSuccess)
+            return IX_ERR_CUDA;
+        ready[dev] = 1;
+    }
+    return IX_OK;
+}
+
+}  // namespace
+}  // namespace dsix
+
+using namespace dsix;
+
+extern "C" size_t dsmla_sparse_decode_workspace_size(int64_t tokens, int heads, int topk) {
+    if (tokens <= 0 || heads <= 0 || topk <= 0) return 0;
+    const int64_t splits = (static_cast<int64_t>(topk) + kSplit - 1) / kSplit;
+    return static_cast<size_t>(tokens * splits * heads) * (kNope + 1) * sizeof(float);
+}
+
+extern "C" int dsmla_sparse_decode(const void* q_nope_bf16, const void* q_pe_bf16, const uint8_t* cache,
+                                   int64_t num_blocks, int block_size, int64_t block_stride_bytes,
+                                   int64_t entry_stride_bytes, const int32_t* indices, int64_t tokens, int heads,
+                                   int topk, float sm_scale, void* out_bf16, float* lse, void* workspace,
+                                   size_t workspace_bytes, ix_stream_t stream) {
+    if (tokens < 0 || num_blocks < 0 || block_stride_bytes < 0 || entry_stride_bytes < 0 || topk < 0)
+        return IX_ERR_SHAPE;
+    if (heads != kH || block_size < 1 || topk < 1 || topk > kMaxTopk) return IX_ERR_UNSUPPORTED;
+    if (!(sm_scale > 0.0f) || !isfinite(sm_scale)) return IX_ERR_UNSUPPORTED;
+    if (tokens == 0) return IX_OK;
+    if (!q_nope_bf16 || !q_pe_bf16 || !indices || !out_bf16 || !lse || (num_blocks > 0 && !cache)) return IX_ERR_NULL;
+    if (entry_stride_bytes < kEntry || block_stride_bytes < static_cast<int64_t>(block_size) * entry_stride_bytes)
+        return IX_ERR_SHAPE;
+    if (!aligned16(q_nope_bf16) || !aligned16(q_pe_bf16) || !aligned16(cache) || !aligned16(out_bf16) ||
+        (block_stride_bytes & 15) || (entry_stride_bytes & 15) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+        (reinterpret_cast<uintptr_t>(indices) & 3u))
+        return IX_ERR_ALIGN;
+    const int splits = (topk + kSplit - 1) / kSplit;
+    const int64_t prow = tokens * splits * kH;
+    if (tokens * kH > INT32_MAX || tokens * splits > INT32_MAX) return IX_ERR_UNSUPPORTED;
+    const size_t need = dsmla_sparse_decode_workspace_size(tokens, heads, topk);
+    if (!workspace || workspace_bytes < need) return IX_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return IX_ERR_ALIGN;
+    int* status = status_ptr();
+    if (!status) return IX_ERR_CUDA;
+    CUtensorMap tmQn{}, tmQp{};
+    if (!make_query_map(&tmQn, q_nope_bf16, kNope, static_cast<uint64_t>(tokens * kH)) ||
+        !make_query_map(&tmQp, q_pe_bf16, 64, static_cast<uint64_t>(tokens * kH)))
+        return IX_ERR_CUDA;
+    const int st = smem_setup();
+    if (st != IX_OK) return st;
+    SmlaArgs a{};
+    a.cache = cache;
+    a.num_blocks = num_blocks;
+    a.block_stride = block_stride_bytes;
+    a.entry_stride = entry_stride_bytes;
+    a.indices = indices;
+    a.tokens = tokens;
+    a.block_size = block_size;
+    a.topk = topk;
+    a.splits = splits;
+    a.scale_log2 = sm_scale * 1.4426950408889634f;
+    a.ws_o = static_cast<float*>(workspace);
+    a.ws_lse = a.ws_o + prow * kNope;
+    a.status = status;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    smla_decode_kernel<<<static_cast<unsigned>(tokens * splits), kThreads, kSmemAlloc, s>>>(tmQn, tmQp, a);
+    if (cudaGetLastError() != cudaSuccess) return IX_ERR_CUDA;
+    const int64_t rows = tokens * kH;
+    smla_combine_kernel<<<static_cast<unsigned>((rows + kCombineWarps - 1) / kCombineWarps), kCombineWarps * 32, 0,
+                          s>>>(a.ws_o, a.ws_lse, rows, splits, static_cast<uint16_t*>(out_bf16), lse);
+    return launch_status();
+}

@@ -2,7 +2,9 @@
  * dsix.h -- C ABI of the GB300 (sm_103a) DeepSeek-V3.2 sparse-attention
  * indexer hot path: indexer-K quantise/write, paged gather, FP8 MQA logits
  * (paged decode and contiguous prefill), per-row top-k with remap to global
- * paged-KV slots, and the fp8_ds_mla cache write.
+ * paged-KV slots, the fp8_ds_mla cache write (alone or fused with the RMSNorm
+ * and RoPE of its token), and the sparse MLA decode attention that consumes the
+ * global indices.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -23,7 +25,8 @@
  *   and ORs a bit into a per-device status word, which ix_device_status()
  *   returns (synchronously) and clears.
  * - Supported shapes: head_dim 128, 64 heads, block_size 64 (the DeepSeek-V3.2
- *   indexer), next_n 1..2.  Anything else returns IX_ERR_UNSUPPORTED.
+ *   indexer), next_n 1..2; 128 query heads for the sparse MLA decode.
+ *   Anything else returns IX_ERR_UNSUPPORTED.
  * - fp8 means OCP E4M3 (bias 7, largest finite 448); conversions round to
  *   nearest even and saturate.
  *
@@ -60,7 +63,7 @@ enum {
     IX_ERR_SHAPE = -2,        /* a size or stride is negative or inconsistent */
     IX_ERR_UNSUPPORTED = -3,  /* head_dim / heads / block_size / next_n / k / ld not supported */
     IX_ERR_ALIGN = -4,        /* a base pointer or stride breaks the stated alignment */
-    IX_ERR_WORKSPACE = -5,    /* reserved */
+    IX_ERR_WORKSPACE = -5,    /* workspace missing or smaller than its stated size */
     IX_ERR_CUDA = -6,         /* the CUDA runtime rejected a launch or a query */
     IX_ERR_DEVICE_CHECK = -7  /* returned by ix_device_status when a device check fired */
 };
@@ -249,6 +252,48 @@ IX_API int dsmla_norm_rope_write(const void* kv_bf16, const void* pe_bf16, const
                       uint8_t* cache, int64_t num_blocks, int block_size,
                       int64_t block_stride_bytes, int64_t entry_stride_bytes,
                       ix_stream_t stream);
+
+/*
+ * dsmla_sparse_decode -- sparse MLA decode attention, the consumer of the
+ * global top-k indices (vLLM PR #47090, prhub summary: the FlashMLA sparse path
+ * takes the bf16 query pair (ql_nope, q_pe) and the fp8_ds_mla cache; ROCm/ATOM
+ * PR #1094, Technical Details: a per-query buffer of global paged-KV indices).
+ * The pages print no attention formula; this entry point computes plain
+ * softmax attention over the selected entries.  For token t and head h, with
+ * the entry of slot g = indices[t*topk + j] >= 0 at
+ * cache + (g / block_size) * block_stride_bytes + (g % block_size) * entry_stride_bytes:
+ *   k[i] = e4m3(code[i]) * scale[i / 128]  (i < 512),  k[512 + i] = rope[i],
+ *   v = k[0, 512),  z_j = sm_scale * (q_nope[t,h] . k[0,512) + q_pe[t,h] . k[512,576)),
+ *   out[t,h,:] = sum_j exp(z_j - m) v_j / sum_j exp(z_j - m),  m = max_j z_j,
+ *   lse[t,h] = m + ln(sum_j exp(z_j - m)).
+ * A negative index names no key; a token with no key gets out = 0 and
+ * lse = -inf.  An index past the pool sets IX_DEV_BAD_SLOT and is treated as
+ * none.  Duplicate indices count once each.
+ * Arithmetic: keys and values are dequantised to bf16 (f32 product, then
+ * nearest-even), both products run on the tensor cores in bf16 with f32
+ * accumulation, the softmax weights are rounded to bf16, the output to bf16.
+ *   q_nope_bf16  bf16 [tokens, heads, 512], contiguous, 16-byte aligned
+ *   q_pe_bf16    bf16 [tokens, heads, 64], contiguous, 16-byte aligned
+ *   cache        fp8_ds_mla entries (see dsmla_quant_write), 16-byte aligned;
+ *                block_stride_bytes and entry_stride_bytes multiples of 16,
+ *                entry_stride_bytes >= 656, block_stride_bytes >=
+ *                block_size * entry_stride_bytes
+ *   indices      int32 [tokens, topk] global slots (-1: none)
+ *   heads        must be 128;  1 <= topk <= 65536;  sm_scale > 0 and finite
+ *   out_bf16     bf16 [tokens, heads, 512], 16-byte aligned (written)
+ *   lse          f32 [tokens, heads] (written)
+ *   workspace    16-byte aligned device scratch of at least
+ *                dsmla_sparse_decode_workspace_size(tokens, heads, topk) bytes
+ *                (per split of 256 indices: its normalised output and lse);
+ *                IX_ERR_WORKSPACE if missing or smaller.  Owned by the caller,
+ *                in use until the call's work on `stream` completes.
+ */
+IX_API size_t dsmla_sparse_decode_workspace_size(int64_t tokens, int heads, int topk);
+IX_API int dsmla_sparse_decode(const void* q_nope_bf16, const void* q_pe_bf16, const uint8_t* cache,
+                    int64_t num_blocks, int block_size, int64_t block_stride_bytes,
+                    int64_t entry_stride_bytes, const int32_t* indices, int64_t tokens,
+                    int heads, int topk, float sm_scale, void* out_bf16, float* lse,
+                    void* workspace, size_t workspace_bytes, ix_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -16,7 +16,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "dsix.h")
 
-IX_OK, IX_ERR_NULL, IX_ERR_SHAPE, IX_ERR_UNSUPPORTED, IX_ERR_ALIGN = 0, -1, -2, -3, -4
+IX_OK, IX_ERR_NULL, IX_ERR_SHAPE, IX_ERR_UNSUPPORTED, IX_ERR_ALIGN, IX_ERR_WORKSPACE = 0, -1, -2, -3, -4, -5
 
 pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and
                                 not os.path.exists("/usr/local/cuda/bin/nvcc"),
@@ -38,7 +38,7 @@ def _declared():
 
 def test_exports_match_header(lib):
     names = _declared()
-    assert len(names) == 9
+    assert len(names) == 11
     for n in names:
         assert hasattr(lib, n), n
     out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True,
@@ -145,6 +145,39 @@ def test_dsmla_norm_rope_host_checks(lib):
     assert f(*args(pe=None)) == IX_ERR_NULL
     assert f(*args(cache=None)) == IX_ERR_NULL
     assert f(*args(kv=None, pe=None, g=None, pos=None, cache=None, n=0)) == IX_OK
+
+
+def test_dsmla_sparse_decode_host_checks(lib):
+    f = lib.dsmla_sparse_decode
+    ws = lib.dsmla_sparse_decode_workspace_size
+    # 3 tokens x 128 heads x ceil(600 / 256) = 3 splits, 513 floats per (split, head)
+    assert ws(3, 128, 600) == 3 * 3 * 128 * 513 * 4
+    assert ws(0, 128, 600) == 0 and ws(3, 128, 0) == 0
+    need = ws(3, 128, 600)
+
+    def args(**kw):
+        return [kw.get("qn", A16), kw.get("qp", A16), kw.get("cache", A16), 8, 64, kw.get("bstride", 64 * 656),
+                kw.get("entry", 656), kw.get("idx", A16), kw.get("tokens", 3), kw.get("heads", 128),
+                kw.get("topk", 600), kw.get("scale", 0.07), kw.get("out", A16), kw.get("lse", A16),
+                kw.get("ws", A16), kw.get("ws_bytes", need), None]
+
+    assert f(*args(tokens=-1)) == IX_ERR_SHAPE
+    assert f(*args(heads=64)) == IX_ERR_UNSUPPORTED
+    assert f(*args(topk=0)) == IX_ERR_UNSUPPORTED
+    assert f(*args(topk=65537)) == IX_ERR_UNSUPPORTED
+    assert f(*args(scale=0.0)) == IX_ERR_UNSUPPORTED
+    assert f(*args(scale=float("inf"))) == IX_ERR_UNSUPPORTED
+    assert f(*args(qn=None)) == IX_ERR_NULL
+    assert f(*args(idx=None)) == IX_ERR_NULL
+    assert f(*args(entry=640)) == IX_ERR_SHAPE
+    assert f(*args(bstride=63 * 656)) == IX_ERR_SHAPE
+    assert f(*args(entry=664, bstride=64 * 664)) == IX_ERR_ALIGN
+    assert f(*args(qp=A1)) == IX_ERR_ALIGN
+    assert f(*args(out=P(0x10008))) == IX_ERR_ALIGN
+    assert f(*args(idx=P(0x10002))) == IX_ERR_ALIGN
+    assert f(*args(ws=None)) == IX_ERR_WORKSPACE
+    assert f(*args(ws_bytes=need - 1)) == IX_ERR_WORKSPACE
+    assert f(*args(tokens=0, qn=None, qp=None, cache=None, idx=None, out=None, lse=None, ws=None)) == IX_OK
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

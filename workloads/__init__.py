@@ -294,3 +294,57 @@ def bf16_bits(x: torch.Tensor) -> np.ndarray:
 
 def u8(x: torch.Tensor) -> np.ndarray:
     return x.contiguous().numpy()
+
+
+@dataclass
+class SparseDecodeInputs:
+    """Inputs of one sparse MLA decode call (attention over the fp8_ds_mla cache).
+
+    The cache entries come from ``nope_bf16`` / ``rope_bf16`` written at
+    ``slots``; ``indices`` [tokens, topk] names, per token, distinct slots drawn
+    from its own context (the shape of a top-k row), padded with -1 when the
+    context is shorter than topk."""
+    q_nope: torch.Tensor  # bf16 [T, 128, 512]
+    q_pe: torch.Tensor  # bf16 [T, 128, 64]
+    nope_bf16: torch.Tensor  # bf16 [n, 512]: values written into the cache
+    rope_bf16: torch.Tensor  # bf16 [n, 64]
+    slots: np.ndarray  # int64 [n]: where entry i is written
+    indices: np.ndarray  # int32 [T, topk]
+    num_blocks: int
+    sm_scale: float
+
+
+MLA_HEADS = 128
+
+
+def sparse_decode_inputs(tokens: int, topk: int, ctx: int, *, seed: int = 0, q_scale: float = 1.0,
+                         block_size: int = BLOCK_SIZE) -> SparseDecodeInputs:
+    """Token t attends over a context of ``ctx`` cached positions held in its
+    own random blocks; its index row takes min(topk, ctx) distinct positions of
+    that context (uniform without replacement, in random order) and pads with
+    -1.  Only the selected positions are written into the cache.  q: N(0,1) *
+    q_scale in bf16; cache values drawn like the fp8_ds_mla inputs above;
+    sm_scale = 1/sqrt(192) (the 128 + 64 query-key head width of DeepSeek-V3)."""
+    g = torch.Generator().manual_seed(seed)
+    blocks_per_ctx = -(-ctx // block_size)
+    num_blocks = tokens * blocks_per_ctx
+    perm = torch.randperm(num_blocks, generator=g).numpy()
+    q_nope = _bf16(torch.randn(tokens, MLA_HEADS, NOPE_DIM, generator=g) * q_scale)
+    q_pe = _bf16(torch.randn(tokens, MLA_HEADS, ROPE_DIM, generator=g) * q_scale)
+    take = min(topk, ctx)
+    indices = np.full((tokens, topk), -1, np.int32)
+    slots = []
+    for t in range(tokens):
+        pos = torch.randperm(ctx, generator=g)[:take].numpy()
+        table = perm[t * blocks_per_ctx:(t + 1) * blocks_per_ctx]
+        gl = table[pos // block_size].astype(np.int64) * block_size + pos % block_size
+        indices[t, :take] = gl
+        slots.append(gl)
+    slots = np.concatenate(slots) if slots else np.zeros(0, np.int64)
+    n = slots.shape[0]
+    nope = torch.randn(n, NOPE_DIM, generator=g)
+    out = torch.rand(n, NOPE_DIM, generator=g) < 0.001
+    nope = _bf16(torch.where(out, nope * 20, nope))
+    rope = _bf16(torch.randn(n, ROPE_DIM, generator=g))
+    return SparseDecodeInputs(q_nope, q_pe, nope, rope, slots.astype(np.int64), indices, num_blocks,
+                              1.0 / math.sqrt(192.0))
