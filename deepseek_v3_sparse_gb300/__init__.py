@@ -24,7 +24,7 @@ __all__ = [
     "DsixError", "load", "ix_status_string", "ix_device_status", "ix_quant_write_k",
     "ix_gather_k", "ix_paged_mqa_logits", "ix_mqa_logits", "ix_topk_to_global",
     "dsmla_quant_write", "dsmla_norm_rope_write", "dsmla_sparse_decode",
-    "dsmla_sparse_decode_workspace_size", "MLA_HEADS", "LIB_PATH", "HEADS", "HEAD_DIM", "BLOCK_SIZE",
+    "dsmla_sparse_decode_workspace_size", "dsmla_sparse_decode_noalloc", "MLA_HEADS", "LIB_PATH", "HEADS", "HEAD_DIM", "BLOCK_SIZE",
 ]
 
 HEADS = 64
@@ -62,6 +62,8 @@ _SIGNATURES = {
     "dsmla_sparse_decode_workspace_size": ([_I64, _I32, _I32], ctypes.c_size_t),
     "dsmla_sparse_decode": ([_P, _P, _P, _I64, _I32, _I64, _I64, _P, _I64, _I32, _I32, ctypes.c_float,
                              _P, _P, _P, ctypes.c_size_t, _P], _I32),
+    "dsmla_sparse_decode_noalloc": ([_P, _P, _P, _I64, _I32, _I64, _I64, _P, _I64, _I32, _I32,
+                                     ctypes.c_float, _P, _P, _P], _I32),
 }
 
 
@@ -250,3 +252,18 @@ def dsmla_sparse_decode(q_nope_bf16: torch.Tensor, q_pe_bf16: torch.Tensor, cach
         _dev(out, "out", _BF16), _dev(lse, "lse", _F32), _dev(workspace, "workspace", (torch.uint8,)),
         workspace.numel(), _stream(stream))
     _check(rc, "dsmla_sparse_decode")
+
+
+def dsmla_sparse_decode_noalloc(q_nope_bf16: torch.Tensor, q_pe_bf16: torch.Tensor, cache: torch.Tensor,
+                                indices: torch.Tensor, sm_scale: float, out: torch.Tensor, lse: torch.Tensor,
+                                stream=None) -> None:
+    """dsmla_sparse_decode with the library's own file-scope scratch (no
+    workspace argument; tokens * ceil(topk / 256) <= 128)."""
+    nb, bs, entry = cache.shape
+    T, H = q_nope_bf16.shape[:2]
+    rc = load().dsmla_sparse_decode_noalloc(
+        _dev(q_nope_bf16, "q_nope_bf16", _BF16), _dev(q_pe_bf16, "q_pe_bf16", _BF16),
+        _dev(cache, "cache", (torch.uint8,)), nb, bs, cache.stride(0), cache.stride(1),
+        _dev(indices, "indices", (torch.int32,)), T, H, indices.shape[1], float(sm_scale),
+        _dev(out, "out", _BF16), _dev(lse, "lse", _F32), _stream(stream))
+    _check(rc, "dsmla_sparse_decode_noalloc")

@@ -18,8 +18,8 @@
 //               into shared memory in the 128-byte-swizzled K-major layout
 //   warps 10-13 softmax and epilogue, one thread per head (= TMEM lane)
 // Phase 1  S[128 heads x 256 keys] = Q K^T (tcgen05 kind::f16, M 128, N 256)
-//          into TMEM columns [0, 256), over nine 64-dim chunks (eight NoPE
-//          chunks, then the RoPE chunk), two stages.
+//          into TMEM columns [0, 256), over nine 64-dim chunks (the RoPE
+//          chunk, then eight NoPE chunks), two stages.
 // Phase 2  the softmax threads read their row of S twice (max, then
 //          exponentials), write P in bf16 as the A operand of the next product
 //          and keep the row sums.
@@ -240,10 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) {
                 uint8_t* qdst = sm + stage * kStage1;
                 mbar_arrive_expect_tx(full1 + stage, kQBytes);
-                if (c < 8)
-                    tma_load_2d(qdst, &tmQn, full1 + stage, c * 64, static_cast<int>(t * kH));
-                else
+                if (c == 0)  // chunk 0: the RoPE part; chunks 1-8: NoPE dims 64 (c - 1) ..
                     tma_load_2d(qdst, &tmQp, full1 + stage, 0, static_cast<int>(t * kH));
+                else
+                    tma_load_2d(qdst, &tmQn, full1 + stage, (c - 1) * 64, static_cast<int>(t * kH));
             }
             __syncwarp();
         }
@@ -314,68 +314,90 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = threadIdx.x - kDeqWarp0 * 32;
         bool ok = true;
         {
-            // phase 1: thread i writes key i's row of each 64-dim chunk
+            // phase 1: thread i writes key i's row of each 64-dim chunk: chunk 0
+            // is the RoPE part (a plain copy), chunks 1-8 the NoPE codes times
+            // their tile scale.  The NoPE loads run two chunks ahead of the
+            // conversion, so their latency overlaps the conversion and the stage
+            // waits.  A key without an entry keeps zero codes and a zero scale.
             const int64_t off = koff[i];
-            const uint8_t* ent = a.cache + (off < 0 ? 0 : off);
-            for (int c = 0; c < kChunks; ++c) {
-                const int stage = c & 1, use = c >> 1;
-                if (use > 0 && !wait_warp(empty1 + stage, (use - 1) & 1, abort_flag, a.status)) {
-                    ok = false;
-                    break;
-                }
-                uint4 o[8];
-                if (off < 0) {
+            const bool valid = off >= 0;
+            const uint8_t* ent = a.cache + (valid ? off : 0);
+            uint4 o[8], ra[4], rb[4];
+            float sa = 0.0f, sb = 0.0f;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) o[q] = make_uint4(0u, 0u, 0u, 0u);
-                } else if (c < 8) {
-                    const uint4* src = reinterpret_cast<const uint4*>(ent + c * 64);
-                    const float sc = __ldg(reinterpret_cast<const float*>(ent + kNope) + (c >> 1));
+            for (int q = 0; q < 8; ++q) o[q] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint4 w = __ldg(src + q);
-                        const uint2 a0 = deq4(w.x, sc), a1 = deq4(w.y, sc), a2 = deq4(w.z, sc), a3 = deq4(w.w, sc);
-                        o[2 * q] = make_uint4(a0.x, a0.y, a1.x, a1.y);
-                        o[2 * q + 1] = make_uint4(a2.x, a2.y, a3.x, a3.y);
-                    }
-                } else {
-                    const uint4* src = reinterpret_cast<const uint4*>(ent + kNope + 16);
+            for (int q = 0; q < 4; ++q) ra[q] = rb[q] = make_uint4(0u, 0u, 0u, 0u);
+            auto load_nope = [&](int n, uint4(&r)[4], float& sc) {  // NoPE dims 64 n .. 64 n + 63
+                const uint4* src = reinterpret_cast<const uint4*>(ent + n * 64);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) o[q] = __ldg(src + q);
-                }
+                for (int q = 0; q < 4; ++q) r[q] = __ldg(src + q);
+                sc = __ldg(reinterpret_cast<const float*>(ent + kNope) + (n >> 1));
+            };
+            auto put_row = [&](int stage) {
                 uint8_t* krow = sm + stage * kStage1 + kQBytes + i * 128;
 #pragma unroll
                 for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(krow + ((q ^ (i & 7)) << 4)) = o[q];
                 fence_proxy_async();
                 mbar_arrive(full1 + stage);
+            };
+            if (valid) {
+                const uint4* rope = reinterpret_cast<const uint4*>(ent + kNope + 16);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) o[q] = __ldg(rope + q);
+                load_nope(0, ra, sa);
+                load_nope(1, rb, sb);
+            }
+            put_row(0);  // chunk 0: stage 0, first use
+            auto nope_step = [&](uint4(&r)[4], float& sc, int n) -> bool {
+                const int c = n + 1, stage = c & 1, use = c >> 1;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint2 a0 = deq4(r[q].x, sc), a1 = deq4(r[q].y, sc), a2 = deq4(r[q].z, sc),
+                                a3 = deq4(r[q].w, sc);
+                    o[2 * q] = make_uint4(a0.x, a0.y, a1.x, a1.y);
+                    o[2 * q + 1] = make_uint4(a2.x, a2.y, a3.x, a3.y);
+                }
+                if (valid && n + 2 < 8) load_nope(n + 2, r, sc);
+                if (use > 0 && !wait_warp(empty1 + stage, (use - 1) & 1, abort_flag, a.status)) return false;
+                put_row(stage);
+                return true;
+            };
+#pragma unroll
+            for (int n = 0; n < 8; n += 2) {
+                if (ok) ok = nope_step(ra, sa, n);
+                if (ok) ok = nope_step(rb, sb, n + 1);
             }
         }
-        // phase 3: V^T tiles; thread i covers 8 keys (g) x 16 dims (e) of a chunk.
-        // The region is reused, so wait until every phase-1 MMA has read it.
-        if (ok) ok = wait_warp(s_full, 0, abort_flag, a.status);
+        // phase 3: V^T tiles; thread i covers 8 keys (g) x 16 dims (e) of a
+        // 64-key chunk.  Chunk 0's codes are loaded before the wait for S, and
+        // each later chunk's right after the previous one is stored (one
+        // register set: a second one spills at this kernel's register budget).
+        // The shared region is reused, so nothing is written before every
+        // phase-1 MMA has read it (s_full).
         const int g = i & 7, e = i >> 3;
-        for (int kc = 0; kc < kKeyChunks && ok; ++kc) {
-            const int stage = kc & 1, use = kc >> 1;
-            if (use > 0 && !wait_warp(empty3 + stage, (use - 1) & 1, abort_flag, a.status)) {
-                ok = false;
-                break;
-            }
-            uint32_t w[8][4];
-            float sc[8];
+        uint32_t wa[8][4];
+        auto load_v = [&](int kc, uint32_t(&w)[8][4]) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const int64_t ko = koff[kc * 64 + g * 8 + kk];
-                if (ko >= 0) {
-                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.cache + ko + e * 16));
-                    w[kk][0] = v.x;
-                    w[kk][1] = v.y;
-                    w[kk][2] = v.z;
-                    w[kk][3] = v.w;
-                    sc[kk] = __ldg(reinterpret_cast<const float*>(a.cache + ko + kNope) + (e >> 3));
-                } else {
-                    w[kk][0] = w[kk][1] = w[kk][2] = w[kk][3] = 0u;
-                    sc[kk] = 0.0f;
-                }
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (ko >= 0) v = __ldg(reinterpret_cast<const uint4*>(a.cache + ko + e * 16));
+                w[kk][0] = v.x;
+                w[kk][1] = v.y;
+                w[kk][2] = v.z;
+                w[kk][3] = v.w;
             }
+        };
+        auto put_v = [&](int kc, const uint32_t(&w)[8][4]) -> bool {
+            const int stage = kc & 1, use = kc >> 1;
+            float sc[8];  // tile scales of the 8 keys (same entries as the codes: L1/L2 hits)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const int64_t ko = koff[kc * 64 + g * 8 + kk];
+                sc[kk] = ko >= 0 ? __ldg(reinterpret_cast<const float*>(a.cache + ko + kNope) + (e >> 3)) : 0.0f;
+            }
+            if (use > 0 && !wait_warp(empty3 + stage, (use - 1) & 1, abort_flag, a.status)) return false;
             uint8_t* vt = sm + stage * kVtBytes;
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
@@ -392,6 +414,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async();
             mbar_arrive(full3 + stage);
+            return true;
+        };
+        load_v(0, wa);  // registers only: may run before the region is free
+        if (ok) ok = wait_warp(s_full, 0, abort_flag, a.status);
+        for (int kc = 0; kc < kKeyChunks && ok; ++kc) {
+            if (kc > 0) load_v(kc, wa);
+            ok = put_v(kc, wa);
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
@@ -484,26 +513,45 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
     const int64_t t = row / kH;
     const int h = static_cast<int>(row % kH);
     float M = -INFINITY;
-    for (int s = 0; s < splits; ++s) M = fmaxf(M, __ldg(ws_lse + (t * splits + s) * kH + h));
+    for (int s = lane; s < splits; s += 32) M = fmaxf(M, __ldg(ws_lse + (t * splits + s) * kH + h));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float4 acc[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = 0.0f;
     if (M != -INFINITY) {
-        for (int s = 0; s < splits; ++s) {
-            const int64_t pr = (t * splits + s) * kH + h;
-            const float ls = __ldg(ws_lse + pr);
-            if (ls == -INFINITY) continue;  // a split without keys (uniform over the warp)
-            const float w = expf(ls - M);
-            L += w;
-            const float4* src = reinterpret_cast<const float4*>(ws_o + pr * kNope);
+        // four splits per round, all their loads in flight before the sums; a
+        // split without keys has weight 0 and an all-zero output
+        for (int s0 = 0; s0 < splits; s0 += 4) {
+            float w[4];
+            float4 v[4][4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 v = __ldg(src + lane + 32 * q);
-                acc[q].x = fmaf(w, v.x, acc[q].x);
-                acc[q].y = fmaf(w, v.y, acc[q].y);
-                acc[q].z = fmaf(w, v.z, acc[q].z);
-                acc[q].w = fmaf(w, v.w, acc[q].w);
+            for (int j = 0; j < 4; ++j) {
+                const int s = s0 + j;
+                w[j] = 0.0f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) v[j][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (s < splits) {
+                    const int64_t pr = (t * splits + s) * kH + h;
+                    const float ls = __ldg(ws_lse + pr);
+                    w[j] = ls == -INFINITY ? 0.0f : expf(ls - M);
+                    const float4* src = reinterpret_cast<const float4*>(ws_o + pr * kNope);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) v[j][q] = __ldg(src + lane + 32 * q);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (s0 + j >= splits || w[j] == 0.0f) continue;
+                L += w[j];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[q].x = fmaf(w[j], v[j][q].x, acc[q].x);
+                    acc[q].y = fmaf(w[j], v[j][q].y, acc[q].y);
+                    acc[q].z = fmaf(w[j], v[j][q].z, acc[q].z);
+                    acc[q].w = fmaf(w[j], v[j][q].w, acc[q].w);
+                }
             }
         }
     }
@@ -514,6 +562,12 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
         dst[lane + 32 * q] = make_uint2(pack_bf16(acc[q].x * inv, acc[q].y * inv), pack_bf16(acc[q].z * inv, acc[q].w * inv));
     if (lane == 0) lse[row] = M == -INFINITY ? -INFINITY : M + logf(L);
 }
+
+// File-scope scratch of dsmla_sparse_decode_noalloc: room for the split
+// outputs of kStaticSplits (token, split) pairs -- a decode batch of 16 tokens
+// at top-2048 -- 33.6 MB of device memory, placed when this module loads.
+constexpr int64_t kStaticSplits = 128;
+static __device__ __align__(256) float g_smla_scratch[kStaticSplits * kH * (kNope + 1)];
 
 // ---------------------------------------------------------------------------
 // host side
@@ -626,4 +680,37 @@ extern "C" int dsmla_sparse_decode(const void* q_nope_bf16, const void* q_pe_bf1
     smla_combine_kernel<<<static_cast<unsigned>((rows + kCombineWarps - 1) / kCombineWarps), kCombineWarps * 32, 0,
                           s>>>(a.ws_o, a.ws_lse, rows, splits, static_cast<uint16_t*>(out_bf16), lse);
     return launch_status();
+}
+
+extern "C" int dsmla_sparse_decode_noalloc(const void* q_nope_bf16, const void* q_pe_bf16, const uint8_t* cache,
+                                           int64_t num_blocks, int block_size, int64_t block_stride_bytes,
+                                           int64_t entry_stride_bytes, const int32_t* indices, int64_t tokens,
+                                           int heads, int topk, float sm_scale, void* out_bf16, float* lse,
+                                           ix_stream_t stream) {
+    // the shape checks come first, so a call that cannot fit fails before any CUDA call
+    if (tokens < 0 || topk < 0) return IX_ERR_SHAPE;
+    if (heads != kH || topk < 1 || topk > kMaxTopk) return IX_ERR_UNSUPPORTED;
+    if (tokens == 0)
+        return dsmla_sparse_decode(q_nope_bf16, q_pe_bf16, cache, num_blocks, block_size, block_stride_bytes,
+                                   entry_stride_bytes, indices, tokens, heads, topk, sm_scale, out_bf16, lse,
+                                   nullptr, 0, stream);
+    const int64_t splits = (static_cast<int64_t>(topk) + kSplit - 1) / kSplit;
+    if (tokens > kStaticSplits || tokens * splits > kStaticSplits) return IX_ERR_WORKSPACE;
+    static std::mutex mu;
+    static std::vector<void*> addr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return IX_ERR_CUDA;
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= static_cast<int>(addr.size())) addr.resize(dev + 1, nullptr);
+        if (!addr[dev] && cudaGetSymbolAddress(&addr[dev], g_smla_scratch) != cudaSuccess) {
+            addr[dev] = nullptr;
+            return IX_ERR_CUDA;
+        }
+        scratch = addr[dev];
+    }
+    return dsmla_sparse_decode(q_nope_bf16, q_pe_bf16, cache, num_blocks, block_size, block_stride_bytes,
+                               entry_stride_bytes, indices, tokens, heads, topk, sm_scale, out_bf16, lse, scratch,
+                               sizeof(g_smla_scratch), stream);
 }

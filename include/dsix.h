@@ -295,6 +295,22 @@ IX_API int dsmla_sparse_decode(const void* q_nope_bf16, const void* q_pe_bf16, c
                     int heads, int topk, float sm_scale, void* out_bf16, float* lse,
                     void* workspace, size_t workspace_bytes, ix_stream_t stream);
 
+/*
+ * dsmla_sparse_decode_noalloc -- dsmla_sparse_decode without a caller
+ * workspace: the split outputs go to scratch the library holds in a file-scope
+ * device array (128 (token, split) pairs: tokens * ceil(topk / 256) <= 128,
+ * e.g. 16 tokens at topk 2048), placed once when the library's module loads.
+ * Nothing is allocated by the call.  Same arguments and results as
+ * dsmla_sparse_decode otherwise; a larger call returns IX_ERR_WORKSPACE before
+ * anything is launched.  The scratch is shared: calls on one device must not
+ * run concurrently (calls on one stream never do).
+ */
+IX_API int dsmla_sparse_decode_noalloc(const void* q_nope_bf16, const void* q_pe_bf16, const uint8_t* cache,
+                    int64_t num_blocks, int block_size, int64_t block_stride_bytes,
+                    int64_t entry_stride_bytes, const int32_t* indices, int64_t tokens,
+                    int heads, int topk, float sm_scale, void* out_bf16, float* lse,
+                    ix_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -38,7 +38,7 @@ def _declared():
 
 def test_exports_match_header(lib):
     names = _declared()
-    assert len(names) == 11
+    assert len(names) == 12
     for n in names:
         assert hasattr(lib, n), n
     out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True,
