@@ -314,53 +314,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = threadIdx.x - kDeqWarp0 * 32;
         bool ok = true;
         {
-            // phase 1: thread i writes key i's row of each 64-dim chunk: chunk 0
-            // is the RoPE part (a plain copy), chunks 1-8 the NoPE codes times
-            // their tile scale.  The NoPE loads run two chunks ahead of the
-            // conversion, so their latency overlaps the conversion and the stage
-            // waits.  A key without an entry keeps zero codes and a zero scale.
-            const int64_t off = koff[i];
-            const bool valid = off >= 0;
-            const uint8_t* ent = a.cache + (valid ? off : 0);
+            // phase 1: four threads per key -- thread i covers keys 64 p + i / 4
+            // (p = 0..3) and, of each 64-dim chunk, the 16 dims 16 (i % 4) ..,
+            // i.e. two 16-byte pieces of the key's 128-byte operand row.  A warp
+            // load then reads 8 keys x 64 contiguous bytes.  Chunk 0 is the RoPE
+            // part (a plain copy), chunks 1-8 the NoPE codes times their tile
+            // scale.  The NoPE loads run two chunks ahead of the conversion.  A
+            // key without an entry keeps zero codes and a zero scale.
+            const int qtr = i & 3, kb = i >> 2;
+            const uint8_t* ent[4];
+            bool valid[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const int64_t off = koff[p * 64 + kb];
+                valid[p] = off >= 0;
+                ent[p] = a.cache + (valid[p] ? off : 0);
+            }
             uint4 o[8], ra[4], rb[4];
-            float sa = 0.0f, sb = 0.0f;
+            float sa[4], sb[4];
 #pragma unroll
             for (int q = 0; q < 8; ++q) o[q] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) ra[q] = rb[q] = make_uint4(0u, 0u, 0u, 0u);
-            auto load_nope = [&](int n, uint4(&r)[4], float& sc) {  // NoPE dims 64 n .. 64 n + 63
-                const uint4* src = reinterpret_cast<const uint4*>(ent + n * 64);
+            for (int p = 0; p < 4; ++p) {
+                ra[p] = rb[p] = make_uint4(0u, 0u, 0u, 0u);
+                sa[p] = sb[p] = 0.0f;
+            }
+            auto load_nope = [&](int n, uint4(&r)[4], float(&sc)[4]) {  // NoPE dims 64 n + 16 qtr ..
 #pragma unroll
-                for (int q = 0; q < 4; ++q) r[q] = __ldg(src + q);
-                sc = __ldg(reinterpret_cast<const float*>(ent + kNope) + (n >> 1));
+                for (int p = 0; p < 4; ++p) {
+                    if (valid[p]) {
+                        r[p] = __ldg(reinterpret_cast<const uint4*>(ent[p] + n * 64 + qtr * 16));
+                        sc[p] = __ldg(reinterpret_cast<const float*>(ent[p] + kNope) + (n >> 1));
+                    }
+                }
             };
-            auto put_row = [&](int stage) {
-                uint8_t* krow = sm + stage * kStage1 + kQBytes + i * 128;
+            auto put_rows = [&](int stage) {
+                uint8_t* kt = sm + stage * kStage1 + kQBytes;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(krow + ((q ^ (i & 7)) << 4)) = o[q];
+                for (int p = 0; p < 4; ++p) {
+                    const int row = p * 64 + kb;
+                    uint8_t* krow = kt + row * 128;
+                    *reinterpret_cast<uint4*>(krow + (((2 * qtr) ^ (row & 7)) << 4)) = o[2 * p];
+                    *reinterpret_cast<uint4*>(krow + (((2 * qtr + 1) ^ (row & 7)) << 4)) = o[2 * p + 1];
+                }
                 fence_proxy_async();
                 mbar_arrive(full1 + stage);
             };
-            if (valid) {
-                const uint4* rope = reinterpret_cast<const uint4*>(ent + kNope + 16);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) o[q] = __ldg(rope + q);
-                load_nope(0, ra, sa);
-                load_nope(1, rb, sb);
+            for (int p = 0; p < 4; ++p) {
+                if (valid[p]) {
+                    const uint4* rope = reinterpret_cast<const uint4*>(ent[p] + kNope + 16 + qtr * 32);
+                    o[2 * p] = __ldg(rope);
+                    o[2 * p + 1] = __ldg(rope + 1);
+                }
             }
-            put_row(0);  // chunk 0: stage 0, first use
-            auto nope_step = [&](uint4(&r)[4], float& sc, int n) -> bool {
+            load_nope(0, ra, sa);
+            load_nope(1, rb, sb);
+            put_rows(0);  // chunk 0: stage 0, first use
+            auto nope_step = [&](uint4(&r)[4], float(&sc)[4], int n) -> bool {
                 const int c = n + 1, stage = c & 1, use = c >> 1;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint2 a0 = deq4(r[q].x, sc), a1 = deq4(r[q].y, sc), a2 = deq4(r[q].z, sc),
-                                a3 = deq4(r[q].w, sc);
-                    o[2 * q] = make_uint4(a0.x, a0.y, a1.x, a1.y);
-                    o[2 * q + 1] = make_uint4(a2.x, a2.y, a3.x, a3.y);
+                for (int p = 0; p < 4; ++p) {
+                    const uint2 a0 = deq4(r[p].x, sc[p]), a1 = deq4(r[p].y, sc[p]), a2 = deq4(r[p].z, sc[p]),
+                                a3 = deq4(r[p].w, sc[p]);
+                    o[2 * p] = make_uint4(a0.x, a0.y, a1.x, a1.y);
+                    o[2 * p + 1] = make_uint4(a2.x, a2.y, a3.x, a3.y);
                 }
-                if (valid && n + 2 < 8) load_nope(n + 2, r, sc);
+                if (n + 2 < 8) load_nope(n + 2, r, sc);
                 if (use > 0 && !wait_warp(empty1 + stage, (use - 1) & 1, abort_flag, a.status)) return false;
-                put_row(stage);
+                put_rows(stage);
                 return true;
             };
 #pragma unroll
@@ -476,16 +498,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const float inv = l_used > 0.0f ? 1.0f / l_used : 0.0f;
             const int64_t prow_idx = (t * a.splits + split) * kH + h;
-            float* dst = a.ws_o + prow_idx * kNope;
+            // Rows leave through shared memory (the V^T region is free once O is
+            // complete): each warp stages 32 heads x 32 columns (rows padded to
+            // 36 floats) and writes them as full 128-byte lines, 4 rows per store.
+            float* tile = reinterpret_cast<float*>(sm) + q4 * (32 * 36);
+            float* wrow0 = a.ws_o + (prow_idx - lane) * kNope;  // row of this warp's first head
             for (int cc = 0; cc < kNope / 32; ++cc) {
                 uint32_t r[32];
                 tmem_ld32(trow + cc * 32, r);
                 tmem_wait_ld(r);
 #pragma unroll
                 for (int k = 0; k < 32; k += 4)
-                    *reinterpret_cast<float4*>(dst + cc * 32 + k) =
+                    *reinterpret_cast<float4*>(tile + lane * 36 + k) =
                         make_float4(__uint_as_float(r[k]) * inv, __uint_as_float(r[k + 1]) * inv,
                                     __uint_as_float(r[k + 2]) * inv, __uint_as_float(r[k + 3]) * inv);
+                __syncwarp();
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int row = it * 4 + (lane >> 3), j = lane & 7;
+                    *reinterpret_cast<float4*>(wrow0 + static_cast<int64_t>(row) * kNope + cc * 32 + 4 * j) =
+                        *reinterpret_cast<const float4*>(tile + row * 36 + 4 * j);
+                }
+                __syncwarp();
             }
             a.ws_lse[prow_idx] = m == -INFINITY ? -INFINITY : (mc + log2f(l_exact)) * 0.69314718055994531f;
         }
