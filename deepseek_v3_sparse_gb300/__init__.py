@@ -117,6 +117,29 @@ def _dev(t: torch.Tensor, name: str, dtypes) -> int:
     return t.data_ptr()
 
 
+def _need(ok: bool, what: str):
+    """Shape consistency the C ABI cannot see (it receives bare pointers): an
+    inconsistent tensor would be read or written past its end."""
+    if not ok:
+        raise DsixError(what)
+
+
+def _rows(t, n: int, name: str, cols: Optional[int] = None, dim: int = 2):
+    """t has `dim` dimensions, at least n rows, and (if given) exactly `cols` columns."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    _need(t.dim() == dim and t.shape[0] >= n and (cols is None or t.shape[-1] == cols),
+          f"{name}: shape {tuple(t.shape)}, expected {dim}-D with >= {n} rows"
+          + ("" if cols is None else f" and {cols} columns"))
+
+
+def _len(t, n: int, name: str):
+    """t holds at least n elements."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    _need(t.numel() >= n, f"{name}: {t.numel()} elements, expected >= {n}")
+
+
 def _opt(t, name, dtypes):
     return None if t is None else _dev(t, name, dtypes)
 
@@ -136,7 +159,10 @@ _I64T = (torch.int64,)
 def ix_quant_write_k(k_bf16: torch.Tensor, slot_mapping: torch.Tensor, cache: torch.Tensor,
                      block_size: int = BLOCK_SIZE, stream=None) -> None:
     """k_bf16 [n, 128] bf16; slot_mapping [n] int64; cache uint8 [num_blocks, 8448]."""
+    _rows(k_bf16, 0, "k_bf16")
     n, d = k_bf16.shape
+    _len(slot_mapping, n, "slot_mapping")
+    _rows(cache, 0, "cache", block_size * (d + 4))
     rc = load().ix_quant_write_k(_dev(k_bf16, "k_bf16", _BF16), n, d,
                                  _dev(slot_mapping, "slot_mapping", _I64T),
                                  _dev(cache, "cache", (torch.uint8,)), cache.shape[0], block_size,
@@ -149,6 +175,11 @@ def ix_gather_k(cache: torch.Tensor, block_table: torch.Tensor, cu_seq_lens: tor
                 head_dim: int = HEAD_DIM, stream=None) -> None:
     """block_table [B, stride] int32; cu_seq_lens [B+1] int32; out_k [cap, 128] fp8/u8;
     out_scale [cap] f32."""
+    _len(cu_seq_lens, 1, "cu_seq_lens")
+    _rows(block_table, cu_seq_lens.numel() - 1, "block_table")
+    _rows(cache, 0, "cache", block_size * (head_dim + 4))
+    _rows(out_k, 0, "out_k", head_dim)
+    _len(out_scale, out_k.shape[0], "out_scale")
     rc = load().ix_gather_k(_dev(cache, "cache", (torch.uint8,)), cache.shape[0], block_size,
                             head_dim, _dev(block_table, "block_table", _I32T), block_table.stride(0),
                             _dev(cu_seq_lens, "cu_seq_lens", _I32T), cu_seq_lens.numel() - 1,
@@ -163,7 +194,13 @@ def ix_paged_mqa_logits(q_fp8: torch.Tensor, w: torch.Tensor, cache: torch.Tenso
                         block_size: int = BLOCK_SIZE, stream=None) -> None:
     """q_fp8 [B, next_n, 64, 128] e4m3 (or its uint8 bits); w [B*next_n, 64] f32;
     logits [B*next_n, ld] f32 (written in place)."""
+    _rows(q_fp8, 0, "q_fp8", dim=4)
     B, next_n, H, D = q_fp8.shape
+    _rows(w, B * next_n, "w", H)
+    _rows(logits, B * next_n, "logits")
+    _len(context_lens, B, "context_lens")
+    _rows(block_table, B, "block_table")
+    _rows(cache, 0, "cache", block_size * (D + 4))
     rc = load().ix_paged_mqa_logits(
         _dev(q_fp8, "q_fp8", _U8), _dev(w, "w", _F32), _dev(cache, "cache", (torch.uint8,)),
         cache.shape[0], block_size, _dev(context_lens, "context_lens", _I32T),
@@ -177,7 +214,14 @@ def ix_mqa_logits(q_fp8: torch.Tensor, w: torch.Tensor, k_fp8: torch.Tensor,
                   logits: torch.Tensor, clean_logits: bool = False, stream=None) -> None:
     """q_fp8 [Tq, 64, 128]; w [Tq, 64]; k_fp8 [Tk, 128]; k_scale [Tk]; ks/ke [Tq] int32;
     logits [Tq, ld] f32."""
+    _rows(q_fp8, 0, "q_fp8", dim=3)
     tq, H, D = q_fp8.shape
+    _rows(w, tq, "w", H)
+    _rows(k_fp8, 0, "k_fp8", D)
+    _len(k_scale, k_fp8.shape[0], "k_scale")
+    _len(ks, tq, "ks")
+    _len(ke, tq, "ke")
+    _rows(logits, tq, "logits")
     rc = load().ix_mqa_logits(
         _dev(q_fp8, "q_fp8", _U8), _dev(w, "w", _F32), _dev(k_fp8, "k_fp8", _U8),
         _dev(k_scale, "k_scale", _F32), _dev(ks, "ks", _I32T), _dev(ke, "ke", _I32T), tq,
@@ -191,7 +235,14 @@ def ix_topk_to_global(logits: torch.Tensor, row_len: torch.Tensor, row_req: torc
                       out_local: Optional[torch.Tensor] = None, block_size: int = BLOCK_SIZE,
                       stream=None) -> None:
     """logits [R, ld] f32; row_len/row_req [R] int32; out_global/out_local [R, k] int32."""
+    _rows(logits, 0, "logits")
     R, ld = logits.shape
+    _len(row_len, R, "row_len")
+    _len(row_req, R, "row_req")
+    _rows(block_table, 0, "block_table")
+    _len(out_global, R * int(k), "out_global")
+    if out_local is not None:
+        _len(out_local, R * int(k), "out_local")
     rc = load().ix_topk_to_global(
         _dev(logits, "logits", _F32), ld, R, _dev(row_len, "row_len", _I32T),
         _dev(row_req, "row_req", _I32T), _dev(block_table, "block_table", _I32T),
@@ -203,6 +254,11 @@ def ix_topk_to_global(logits: torch.Tensor, row_len: torch.Tensor, row_req: torc
 def dsmla_quant_write(nope_bf16: torch.Tensor, rope_bf16: torch.Tensor,
                       slot_mapping: torch.Tensor, cache: torch.Tensor, stream=None) -> None:
     """nope [n, 512] bf16; rope [n, 64] bf16; cache uint8 [num_blocks, block_size, 656+]."""
+    _rows(nope_bf16, 0, "nope_bf16", 512)
+    n = nope_bf16.shape[0]
+    _rows(rope_bf16, n, "rope_bf16", 64)
+    _len(slot_mapping, n, "slot_mapping")
+    _rows(cache, 0, "cache", dim=3)
     nb, bs, entry = cache.shape
     rc = load().dsmla_quant_write(
         _dev(nope_bf16, "nope_bf16", _BF16), _dev(rope_bf16, "rope_bf16", _BF16),
@@ -217,6 +273,14 @@ def dsmla_norm_rope_write(kv_bf16: torch.Tensor, pe_bf16: torch.Tensor, gamma_bf
                           slot_mapping: torch.Tensor, cache: torch.Tensor, stream=None) -> None:
     """kv [n, 512] bf16; pe [n, 64] bf16; gamma [512] bf16; positions [n] int64;
     cos_sin [max_pos, 64] f32; cache uint8 [num_blocks, block_size, 656+]."""
+    _rows(kv_bf16, 0, "kv_bf16", 512)
+    n = kv_bf16.shape[0]
+    _rows(pe_bf16, n, "pe_bf16", 64)
+    _len(gamma_bf16, 512, "gamma_bf16")
+    _len(positions, n, "positions")
+    _rows(cos_sin, 0, "cos_sin", 64)
+    _len(slot_mapping, n, "slot_mapping")
+    _rows(cache, 0, "cache", dim=3)
     nb, bs, entry = cache.shape
     rc = load().dsmla_norm_rope_write(
         _dev(kv_bf16, "kv_bf16", _BF16), _dev(pe_bf16, "pe_bf16", _BF16),
@@ -228,6 +292,19 @@ def dsmla_norm_rope_write(kv_bf16: torch.Tensor, pe_bf16: torch.Tensor, gamma_bf
 
 
 MLA_HEADS = 128
+
+
+def _sparse_decode_shapes(q_nope, q_pe, cache, indices, out, lse):
+    _rows(q_nope, 0, "q_nope_bf16", 512, dim=3)
+    T, H = q_nope.shape[:2]
+    _rows(q_pe, T, "q_pe_bf16", 64, dim=3)
+    _need(q_pe.shape[1] == H, f"q_pe_bf16: {q_pe.shape[1]} heads, q_nope_bf16 has {H}")
+    _rows(indices, T, "indices")
+    _rows(out, T, "out", 512, dim=3)
+    _need(out.shape[1] == H, f"out: {out.shape[1]} heads, expected {H}")
+    _rows(lse, T, "lse", H)
+    _rows(cache, 0, "cache", dim=3)
+    return T, H, indices.shape[1]
 
 
 def dsmla_sparse_decode_workspace_size(tokens: int, heads: int, topk: int) -> int:
@@ -242,9 +319,8 @@ def dsmla_sparse_decode(q_nope_bf16: torch.Tensor, q_pe_bf16: torch.Tensor, cach
     [num_blocks, block_size, 656+]; indices int32 [T, topk] global slots (-1:
     none); out [T, 128, 512] bf16 and lse [T, 128] f32 (written); workspace
     uint8 of at least dsmla_sparse_decode_workspace_size(T, 128, topk) bytes."""
+    T, H, topk = _sparse_decode_shapes(q_nope_bf16, q_pe_bf16, cache, indices, out, lse)
     nb, bs, entry = cache.shape
-    T, H = q_nope_bf16.shape[:2]
-    topk = indices.shape[1]
     rc = load().dsmla_sparse_decode(
         _dev(q_nope_bf16, "q_nope_bf16", _BF16), _dev(q_pe_bf16, "q_pe_bf16", _BF16),
         _dev(cache, "cache", (torch.uint8,)), nb, bs, cache.stride(0), cache.stride(1),
@@ -259,11 +335,11 @@ def dsmla_sparse_decode_noalloc(q_nope_bf16: torch.Tensor, q_pe_bf16: torch.Tens
                                 stream=None) -> None:
     """dsmla_sparse_decode with the library's own file-scope scratch (no
     workspace argument; tokens * ceil(topk / 256) <= 128)."""
+    T, H, topk = _sparse_decode_shapes(q_nope_bf16, q_pe_bf16, cache, indices, out, lse)
     nb, bs, entry = cache.shape
-    T, H = q_nope_bf16.shape[:2]
     rc = load().dsmla_sparse_decode_noalloc(
         _dev(q_nope_bf16, "q_nope_bf16", _BF16), _dev(q_pe_bf16, "q_pe_bf16", _BF16),
         _dev(cache, "cache", (torch.uint8,)), nb, bs, cache.stride(0), cache.stride(1),
-        _dev(indices, "indices", (torch.int32,)), T, H, indices.shape[1], float(sm_scale),
+        _dev(indices, "indices", (torch.int32,)), T, H, topk, float(sm_scale),
         _dev(out, "out", _BF16), _dev(lse, "lse", _F32), _stream(stream))
     _check(rc, "dsmla_sparse_decode_noalloc")
