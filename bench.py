@@ -452,9 +452,11 @@ class OracleSampler:
         hist = ~wl.is_new
         oracle.quant_write_k(W.bf16_bits(wl.k_bf16[torch.from_numpy(hist)]), wl.slot[hist],
                              self.cache, 64)
+        # the fp8_ds_mla pool is written to before the clock starts, so the timed
+        # write does not also pay for the first touch of its pages
+        dcache = np.ones((wl.num_blocks, 64, 656), np.uint8)
         t = time.perf_counter()  # whole-step cache writes and gather, timed once
         oracle.quant_write_k(W.bf16_bits(wl.new_k), wl.new_slot, self.cache, 64)
-        dcache = np.zeros((wl.num_blocks, 64, 656), np.uint8)
         oracle.dsmla_quant_write(W.bf16_bits(wl.nope_bf16), W.bf16_bits(wl.rope_bf16),
                                  wl.new_slot, dcache, 64)
         cu = wl.prefill_gather()
@@ -503,6 +505,43 @@ class OracleSampler:
                 f"over {self.n} rows ({self.pairs} pairs) spread over the chunks, extrapolated "
                 f"per key / per pair to one step ({self.full_keys} decode keys, "
                 f"{self.full_pairs} prefill pairs)")
+
+
+def next_row_cpu_baselines(wl, rows):
+    """The oracle timed on the inputs of the rows timed beside the step (the
+    same draws as the GPU lines): the fused norm/RoPE write of all the step's
+    new tokens, and the sparse MLA decode of the whole decode batch.  Each
+    is small enough to time whole.  Returns name -> cpu_baseline entry."""
+    import oracle
+    import workloads as W
+    oracle.build()
+    out = {}
+    if "dsmla_norm_rope_write" in rows and wl.nope_bf16 is not None:
+        pos = wl.new_positions()
+        gamma, table = W.norm_rope_params(int(pos.max()) + 1)
+        n = len(pos)
+        dense = np.ones((-(-n // 64), 64, 656), np.uint8)  # a compact pool, pages touched up front
+        t = time.perf_counter()
+        oracle.dsmla_norm_rope_write(W.bf16_bits(wl.nope_bf16), W.bf16_bits(wl.rope_bf16),
+                                     W.bf16_bits(gamma), 1e-6, pos, table.numpy(),
+                                     np.arange(n, dtype=np.int64), dense, 64)
+        dt = time.perf_counter() - t
+        out["dsmla_norm_rope_write"] = {
+            "value": n / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"all {n} new tokens into a compact pool, timed whole ({dt:.3f} s)"}
+    if "dsmla_sparse_decode" in rows and wl.n_decode > 0:
+        T = wl.n_decode * wl.next_n
+        x = W.sparse_decode_inputs(T, wl.topk, int(wl.context_lens.max()), seed=17)
+        dense = np.zeros((x.num_blocks, 64, 656), np.uint8)
+        oracle.dsmla_quant_write(W.bf16_bits(x.nope_bf16), W.bf16_bits(x.rope_bf16), x.slots, dense, 64)
+        t = time.perf_counter()
+        oracle.dsmla_sparse_decode(W.bf16_bits(x.q_nope), W.bf16_bits(x.q_pe), dense, 64, x.indices,
+                                   x.sm_scale)
+        dt = time.perf_counter() - t
+        out["dsmla_sparse_decode"] = {
+            "value": T / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"the whole batch of {T} tokens x 128 heads x top-{wl.topk}, timed whole ({dt:.3f} s)"}
+    return out
 
 
 def reference_arm(args, world, rank):
@@ -627,6 +666,8 @@ def main():
                                 "cores": oracle.num_threads(), "kind": "oracle",
                                 "sample": s.describe(),
                                 "sample_seconds": time.perf_counter() - w0 + s.t_fixed}
+        for n, cb in next_row_cpu_baselines(wl, set(line.get("next_rows", {}))).items():
+            line["next_rows"][n]["cpu_baseline"] = cb
     print(json.dumps(line), flush=True)
 
 

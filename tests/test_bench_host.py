@@ -87,3 +87,16 @@ def test_committed_traffic_profile_parses():
     t = bench.measured_traffic("mixed_16x131072dec_4x2048pf")
     assert set(t) <= set(bench.KERNEL_SOURCES)
     assert all(isinstance(v, int) and v > 0 for v in t.values())
+
+
+def test_next_row_cpu_baselines_small_workload():
+    # the oracle legs beside the next rows run on the host alone
+    import workloads as W
+    wl = W.build("mix", decode_ctx=[500, 700], next_n=1, prefill=[(900, 300)], topk=128, seed=2,
+                 dsmla=True)
+    out = bench.next_row_cpu_baselines(wl, {"dsmla_norm_rope_write", "dsmla_sparse_decode"})
+    assert set(out) == {"dsmla_norm_rope_write", "dsmla_sparse_decode"}
+    for v in out.values():
+        assert v["value"] > 0 and v["unit"] == "tokens/s" and v["kind"] == "oracle" and v["cores"] >= 1
+    assert "2 tokens" in out["dsmla_sparse_decode"]["sample"]
+    assert bench.next_row_cpu_baselines(wl, set()) == {}
