@@ -187,3 +187,26 @@ def test_block_and_entry_strides():
                                             block_stride=bstride, entry_stride=entry)
     assert ok
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_dominant_key_is_exact_and_overflow_free():
+    # Scores of order 1e4 (far beyond exp's range) with one key ahead of all
+    # others by hundreds: every other weight underflows to exactly 0 after the
+    # max is subtracted, so the output is that key's value and the lse its
+    # score, bit for bit -- a sum of exp(z) without the max would overflow.
+    rng = np.random.default_rng(8)
+    scales = np.full((2, BS, 4), 0.015625, np.float32)
+    cache = make_cache(2, rng, scales=scales)
+    flat = cache.reshape(-1, ENTRY)
+    flat[:, 528:656] = 0                             # RoPE zero: scores from dim 0 alone
+    codes = np.array([0x50, 0x48, 0x40, 0x38, 0x30], np.uint8)   # 8, 4, 2, 1, 0.5 before scaling
+    slots = [3, 9, 1, 12, 6]
+    for c, g in zip(codes, slots):
+        flat[g, 0] = c
+    qn = np.zeros((1, 1, 512), np.float32)
+    qn[0, 0, 0] = 2.0 ** 16                          # exact in bf16
+    out, lse, ok = run(bf16_bits(qn), np.zeros((1, 1, 64), np.uint16), cache, [slots], 1.0)
+    assert ok
+    k0 = torch_key(cache, slots[0])
+    assert np.array_equal(out[0, 0], k0[:512])
+    assert lse[0, 0] == 2.0 ** 16 * k0[0] == 8192.0   # 8 * 2^-6 * 2^16; the next score is 4096
