@@ -287,6 +287,22 @@ IX_API int dsmla_norm_rope_write(const void* kv_bf16, const void* pe_bf16, const
  *                (per split of 256 indices: its normalised output and lse);
  *                IX_ERR_WORKSPACE if missing or smaller.  Owned by the caller,
  *                in use until the call's work on `stream` completes.
+ * Errors, checked on the host in this order before anything is launched:
+ *   IX_ERR_SHAPE        tokens, num_blocks, a stride or topk negative
+ *   IX_ERR_UNSUPPORTED  heads != 128, block_size < 1, topk outside [1, 65536],
+ *                       sm_scale not positive and finite
+ *   IX_OK               tokens == 0 (nothing is read or written)
+ *   IX_ERR_NULL         a pointer is NULL (cache may be NULL when num_blocks == 0)
+ *   IX_ERR_SHAPE        entry_stride_bytes < 656 or block_stride_bytes <
+ *                       block_size * entry_stride_bytes
+ *   IX_ERR_ALIGN        a base or stride breaks the alignment above (indices and
+ *                       lse need 4 bytes)
+ *   IX_ERR_UNSUPPORTED  tokens * 128 or tokens * ceil(topk / 256) above INT32_MAX
+ *   IX_ERR_WORKSPACE    workspace NULL or smaller than its size
+ *   IX_ERR_ALIGN        workspace not 16-byte aligned
+ *   IX_ERR_CUDA         the tensor-map encoder or a launch failed
+ * dsmla_sparse_decode_workspace_size returns 0 when tokens, heads or topk is
+ * not positive.
  */
 IX_API size_t dsmla_sparse_decode_workspace_size(int64_t tokens, int heads, int topk);
 IX_API int dsmla_sparse_decode(const void* q_nope_bf16, const void* q_pe_bf16, const uint8_t* cache,
