@@ -110,6 +110,10 @@ def _dev(t: torch.Tensor, name: str, dtypes) -> int:
         raise TypeError(f"{name}: expected a torch.Tensor")
     if not t.is_cuda:
         raise DsixError(f"{name}: must be a CUDA tensor")
+    if t.device.index is not None and t.device.index != torch.cuda.current_device():
+        # the library launches on the current device: a tensor of another
+        # device would hand its pointer to kernels that cannot reach it
+        raise DsixError(f"{name}: on {t.device}, but the current device is cuda:{torch.cuda.current_device()}")
     if t.dtype not in dtypes:
         raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
     if not t.is_contiguous():

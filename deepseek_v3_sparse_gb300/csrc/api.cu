@@ -35,6 +35,26 @@ int launch_status() {
     return e == cudaSuccess ? IX_OK : IX_ERR_CUDA;
 }
 
+// The calling thread's current CUDA context (the device's primary context once
+// the runtime has used the device), through the driver entry point; NULL when
+// there is none yet or on error.
+void* current_context() {
+    using Fn = CUresult (*)(CUcontext*);
+    static std::once_flag once;
+    static Fn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<Fn>(p);
+    });
+    if (!fn) return nullptr;
+    CUcontext c = nullptr;
+    if (fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+
 int num_sms() {
     static std::mutex mu;
     static std::vector<int> cache;

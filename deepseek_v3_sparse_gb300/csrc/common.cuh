@@ -31,6 +31,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 int launch_status();  // maps cudaGetLastError() to IX_OK / IX_ERR_CUDA
 int num_sms();        // SMs of the current device (cached per device), -1 on error
 int* status_ptr();    // device address of the current device's status word
+void* current_context();  // the calling thread's current CUDA context, NULL on error
 
 // ---------------------------------------------------------------------------
 // small device utilities

@@ -522,6 +522,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
             a.ws_lse[prow_idx] = m == -INFINITY ? -INFINITY : (mc + log2f(l_exact)) * 0.69314718055994531f;
+        } else {
+            // a wait gave up: this split's output was not written, so its lse is
+            // set to -inf and the merge gives it weight 0 (IX_DEV_TIMEOUT is set)
+            a.ws_lse[(t * a.splits + split) * kH + h] = -INFINITY;
         }
     }
     tc_fence_before();
@@ -662,16 +666,23 @@ extern "C" size_t dsmla_sparse_decode_workspace_size(int64_t tokens, int heads, 
     return static_cast<size_t>(tokens * splits * heads) * (kNope + 1) * sizeof(float);
 }
 
-extern "C" int dsmla_sparse_decode(const void* q_nope_bf16, const void* q_pe_bf16, const uint8_t* cache,
-                                   int64_t num_blocks, int block_size, int64_t block_stride_bytes,
-                                   int64_t entry_stride_bytes, const int32_t* indices, int64_t tokens, int heads,
-                                   int topk, float sm_scale, void* out_bf16, float* lse, void* workspace,
-                                   size_t workspace_bytes, ix_stream_t stream) {
+namespace dsix {
+namespace {
+// The argument checks both sparse decode entry points run first, in this
+// order; `empty` is set when tokens == 0 (nothing to do, IX_OK).
+int smla_check(const void* q_nope_bf16, const void* q_pe_bf16, const uint8_t* cache, int64_t num_blocks,
+               int block_size, int64_t block_stride_bytes, int64_t entry_stride_bytes, const int32_t* indices,
+               int64_t tokens, int heads, int topk, float sm_scale, const void* out_bf16, const float* lse,
+               bool* empty) {
+    *empty = false;
     if (tokens < 0 || num_blocks < 0 || block_stride_bytes < 0 || entry_stride_bytes < 0 || topk < 0)
         return IX_ERR_SHAPE;
     if (heads != kH || block_size < 1 || topk < 1 || topk > kMaxTopk) return IX_ERR_UNSUPPORTED;
     if (!(sm_scale > 0.0f) || !isfinite(sm_scale)) return IX_ERR_UNSUPPORTED;
-    if (tokens == 0) return IX_OK;
+    if (tokens == 0) {
+        *empty = true;
+        return IX_OK;
+    }
     if (!q_nope_bf16 || !q_pe_bf16 || !indices || !out_bf16 || !lse || (num_blocks > 0 && !cache)) return IX_ERR_NULL;
     if (entry_stride_bytes < kEntry || block_stride_bytes < static_cast<int64_t>(block_size) * entry_stride_bytes)
         return IX_ERR_SHAPE;
@@ -679,9 +690,24 @@ extern "C" int dsmla_sparse_decode(const void* q_nope_bf16, const void* q_pe_bf1
         (block_stride_bytes & 15) || (entry_stride_bytes & 15) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
         (reinterpret_cast<uintptr_t>(indices) & 3u))
         return IX_ERR_ALIGN;
+    const int64_t splits = (static_cast<int64_t>(topk) + kSplit - 1) / kSplit;
+    if (tokens * kH > INT32_MAX || tokens * splits > INT32_MAX) return IX_ERR_UNSUPPORTED;
+    return IX_OK;
+}
+}  // namespace
+}  // namespace dsix
+
+extern "C" int dsmla_sparse_decode(const void* q_nope_bf16, const void* q_pe_bf16, const uint8_t* cache,
+                                   int64_t num_blocks, int block_size, int64_t block_stride_bytes,
+                                   int64_t entry_stride_bytes, const int32_t* indices, int64_t tokens, int heads,
+                                   int topk, float sm_scale, void* out_bf16, float* lse, void* workspace,
+                                   size_t workspace_bytes, ix_stream_t stream) {
+    bool empty = false;
+    const int chk = smla_check(q_nope_bf16, q_pe_bf16, cache, num_blocks, block_size, block_stride_bytes,
+                               entry_stride_bytes, indices, tokens, heads, topk, sm_scale, out_bf16, lse, &empty);
+    if (chk != IX_OK || empty) return chk;
     const int splits = (topk + kSplit - 1) / kSplit;
     const int64_t prow = tokens * splits * kH;
-    if (tokens * kH > INT32_MAX || tokens * splits > INT32_MAX) return IX_ERR_UNSUPPORTED;
     const size_t need = dsmla_sparse_decode_workspace_size(tokens, heads, topk);
     if (!workspace || workspace_bytes < need) return IX_ERR_WORKSPACE;
     if (!aligned16(workspace)) return IX_ERR_ALIGN;
@@ -721,28 +747,42 @@ extern "C" int dsmla_sparse_decode_noalloc(const void* q_nope_bf16, const void* 
                                            int64_t entry_stride_bytes, const int32_t* indices, int64_t tokens,
                                            int heads, int topk, float sm_scale, void* out_bf16, float* lse,
                                            ix_stream_t stream) {
-    // the shape checks come first, so a call that cannot fit fails before any CUDA call
-    if (tokens < 0 || topk < 0) return IX_ERR_SHAPE;
-    if (heads != kH || topk < 1 || topk > kMaxTopk) return IX_ERR_UNSUPPORTED;
-    if (tokens == 0)
-        return dsmla_sparse_decode(q_nope_bf16, q_pe_bf16, cache, num_blocks, block_size, block_stride_bytes,
-                                   entry_stride_bytes, indices, tokens, heads, topk, sm_scale, out_bf16, lse,
-                                   nullptr, 0, stream);
+    // the same argument checks as dsmla_sparse_decode, in the same order; the
+    // capacity check takes the place of its workspace check, before any CUDA call
+    bool empty = false;
+    const int chk = smla_check(q_nope_bf16, q_pe_bf16, cache, num_blocks, block_size, block_stride_bytes,
+                               entry_stride_bytes, indices, tokens, heads, topk, sm_scale, out_bf16, lse, &empty);
+    if (chk != IX_OK || empty) return chk;
     const int64_t splits = (static_cast<int64_t>(topk) + kSplit - 1) / kSplit;
     if (tokens > kStaticSplits || tokens * splits > kStaticSplits) return IX_ERR_WORKSPACE;
+    // The scratch's device address, looked up once per device and context: a
+    // context created after a reset of the device places the module (and the
+    // array) anew, so the cached address is refreshed when the context changes.
     static std::mutex mu;
-    static std::vector<void*> addr;
+    struct Entry {
+        void* ctx;
+        void* addr;
+    };
+    static std::vector<Entry> cached;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return IX_ERR_CUDA;
     void* scratch = nullptr;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (dev >= static_cast<int>(addr.size())) addr.resize(dev + 1, nullptr);
-        if (!addr[dev] && cudaGetSymbolAddress(&addr[dev], g_smla_scratch) != cudaSuccess) {
-            addr[dev] = nullptr;
-            return IX_ERR_CUDA;
+        if (dev >= static_cast<int>(cached.size())) cached.resize(dev + 1, Entry{nullptr, nullptr});
+        Entry& e = cached[dev];
+        void* ctx = current_context();  // NULL before the runtime's first use of the device
+        if (!ctx || e.ctx != ctx || !e.addr) {
+            e.ctx = nullptr;
+            e.addr = nullptr;
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_smla_scratch) != cudaSuccess) return IX_ERR_CUDA;
+            ctx = current_context();  // the lookup has made the device's context current
+            if (!ctx) return IX_ERR_CUDA;
+            e.ctx = ctx;
+            e.addr = p;
         }
-        scratch = addr[dev];
+        scratch = e.addr;
     }
     return dsmla_sparse_decode(q_nope_bf16, q_pe_bf16, cache, num_blocks, block_size, block_stride_bytes,
                                entry_stride_bytes, indices, tokens, heads, topk, sm_scale, out_bf16, lse, scratch,

@@ -302,7 +302,9 @@ IX_API int dsmla_norm_rope_write(const void* kv_bf16, const void* pe_bf16, const
  *   IX_ERR_ALIGN        workspace not 16-byte aligned
  *   IX_ERR_CUDA         the tensor-map encoder or a launch failed
  * dsmla_sparse_decode_workspace_size returns 0 when tokens, heads or topk is
- * not positive.
+ * not positive.  If a pipeline wait gives up (IX_DEV_TIMEOUT in the device
+ * status word, never expected), the splits it cut short are left out of the
+ * merge, so out and lse are then incomplete.
  */
 IX_API size_t dsmla_sparse_decode_workspace_size(int64_t tokens, int heads, int topk);
 IX_API int dsmla_sparse_decode(const void* q_nope_bf16, const void* q_pe_bf16, const uint8_t* cache,
@@ -317,9 +319,14 @@ IX_API int dsmla_sparse_decode(const void* q_nope_bf16, const void* q_pe_bf16, c
  * device array (128 (token, split) pairs: tokens * ceil(topk / 256) <= 128,
  * e.g. 16 tokens at topk 2048), placed once when the library's module loads.
  * Nothing is allocated by the call.  Same arguments and results as
- * dsmla_sparse_decode otherwise; a larger call returns IX_ERR_WORKSPACE before
- * anything is launched.  The scratch is shared: calls on one device must not
- * run concurrently (calls on one stream never do).
+ * dsmla_sparse_decode otherwise.  Its host checks are dsmla_sparse_decode's,
+ * in the same order, with the capacity check in place of the workspace check:
+ * a call past the scratch returns IX_ERR_WORKSPACE only when every earlier
+ * check passed, and before anything is launched.  The scratch's device address
+ * is looked up on the first call on a device (and again whenever the device's
+ * context has changed, e.g. after a reset); make that first call before any
+ * stream capture.  The scratch is shared: calls on one device must not run
+ * concurrently (calls on one stream never do).
  */
 IX_API int dsmla_sparse_decode_noalloc(const void* q_nope_bf16, const void* q_pe_bf16, const uint8_t* cache,
                     int64_t num_blocks, int block_size, int64_t block_stride_bytes,

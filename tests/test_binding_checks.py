@@ -158,3 +158,22 @@ def test_step_calls_pass_the_checks(dsix, monkeypatch):
         seen.clear()
         make_step(wl, "cpu").run()
         assert "ix_paged_mqa_logits" in seen and "ix_topk_to_global" in seen
+
+
+def test_tensor_on_another_device_is_refused(dsix, monkeypatch):
+    """The library launches on the current device; a tensor that lives on
+    another one is refused before its pointer is taken (a CUDA tensor is faked
+    on the CPU: nothing is launched)."""
+    class OnCuda1(torch.Tensor):
+        @property
+        def is_cuda(self):
+            return True
+
+        @property
+        def device(self):
+            return torch.device("cuda", 1)
+
+    t = torch.zeros(16, dtype=torch.float32).as_subclass(OnCuda1)
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    with pytest.raises(dsix.DsixError, match="current device"):
+        dsix._dev(t, "logits", (torch.float32,))
