@@ -228,6 +228,98 @@ def algorithmic(wl):
     return dec_keys, pairs
 
 
+def spread(ms_list):
+    """min / median / max (ms) of per-launch event times, and the launch count."""
+    v = np.asarray(ms_list, dtype=np.float64)
+    return {"min": float(v.min()), "median": float(np.median(v)), "max": float(v.max()), "n": int(v.size)}
+
+
+NOMINAL_FP8_TFLOPS = 4500.0  # dense FP8 tensor peak of a GB300 (nominal)
+NOMINAL_HBM_GBS = 8000.0     # HBM3e, the round figure the targets are stated against
+
+
+def config_entries(dev, stream, n_launch=60):
+    """The three single-kernel configurations (batch-32 decode, next_n=2 MTP
+    decode over 128 requests, 8192-token causal prefill), each timed launch by
+    launch with L2 flushed before every launch (a 256 MB read), logits kernel
+    and top-k back to back as the step runs them.  Per configuration: per-kernel
+    mean and min/median/max over the launches, the algorithmic rate (132 B per
+    key, keys read once per request; 16384 flop per visible (query, key) pair)
+    and its fraction of the measured and of the nominal peak."""
+    import deepseek_v3_sparse_gb300 as dsix
+    import workloads as W
+    from workloads.device import make_step
+    pk, pk_kind = peaks()
+    fp8_meas = 2.0 * pk["bf16_tflops"]
+    flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+    out = {}
+    for name, fn in (("decode_b32", W.decode_b32), ("decode_mtp2_b128", W.decode_mtp2_b128),
+                     ("prefill_8k", W.prefill_8k)):
+        wl = fn(seed=0)
+        st = make_step(wl, dev)
+        st.run(stream=stream)
+        if wl.n_decode:
+            d = st.decode
+            logits = lambda: dsix.ix_paged_mqa_logits(d.q, d.w, st.cache, d.context_lens, st.block_table,
+                                                      st.dec_logits, stream=stream)
+            topk = lambda: dsix.ix_topk_to_global(st.dec_logits, d.row_len, d.row_req, st.block_table,
+                                                  wl.topk, st.dec_global, None, stream=stream)
+            rows = wl.n_decode * wl.next_n
+        else:
+            p = st.prefill
+            logits = lambda: dsix.ix_mqa_logits(p.q, p.w, st.k_fp8, st.k_scale, p.ks, p.ke, st.pf_logits,
+                                                stream=stream)
+            topk = lambda: dsix.ix_topk_to_global(st.pf_logits, p.row_len, p.row_req, st.block_table,
+                                                  wl.topk, st.pf_global, None, stream=stream)
+            rows = wl.n_prefill_rows
+        for _ in range(3):
+            logits()
+            topk()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_launch)]
+        for e in evs:
+            torch.sum(flush, 0, out=sink)
+            e[0].record(stream)
+            logits()
+            e[1].record(stream)
+            topk()
+            e[2].record(stream)
+        torch.cuda.synchronize()
+        if dsix.ix_device_status() != 0:
+            raise RuntimeError(f"device status set in the {name} timing")
+        lg = [a.elapsed_time(b) for a, b, _ in evs]
+        tk = [b.elapsed_time(c) for _, b, c in evs]
+        pair = [a.elapsed_time(c) for a, _, c in evs]
+        dec_keys, pairs = algorithmic(wl)
+        e = {"workload": wl.name, "rows": rows, "top_k": wl.topk,
+             "l2": "flushed before every launch (256 MB read)",
+             "logits": {"ms": float(np.mean(lg)), **{f"ms_{k}": v for k, v in spread(lg).items()}},
+             "topk": {"ms": float(np.mean(tk)), **{f"ms_{k}": v for k, v in spread(tk).items()}},
+             "logits_plus_topk": {"ms": float(np.mean(pair)),
+                                  "query_tokens_per_s": rows / (float(np.mean(pair)) / 1e3)}}
+        ms = e["logits"]["ms"]
+        if wl.n_decode:
+            gbs = dec_keys * DECODE_BYTES_PER_KEY / (ms / 1e3) / 1e9
+            gbs_med = dec_keys * DECODE_BYTES_PER_KEY / (e["logits"]["ms_median"] / 1e3) / 1e9
+            e["logits"].update(achieved=gbs, unit="GB/s", units=dec_keys,
+                               per_unit=f"{DECODE_BYTES_PER_KEY} B per key, read once per request",
+                               peak=pk["hbm_gbs"], peak_kind=f"{pk_kind} copy bandwidth",
+                               frac=gbs / pk["hbm_gbs"], frac_at_median=gbs_med / pk["hbm_gbs"],
+                               frac_of_8tbs=gbs / NOMINAL_HBM_GBS, target=0.70)
+        else:
+            tfs = pairs * PREFILL_FLOP_PER_PAIR / (ms / 1e3) / 1e12
+            tfs_med = pairs * PREFILL_FLOP_PER_PAIR / (e["logits"]["ms_median"] / 1e3) / 1e12
+            e["logits"].update(achieved=tfs, unit="TFLOP/s", units=pairs,
+                               per_unit=f"{PREFILL_FLOP_PER_PAIR} flop per visible (query, key) pair",
+                               peak=fp8_meas, peak_kind=f"{pk_kind}: fp8 = 2 x cuBLAS bf16 burst {pk['bf16_tflops']}",
+                               frac=tfs / fp8_meas, frac_at_median=tfs_med / fp8_meas,
+                               frac_of_nominal_fp8=tfs / NOMINAL_FP8_TFLOPS, target=0.50)
+        out[name] = e
+        del st
+        torch.cuda.empty_cache()
+    return out
+
+
 def gpu_arm(args, world, rank, local):
     import deepseek_v3_sparse_gb300 as dsix
     from deepseek_v3_sparse_gb300 import build as libbuild
@@ -272,6 +364,7 @@ def gpu_arm(args, world, rank, local):
         step.run(stream=stream, events={n: ev[n][i] for n in names})
     torch.cuda.synchronize()
     kern_ms = {n: float(np.mean([a.elapsed_time(b) for a, b in ev[n]])) for n in names}
+    kern_spread = {n: spread([a.elapsed_time(b) for a, b in ev[n]]) for n in names}
     status = dsix.ix_device_status()
 
     # ---- the next row beyond the step: fused RMSNorm + RoPE + fp8_ds_mla write of
@@ -429,7 +522,9 @@ def gpu_arm(args, world, rank, local):
 
     dec_keys, pairs = algorithmic(wl)
     rows = int(wl.n_decode * wl.next_n + wl.n_prefill_rows)
-    return dict(wl=wl, step=step, elapsed_ms=elapsed_ms, kern_ms=kern_ms, clocks=clk,
+    configs = {} if args.no_configs else config_entries(dev, stream)
+    return dict(wl=wl, step=step, elapsed_ms=elapsed_ms, kern_ms=kern_ms, kern_spread=kern_spread,
+                configs=configs, clocks=clk,
                 status=status, e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h,
                 dec_keys=dec_keys, pairs=pairs, rows=rows, next_rows=next_rows)
 
@@ -438,10 +533,15 @@ def gpu_arm(args, world, rank, local):
 # CPU oracle (baseline leg / reference arm)
 # ---------------------------------------------------------------------------
 class OracleSampler:
-    """The oracle timed on bounded samples of the workload.  Set-up (the cache
-    of already-cached positions) is done once; each sample times a slice of a
-    decode row and whole prefill rows (logits + top-k), rotating over rows;
-    per-key / per-pair costs extrapolate to one whole step."""
+    """The oracle on whole-row samples of the workload, every figure measured
+    (nothing is extrapolated).  One sample step runs the oracle, as it stands,
+    on one decode row with all its keys and on the prefill rows that go with it
+    in the step's own decode:prefill proportion (8192 / 16 = 512 rows for the
+    mixed workload), and on the matching share of the fixed work: the cache
+    writes (indexer K and fp8_ds_mla) of exactly those rows' new tokens, and a
+    gather of the same share of the prefill contexts.  value = rows processed /
+    time taken.  Set-up (the cache of already-cached positions, the gathered K
+    the prefill rows read) is done once and not timed."""
 
     def __init__(self, wl):
         import oracle
@@ -452,59 +552,89 @@ class OracleSampler:
         hist = ~wl.is_new
         oracle.quant_write_k(W.bf16_bits(wl.k_bf16[torch.from_numpy(hist)]), wl.slot[hist],
                              self.cache, 64)
-        # the fp8_ds_mla pool is written to before the clock starts, so the timed
-        # write does not also pay for the first touch of its pages
-        dcache = np.ones((wl.num_blocks, 64, 656), np.uint8)
-        t = time.perf_counter()  # whole-step cache writes and gather, timed once
         oracle.quant_write_k(W.bf16_bits(wl.new_k), wl.new_slot, self.cache, 64)
-        oracle.dsmla_quant_write(W.bf16_bits(wl.nope_bf16), W.bf16_bits(wl.rope_bf16),
-                                 wl.new_slot, dcache, 64)
         cu = wl.prefill_gather()
+        self.cu = cu
         self.kf = np.zeros((int(cu[-1]), 128), np.uint8)
         self.ksc = np.zeros(int(cu[-1]), np.float32)
         oracle.gather_k(self.cache, 64, 128, wl.prefill_block_table(), cu, self.kf, self.ksc)
-        self.t_fixed = time.perf_counter() - t
-        del dcache
         self.ks, self.ke, self.rl, self.rq = wl.prefill_rows()
-        self.full_keys = int(wl.context_lens.astype(np.int64).sum())
-        self.full_pairs = int(self.rl.astype(np.int64).sum())
-        self.keys = self.pairs = 0
-        self.t_keys = self.t_pairs = 0.0
+        self.n_dec = wl.n_decode * wl.next_n
+        self.dec_len, self.dec_req = wl.decode_rows()
+        self.pf_per_dec = max(1, wl.n_prefill_rows // max(1, self.n_dec))
+        # new tokens: flat index (request-major over cached positions) -> rank among new tokens
+        self.new_rank = np.cumsum(wl.is_new) - 1
+        self.req_off = np.concatenate([[0], np.cumsum(wl.req_ctx)]).astype(np.int64)
+        # the fp8_ds_mla pool is written to before the clock starts, so the timed
+        # writes do not also pay for the first touch of its pages
+        self.dcache = np.ones((wl.num_blocks, 64, 656), np.uint8)
+        self.gather_share = int(cu[-1]) * self.pf_per_dec // max(1, wl.n_prefill_rows)
+        self.kf_share = np.zeros((max(1, self.gather_share), 128), np.uint8)
+        self.ksc_share = np.zeros(max(1, self.gather_share), np.float32)
+        self.rows = self.steps = 0
+        self.t = 0.0
         self.n = 0
 
-    def sample(self, dec_keys: int = 2048, pf_rows: int = 0):
-        wl, o, W = self.wl, self.o, self.W
-        pf_rows = pf_rows or o.num_threads()  # one row per thread: rows run in parallel
-        ctx = wl.context_lens.copy()
-        ctx[0] = dec_keys
-        t = time.perf_counter()
-        lg = o.paged_mqa_logits(W.u8(wl.q_decode), wl.w_decode.numpy(), self.cache, 64, ctx,
-                                wl.block_table, ld=dec_keys, clean=False, rows=[0])
-        o.topk_to_global(lg, np.array([dec_keys], np.int32), np.zeros(1, np.int32),
-                         wl.block_table, 64, wl.topk)
-        self.t_keys += time.perf_counter() - t
-        self.keys += dec_keys
-        T = len(self.ks)
-        rows = np.array([(int((self.n + j) * 0.6180339887 * T)) % T for j in range(pf_rows)],
-                        dtype=np.int64)
-        self.n += pf_rows
-        t = time.perf_counter()
-        plg = o.mqa_logits(W.u8(wl.q_prefill), wl.w_prefill.numpy(), self.kf, self.ksc, self.ks,
-                           self.ke, ld=int(self.rl[rows].max()), clean=False, rows=rows)
-        o.topk_to_global(plg, self.rl[rows], self.rq[rows], wl.block_table, 64, wl.topk)
-        self.t_pairs += time.perf_counter() - t
-        self.pairs += int(self.rl[rows].astype(np.int64).sum())
+    def reset(self):
+        self.rows = self.steps = 0
+        self.t = 0.0
 
-    def step_seconds(self) -> float:
-        return (self.t_fixed + self.t_keys / self.keys * self.full_keys
-                + self.t_pairs / self.pairs * self.full_pairs)
+    def _new_of(self, req, pos):
+        """Rank among the new tokens of request req's cached position pos."""
+        return int(self.new_rank[self.req_off[req] + pos])
+
+    def sample(self):
+        wl, o, W = self.wl, self.o, self.W
+        d = self.n % max(1, self.n_dec)
+        T = len(self.ks)
+        pf = np.array(sorted({int((self.n * self.pf_per_dec + j) * 0.6180339887 * T) % T
+                              for j in range(self.pf_per_dec)}), dtype=np.int64) if T else np.zeros(0, np.int64)
+        self.n += 1
+        # the new tokens of these rows: the decode row's own token, and each prefill
+        # row's token (row i of a chunk is position ctx - chunk_len + i of its request)
+        toks = []
+        if self.n_dec:
+            b, j = d // wl.next_n, d % wl.next_n
+            toks.append(self._new_of(b, int(wl.req_ctx[b]) - wl.next_n + j))
+        for t in pf:
+            r = int(self.rq[t])
+            toks.append(self._new_of(r, int(self.rl[t]) - 1))
+        toks = np.array(toks, dtype=np.int64)
+        new_k = wl.new_k[torch.from_numpy(toks)]
+        slots = wl.new_slot[toks]
+        t0 = time.perf_counter()
+        o.quant_write_k(W.bf16_bits(new_k), slots, self.cache, 64)
+        if wl.nope_bf16 is not None:
+            sel = torch.from_numpy(toks)
+            o.dsmla_quant_write(W.bf16_bits(wl.nope_bf16[sel]), W.bf16_bits(wl.rope_bf16[sel]), slots,
+                                self.dcache, 64)
+        if len(pf) and self.gather_share > 0:
+            c = int(np.searchsorted(self.cu, int(self.ks[pf[0]]), side="right") - 1)
+            o.gather_k(self.cache, 64, 128, wl.prefill_block_table()[c:c + 1],
+                       np.array([0, self.gather_share], np.int32), self.kf_share, self.ksc_share)
+        if self.n_dec:
+            L = int(self.dec_len[d])
+            lg = o.paged_mqa_logits(W.u8(wl.q_decode), wl.w_decode.numpy(), self.cache, 64,
+                                    wl.context_lens, wl.block_table, ld=max(4, (L + 3) // 4 * 4),
+                                    clean=False, rows=[d])
+            o.topk_to_global(lg, self.dec_len[d:d + 1], self.dec_req[d:d + 1], wl.block_table, 64, wl.topk)
+        if len(pf):
+            plg = o.mqa_logits(W.u8(wl.q_prefill), wl.w_prefill.numpy(), self.kf, self.ksc, self.ks,
+                               self.ke, ld=int(self.rl[pf].max() + 3) // 4 * 4, clean=False, rows=pf)
+            o.topk_to_global(plg, self.rl[pf], self.rq[pf], wl.block_table, 64, wl.topk)
+        self.t += time.perf_counter() - t0
+        self.rows += (1 if self.n_dec else 0) + len(pf)
+        self.steps += 1
+
+    def value(self) -> float:
+        return self.rows / self.t
 
     def describe(self) -> str:
-        return (f"oracle on the host cores: new-token cache writes, fp8_ds_mla write and gather "
-                f"timed whole; decode logits+top-k over {self.keys} keys and prefill logits+top-k "
-                f"over {self.n} rows ({self.pairs} pairs) spread over the chunks, extrapolated "
-                f"per key / per pair to one step ({self.full_keys} decode keys, "
-                f"{self.full_pairs} prefill pairs)")
+        return (f"oracle on the host cores, measured on {self.steps} sample steps of whole rows "
+                f"({self.rows} rows in {self.t:.2f} s): each step 1 decode row with all its keys + "
+                f"{self.pf_per_dec} prefill rows (the step's decode:prefill mix), the cache writes of "
+                f"those rows' new tokens and a gather of {self.gather_share} cached tokens (the same "
+                f"share of the step's prefill contexts); value = rows / time")
 
 
 def next_row_cpu_baselines(wl, rows):
@@ -550,24 +680,26 @@ def reference_arm(args, world, rank):
     if rank != 0:
         return
     wl = W.mixed_long(seed=0)
-    rows = int(wl.n_decode * wl.next_n + wl.n_prefill_rows)
     s = OracleSampler(wl)
     for _ in range(args.warmup):
         s.sample()
-    s.keys = s.pairs = 0
-    s.t_keys = s.t_pairs = 0.0
+    s.reset()
+    # each sample step takes about a second on the host cores: the timed steps
+    # stop early (and the line says how many ran) once two minutes have passed
     w0 = time.perf_counter()
     for _ in range(args.steps):
         s.sample()
+        if time.perf_counter() - w0 > 120.0:
+            break
     wall = time.perf_counter() - w0
-    est = s.step_seconds()
-    value = rows / est
+    value = s.value()
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": est * 1e3, "higher_is_better": True, "scaling": "weak",
+            "n_gpus": args.gpus, "steps": s.steps, "steps_requested": args.steps, "warmup": args.warmup,
+            "ms_per_step": s.t / s.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64 (exact fp8 products, double head sum)",
             "data": "synthetic (seeded; no dataset, no weights)",
-            "config": workload_config(wl),
+            "config": {**workload_config(wl), "parallelism": "replicas x1 (rank 0 only)",
+                       "step": "one sample step: 1 decode row + its share of prefill rows, whole rows"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
                              "kind": "oracle", "sample": s.describe()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -584,6 +716,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="dsix", choices=["dsix", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration timing of the decode, MTP and prefill kernels")
     ap.add_argument("--workload", default="mixed_long",
                     help="named workload; the benchmark line is mixed_long, the others are "
                          "for profiling single kernels")
@@ -622,6 +756,13 @@ def main():
     for n in ("topk_decode", "topk_prefill"):
         if n in km:
             kernels[n] = {"ms": km[n]}
+    for n, kd in kernels.items():
+        sp = r["kern_spread"][n]
+        kd.update({f"ms_{k}": v for k, v in sp.items()})
+        if "frac" in kd:  # the fraction at the median launch time too
+            kd["frac_at_median"] = kd["frac"] * kd["ms"] / sp["median"]
+    if "mqa_logits" in kernels:
+        kernels["mqa_logits"]["frac_of_nominal_fp8"] = pf_tflops / NOMINAL_FP8_TFLOPS
     traffic = measured_traffic(workload_config(wl)["workload"])
     for n, kd in kernels.items():
         kd["traffic"] = traffic.get(n)
@@ -632,7 +773,10 @@ def main():
                 "unit": kd["unit"], "frac": kd["frac"], "traffic": kd["traffic"],
                 "traffic_unit": "bytes per launch (ncu dram read + write; null once the kernel changed)",
                 "peak_kind": (f"{pk_kind}: fp8 = 2 x cuBLAS bf16 burst {pk['bf16_tflops']} TFLOP/s"
-                              if dominant == "mqa_logits" else f"{pk_kind} copy bandwidth")}
+                              if dominant == "mqa_logits" else f"{pk_kind} copy bandwidth"),
+                "frac_of_nominal": (kd["achieved"] / NOMINAL_FP8_TFLOPS if dominant == "mqa_logits"
+                                    else kd["achieved"] / NOMINAL_HBM_GBS),
+                "nominal_peak": NOMINAL_FP8_TFLOPS if dominant == "mqa_logits" else NOMINAL_HBM_GBS}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -645,6 +789,8 @@ def main():
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
             "gpu_launches": step.kernels_per_step() * args.steps,
             "clocks": r["clocks"], "device_status": r["status"]}
+    if r["configs"]:
+        line["configs"] = r["configs"]
     for n, d in r["next_rows"].items():  # rows beyond the step, timed on their own
         if n == "dsmla_sparse_decode":
             line.setdefault("next_rows", {})[n] = sparse_decode_line(d, pk)
@@ -659,13 +805,13 @@ def main():
     if not args.no_cpu_baseline:
         import oracle
         s = OracleSampler(wl)
-        w0 = time.perf_counter()
-        while time.perf_counter() - w0 < 12.0 or s.n < 8:
-            s.sample(dec_keys=8192)
-        line["cpu_baseline"] = {"value": r["rows"] / s.step_seconds(), "unit": UNIT,
+        s.sample()  # warm-up (page faults, thread pool)
+        s.reset()
+        while s.t < 10.0 or s.steps < 3:
+            s.sample()
+        line["cpu_baseline"] = {"value": s.value(), "unit": UNIT,
                                 "cores": oracle.num_threads(), "kind": "oracle",
-                                "sample": s.describe(),
-                                "sample_seconds": time.perf_counter() - w0 + s.t_fixed}
+                                "sample": s.describe(), "sample_seconds": s.t}
         for n, cb in next_row_cpu_baselines(wl, set(line.get("next_rows", {}))).items():
             line["next_rows"][n]["cpu_baseline"] = cb
     print(json.dumps(line), flush=True)

@@ -100,3 +100,22 @@ def test_next_row_cpu_baselines_small_workload():
         assert v["value"] > 0 and v["unit"] == "tokens/s" and v["kind"] == "oracle" and v["cores"] >= 1
     assert "2 tokens" in out["dsmla_sparse_decode"]["sample"]
     assert bench.next_row_cpu_baselines(wl, set()) == {}
+
+
+def test_oracle_sampler_counts_whole_rows_it_measured():
+    """The CPU baseline is measured, not extrapolated: a sample step runs whole
+    rows (one decode row, its share of prefill rows) and the value is the rows
+    it ran over the time it took."""
+    import workloads as W
+    wl = W.build("small_mixed", decode_ctx=[300, 200], next_n=1, prefill=[(256, 64), (128, 64)],
+                 topk=64, seed=3, dsmla=True)
+    s = bench.OracleSampler(wl)
+    assert s.pf_per_dec == 64  # 128 prefill rows for 2 decode rows
+    s.sample()
+    s.reset()
+    for _ in range(3):
+        s.sample()
+    assert s.steps == 3
+    assert 3 <= s.rows <= 3 * 65
+    assert s.value() == pytest.approx(s.rows / s.t)
+    assert "3 sample steps" in s.describe()
