@@ -257,63 +257,92 @@ def config_entries(dev, stream, n_launch=60):
     for name, fn in (("decode_b32", W.decode_b32), ("decode_mtp2_b128", W.decode_mtp2_b128),
                      ("prefill_8k", W.prefill_8k)):
         wl = fn(seed=0)
-        st = make_step(wl, dev)
+        st = make_step(wl, dev, fused=True)
         st.run(stream=stream)
+        R = st.decode.w.shape[0] if wl.n_decode else st.prefill.w.shape[0]
         if wl.n_decode:
             d = st.decode
+            rows = wl.n_decode * wl.next_n
+            hist = lambda: dsix.ix_paged_mqa_logits_hist(d.q, d.w, st.cache, d.context_lens, st.block_table,
+                                                         st.dec_logits, wl.topk, st.dec_ws, stream=stream)
+            sel = lambda: dsix.ix_topk_from_hist(st.dec_logits, d.row_len, d.row_req, st.block_table, wl.topk,
+                                                 st.dec_global, st.dec_ws, stream=stream)
             logits = lambda: dsix.ix_paged_mqa_logits(d.q, d.w, st.cache, d.context_lens, st.block_table,
                                                       st.dec_logits, stream=stream)
             topk = lambda: dsix.ix_topk_to_global(st.dec_logits, d.row_len, d.row_req, st.block_table,
                                                   wl.topk, st.dec_global, None, stream=stream)
-            rows = wl.n_decode * wl.next_n
         else:
             p = st.prefill
+            rows = wl.n_prefill_rows
+            hist = lambda: dsix.ix_mqa_logits_hist(p.q, p.w, st.k_fp8, st.k_scale, p.ks, p.ke, st.pf_logits,
+                                                   wl.topk, st.pf_ws, stream=stream)
+            sel = lambda: dsix.ix_topk_from_hist(st.pf_logits, p.row_len, p.row_req, st.block_table, wl.topk,
+                                                 st.pf_global, st.pf_ws, stream=stream)
             logits = lambda: dsix.ix_mqa_logits(p.q, p.w, st.k_fp8, st.k_scale, p.ks, p.ke, st.pf_logits,
                                                 stream=stream)
             topk = lambda: dsix.ix_topk_to_global(st.pf_logits, p.row_len, p.row_req, st.block_table,
                                                   wl.topk, st.pf_global, None, stream=stream)
-            rows = wl.n_prefill_rows
         for _ in range(3):
+            hist()
+            sel()
             logits()
             topk()
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_launch)]
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_launch)]
         for e in evs:
             torch.sum(flush, 0, out=sink)
             e[0].record(stream)
-            logits()
+            hist()
             e[1].record(stream)
-            topk()
+            sel()
             e[2].record(stream)
+            torch.sum(flush, 0, out=sink)
+            e[3].record(stream)
+            logits()
+            e[4].record(stream)
+            topk()
+            e[5].record(stream)
         torch.cuda.synchronize()
         if dsix.ix_device_status() != 0:
             raise RuntimeError(f"device status set in the {name} timing")
-        lg = [a.elapsed_time(b) for a, b, _ in evs]
-        tk = [b.elapsed_time(c) for _, b, c in evs]
-        pair = [a.elapsed_time(c) for a, _, c in evs]
+        t = lambda i, j: [e[i].elapsed_time(e[j]) for e in evs]
         dec_keys, pairs = algorithmic(wl)
+
+        def kern(ms_list):
+            return {"ms": float(np.mean(ms_list)), **{f"ms_{k}": v for k, v in spread(ms_list).items()}}
+
+        def rate(kd):
+            ms = kd["ms"]
+            if wl.n_decode:
+                gbs = dec_keys * DECODE_BYTES_PER_KEY / (ms / 1e3) / 1e9
+                gbs_med = dec_keys * DECODE_BYTES_PER_KEY / (kd["ms_median"] / 1e3) / 1e9
+                kd.update(achieved=gbs, unit="GB/s", units=dec_keys,
+                          per_unit=f"{DECODE_BYTES_PER_KEY} B per key, read once per request",
+                          peak=pk["hbm_gbs"], peak_kind=f"{pk_kind} copy bandwidth",
+                          frac=gbs / pk["hbm_gbs"], frac_at_median=gbs_med / pk["hbm_gbs"],
+                          frac_of_8tbs=gbs / NOMINAL_HBM_GBS, target=0.70)
+            else:
+                tfs = pairs * PREFILL_FLOP_PER_PAIR / (ms / 1e3) / 1e12
+                tfs_med = pairs * PREFILL_FLOP_PER_PAIR / (kd["ms_median"] / 1e3) / 1e12
+                kd.update(achieved=tfs, unit="TFLOP/s", units=pairs,
+                          per_unit=f"{PREFILL_FLOP_PER_PAIR} flop per visible (query, key) pair",
+                          peak=fp8_meas, peak_kind=f"{pk_kind}: fp8 = 2 x cuBLAS bf16 burst {pk['bf16_tflops']}",
+                          frac=tfs / fp8_meas, frac_at_median=tfs_med / fp8_meas,
+                          frac_of_nominal_fp8=tfs / NOMINAL_FP8_TFLOPS, target=0.50)
+            return kd
+
+        fused_pair = [a + b for a, b in zip(t(0, 1), t(1, 2))]
+        unfused_pair = [a + b for a, b in zip(t(3, 4), t(4, 5))]
         e = {"workload": wl.name, "rows": rows, "top_k": wl.topk,
-             "l2": "flushed before every launch (256 MB read)",
-             "logits": {"ms": float(np.mean(lg)), **{f"ms_{k}": v for k, v in spread(lg).items()}},
-             "topk": {"ms": float(np.mean(tk)), **{f"ms_{k}": v for k, v in spread(tk).items()}},
-             "logits_plus_topk": {"ms": float(np.mean(pair)),
-                                  "query_tokens_per_s": rows / (float(np.mean(pair)) / 1e3)}}
-        ms = e["logits"]["ms"]
-        if wl.n_decode:
-            gbs = dec_keys * DECODE_BYTES_PER_KEY / (ms / 1e3) / 1e9
-            gbs_med = dec_keys * DECODE_BYTES_PER_KEY / (e["logits"]["ms_median"] / 1e3) / 1e9
-            e["logits"].update(achieved=gbs, unit="GB/s", units=dec_keys,
-                               per_unit=f"{DECODE_BYTES_PER_KEY} B per key, read once per request",
-                               peak=pk["hbm_gbs"], peak_kind=f"{pk_kind} copy bandwidth",
-                               frac=gbs / pk["hbm_gbs"], frac_at_median=gbs_med / pk["hbm_gbs"],
-                               frac_of_8tbs=gbs / NOMINAL_HBM_GBS, target=0.70)
-        else:
-            tfs = pairs * PREFILL_FLOP_PER_PAIR / (ms / 1e3) / 1e12
-            tfs_med = pairs * PREFILL_FLOP_PER_PAIR / (e["logits"]["ms_median"] / 1e3) / 1e12
-            e["logits"].update(achieved=tfs, unit="TFLOP/s", units=pairs,
-                               per_unit=f"{PREFILL_FLOP_PER_PAIR} flop per visible (query, key) pair",
-                               peak=fp8_meas, peak_kind=f"{pk_kind}: fp8 = 2 x cuBLAS bf16 burst {pk['bf16_tflops']}",
-                               frac=tfs / fp8_meas, frac_at_median=tfs_med / fp8_meas,
-                               frac_of_nominal_fp8=tfs / NOMINAL_FP8_TFLOPS, target=0.50)
+             "l2": "flushed before each logits launch (256 MB read); the top-k follows its logits",
+             "logits": rate(kern(t(0, 1))),
+             "topk": kern(t(1, 2)),
+             "logits_plus_topk": {"ms": float(np.mean(fused_pair)),
+                                  "query_tokens_per_s": rows / (float(np.mean(fused_pair)) / 1e3)},
+             "unfused": {"logits": rate(kern(t(3, 4))), "topk": kern(t(4, 5)),
+                         "logits_plus_topk": {"ms": float(np.mean(unfused_pair)),
+                                              "query_tokens_per_s": rows / (float(np.mean(unfused_pair)) / 1e3)}},
+             "note": "logits / topk: the two kernels of the fused call (histogram logits kernel, selection "
+                     "from the histograms); unfused: the standalone logits kernel and top-k"}
         out[name] = e
         del st
         torch.cuda.empty_cache()
@@ -330,7 +359,7 @@ def gpu_arm(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = W.NAMED[args.workload](seed=rank)
-    step = make_step(wl, dev)
+    step = make_step(wl, dev, fused=not args.unfused)
     stream = torch.cuda.current_stream(dev)
     names = []
     if wl.prefill_req:
@@ -360,8 +389,8 @@ def gpu_arm(args, world, rank, local):
     n_ev = min(args.steps, 200)
     ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(n_ev)] for n in names}
-    for i in range(n_ev):
-        step.run(stream=stream, events={n: ev[n][i] for n in names})
+    for i in range(n_ev):  # a fused step issues its fused calls as their two halves here
+        step.run(stream=stream, events={n: ev[n][i] for n in names}, split=True)
     torch.cuda.synchronize()
     kern_ms = {n: float(np.mean([a.elapsed_time(b) for a, b in ev[n]])) for n in names}
     kern_spread = {n: spread([a.elapsed_time(b) for a, b in ev[n]]) for n in names}
@@ -444,7 +473,7 @@ def gpu_arm(args, world, rank, local):
     # each buffer's reuse (a set's inputs are rewritten only after the step that
     # read them ran, its indices only after they were copied out).
     e2e_steps = min(args.steps, 200)
-    steps = [step, make_step(wl, dev)]
+    steps = [step, make_step(wl, dev, fused=not args.unfused)]
     host_src = {
         "new_k": wl.new_k.pin_memory(),
         "new_slot": torch.from_numpy(wl.new_slot.copy()).pin_memory(),
@@ -716,6 +745,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="dsix", choices=["dsix", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="run each logits call and its top-k as separate calls (default: the fused calls)")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-configuration timing of the decode, MTP and prefill kernels")
     ap.add_argument("--workload", default="mixed_long",
@@ -782,7 +813,8 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "fp8_e4m3 x fp8_e4m3 -> f32 (logits); u8/bf16 cache writes",
             "data": "synthetic (seeded; random-init inputs of the indexer shapes; no dataset)",
-            "config": {**workload_config(wl), "parallelism": f"replicas x{world}"},
+            "config": {**workload_config(wl), "parallelism": f"replicas x{world}",
+                       "fused_logits_topk": not args.unfused},
             "roofline": roofline, "kernels": kernels,
             "prefill_tflops": pf_tflops, "decode_hbm_gbs": dec_gbs,
             "e2e": {"value": job_throughput(world, r["rows"], r["e2e_steps"], e2e_ms), "unit": UNIT,

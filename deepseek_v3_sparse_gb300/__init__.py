@@ -23,6 +23,8 @@ import torch
 __all__ = [
     "DsixError", "load", "ix_status_string", "ix_device_status", "ix_quant_write_k",
     "ix_gather_k", "ix_paged_mqa_logits", "ix_mqa_logits", "ix_topk_to_global",
+    "ix_topk_hist_workspace_size", "ix_paged_mqa_logits_topk", "ix_mqa_logits_topk",
+    "ix_paged_mqa_logits_hist", "ix_mqa_logits_hist", "ix_topk_from_hist",
     "dsmla_quant_write", "dsmla_norm_rope_write", "dsmla_sparse_decode",
     "dsmla_sparse_decode_workspace_size", "dsmla_sparse_decode_noalloc", "MLA_HEADS", "LIB_PATH", "HEADS", "HEAD_DIM", "BLOCK_SIZE",
 ]
@@ -56,6 +58,17 @@ _SIGNATURES = {
                              _I64, _I32, _P], _I32),
     "ix_mqa_logits": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64, _I32, _P], _I32),
     "ix_topk_to_global": ([_P, _I64, _I64, _P, _P, _P, _I64, _I32, _I32, _P, _P, _P], _I32),
+    "ix_topk_hist_workspace_size": ([_I64], ctypes.c_size_t),
+    "ix_paged_mqa_logits_topk": ([_P, _P, _P, _I64, _I32, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _I64,
+                                  _I32, _P, _P, _P, ctypes.c_size_t, _P], _I32),
+    "ix_mqa_logits_topk": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64, _P, _P, _I64, _I32,
+                            _I32, _P, _P, _P, ctypes.c_size_t, _P], _I32),
+    "ix_paged_mqa_logits_hist": ([_P, _P, _P, _I64, _I32, _P, _P, _I64, _I32, _I32, _I32, _I32, _P, _I64,
+                                  _I32, _P, ctypes.c_size_t, _P], _I32),
+    "ix_mqa_logits_hist": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64, _I32, _P,
+                            ctypes.c_size_t, _P], _I32),
+    "ix_topk_from_hist": ([_P, _I64, _I64, _P, _P, _P, _I64, _I32, _I32, _P, _P, _P, ctypes.c_size_t, _P],
+                          _I32),
     "dsmla_quant_write": ([_P, _P, _I64, _P, _P, _I64, _I32, _I64, _I64, _P], _I32),
     "dsmla_norm_rope_write": ([_P, _P, _P, ctypes.c_float, _P, _P, _I64, _P, _I64, _P, _I64, _I32,
                                _I64, _I64, _P], _I32),
@@ -253,6 +266,141 @@ def ix_topk_to_global(logits: torch.Tensor, row_len: torch.Tensor, row_req: torc
         block_table.stride(0), block_size, int(k), _opt(out_local, "out_local", _I32T),
         _dev(out_global, "out_global", _I32T), _stream(stream))
     _check(rc, "ix_topk_to_global")
+
+
+def ix_topk_hist_workspace_size(rows: int) -> int:
+    """Bytes of the fused calls' histogram workspace for `rows` logits rows (zero it
+    once when it is allocated; every completed call leaves it zero)."""
+    return int(load().ix_topk_hist_workspace_size(int(rows)))
+
+
+def _workspace(ws: torch.Tensor, rows: int):
+    _need(isinstance(ws, torch.Tensor) and ws.numel() * ws.element_size() >= ix_topk_hist_workspace_size(rows),
+          f"workspace: fewer than {ix_topk_hist_workspace_size(rows)} bytes for {rows} rows")
+    return _dev(ws, "workspace", (torch.uint8, torch.int32, torch.float32)), ws.numel() * ws.element_size()
+
+
+def ix_paged_mqa_logits_topk(q_fp8: torch.Tensor, w: torch.Tensor, cache: torch.Tensor,
+                             context_lens: torch.Tensor, block_table: torch.Tensor, logits: torch.Tensor,
+                             k: int, out_global: torch.Tensor, workspace: torch.Tensor,
+                             out_local: Optional[torch.Tensor] = None, block_size: int = BLOCK_SIZE,
+                             stream=None) -> None:
+    """Decode logits over the paged cache and the top-k of their rows in one call
+    (see ix_paged_mqa_logits and ix_topk_to_global); logits [B*next_n, ld] f32 is
+    written and read back; out_global/out_local [B*next_n, k] int32."""
+    _rows(q_fp8, 0, "q_fp8", dim=4)
+    B, next_n, H, D = q_fp8.shape
+    R = B * next_n
+    _rows(w, R, "w", H)
+    _rows(logits, R, "logits")
+    _len(context_lens, B, "context_lens")
+    _rows(block_table, B, "block_table")
+    _rows(cache, 0, "cache", block_size * (D + 4))
+    _len(out_global, R * int(k), "out_global")
+    if out_local is not None:
+        _len(out_local, R * int(k), "out_local")
+    wp, wb = _workspace(workspace, R)
+    rc = load().ix_paged_mqa_logits_topk(
+        _dev(q_fp8, "q_fp8", _U8), _dev(w, "w", _F32), _dev(cache, "cache", (torch.uint8,)),
+        cache.shape[0], block_size, _dev(context_lens, "context_lens", _I32T),
+        _dev(block_table, "block_table", _I32T), block_table.stride(0), B, next_n, H, D,
+        _dev(logits, "logits", _F32), logits.shape[1], int(k), _opt(out_local, "out_local", _I32T),
+        _dev(out_global, "out_global", _I32T), wp, wb, _stream(stream))
+    _check(rc, "ix_paged_mqa_logits_topk")
+
+
+def ix_mqa_logits_topk(q_fp8: torch.Tensor, w: torch.Tensor, k_fp8: torch.Tensor, k_scale: torch.Tensor,
+                       ks: torch.Tensor, ke: torch.Tensor, logits: torch.Tensor, row_req: torch.Tensor,
+                       block_table: torch.Tensor, k: int, out_global: torch.Tensor, workspace: torch.Tensor,
+                       out_local: Optional[torch.Tensor] = None, block_size: int = BLOCK_SIZE,
+                       stream=None) -> None:
+    """Prefill logits over contiguous K and the top-k of their rows in one call
+    (see ix_mqa_logits and ix_topk_to_global); row t has ke[t] - ks[t] keys and is
+    remapped through block_table[row_req[t]]."""
+    _rows(q_fp8, 0, "q_fp8", dim=3)
+    tq, H, D = q_fp8.shape
+    _rows(w, tq, "w", H)
+    _rows(k_fp8, 0, "k_fp8", D)
+    _len(k_scale, k_fp8.shape[0], "k_scale")
+    _len(ks, tq, "ks")
+    _len(ke, tq, "ke")
+    _len(row_req, tq, "row_req")
+    _rows(logits, tq, "logits")
+    _rows(block_table, 0, "block_table")
+    _len(out_global, tq * int(k), "out_global")
+    if out_local is not None:
+        _len(out_local, tq * int(k), "out_local")
+    wp, wb = _workspace(workspace, tq)
+    rc = load().ix_mqa_logits_topk(
+        _dev(q_fp8, "q_fp8", _U8), _dev(w, "w", _F32), _dev(k_fp8, "k_fp8", _U8),
+        _dev(k_scale, "k_scale", _F32), _dev(ks, "ks", _I32T), _dev(ke, "ke", _I32T), tq, k_fp8.shape[0], H, D,
+        _dev(logits, "logits", _F32), logits.shape[1], _dev(row_req, "row_req", _I32T),
+        _dev(block_table, "block_table", _I32T), block_table.stride(0), block_size, int(k),
+        _opt(out_local, "out_local", _I32T), _dev(out_global, "out_global", _I32T), wp, wb, _stream(stream))
+    _check(rc, "ix_mqa_logits_topk")
+
+
+def ix_paged_mqa_logits_hist(q_fp8: torch.Tensor, w: torch.Tensor, cache: torch.Tensor,
+                             context_lens: torch.Tensor, block_table: torch.Tensor, logits: torch.Tensor,
+                             k: int, workspace: torch.Tensor, block_size: int = BLOCK_SIZE, stream=None) -> None:
+    """First half of ix_paged_mqa_logits_topk: the logits and the row histograms."""
+    _rows(q_fp8, 0, "q_fp8", dim=4)
+    B, next_n, H, D = q_fp8.shape
+    R = B * next_n
+    _rows(w, R, "w", H)
+    _rows(logits, R, "logits")
+    _len(context_lens, B, "context_lens")
+    _rows(block_table, B, "block_table")
+    _rows(cache, 0, "cache", block_size * (D + 4))
+    wp, wb = _workspace(workspace, R)
+    rc = load().ix_paged_mqa_logits_hist(
+        _dev(q_fp8, "q_fp8", _U8), _dev(w, "w", _F32), _dev(cache, "cache", (torch.uint8,)),
+        cache.shape[0], block_size, _dev(context_lens, "context_lens", _I32T),
+        _dev(block_table, "block_table", _I32T), block_table.stride(0), B, next_n, H, D,
+        _dev(logits, "logits", _F32), logits.shape[1], int(k), wp, wb, _stream(stream))
+    _check(rc, "ix_paged_mqa_logits_hist")
+
+
+def ix_mqa_logits_hist(q_fp8: torch.Tensor, w: torch.Tensor, k_fp8: torch.Tensor, k_scale: torch.Tensor,
+                       ks: torch.Tensor, ke: torch.Tensor, logits: torch.Tensor, k: int, workspace: torch.Tensor,
+                       stream=None) -> None:
+    """First half of ix_mqa_logits_topk: the logits and the row histograms."""
+    _rows(q_fp8, 0, "q_fp8", dim=3)
+    tq, H, D = q_fp8.shape
+    _rows(w, tq, "w", H)
+    _rows(k_fp8, 0, "k_fp8", D)
+    _len(k_scale, k_fp8.shape[0], "k_scale")
+    _len(ks, tq, "ks")
+    _len(ke, tq, "ke")
+    _rows(logits, tq, "logits")
+    wp, wb = _workspace(workspace, tq)
+    rc = load().ix_mqa_logits_hist(
+        _dev(q_fp8, "q_fp8", _U8), _dev(w, "w", _F32), _dev(k_fp8, "k_fp8", _U8),
+        _dev(k_scale, "k_scale", _F32), _dev(ks, "ks", _I32T), _dev(ke, "ke", _I32T), tq, k_fp8.shape[0], H, D,
+        _dev(logits, "logits", _F32), logits.shape[1], int(k), wp, wb, _stream(stream))
+    _check(rc, "ix_mqa_logits_hist")
+
+
+def ix_topk_from_hist(logits: torch.Tensor, row_len: torch.Tensor, row_req: torch.Tensor,
+                      block_table: torch.Tensor, k: int, out_global: torch.Tensor, workspace: torch.Tensor,
+                      out_local: Optional[torch.Tensor] = None, block_size: int = BLOCK_SIZE,
+                      stream=None) -> None:
+    """Second half of the fused calls: the selection from the row histograms."""
+    _rows(logits, 0, "logits")
+    R, ld = logits.shape
+    _len(row_len, R, "row_len")
+    _len(row_req, R, "row_req")
+    _rows(block_table, 0, "block_table")
+    _len(out_global, R * int(k), "out_global")
+    if out_local is not None:
+        _len(out_local, R * int(k), "out_local")
+    wp, wb = _workspace(workspace, R)
+    rc = load().ix_topk_from_hist(
+        _dev(logits, "logits", _F32), ld, R, _dev(row_len, "row_len", _I32T),
+        _dev(row_req, "row_req", _I32T), _dev(block_table, "block_table", _I32T),
+        block_table.stride(0), block_size, int(k), _opt(out_local, "out_local", _I32T),
+        _dev(out_global, "out_global", _I32T), wp, wb, _stream(stream))
+    _check(rc, "ix_topk_from_hist")
 
 
 def dsmla_quant_write(nope_bf16: torch.Tensor, rope_bf16: torch.Tensor,

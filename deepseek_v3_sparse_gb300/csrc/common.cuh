@@ -304,6 +304,56 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
     return static_cast<uint32_t>(r);
 }
 
+// ---------------------------------------------------------------------------
+// top-k radix keys and the per-row histogram of their first digit
+// ---------------------------------------------------------------------------
+// Order-preserving 32-bit key of a float: f + 0 turns -0.0 into +0.0 (round
+// to nearest) and leaves every other value alone; then negative floats flip
+// all bits, others only the sign bit.  Larger floats get larger keys.
+__device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t b = __float_as_uint(__fadd_rn(f, 0.0f));
+    return b ^ (static_cast<uint32_t>(static_cast<int32_t>(b) >> 31) | 0x80000000u);
+}
+
+// First radix digit of a key: its top 11 bits (sign, exponent, two mantissa
+// bits).  A row's histogram over this digit is kept as 64 coarse bins (the sum
+// of 32 consecutive fine bins each) followed by the 2048 fine bins, all u32.
+constexpr int kDigitShift = 21;
+constexpr int kHistFine = 2048;
+constexpr int kHistCoarse = 64;
+constexpr int kHistRowWords = kHistCoarse + kHistFine;
+
+// Longest row the top-k kernels take (a cluster of 8 CTAs x 32768 keys), and
+// the longest row the fused path's warp-per-row selection takes.
+constexpr int64_t kTopkMaxLd = 262144;
+constexpr int64_t kSelMaxLd = 65536;
+
+// The selection that completes a histogram logits kernel (topk.cu): rows
+// given by row_len / row_req when row_len != NULL, else the logits kernel's own
+// rows (decode rows when context_lens != NULL, else prefill rows with ks / ke /
+// row_req), clamped the same way.
+struct SelectRows {
+    const float* logits;
+    int64_t ld;
+    int64_t rows;
+    const int32_t* row_len;
+    const int32_t* context_lens;
+    int next_n;
+    const int32_t* ks;
+    const int32_t* ke;
+    int64_t tk;
+    const int32_t* row_req;
+    const int32_t* block_table;
+    int64_t bt_stride;
+    int block_size;
+    int k;
+    int32_t* out_local;
+    int32_t* out_global;
+    uint32_t* hist;
+    int* status;
+};
+int select_after_logits(const SelectRows& q, cudaStream_t stream);
+
 __device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xFFFF0000u); }
 

@@ -66,16 +66,19 @@ constexpr int kThreads = 64 + kEpiGroups * 128;  // producer + MMA warps + 4 war
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kFirstEpiWarp = 2;
-constexpr int kSmemGroups = 2048;
 constexpr int kTmemCols = 512;
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 100 ms
 
-template <bool kPaged>
+// TK: the variant that also builds, per row, the histogram of the first radix
+// digit of every logit (the ix_*_topk entry points).
+template <bool kPaged, bool TK = false>
 struct Cfg;
 
-template <>
-struct Cfg<true> {  // decode over the paged cache
+template <bool TK>
+struct Cfg<true, TK> {  // decode over the paged cache
     static constexpr int kStages = 8;
+    static constexpr int kSmemGroups = 2048;
+    static constexpr int kHistWords = TK ? 2 * 2048 : 0;  // next_n <= 2 rows, one u32 per bin
     static constexpr int kQBytes = 2 * kHeads * kDim;  // next_n <= 2
     static constexpr int kWFloats = 2 * kHeads;
     static constexpr int kSlots = 4;
@@ -84,10 +87,14 @@ struct Cfg<true> {  // decode over the paged cache
     static constexpr int kGroupsPerJob = 1;  // epilogue warpgroups sharing one job
 };
 
-template <>
-struct Cfg<false> {  // prefill over contiguous K
+template <bool TK>
+struct Cfg<false, TK> {  // prefill over contiguous K
     static constexpr int kRows = 8;
-    static constexpr int kStages = 4;
+    // the histogram variant gives up one K stage and half of the per-group
+    // schedule cache to hold its 8 row histograms
+    static constexpr int kStages = TK ? 3 : 4;
+    static constexpr int kSmemGroups = TK ? 1024 : 2048;
+    static constexpr int kHistWords = TK ? 8 * 1024 : 0;  // 8 rows, two u16 bins per word
     static constexpr int kQBytes = kRows * kHeads * kDim;  // 64 KB
     static constexpr int kWFloats = kRows * kHeads;
     static constexpr int kSlots = 2;
@@ -97,16 +104,17 @@ struct Cfg<false> {  // prefill over contiguous K
     static_assert(kRows == 4 * kJobsPerTile && kGroupsPerJob == kEpiGroups, "one job row per warpgroup");
 };
 
-template <bool P>
+template <bool P, bool TK = false>
 struct Smem {
-    using C = Cfg<P>;
+    using C = Cfg<P, TK>;
     static constexpr int kQ = 0;                                     // 2 Q buffers
     static constexpr int kK = kQ + 2 * C::kQBytes;                   // K stages
     static constexpr int kW = kK + C::kStages * kTileBytes;          // 2 head-weight buffers
     static constexpr int kTiles = kW + 2 * C::kWFloats * 4;          // tiles per group
-    static constexpr int kKbeg = kTiles + kSmemGroups * 4;            // first key of each group
-    static constexpr int kBar = kKbeg + kSmemGroups * 4;
-    static constexpr int kNumBars = 2 * C::kStages + 4 + 2 * C::kSlots + 1;
+    static constexpr int kKbeg = kTiles + C::kSmemGroups * 4;         // first key of each group
+    static constexpr int kHist = kKbeg + C::kSmemGroups * 4;          // row histograms (TK)
+    static constexpr int kBar = kHist + C::kHistWords * 4;
+    static constexpr int kNumBars = 2 * C::kStages + 4 + 2 * C::kSlots + 1 + 4;  // + 4 histogram barriers
     static constexpr int kMisc = kBar + kNumBars * 8;
     static constexpr int kScan = kMisc + 64;
     static constexpr int kTotal = kScan + 64 * 4;
@@ -135,6 +143,10 @@ struct LogitsArgs {
     const int32_t* ke;
     int64_t tq;
     int64_t tk;
+    // histogram variant: rows with more than k visible keys add the first radix
+    // digit of each of their logits to hist[row * kHistRowWords ...]
+    uint32_t* hist;
+    int k;
 };
 
 // ---------------------------------------------------------------------------
@@ -229,13 +241,14 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) 
     return r;
 }
 
-// Walks the flattened (group, tile) units of this CTA.
+// Walks the flattened (group, tile) units of this CTA.  Groups below `cap`
+// have their tile counts cached in shared memory.
 template <bool P>
 struct Cursor {
-    int g, t, ntiles, left;
+    int g, t, ntiles, left, cap;
     __device__ __forceinline__ int tiles_of(const LogitsArgs& a, const int* s_tiles, int gg) const {
         if (gg >= a.num_groups) return 0;
-        return gg < kSmemGroups ? s_tiles[gg] : group_tiles<P>(a, gg, false);
+        return gg < cap ? s_tiles[gg] : group_tiles<P>(a, gg, false);
     }
     // Returns true when the next unit starts a new group.  Never walks past
     // the last group: if the unit count and the groups disagree, it stops.
@@ -400,12 +413,12 @@ __device__ __forceinline__ float head_sums_16x256b(uint32_t tbase, const uint64_
     return ((odd ? x1 : x0) + r) * 0x1p25f;  // undo the ReLU's 2^-25 (exact)
 }
 
-template <bool P, int NN>
+template <bool P, int NN, bool TK>
 __global__ void __launch_bounds__(kThreads, 1)
     logits_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
                   const LogitsArgs a) {
-    using C = Cfg<P>;
-    using S = Smem<P>;
+    using C = Cfg<P, TK>;
+    using S = Smem<P, TK>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -421,6 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* acc_full = qw_empty + 2;
     uint64_t* acc_empty = acc_full + C::kSlots;
     uint64_t* mma_done = acc_empty + C::kSlots;
+    uint64_t* hbar = mma_done + 1;  // histogram hand-offs (TK): one per warpgroup (prefill), [0] (decode)
+    uint32_t* s_hist = reinterpret_cast<uint32_t*>(sm + S::kHist);
     int* misc = reinterpret_cast<int*>(sm + S::kMisc);  // tmem base, abort, g0, t0, units
     int* scan = reinterpret_cast<int*>(sm + S::kScan);
     volatile int* abort_flag = misc + 1;
@@ -441,6 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(acc_empty + i, 4 * C::kGroupsPerJob);
         }
         mbar_init(mma_done, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(hbar + i, P ? 4 * kEpiGroups : 4);
         fence_barrier_init();
         misc[1] = 0;
         misc[4] = 0;
@@ -452,6 +468,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(reinterpret_cast<uint32_t*>(misc), kTmemCols);
         tmem_relinquish();
     }
+    if constexpr (TK) {
+        for (int i = threadIdx.x; i < C::kHistWords; i += kThreads) s_hist[i] = 0u;
+    }
 
     // ---- schedule: split the flattened unit list evenly across CTAs ----
     const int G = a.num_groups;
@@ -460,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kb, ke;
         group_range<P>(a, g, kb, ke, blockIdx.x == 0);
         const int n = ke > kb ? (ke - kb + kTile - 1) / kTile : 0;
-        if (g < kSmemGroups) {
+        if (g < C::kSmemGroups) {
             s_tiles[g] = n;
             s_kbeg[g] = kb;
         }
@@ -481,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int running = 0;
         for (int base = 0; base < G && running <= u0; base += kThreads) {
             const int g = base + threadIdx.x;
-            const int n = g < G ? (g < kSmemGroups ? s_tiles[g] : group_tiles<P>(a, g, false)) : 0;
+            const int n = g < G ? (g < C::kSmemGroups ? s_tiles[g] : group_tiles<P>(a, g, false)) : 0;
             int chunk;
             const int excl = block_excl_scan(n, scan, &chunk) + running;
             if (n > 0 && excl <= u0 && u0 < excl + n) {
@@ -500,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // key range of a group; prefill groups' first keys were kept in shared
     // memory by the schedule (their end is not needed past it)
     auto group_bounds = [&](int gg, int& kb, int& ke) {
-        if (!P && gg < kSmemGroups) {
+        if (!P && gg < C::kSmemGroups) {
             kb = s_kbeg[gg];
             ke = 0;
         } else {
@@ -513,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         cur.g = misc[2];
         cur.t = misc[3];
         cur.left = units;
+        cur.cap = C::kSmemGroups;
         cur.ntiles = cur.tiles_of(a, s_tiles, cur.g);
 
         if (warp == kProducerWarp) {
@@ -674,15 +694,71 @@ __global__ void __launch_bounds__(kThreads, 1)
             int rs0[2], rs1[2];  // visible key range of rows wg and 4 + wg
             float* orow[2];      // their logits rows
             uint64_t w2[2][8];   // packed head-weight pairs of those rows
-            bool new_group = true, have_group = false;
+            bool new_group = true, have_group = false, live = true;
+            // TK: the warpgroup's two rows keep their digit histograms in shared
+            // memory (two u16 counters per word); a hand-off adds them to the
+            // rows' global histograms and clears them.  It runs when the group
+            // ends, and every 256 tiles of one group so no u16 counter overflows.
+            bool hw0 = false, hw1 = false;  // rows wg and 4 + wg have more than k keys
+            int64_t hr0 = 0, hr1 = 0;       // their row indices
+            uint32_t hsync = 0;             // waits done on this warpgroup's hand-off barrier
+            int gtiles = 0;                 // tiles of the current group since the last hand-off
+            auto hflush = [&]() -> bool {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(hbar + wg);
+                if (!wait_warp(hbar + wg, hsync & 1, abort_flag, a.status)) return false;
+                ++hsync;
+                // warp `quad` of the warpgroup takes words [512 quad, 512 quad + 512) of
+                // its 2 x 1024 words, 16 per lane: 32 fine bins = one coarse bin
+                const int w0 = 512 * quad + 16 * lane;
+                const int hh = w0 >> 10, wr = w0 & 1023;
+                uint4* src = reinterpret_cast<uint4*>(s_hist + (4 * hh + wg) * 1024 + wr);
+                uint32_t x[16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 v = src[i];
+                    x[4 * i] = v.x;
+                    x[4 * i + 1] = v.y;
+                    x[4 * i + 2] = v.z;
+                    x[4 * i + 3] = v.w;
+                    src[i] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                if (hh ? hw1 : hw0) {
+                    uint32_t* G = a.hist + (hh ? hr1 : hr0) * kHistRowWords;
+                    uint32_t csum = 0;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const uint32_t lo = x[i] & 0xFFFFu, hi = x[i] >> 16;
+                        if (lo) atomicAdd(G + kHistCoarse + 2 * (wr + i), lo);
+                        if (hi) atomicAdd(G + kHistCoarse + 2 * (wr + i) + 1, hi);
+                        csum += lo + hi;
+                    }
+                    if (csum) atomicAdd(G + (wr >> 4), csum);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(hbar + wg);
+                if (!wait_warp(hbar + wg, hsync & 1, abort_flag, a.status)) return false;
+                ++hsync;
+                return true;
+            };
             while (cur.left > 0) {
                 const int g = cur.g;
                 if (new_group) {
+                    if constexpr (TK) {
+                        if (have_group && !hflush()) {
+                            live = false;
+                            break;
+                        }
+                        gtiles = 0;
+                    }
                     if (have_group) {
                         __syncwarp();
                         if (lane == 0) mbar_arrive(qw_empty + ((qi - 1) & 1));
                     }
-                    if (!wait_warp(qw_full + (qi & 1), (qi >> 1) & 1, abort_flag, a.status)) break;
+                    if (!wait_warp(qw_full + (qi & 1), (qi >> 1) & 1, abort_flag, a.status)) {
+                        live = false;
+                        break;
+                    }
                     have_group = true;
                     group_bounds(g, kbeg, kend);
                     const float* wq = sW + (qi & 1) * C::kWFloats;
@@ -700,6 +776,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float2 wv = *reinterpret_cast<const float2*>(wr + 8 * j);
                             w2[h][j] = pack2(wv.x, wv.y);
                         }
+                    }
+                    if constexpr (TK) {
+                        hr0 = static_cast<int64_t>(g) * C::kRows + wg;
+                        hr1 = hr0 + 4;
+                        hw0 = hr0 < a.tq && rs1[0] - rs0[0] > a.k;
+                        hw1 = hr1 < a.tq && rs1[1] - rs0[1] > a.k;
                     }
                 }
                 const int s = kbeg + cur.t * kTile + m;  // key index
@@ -720,10 +802,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                             __syncwarp();
                             if (lane == 0) mbar_arrive(acc_empty + slot);
                         });
-                    if (s >= rs0[h] && s < rs1[h]) orow[h][s - rs0[h]] = sum * ksc;
+                    if (s >= rs0[h] && s < rs1[h]) {
+                        const float v = sum * ksc;
+                        orow[h][s - rs0[h]] = v;
+                        if constexpr (TK) {
+                            if (h ? hw1 : hw0) {
+                                const uint32_t d = order_key(v) >> kDigitShift;
+                                atomicAdd(s_hist + (4 * h + wg) * 1024 + (d >> 1), 1u << ((d & 1u) << 4));
+                            }
+                        }
+                    }
                 }
-                if (!ok) break;
+                if (!ok) {
+                    live = false;
+                    break;
+                }
                 new_group = cur.advance(a, s_tiles);
+                if constexpr (TK) {
+                    if (!new_group && cur.left > 0 && ++gtiles == 256) {  // long rows: keep the u16 counters small
+                        gtiles = 0;
+                        if (!hflush()) {
+                            live = false;
+                            break;
+                        }
+                    }
+                }
+            }
+            if constexpr (TK) {
+                if (live && have_group) hflush();
             }
         } else {
             // ------------------------------------------------------------ decode epilogue
@@ -736,21 +842,71 @@ __global__ void __launch_bounds__(kThreads, 1)
             int qi = 0, job = 0;
             int kbeg = 0, kend = 0;
             int rs1[NN];  // visible length of each row of the group
-            bool new_group = true, have_group = false;
+            bool new_group = true, have_group = false, live = true;
+            // TK: the group's rows keep one u32 digit histogram each in shared
+            // memory, shared by all 16 epilogue warps (jobs rotate over the
+            // warpgroups); when the group ends every warp hands off its share.
+            bool hw[NN];          // the row has more than k visible keys
+            int64_t hrow0 = 0;    // first row of the group
+            uint32_t hsync = 0;   // waits done on the hand-off barrier
+            auto hflush = [&]() -> bool {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(hbar);
+                if (!wait_warp(hbar, hsync & 1, abort_flag, a.status)) return false;
+                ++hsync;
+                const int et = threadIdx.x - kFirstEpiWarp * 32;  // 0..511: fine bins 4 et .. 4 et + 3
+#pragma unroll
+                for (int j = 0; j < NN; ++j) {
+                    uint4* src = reinterpret_cast<uint4*>(s_hist + j * kHistFine + 4 * et);
+                    const uint4 v = *src;
+                    *src = make_uint4(0u, 0u, 0u, 0u);
+                    if (hw[j]) {  // uniform over the CTA
+                        uint32_t* G = a.hist + (hrow0 + j) * kHistRowWords;
+                        if (v.x) atomicAdd(G + kHistCoarse + 4 * et, v.x);
+                        if (v.y) atomicAdd(G + kHistCoarse + 4 * et + 1, v.y);
+                        if (v.z) atomicAdd(G + kHistCoarse + 4 * et + 2, v.z);
+                        if (v.w) atomicAdd(G + kHistCoarse + 4 * et + 3, v.w);
+                        uint32_t csum = (v.x + v.y) + (v.z + v.w);  // a coarse bin = 8 consecutive threads
+                        csum += __shfl_xor_sync(0xffffffffu, csum, 1);
+                        csum += __shfl_xor_sync(0xffffffffu, csum, 2);
+                        csum += __shfl_xor_sync(0xffffffffu, csum, 4);
+                        if ((lane & 7) == 0 && csum) atomicAdd(G + (et >> 3), csum);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(hbar);
+                if (!wait_warp(hbar, hsync & 1, abort_flag, a.status)) return false;
+                ++hsync;
+                return true;
+            };
             while (cur.left > 0) {
                 const int g = cur.g;
                 if (new_group) {
+                    if constexpr (TK) {
+                        if (have_group && !hflush()) {
+                            live = false;
+                            break;
+                        }
+                    }
                     if (have_group) {
                         __syncwarp();
                         if (lane == 0) mbar_arrive(qw_empty + ((qi - 1) & 1));
                     }
-                    if (!wait_warp(qw_full + (qi & 1), (qi >> 1) & 1, abort_flag, a.status)) break;
+                    if (!wait_warp(qw_full + (qi & 1), (qi >> 1) & 1, abort_flag, a.status)) {
+                        live = false;
+                        break;
+                    }
                     ++qi;
                     have_group = true;
                     group_bounds(g, kbeg, kend);
                     const int ctx = __ldg(a.context_lens + g);
 #pragma unroll
                     for (int j = 0; j < NN; ++j) rs1[j] = decode_row_len(a, ctx, j, false);
+                    if constexpr (TK) {
+                        hrow0 = static_cast<int64_t>(g) * NN;
+#pragma unroll
+                        for (int j = 0; j < NN; ++j) hw[j] = rs1[j] > a.k;
+                    }
                 }
                 const float* wq = sW + ((qi - 1) & 1) * C::kWFloats;
                 const int s = kbeg + cur.t * kTile + m;  // key index
@@ -780,13 +936,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (lane == 0) mbar_arrive(acc_empty + slot);
                         });
 #pragma unroll
-                        for (int i = 0; i < NN; ++i)
-                            if (s < rs1[i]) a.logits[(static_cast<int64_t>(g) * NN + i) * a.ld + s] = sums[i] * ksc;
+                        for (int i = 0; i < NN; ++i) {
+                            if (s < rs1[i]) {
+                                const float v = sums[i] * ksc;
+                                a.logits[(static_cast<int64_t>(g) * NN + i) * a.ld + s] = v;
+                                if constexpr (TK) {
+                                    if (hw[i]) atomicAdd(s_hist + i * kHistFine + (order_key(v) >> kDigitShift), 1u);
+                                }
+                            }
+                        }
                     }
                 }
                 ++job;
-                if (!ok) break;
+                if (!ok) {
+                    live = false;
+                    break;
+                }
                 new_group = cur.advance(a, s_tiles);
+            }
+            if constexpr (TK) {
+                if (live && have_group) hflush();
             }
         }
     }
@@ -850,7 +1019,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool P, int NN>
+template <bool P, int NN, bool TK = false>
 int launch(const CUtensorMap& tmK, const CUtensorMap& tmQ,
            const LogitsArgs& a, int64_t rows, int clean, cudaStream_t stream) {
     static std::mutex mu;
@@ -861,8 +1030,8 @@ int launch(const CUtensorMap& tmK, const CUtensorMap& tmQ,
         std::lock_guard<std::mutex> lock(mu);
         if (dev >= static_cast<int>(ready.size())) ready.resize(dev + 1, 0);
         if (!ready[dev]) {
-            if (cudaFuncSetAttribute(logits_kernel<P, NN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     Smem<P>::kAlloc) != cudaSuccess)
+            if (cudaFuncSetAttribute(logits_kernel<P, NN, TK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Smem<P, TK>::kAlloc) != cudaSuccess)
                 return IX_ERR_CUDA;
             ready[dev] = 1;
         }
@@ -870,7 +1039,7 @@ int launch(const CUtensorMap& tmK, const CUtensorMap& tmQ,
     const int sms = num_sms();
     if (sms <= 0) return IX_ERR_CUDA;
     if (a.num_groups > 0) {
-        logits_kernel<P, NN><<<sms, kThreads, Smem<P>::kAlloc, stream>>>(tmK, tmQ, a);
+        logits_kernel<P, NN, TK><<<sms, kThreads, Smem<P, TK>::kAlloc, stream>>>(tmK, tmQ, a);
         if (launch_status() != IX_OK) return IX_ERR_CUDA;
     }
     if (clean && rows > 0) {
@@ -886,29 +1055,40 @@ int launch(const CUtensorMap& tmK, const CUtensorMap& tmQ,
 
 using namespace dsix;
 
-extern "C" int ix_paged_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t* cache,
-                                   int64_t num_blocks, int block_size,
-                                   const int32_t* context_lens, const int32_t* block_table,
-                                   int64_t bt_stride, int batch, int next_n, int heads,
-                                   int head_dim, float* logits, int64_t ld, int clean_logits,
-                                   ix_stream_t stream) {
+namespace dsix {
+namespace {
+
+// Host checks of ix_paged_mqa_logits and its fused forms (no CUDA call).
+int paged_check(const uint8_t* q_fp8, const float* w, const uint8_t* cache, int64_t num_blocks, int block_size,
+                const int32_t* context_lens, const int32_t* block_table, int64_t bt_stride, int batch, int next_n,
+                int heads, int head_dim, float* logits, int64_t ld, bool* empty) {
+    *empty = false;
     if (batch < 0 || num_blocks < 0 || ld < 0 || bt_stride < 0) return IX_ERR_SHAPE;
     if (heads != kHeads || head_dim != kDim || block_size != kBlk || next_n < 1 || next_n > 2)
         return IX_ERR_UNSUPPORTED;
-    if (batch == 0 || ld == 0) return IX_OK;
+    if (batch == 0 || ld == 0) {
+        *empty = true;
+        return IX_OK;
+    }
     if (ld % 4 != 0 || ld > (1ll << 30)) return IX_ERR_UNSUPPORTED;
     if (num_blocks < 1 || bt_stride < 1) return IX_ERR_SHAPE;
     if (!q_fp8 || !w || !cache || !context_lens || !block_table || !logits) return IX_ERR_NULL;
     if (!aligned16(q_fp8) || !aligned16(w) || !aligned16(cache) || !aligned16(logits))
         return IX_ERR_ALIGN;
+    return IX_OK;
+}
+
+// Set-up after paged_check: tensor maps and kernel arguments.
+int paged_prepare(const uint8_t* q_fp8, const float* w, const uint8_t* cache, int64_t num_blocks,
+                  const int32_t* context_lens, const int32_t* block_table, int64_t bt_stride, int batch, int next_n,
+                  float* logits, int64_t ld, CUtensorMap* tmK, CUtensorMap* tmQ, LogitsArgs* a) {
     int* st = status_ptr();
     if (!st) return IX_ERR_CUDA;
-    CUtensorMap tmK, tmQ;
     {
         const uint64_t dims[3] = {kDim, kBlk, static_cast<uint64_t>(num_blocks)};
         const uint64_t strides[2] = {kDim, kBlk * (kDim + 4)};
         const uint32_t box[3] = {kDim, kBlk, 1};
-        if (!make_map(&tmK, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, cache, dims, strides, box,
+        if (!make_map(tmK, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, cache, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_128B))
             return IX_ERR_CUDA;
     }
@@ -916,22 +1096,114 @@ extern "C" int ix_paged_mqa_logits(const uint8_t* q_fp8, const float* w, const u
         const uint64_t dims[2] = {kDim, static_cast<uint64_t>(batch) * next_n * kHeads};
         const uint64_t strides[1] = {kDim};
         const uint32_t box[2] = {kDim, static_cast<uint32_t>(next_n * kHeads)};
-        if (!make_map(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q_fp8, dims, strides, box,
+        if (!make_map(tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q_fp8, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_128B))
             return IX_ERR_CUDA;
     }
-    LogitsArgs a{};
-    a.w = w;
-    a.logits = logits;
-    a.ld = ld;
-    a.num_groups = batch;
-    a.status = st;
-    a.context_lens = context_lens;
-    a.bt = block_table;
-    a.bt_stride = bt_stride;
-    a.next_n = next_n;
-    a.num_blocks = num_blocks;
-    a.cache = cache;
+    *a = LogitsArgs{};
+    a->w = w;
+    a->logits = logits;
+    a->ld = ld;
+    a->num_groups = batch;
+    a->status = st;
+    a->context_lens = context_lens;
+    a->bt = block_table;
+    a->bt_stride = bt_stride;
+    a->next_n = next_n;
+    a->num_blocks = num_blocks;
+    a->cache = cache;
+    return IX_OK;
+}
+
+// Host checks of ix_mqa_logits and its fused forms (no CUDA call).
+int contiguous_check(const uint8_t* q_fp8, const float* w, const uint8_t* k_fp8, const float* k_scale,
+                     const int32_t* ks, const int32_t* ke, int64_t tq, int64_t tk, int heads, int head_dim,
+                     float* logits, int64_t ld, bool* empty) {
+    *empty = false;
+    if (tq < 0 || tk < 0 || ld < 0) return IX_ERR_SHAPE;
+    if (heads != kHeads || head_dim != kDim) return IX_ERR_UNSUPPORTED;
+    if (tq == 0 || ld == 0) {
+        *empty = true;
+        return IX_OK;
+    }
+    if (ld % 4 != 0 || ld > (1ll << 30) || tk >= (1ll << 31) || tq * kHeads >= (1ll << 31))
+        return IX_ERR_UNSUPPORTED;
+    if (!q_fp8 || !w || !ks || !ke || !logits) return IX_ERR_NULL;
+    if (tk > 0 && (!k_fp8 || !k_scale)) return IX_ERR_NULL;
+    if (!aligned16(q_fp8) || !aligned16(w) || !aligned16(logits) ||
+        (tk > 0 && (!aligned16(k_fp8) || !aligned16(k_scale))))
+        return IX_ERR_ALIGN;
+    return IX_OK;
+}
+
+// Set-up after contiguous_check: tensor maps and kernel arguments.
+int contiguous_prepare(const uint8_t* q_fp8, const float* w, const uint8_t* k_fp8, const float* k_scale,
+                       const int32_t* ks, const int32_t* ke, int64_t tq, int64_t tk, float* logits, int64_t ld,
+                       CUtensorMap* tmK, CUtensorMap* tmQ, LogitsArgs* a) {
+    int* st = status_ptr();
+    if (!st) return IX_ERR_CUDA;
+    *a = LogitsArgs{};
+    a->w = w;
+    a->logits = logits;
+    a->ld = ld;
+    a->num_groups = tk > 0 ? static_cast<int>((tq + Cfg<false>::kRows - 1) / Cfg<false>::kRows) : 0;
+    a->status = st;
+    a->k_scale = k_scale;
+    a->ks = ks;
+    a->ke = ke;
+    a->tq = tq;
+    a->tk = tk;
+    *tmK = CUtensorMap{};
+    *tmQ = CUtensorMap{};
+    if (tk > 0) {
+        {
+            const uint64_t dims[2] = {kDim, static_cast<uint64_t>(tk)};
+            const uint64_t strides[1] = {kDim};
+            const uint32_t box[2] = {kDim, kTile};
+            if (!make_map(tmK, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k_fp8, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+                return IX_ERR_CUDA;
+        }
+        {
+            const uint64_t dims[2] = {kDim, static_cast<uint64_t>(tq) * kHeads};
+            const uint64_t strides[1] = {kDim};
+            const uint32_t box[2] = {kDim, 256};
+            if (!make_map(tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q_fp8, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+                return IX_ERR_CUDA;
+        }
+    }
+    return IX_OK;
+}
+
+// Checks of the histogram arguments (k, workspace) of the *_hist and fused entry points.
+int hist_checks(int64_t ld, int k, void* workspace, size_t workspace_bytes, int64_t rows) {
+    if (k < 1 || ld > kTopkMaxLd) return IX_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < static_cast<size_t>(rows) * kHistRowWords * 4) return IX_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return IX_ERR_ALIGN;
+    return IX_OK;
+}
+
+}  // namespace
+}  // namespace dsix
+
+using namespace dsix;
+
+extern "C" int ix_paged_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t* cache,
+                                   int64_t num_blocks, int block_size,
+                                   const int32_t* context_lens, const int32_t* block_table,
+                                   int64_t bt_stride, int batch, int next_n, int heads,
+                                   int head_dim, float* logits, int64_t ld, int clean_logits,
+                                   ix_stream_t stream) {
+    CUtensorMap tmK, tmQ;
+    LogitsArgs a;
+    bool empty = false;
+    int chk = paged_check(q_fp8, w, cache, num_blocks, block_size, context_lens, block_table, bt_stride, batch,
+                          next_n, heads, head_dim, logits, ld, &empty);
+    if (chk != IX_OK || empty) return chk;
+    chk = paged_prepare(q_fp8, w, cache, num_blocks, context_lens, block_table, bt_stride, batch, next_n, logits,
+                        ld, &tmK, &tmQ, &a);
+    if (chk != IX_OK) return chk;
     const int64_t rows = static_cast<int64_t>(batch) * next_n;
     cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
     return next_n == 1 ? launch<true, 1>(tmK, tmQ, a, rows, clean_logits, st_)
@@ -942,48 +1214,141 @@ extern "C" int ix_mqa_logits(const uint8_t* q_fp8, const float* w, const uint8_t
                              const float* k_scale, const int32_t* ks, const int32_t* ke, int64_t tq,
                              int64_t tk, int heads, int head_dim, float* logits, int64_t ld,
                              int clean_logits, ix_stream_t stream) {
-    if (tq < 0 || tk < 0 || ld < 0) return IX_ERR_SHAPE;
-    if (heads != kHeads || head_dim != kDim) return IX_ERR_UNSUPPORTED;
-    if (tq == 0 || ld == 0) return IX_OK;
-    if (ld % 4 != 0 || ld > (1ll << 30) || tk >= (1ll << 31) || tq * kHeads >= (1ll << 31))
-        return IX_ERR_UNSUPPORTED;
-    if (!q_fp8 || !w || !ks || !ke || !logits) return IX_ERR_NULL;
-    if (tk > 0 && (!k_fp8 || !k_scale)) return IX_ERR_NULL;
-    if (!aligned16(q_fp8) || !aligned16(w) || !aligned16(logits) ||
-        (tk > 0 && (!aligned16(k_fp8) || !aligned16(k_scale))))
-        return IX_ERR_ALIGN;
-    int* st = status_ptr();
-    if (!st) return IX_ERR_CUDA;
-    LogitsArgs a{};
-    a.w = w;
-    a.logits = logits;
-    a.ld = ld;
-    a.num_groups = tk > 0 ? static_cast<int>((tq + Cfg<false>::kRows - 1) / Cfg<false>::kRows) : 0;
-    a.status = st;
-    a.k_scale = k_scale;
-    a.ks = ks;
-    a.ke = ke;
-    a.tq = tq;
-    a.tk = tk;
-    CUtensorMap tmK{}, tmQ{};
-    if (tk > 0) {
-        {
-            const uint64_t dims[2] = {kDim, static_cast<uint64_t>(tk)};
-            const uint64_t strides[1] = {kDim};
-            const uint32_t box[2] = {kDim, kTile};
-            if (!make_map(&tmK, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k_fp8, dims, strides, box,
-                          CU_TENSOR_MAP_SWIZZLE_128B))
-                return IX_ERR_CUDA;
-        }
-        {
-            const uint64_t dims[2] = {kDim, static_cast<uint64_t>(tq) * kHeads};
-            const uint64_t strides[1] = {kDim};
-            const uint32_t box[2] = {kDim, 256};
-            if (!make_map(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q_fp8, dims, strides, box,
-                          CU_TENSOR_MAP_SWIZZLE_128B))
-                return IX_ERR_CUDA;
-        }
-    }
-    return launch<false, 1>(tmK, tmQ, a, tq, clean_logits,
-                            reinterpret_cast<cudaStream_t>(stream));
+    CUtensorMap tmK, tmQ;
+    LogitsArgs a;
+    bool empty = false;
+    int chk = contiguous_check(q_fp8, w, k_fp8, k_scale, ks, ke, tq, tk, heads, head_dim, logits, ld, &empty);
+    if (chk != IX_OK || empty) return chk;
+    chk = contiguous_prepare(q_fp8, w, k_fp8, k_scale, ks, ke, tq, tk, logits, ld, &tmK, &tmQ, &a);
+    if (chk != IX_OK) return chk;
+    return launch<false, 1>(tmK, tmQ, a, tq, clean_logits, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t ix_topk_hist_workspace_size(int64_t rows) {
+    return rows > 0 ? static_cast<size_t>(rows) * kHistRowWords * sizeof(uint32_t) : 0;
+}
+
+extern "C" int ix_paged_mqa_logits_hist(const uint8_t* q_fp8, const float* w, const uint8_t* cache,
+                                        int64_t num_blocks, int block_size, const int32_t* context_lens,
+                                        const int32_t* block_table, int64_t bt_stride, int batch, int next_n,
+                                        int heads, int head_dim, float* logits, int64_t ld, int k,
+                                        void* workspace, size_t workspace_bytes, ix_stream_t stream) {
+    CUtensorMap tmK, tmQ;
+    LogitsArgs a;
+    bool empty = false;
+    int chk = paged_check(q_fp8, w, cache, num_blocks, block_size, context_lens, block_table, bt_stride, batch,
+                          next_n, heads, head_dim, logits, ld, &empty);
+    if (chk != IX_OK || empty) return chk;
+    const int64_t rows = static_cast<int64_t>(batch) * next_n;
+    chk = hist_checks(ld, k, workspace, workspace_bytes, rows);
+    if (chk != IX_OK) return chk;
+    chk = paged_prepare(q_fp8, w, cache, num_blocks, context_lens, block_table, bt_stride, batch, next_n, logits,
+                        ld, &tmK, &tmQ, &a);
+    if (chk != IX_OK) return chk;
+    a.hist = static_cast<uint32_t*>(workspace);
+    a.k = k;
+    cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+    return next_n == 1 ? launch<true, 1, true>(tmK, tmQ, a, rows, 0, st_) : launch<true, 2, true>(tmK, tmQ, a, rows, 0, st_);
+}
+
+extern "C" int ix_mqa_logits_hist(const uint8_t* q_fp8, const float* w, const uint8_t* k_fp8,
+                                  const float* k_scale, const int32_t* ks, const int32_t* ke, int64_t tq,
+                                  int64_t tk, int heads, int head_dim, float* logits, int64_t ld, int k,
+                                  void* workspace, size_t workspace_bytes, ix_stream_t stream) {
+    CUtensorMap tmK, tmQ;
+    LogitsArgs a;
+    bool empty = false;
+    int chk = contiguous_check(q_fp8, w, k_fp8, k_scale, ks, ke, tq, tk, heads, head_dim, logits, ld, &empty);
+    if (chk != IX_OK || empty) return chk;
+    chk = hist_checks(ld, k, workspace, workspace_bytes, tq);
+    if (chk != IX_OK) return chk;
+    chk = contiguous_prepare(q_fp8, w, k_fp8, k_scale, ks, ke, tq, tk, logits, ld, &tmK, &tmQ, &a);
+    if (chk != IX_OK) return chk;
+    a.hist = static_cast<uint32_t*>(workspace);
+    a.k = k;
+    return launch<false, 1, true>(tmK, tmQ, a, tq, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int ix_paged_mqa_logits_topk(const uint8_t* q_fp8, const float* w, const uint8_t* cache,
+                                        int64_t num_blocks, int block_size, const int32_t* context_lens,
+                                        const int32_t* block_table, int64_t bt_stride, int batch, int next_n,
+                                        int heads, int head_dim, float* logits, int64_t ld, int k,
+                                        int32_t* out_local, int32_t* out_global, void* workspace,
+                                        size_t workspace_bytes, ix_stream_t stream) {
+    // every argument is checked before the first launch
+    CUtensorMap tmK, tmQ;
+    LogitsArgs a;
+    bool empty = false;
+    int chk = paged_check(q_fp8, w, cache, num_blocks, block_size, context_lens, block_table, bt_stride, batch,
+                          next_n, heads, head_dim, logits, ld, &empty);
+    if (chk != IX_OK || empty) return chk;
+    const int64_t rows = static_cast<int64_t>(batch) * next_n;
+    chk = hist_checks(ld, k, workspace, workspace_bytes, rows);
+    if (chk != IX_OK) return chk;
+    if (!out_global) return IX_ERR_NULL;
+    chk = paged_prepare(q_fp8, w, cache, num_blocks, context_lens, block_table, bt_stride, batch, next_n, logits,
+                        ld, &tmK, &tmQ, &a);
+    if (chk != IX_OK) return chk;
+    a.hist = static_cast<uint32_t*>(workspace);
+    a.k = k;
+    cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+    chk = next_n == 1 ? launch<true, 1, true>(tmK, tmQ, a, rows, 0, st_) : launch<true, 2, true>(tmK, tmQ, a, rows, 0, st_);
+    if (chk != IX_OK) return chk;
+    SelectRows q{};
+    q.logits = logits;
+    q.ld = ld;
+    q.rows = rows;
+    q.context_lens = context_lens;
+    q.next_n = next_n;
+    q.block_table = block_table;
+    q.bt_stride = bt_stride;
+    q.block_size = block_size;
+    q.k = k;
+    q.out_local = out_local;
+    q.out_global = out_global;
+    q.hist = a.hist;
+    q.status = a.status;
+    return select_after_logits(q, st_);
+}
+
+extern "C" int ix_mqa_logits_topk(const uint8_t* q_fp8, const float* w, const uint8_t* k_fp8,
+                                  const float* k_scale, const int32_t* ks, const int32_t* ke, int64_t tq,
+                                  int64_t tk, int heads, int head_dim, float* logits, int64_t ld,
+                                  const int32_t* row_req, const int32_t* block_table, int64_t bt_stride,
+                                  int block_size, int k, int32_t* out_local, int32_t* out_global,
+                                  void* workspace, size_t workspace_bytes, ix_stream_t stream) {
+    CUtensorMap tmK, tmQ;
+    LogitsArgs a;
+    bool empty = false;
+    int chk = contiguous_check(q_fp8, w, k_fp8, k_scale, ks, ke, tq, tk, heads, head_dim, logits, ld, &empty);
+    if (chk != IX_OK || empty) return chk;
+    chk = hist_checks(ld, k, workspace, workspace_bytes, tq);
+    if (chk != IX_OK) return chk;
+    if (bt_stride < 0) return IX_ERR_SHAPE;
+    if (block_size < 1) return IX_ERR_UNSUPPORTED;
+    if (!row_req || !block_table || !out_global) return IX_ERR_NULL;
+    chk = contiguous_prepare(q_fp8, w, k_fp8, k_scale, ks, ke, tq, tk, logits, ld, &tmK, &tmQ, &a);
+    if (chk != IX_OK) return chk;
+    a.hist = static_cast<uint32_t*>(workspace);
+    a.k = k;
+    cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+    chk = launch<false, 1, true>(tmK, tmQ, a, tq, 0, st_);
+    if (chk != IX_OK) return chk;
+    SelectRows q{};
+    q.logits = logits;
+    q.ld = ld;
+    q.rows = tq;
+    q.ks = ks;
+    q.ke = ke;
+    q.tk = tk;
+    q.row_req = row_req;
+    q.block_table = block_table;
+    q.bt_stride = bt_stride;
+    q.block_size = block_size;
+    q.k = k;
+    q.out_local = out_local;
+    q.out_global = out_global;
+    q.hist = a.hist;
+    q.status = a.status;
+    return select_after_logits(q, st_);
 }

@@ -40,13 +40,27 @@ constexpr int kMaxPer = 64;
 constexpr int kSliceCap = kThreads * kMaxPer;  // keys per CTA
 constexpr int kBins = 2048;
 constexpr int kStage = 4096;  // selected indices staged in shared memory before the write-out
+static_assert(kTopkMaxLd == static_cast<int64_t>(kMaxCluster) * kSliceCap, "longest row of the cluster kernel");
 
 struct TopkArgs {
     const float* logits;
     int64_t ld;
     int64_t rows;
+    // row geometry: kRowsGiven (row_len / row_req arrays), kRowsDecode (the
+    // paged logits' rows: context_lens, next_n) or kRowsPrefill (ks / ke, tk;
+    // row_req), each clamped exactly as the logits kernels clamp them
+    int geom;
     const int32_t* row_len;
     const int32_t* row_req;
+    const int32_t* context_lens;
+    int next_n;
+    const int32_t* ks;
+    const int32_t* ke;
+    int64_t tk;
+    // fused path: the rows' first-digit histograms written by the logits kernel
+    // (read and cleared here); nullptr otherwise
+    uint32_t* hist;
+    int* status;
     const int32_t* bt;
     int64_t bt_stride;
     int block_size;
@@ -57,11 +71,83 @@ struct TopkArgs {
     int slice;  // keys per CTA (multiple of 4, <= kThreads * PER)
 };
 
-__device__ __forceinline__ uint32_t order_key(float f) {
-    // f + 0 turns -0.0 into +0.0 (round to nearest) and leaves every other
-    // value alone; then negative floats flip all bits, others only the sign bit
-    const uint32_t b = __float_as_uint(__fadd_rn(f, 0.0f));
-    return b ^ (static_cast<uint32_t>(static_cast<int32_t>(b) >> 31) | 0x80000000u);
+enum { kRowsGiven = 0, kRowsDecode = 1, kRowsPrefill = 2 };
+
+// Visible length L (clamped to [0, ld]) and request b of row r.
+__device__ __forceinline__ void row_geom(const TopkArgs& a, int64_t r, int64_t& L, int& b) {
+    if (a.geom == kRowsDecode) {
+        b = static_cast<int>(r / a.next_n);
+        L = static_cast<int64_t>(__ldg(a.context_lens + b)) - a.next_n + 1 + r % a.next_n;
+    } else if (a.geom == kRowsPrefill) {
+        b = __ldg(a.row_req + r);
+        int64_t x0 = __ldg(a.ks + r), x1 = __ldg(a.ke + r);
+        if (x0 < 0 || x1 > a.tk || x1 < x0) {
+            x0 = x0 < 0 ? 0 : x0;
+            x1 = x1 > a.tk ? a.tk : x1;
+            if (x1 < x0) x1 = x0;
+        }
+        L = x1 - x0;
+    } else {
+        b = __ldg(a.row_req + r);
+        L = __ldg(a.row_len + r);
+    }
+    L = L < 0 ? 0 : (L > a.ld ? a.ld : L);
+}
+
+__device__ __forceinline__ int warp_incl_scan(int x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
+
+// One warp reads the first-digit histogram H of a row with more than k keys
+// (64 coarse bins, then 2048 fine bins) and finds the digit d that holds the
+// k-th largest key: res = {d, keys in digits above d, keys in d}.  It then
+// clears every bin it may have counted (each non-zero coarse bin and its 32
+// fine bins), so the workspace is all zero again.  Every lane returns res.
+// Returns false when the histogram does not hold exactly the row's L keys (a
+// workspace that was not zero before use).
+__device__ __forceinline__ bool hist_pick(uint32_t* H, int k, int64_t L, int (&res)[3]) {
+    const int lane = threadIdx.x & 31;
+    // lane l: coarse bins 63 - 2l (hi) and 62 - 2l (lo); lane 0 holds the top
+    const uint2 cc = *reinterpret_cast<const uint2*>(H + 62 - 2 * lane);
+    const int c_hi = static_cast<int>(cc.y), c_lo = static_cast<int>(cc.x);
+    const int sum = c_hi + c_lo;
+    const int incl = warp_incl_scan(sum);
+    const bool consistent = __shfl_sync(0xffffffffu, incl, 31) == L;
+    const unsigned hit = __ballot_sync(0xffffffffu, incl >= k);
+    const int f = hit ? __ffs(hit) - 1 : 31;
+    const int excl_f = __shfl_sync(0xffffffffu, incl - sum, f);
+    const int chi_f = __shfl_sync(0xffffffffu, c_hi, f);
+    const bool in_hi = excl_f + chi_f >= k;
+    const int cb = in_hi ? 63 - 2 * f : 62 - 2 * f;
+    const int above = in_hi ? excl_f : excl_f + chi_f;
+    // the coarse bin's 32 fine bins, lane 0 the highest
+    const int fv = static_cast<int>(H[kHistCoarse + cb * 32 + 31 - lane]);
+    const int incl2 = warp_incl_scan(fv) + above;
+    const unsigned hit2 = __ballot_sync(0xffffffffu, incl2 >= k);
+    const int f2 = hit2 ? __ffs(hit2) - 1 : 31;
+    res[0] = cb * 32 + 31 - f2;
+    res[2] = __shfl_sync(0xffffffffu, fv, f2);
+    res[1] = __shfl_sync(0xffffffffu, incl2, f2) - res[2];
+    __syncwarp();
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    if (c_hi) {
+        uint4* fb = reinterpret_cast<uint4*>(H + kHistCoarse + (63 - 2 * lane) * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) fb[i] = z;
+    }
+    if (c_lo) {
+        uint4* fb = reinterpret_cast<uint4*>(H + kHistCoarse + (62 - 2 * lane) * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) fb[i] = z;
+    }
+    if (sum) *reinterpret_cast<uint2*>(H + 62 - 2 * lane) = make_uint2(0u, 0u);
+    return consistent;
 }
 
 __device__ __forceinline__ void emit(const TopkArgs& a, int64_t r, int b, int pos, int s) {
@@ -149,7 +235,9 @@ __device__ __forceinline__ void block_pick(int* h, int nb, int k_rem, int* out, 
 }
 
 // Short slices keep several CTAs per SM resident to hide the per-row phase latency.
-template <int PER>
+// HIST: the rows' first-digit histograms come from the logits kernel, so the
+// key min / max and the first histogram pass over all keys are skipped.
+template <int PER, bool HIST>
 __global__ void __launch_bounds__(kThreads, PER <= 4 ? 3 : (PER <= 32 ? 2 : 1))
     topk_kernel(const TopkArgs a) {
     cg::cluster_group cluster = cg::this_cluster();
@@ -178,9 +266,9 @@ __global__ void __launch_bounds__(kThreads, PER <= 4 ? 3 : (PER <= 32 ? 2 : 1))
     const int64_t cid = blockIdx.x / C;
     const int64_t nclusters = gridDim.x / C;
     for (int64_t r = cid; r < a.rows; r += nclusters) {
-        int64_t L = __ldg(a.row_len + r);
-        L = L < 0 ? 0 : (L > a.ld ? a.ld : L);
-        const int b = __ldg(a.row_req + r);
+        int64_t L;
+        int b;
+        row_geom(a, r, L, b);
         if (L <= a.k) {
             for (int i = rank * kThreads + tid; i < a.k; i += C * kThreads)
                 emit(a, r, b, i, i < L ? i : -1);
@@ -216,48 +304,70 @@ __global__ void __launch_bounds__(kThreads, PER <= 4 ? 3 : (PER <= 32 ? 2 : 1))
                 }
             }
         }
-        // Bits every key of the row shares need no histogram (a row of logits
-        // often spans one or two binades): the digits start below them.  Key
-        // min / max over the row: warps, then CTAs through rank 0.
-        kmin = __reduce_min_sync(0xffffffffu, kmin);
-        kmax = __reduce_max_sync(0xffffffffu, kmax);
-        if ((tid & 31) == 0) {
-            mmx[2 * warp] = kmin;
-            mmx[2 * warp + 1] = kmax;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            for (int i = 1; i < kThreads / 32; ++i) {
-                kmin = min(kmin, mmx[2 * i]);
-                kmax = max(kmax, mmx[2 * i + 1]);
+        int shift, k_rem;
+        uint32_t prefix;
+        bool done;
+        if constexpr (HIST) {
+            // the threshold digit from the row's histogram: one warp of rank 0
+            // reads (and clears) it and hands the result to every CTA
+            if (rank == 0 && warp == 0) {
+                int hr[3];
+                if (!hist_pick(a.hist + r * kHistRowWords, a.k, L, hr) && tid == 0) flag(a.status, IX_DEV_BAD_HIST);
+                if ((tid & 31) < 3)
+                    for (int j = 0; j < C; ++j) cluster.map_shared_rank(res, j)[tid & 31] = hr[tid & 31];
             }
-            cmm0[2 * rank] = kmin;
-            cmm0[2 * rank + 1] = kmax;
-        }
-        if (C > 1)
-            cluster.sync();
-        else
+            if (C > 1)
+                cluster.sync();
+            else
+                __syncthreads();
+            shift = kDigitShift;
+            prefix = static_cast<uint32_t>(res[0]);
+            k_rem = a.k - res[1];
+            done = res[2] == k_rem;
+        } else {
+            // Bits every key of the row shares need no histogram (a row of logits
+            // often spans one or two binades): the digits start below them.  Key
+            // min / max over the row: warps, then CTAs through rank 0.
+            kmin = __reduce_min_sync(0xffffffffu, kmin);
+            kmax = __reduce_max_sync(0xffffffffu, kmax);
+            if ((tid & 31) == 0) {
+                mmx[2 * warp] = kmin;
+                mmx[2 * warp + 1] = kmax;
+            }
             __syncthreads();
-        kmin = cmm0[0];
-        kmax = cmm0[1];
-#pragma unroll
-        for (int i = 1; i < kMaxCluster; ++i) {  // unrolled: the remote loads go out together
-            if (i < C) {
-                kmin = min(kmin, cmm0[2 * i]);
-                kmax = max(kmax, cmm0[2 * i + 1]);
+            if (tid == 0) {
+                for (int i = 1; i < kThreads / 32; ++i) {
+                    kmin = min(kmin, mmx[2 * i]);
+                    kmax = max(kmax, mmx[2 * i + 1]);
+                }
+                cmm0[2 * rank] = kmin;
+                cmm0[2 * rank + 1] = kmax;
             }
+            if (C > 1)
+                cluster.sync();
+            else
+                __syncthreads();
+            kmin = cmm0[0];
+            kmax = cmm0[1];
+#pragma unroll
+            for (int i = 1; i < kMaxCluster; ++i) {  // unrolled: the remote loads go out together
+                if (i < C) {
+                    kmin = min(kmin, cmm0[2 * i]);
+                    kmax = max(kmax, cmm0[2 * i + 1]);
+                }
+            }
+            shift = 32 - __clz(kmin ^ kmax);  // bits below the common prefix; 0 when all keys are equal
+            prefix = shift >= 32 ? 0u : (kmin >> shift);
+            k_rem = a.k;
+            done = shift == 0;
         }
-        int shift = 32 - __clz(kmin ^ kmax);  // bits below the common prefix; 0 when all keys are equal
-        uint32_t prefix = shift >= 32 ? 0u : (kmin >> shift);
-        int k_rem = a.k;
-        bool done = shift == 0;
         for (int p = 0; !done; ++p) {
             const int nbits = shift < 11 ? shift : 11;
             const int nb = 1 << nbits;
             const int sh = shift - nbits;
 #pragma unroll
             for (int j = 0; j < PER; ++j) {
-                if (j < nv && (p == 0 || (key[j] >> shift) == prefix))
+                if (j < nv && ((!HIST && p == 0) || (key[j] >> shift) == prefix))
                     atomicAdd(hist + ((key[j] >> sh) & (nb - 1)), 1);
             }
             if (C > 1) {
@@ -669,7 +779,208 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
     }
 }
 
-template <int PER>
+// ---------------------------------------------------------------------------
+// Fused path, many rows: one WARP per row, finishing the selection that the
+// logits kernel started with the row's first-digit histogram.  No block
+// barriers, up to 48 rows in flight per SM.
+//   1. hist_pick: the digit d that holds the k-th largest key, the keys above
+//      it (all selected) and the count c of keys in it.
+//   2. If not all c keys of d are taken: the keys of digit d (read from the
+//      logits row once, in index order) go to shared memory when c <= kSelCap,
+//      and 7-bit radix levels over them settle the remaining 21 bits; past
+//      kSelCap the levels re-read the row instead.  The result is a prefix of
+//      the key (of `sh` bits below the top) above which everything is taken,
+//      and `take`: how many keys equal to the prefix are taken, the lowest
+//      indices first.
+//   3. One pass over the row emits the selection in ascending index order
+//      with the remap (ballot/popc positions, stores in order).
+// ---------------------------------------------------------------------------
+constexpr int kSelWarps = 8;
+constexpr int kSelCap = 512;
+constexpr int kSelBits = 7;
+
+// Warp-wide pick over `nb` (<= 128) bins h[] from the top: lane l owns bins
+// nb-1-4l .. nb-4-4l.  Returns the bin holding the take-th key, the keys above
+// it and the keys in it (every lane).
+__device__ __forceinline__ void warp_pick(const uint32_t* h, int nb, int take, int& d, int& above, int& cnt) {
+    const int lane = threadIdx.x & 31;
+    int c[4], sum = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int bin = nb - 1 - 4 * lane - q;
+        c[q] = bin >= 0 ? static_cast<int>(h[bin]) : 0;
+        sum += c[q];
+    }
+    const int incl = warp_incl_scan(sum);
+    const unsigned hit = __ballot_sync(0xffffffffu, incl >= take);
+    const int f = hit ? __ffs(hit) - 1 : 31;
+    int dd = 0, ab = 0, cn = 0;
+    if (lane == f) {
+        int acc = incl - sum;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (acc + c[q] >= take || q == 3) {
+                dd = nb - 1 - 4 * lane - q;
+                ab = acc;
+                cn = c[q];
+                break;
+            }
+            acc += c[q];
+        }
+    }
+    d = __shfl_sync(0xffffffffu, dd, f);
+    above = __shfl_sync(0xffffffffu, ab, f);
+    cnt = __shfl_sync(0xffffffffu, cn, f);
+}
+
+// Keys of the 128-key chunk starting at c0 held by this lane (keys c0 + 4 lane
+// .. + 3); valid bits for keys below L.
+__device__ __forceinline__ unsigned chunk_keys(const float* row, int c0, int L, uint32_t (&key)[4]) {
+    const int i0 = c0 + 4 * (threadIdx.x & 31);
+    unsigned valid = 0;
+    if (i0 < L) {  // i0 + 3 < ld: ld is a multiple of 4 and L <= ld
+        const float4 v = __ldg(reinterpret_cast<const float4*>(row + i0));
+        key[0] = order_key(v.x);
+        key[1] = order_key(v.y);
+        key[2] = order_key(v.z);
+        key[3] = order_key(v.w);
+        const int n = L - i0;
+        valid = n >= 4 ? 0xFu : ((1u << n) - 1u);
+    } else {
+        key[0] = key[1] = key[2] = key[3] = 0u;
+    }
+    return valid;
+}
+
+__device__ __forceinline__ int warp_excl_scan(int x, int& total) {
+    const int incl = warp_incl_scan(x);
+    total = __shfl_sync(0xffffffffu, incl, 31);
+    return incl - x;
+}
+
+__global__ void __launch_bounds__(kSelWarps * 32) select_warp_kernel(const TopkArgs a) {
+    __shared__ uint32_t s_key[kSelWarps][kSelCap];
+    __shared__ int32_t s_idx[kSelWarps][kSelCap];
+    __shared__ uint32_t s_h[kSelWarps][1 << kSelBits];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t* ck = s_key[warp];
+    int32_t* ci = s_idx[warp];
+    uint32_t* wh = s_h[warp];
+    const int64_t nw = static_cast<int64_t>(gridDim.x) * kSelWarps;
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * kSelWarps + warp; r < a.rows; r += nw) {
+        int64_t L64;
+        int b;
+        row_geom(a, r, L64, b);
+        const int L = static_cast<int>(L64);
+        if (L <= a.k) {
+            for (int i = lane; i < a.k; i += 32) emit(a, r, b, i, i < L ? i : -1);
+            continue;
+        }
+        int hr[3];
+        if (!hist_pick(a.hist + r * kHistRowWords, a.k, L, hr) && lane == 0) flag(a.status, IX_DEV_BAD_HIST);
+        uint32_t prefix = static_cast<uint32_t>(hr[0]);
+        int take = a.k - hr[1], cnt = hr[2], sh = kDigitShift;
+        const float* row = a.logits + r * a.ld;
+        if (cnt != take) {
+            const bool in_smem = cnt <= kSelCap;
+            int ncand = 0;
+            if (in_smem) {  // the keys of the threshold digit, in index order
+                for (int c0 = 0; c0 < L; c0 += 128) {
+                    uint32_t key[4];
+                    const unsigned valid = chunk_keys(row, c0, L, key);
+                    unsigned eq = 0;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) eq |= (((valid >> j) & 1u) && (key[j] >> sh) == prefix) ? (1u << j) : 0u;
+                    int tot;
+                    int pos = ncand + warp_excl_scan(__popc(eq), tot);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if ((eq >> j) & 1u) {
+                            if (pos < kSelCap) {
+                                ck[pos] = key[j];
+                                ci[pos] = c0 + 4 * lane + j;
+                            }
+                            ++pos;
+                        }
+                    }
+                    ncand += tot;
+                }
+                ncand = min(ncand, kSelCap);
+                __syncwarp();
+            }
+            while (cnt != take && sh > 0) {
+                const int nb = sh < kSelBits ? sh : kSelBits, nsh = sh - nb;
+                const uint32_t m = (1u << nb) - 1u;
+                for (int i = lane; i < (1 << kSelBits); i += 32) wh[i] = 0u;
+                __syncwarp();
+                if (in_smem) {
+                    for (int i = lane; i < ncand; i += 32) {
+                        const uint32_t key = ck[i];
+                        if ((key >> sh) == prefix) atomicAdd(wh + ((key >> nsh) & m), 1u);
+                    }
+                } else {
+                    for (int c0 = 0; c0 < L; c0 += 128) {
+                        uint32_t key[4];
+                        const unsigned valid = chunk_keys(row, c0, L, key);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (((valid >> j) & 1u) && (key[j] >> sh) == prefix) atomicAdd(wh + ((key[j] >> nsh) & m), 1u);
+                    }
+                }
+                __syncwarp();
+                int d, above, c;
+                warp_pick(wh, 1 << nb, take, d, above, c);
+                prefix = (prefix << nb) | static_cast<uint32_t>(d);
+                take -= above;
+                cnt = c;
+                sh = nsh;
+                __syncwarp();
+            }
+        }
+        // emit: keys above the prefix, and the first `take` keys equal to it
+        int pos0 = 0, eq0 = 0;
+        for (int c0 = 0; c0 < L; c0 += 128) {
+            uint32_t key[4];
+            const unsigned valid = chunk_keys(row, c0, L, key);
+            unsigned gt = 0, eq = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if ((valid >> j) & 1u) {
+                    const uint32_t v = key[j] >> sh;
+                    gt |= v > prefix ? (1u << j) : 0u;
+                    eq |= v == prefix ? (1u << j) : 0u;
+                }
+            }
+            int eq_tot;
+            int er = eq0 + warp_excl_scan(__popc(eq), eq_tot);
+            unsigned sel = gt;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if ((eq >> j) & 1u) {
+                    if (er < take) sel |= 1u << j;
+                    ++er;
+                }
+            }
+            int s_tot;
+            int pos = pos0 + warp_excl_scan(__popc(sel), s_tot);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if ((sel >> j) & 1u) {
+                    if (pos < a.k) emit(a, r, b, pos, c0 + 4 * lane + j);
+                    ++pos;
+                }
+            }
+            pos0 += s_tot;
+            eq0 += eq_tot;
+        }
+        if (pos0 != a.k) {  // the histogram did not match the row: workspace not cleared before use
+            if (lane == 0) flag(a.status, IX_DEV_BAD_HIST);
+            for (int i = pos0 + lane; i < a.k; i += 32) emit(a, r, b, i, -1);
+        }
+    }
+}
+
+template <int PER, bool HIST>
 int cluster_setup() {  // the carve-out attribute, once per device
     static std::mutex mu;
     static std::vector<char> ready;
@@ -678,7 +989,7 @@ int cluster_setup() {  // the carve-out attribute, once per device
     std::lock_guard<std::mutex> lock(mu);
     if (dev >= static_cast<int>(ready.size())) ready.resize(dev + 1, 0);
     if (!ready[dev]) {
-        if (cudaFuncSetAttribute(topk_kernel<PER>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        if (cudaFuncSetAttribute(topk_kernel<PER, HIST>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return IX_ERR_CUDA;
         ready[dev] = 1;
@@ -686,9 +997,9 @@ int cluster_setup() {  // the carve-out attribute, once per device
     return IX_OK;
 }
 
-template <int PER>
+template <int PER, bool HIST>
 int launch_per(const TopkArgs& a, int C, int64_t clusters, cudaStream_t stream) {
-    const int st = cluster_setup<PER>();
+    const int st = cluster_setup<PER, HIST>();
     if (st != IX_OK) return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * C));
@@ -702,14 +1013,81 @@ int launch_per(const TopkArgs& a, int C, int64_t clusters, cudaStream_t stream) 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, topk_kernel<PER>, a) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, topk_kernel<PER, HIST>, a) != cudaSuccess) {
         cudaGetLastError();
         return IX_ERR_CUDA;
     }
     return launch_status();
 }
 
+// Cluster size for rows of ld keys: slices within the per-CTA cap, and enough
+// CTAs to fill the GPU.
+int cluster_size(int64_t ld, int64_t rows, int sms, int* slice) {
+    auto slice_of = [&](int c) { return static_cast<int>(((ld + c - 1) / c + 3) / 4 * 4); };
+    int C = 1;
+    while (C < kMaxCluster &&
+           (slice_of(C) > kSliceCap || (rows * C < 2 * sms && slice_of(2 * C) >= 2048)))
+        C *= 2;
+    *slice = ld > 0 ? slice_of(C) : 4;
+    return C;
+}
+
+template <bool HIST>
+int launch_cluster(TopkArgs a, int sms, cudaStream_t s) {
+    const int C = cluster_size(a.ld, a.rows, sms, &a.slice);
+    const int64_t max_clusters = static_cast<int64_t>(sms) * 3 / C;
+    const int64_t clusters = a.rows < max_clusters ? a.rows : max_clusters;
+    const int per_needed = (a.slice + kThreads - 1) / kThreads;
+    if (per_needed <= 4) return launch_per<4, HIST>(a, C, clusters, s);
+    if (per_needed <= 8) return launch_per<8, HIST>(a, C, clusters, s);
+    if (per_needed <= 16) return launch_per<16, HIST>(a, C, clusters, s);
+    if (per_needed <= 32) return launch_per<32, HIST>(a, C, clusters, s);
+    return launch_per<64, HIST>(a, C, clusters, s);
+}
+
+void set_block_size(TopkArgs& a, int block_size) {
+    a.block_size = block_size;
+    a.bs_shift = (block_size & (block_size - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(block_size)) : -1;
+}
+
 }  // namespace
+
+// The selection that follows a histogram logits kernel (see common.cuh).
+int select_after_logits(const SelectRows& q, cudaStream_t s) {
+    const int sms = num_sms();
+    if (sms <= 0) return IX_ERR_CUDA;
+    TopkArgs a{};
+    a.logits = q.logits;
+    a.ld = q.ld;
+    a.rows = q.rows;
+    a.geom = q.row_len ? kRowsGiven : (q.context_lens ? kRowsDecode : kRowsPrefill);
+    a.row_len = q.row_len;
+    a.context_lens = q.context_lens;
+    a.next_n = q.next_n;
+    a.ks = q.ks;
+    a.ke = q.ke;
+    a.tk = q.tk;
+    a.row_req = q.row_req;
+    a.bt = q.block_table;
+    a.bt_stride = q.bt_stride;
+    set_block_size(a, q.block_size);
+    a.k = q.k;
+    a.out_local = q.out_local;
+    a.out_global = q.out_global;
+    a.hist = q.hist;
+    a.status = q.status;
+    if (a.rows == 0) return IX_OK;
+    if (a.ld <= kSelMaxLd && a.rows >= 2 * static_cast<int64_t>(sms)) {
+        const int64_t cap = static_cast<int64_t>(sms) * 6;  // 6 CTAs of 8 warps per SM
+        const unsigned grid = static_cast<unsigned>((a.rows + kSelWarps - 1) / kSelWarps < cap
+                                                        ? (a.rows + kSelWarps - 1) / kSelWarps
+                                                        : cap);
+        select_warp_kernel<<<grid, kSelWarps * 32, 0, s>>>(a);
+        return launch_status();
+    }
+    return launch_cluster<true>(a, sms, s);
+}
+
 }  // namespace dsix
 
 using namespace dsix;
@@ -722,34 +1100,25 @@ extern "C" int ix_topk_to_global(const float* logits, int64_t ld, int64_t rows,
     if (ld < 0 || rows < 0 || bt_stride < 0) return IX_ERR_SHAPE;
     if (k < 1 || block_size < 1) return IX_ERR_UNSUPPORTED;
     if (rows == 0) return IX_OK;
-    if (ld % 4 != 0 || ld > static_cast<int64_t>(kMaxCluster) * kSliceCap) return IX_ERR_UNSUPPORTED;
+    if (ld % 4 != 0 || ld > kTopkMaxLd) return IX_ERR_UNSUPPORTED;
     if (!row_len || !row_req || !block_table || !out_global || (ld > 0 && !logits))
         return IX_ERR_NULL;
     if (ld > 0 && !aligned16(logits)) return IX_ERR_ALIGN;
     const int sms = num_sms();
     if (sms <= 0) return IX_ERR_CUDA;
-    // cluster size: slices within the per-CTA cap, and enough CTAs to fill the GPU
-    auto slice_of = [&](int c) { return static_cast<int>(((ld + c - 1) / c + 3) / 4 * 4); };
-    int C = 1;
-    while (C < kMaxCluster &&
-           (slice_of(C) > kSliceCap || (rows * C < 2 * sms && slice_of(2 * C) >= 2048)))
-        C *= 2;
     TopkArgs a{};
     a.logits = logits;
     a.ld = ld;
     a.rows = rows;
+    a.geom = kRowsGiven;
     a.row_len = row_len;
     a.row_req = row_req;
     a.bt = block_table;
     a.bt_stride = bt_stride;
-    a.block_size = block_size;
-    a.bs_shift = (block_size & (block_size - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(block_size)) : -1;
+    set_block_size(a, block_size);
     a.k = k;
     a.out_local = out_local;
     a.out_global = out_global;
-    a.slice = ld > 0 ? slice_of(C) : 4;
-    const int64_t max_clusters = static_cast<int64_t>(sms) * 3 / C;
-    const int64_t clusters = rows < max_clusters ? rows : max_clusters;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (ld <= kBlkMaxLd && rows >= 2 * static_cast<int64_t>(sms)) {
         // resident CTAs per SM: 4 at PER = 32 (registers bounded to 64), 2 at PER = 64
@@ -761,10 +1130,36 @@ extern "C" int ix_topk_to_global(const float* logits, int64_t ld, int64_t rows,
             topk_block_kernel<64><<<grid, kBlkThreads, 0, s>>>(a);
         return launch_status();
     }
-    const int per_needed = (a.slice + kThreads - 1) / kThreads;
-    if (per_needed <= 4) return launch_per<4>(a, C, clusters, s);
-    if (per_needed <= 8) return launch_per<8>(a, C, clusters, s);
-    if (per_needed <= 16) return launch_per<16>(a, C, clusters, s);
-    if (per_needed <= 32) return launch_per<32>(a, C, clusters, s);
-    return launch_per<64>(a, C, clusters, s);
+    return launch_cluster<false>(a, sms, s);
+}
+
+extern "C" int ix_topk_from_hist(const float* logits, int64_t ld, int64_t rows, const int32_t* row_len,
+                                 const int32_t* row_req, const int32_t* block_table, int64_t bt_stride,
+                                 int block_size, int k, int32_t* out_local, int32_t* out_global,
+                                 void* workspace, size_t workspace_bytes, ix_stream_t stream) {
+    if (ld < 0 || rows < 0 || bt_stride < 0) return IX_ERR_SHAPE;
+    if (k < 1 || block_size < 1) return IX_ERR_UNSUPPORTED;
+    if (rows == 0) return IX_OK;
+    if (ld % 4 != 0 || ld > kTopkMaxLd) return IX_ERR_UNSUPPORTED;
+    if (!row_len || !row_req || !block_table || !out_global || (ld > 0 && !logits)) return IX_ERR_NULL;
+    if (ld > 0 && !aligned16(logits)) return IX_ERR_ALIGN;
+    if (!workspace || workspace_bytes < static_cast<size_t>(rows) * kHistRowWords * 4) return IX_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return IX_ERR_ALIGN;
+    int* st = status_ptr();
+    if (!st) return IX_ERR_CUDA;
+    SelectRows q{};
+    q.logits = logits;
+    q.ld = ld;
+    q.rows = rows;
+    q.row_len = row_len;
+    q.row_req = row_req;
+    q.block_table = block_table;
+    q.bt_stride = bt_stride;
+    q.block_size = block_size;
+    q.k = k;
+    q.out_local = out_local;
+    q.out_global = out_global;
+    q.hist = static_cast<uint32_t*>(workspace);
+    q.status = st;
+    return select_after_logits(q, reinterpret_cast<cudaStream_t>(stream));
 }

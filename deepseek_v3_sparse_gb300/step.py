@@ -10,6 +10,11 @@ Order of a step (the new tokens' caches are written before anything reads them):
   6. ix_topk_to_global    top-k + remap, once for the decode rows and once for the
                           prefill rows (they live in logits buffers of different ld)
 
+With ``fused=True`` each logits call and its top-k are one call
+(ix_paged_mqa_logits_topk, ix_mqa_logits_topk): the logits kernel also builds
+each row's first-digit histogram and the selection starts from it.  Each
+fused call keeps a histogram workspace of its own, zeroed once here.
+
 All buffers are allocated once here (torch, on the device); ``run`` allocates
 nothing and never synchronises, so it can be captured in a CUDA graph.
 """
@@ -21,8 +26,9 @@ from typing import Optional
 import torch
 
 from . import (BLOCK_SIZE, DSMLA_ENTRY_BYTES, HEAD_DIM, HEADS, INDEXER_BLOCK_BYTES,
-               dsmla_quant_write, ix_gather_k, ix_mqa_logits, ix_paged_mqa_logits,
-               ix_quant_write_k, ix_topk_to_global)
+               dsmla_quant_write, ix_gather_k, ix_mqa_logits, ix_mqa_logits_hist, ix_mqa_logits_topk,
+               ix_paged_mqa_logits, ix_paged_mqa_logits_hist, ix_paged_mqa_logits_topk,
+               ix_quant_write_k, ix_topk_from_hist, ix_topk_hist_workspace_size, ix_topk_to_global)
 
 
 def round_up(x: int, m: int) -> int:
@@ -58,7 +64,9 @@ class IndexerStep:
                  new_k: torch.Tensor, new_slot: torch.Tensor,
                  decode: Optional[DecodePart] = None, prefill: Optional[PrefillPart] = None,
                  nope: Optional[torch.Tensor] = None, rope: Optional[torch.Tensor] = None,
-                 clean_logits: bool = False, with_local: bool = False):
+                 clean_logits: bool = False, with_local: bool = False, fused: bool = False):
+        if fused and clean_logits:
+            raise ValueError("the fused calls leave the logits past each row's end untouched (no clean_logits)")
         dev = block_table.device
         self.num_blocks = num_blocks
         self.block_table = block_table
@@ -70,6 +78,7 @@ class IndexerStep:
         self.nope = nope
         self.rope = rope
         self.clean = clean_logits
+        self.fused = fused
         self.cache = torch.zeros(num_blocks, INDEXER_BLOCK_BYTES, dtype=torch.uint8, device=dev)
         self.dsmla_cache = None
         if nope is not None:
@@ -81,6 +90,8 @@ class IndexerStep:
             self.dec_logits = torch.empty(R, decode.ld, dtype=torch.float32, device=dev)
             self.dec_global = torch.empty(R, topk, **i32)
             self.dec_local = torch.empty(R, topk, **i32) if with_local else None
+            self.dec_ws = (torch.zeros(ix_topk_hist_workspace_size(R), dtype=torch.uint8, device=dev)
+                           if fused else None)
         if prefill is not None:
             T = prefill.w.shape[0]
             self.k_fp8 = torch.empty(max(prefill.gathered, 1), HEAD_DIM, dtype=torch.uint8,
@@ -90,6 +101,8 @@ class IndexerStep:
             self.pf_logits = torch.empty(T, prefill.ld, dtype=torch.float32, device=dev)
             self.pf_global = torch.empty(T, topk, **i32)
             self.pf_local = torch.empty(T, topk, **i32) if with_local else None
+            self.pf_ws = (torch.zeros(ix_topk_hist_workspace_size(T), dtype=torch.uint8, device=dev)
+                          if fused else None)
 
     def write_history(self, k_bf16: torch.Tensor, slots: torch.Tensor, chunk: int = 1 << 20):
         """Fill the indexer-K cache with already-cached positions (set-up, not a step)."""
@@ -97,6 +110,8 @@ class IndexerStep:
             ix_quant_write_k(k_bf16[i:i + chunk], slots[i:i + chunk], self.cache)
 
     def kernels_per_step(self) -> int:
+        """Kernel launches of one step (a fused call launches two kernels, as
+        does the unfused pair)."""
         n = 1 + (self.nope is not None)
         if self.prefill is not None:
             n += 3 + (1 if self.clean else 0)
@@ -104,9 +119,11 @@ class IndexerStep:
             n += 2 + (1 if self.clean else 0)
         return n
 
-    def run(self, stream=None, events=None):
+    def run(self, stream=None, events=None, split: bool = False):
         """One step.  ``events``: optional dict name -> (start, end) CUDA events
-        recorded around the logits and top-k launches on ``stream``.
+        recorded around the logits and top-k launches on ``stream``.  With
+        ``split`` a fused step issues each fused call as its two halves (the
+        same kernels, in the same order), so events can bracket each kernel.
 
         Order: cache writes, then the decode pair (paged logits streaming the
         cache, top-k), then the prefill pair (gather, logits, top-k).  The
@@ -127,18 +144,43 @@ class IndexerStep:
             dsmla_quant_write(self.nope, self.rope, self.new_slot, self.dsmla_cache, stream=s)
         if self.decode is not None:
             d = self.decode
-            timed("paged_mqa_logits", lambda: ix_paged_mqa_logits(
-                d.q, d.w, self.cache, d.context_lens, self.block_table, self.dec_logits,
-                clean_logits=self.clean, stream=s))
-            timed("topk_decode", lambda: ix_topk_to_global(
-                self.dec_logits, d.row_len, d.row_req, self.block_table, self.topk,
-                self.dec_global, self.dec_local, stream=s))
+            if self.fused and not split:
+                timed("paged_mqa_logits_topk", lambda: ix_paged_mqa_logits_topk(
+                    d.q, d.w, self.cache, d.context_lens, self.block_table, self.dec_logits, self.topk,
+                    self.dec_global, self.dec_ws, out_local=self.dec_local, stream=s))
+            elif self.fused:
+                timed("paged_mqa_logits", lambda: ix_paged_mqa_logits_hist(
+                    d.q, d.w, self.cache, d.context_lens, self.block_table, self.dec_logits, self.topk,
+                    self.dec_ws, stream=s))
+                timed("topk_decode", lambda: ix_topk_from_hist(
+                    self.dec_logits, d.row_len, d.row_req, self.block_table, self.topk, self.dec_global,
+                    self.dec_ws, out_local=self.dec_local, stream=s))
+            else:
+                timed("paged_mqa_logits", lambda: ix_paged_mqa_logits(
+                    d.q, d.w, self.cache, d.context_lens, self.block_table, self.dec_logits,
+                    clean_logits=self.clean, stream=s))
+                timed("topk_decode", lambda: ix_topk_to_global(
+                    self.dec_logits, d.row_len, d.row_req, self.block_table, self.topk,
+                    self.dec_global, self.dec_local, stream=s))
         if self.prefill is not None:
             p = self.prefill
             ix_gather_k(self.cache, self.pf_bt, p.cu_seq_lens, self.k_fp8, self.k_scale, stream=s)
-            timed("mqa_logits", lambda: ix_mqa_logits(
-                p.q, p.w, self.k_fp8, self.k_scale, p.ks, p.ke, self.pf_logits,
-                clean_logits=self.clean, stream=s))
-            timed("topk_prefill", lambda: ix_topk_to_global(
-                self.pf_logits, p.row_len, p.row_req, self.block_table, self.topk,
-                self.pf_global, self.pf_local, stream=s))
+            if self.fused and not split:
+                timed("mqa_logits_topk", lambda: ix_mqa_logits_topk(
+                    p.q, p.w, self.k_fp8, self.k_scale, p.ks, p.ke, self.pf_logits, p.row_req,
+                    self.block_table, self.topk, self.pf_global, self.pf_ws, out_local=self.pf_local,
+                    stream=s))
+            elif self.fused:
+                timed("mqa_logits", lambda: ix_mqa_logits_hist(
+                    p.q, p.w, self.k_fp8, self.k_scale, p.ks, p.ke, self.pf_logits, self.topk, self.pf_ws,
+                    stream=s))
+                timed("topk_prefill", lambda: ix_topk_from_hist(
+                    self.pf_logits, p.row_len, p.row_req, self.block_table, self.topk, self.pf_global,
+                    self.pf_ws, out_local=self.pf_local, stream=s))
+            else:
+                timed("mqa_logits", lambda: ix_mqa_logits(
+                    p.q, p.w, self.k_fp8, self.k_scale, p.ks, p.ke, self.pf_logits,
+                    clean_logits=self.clean, stream=s))
+                timed("topk_prefill", lambda: ix_topk_to_global(
+                    self.pf_logits, p.row_len, p.row_req, self.block_table, self.topk,
+                    self.pf_global, self.pf_local, stream=s))

@@ -75,7 +75,8 @@ enum {
     IX_DEV_ROW_TOO_LONG = 4,    /* a visible row is longer than ld: columns >= ld dropped */
     IX_DEV_BAD_RANGE = 8,       /* ks/ke outside [0, tk], or cu_seq_lens past out_capacity */
     IX_DEV_TIMEOUT = 16,        /* a pipeline wait gave up (never expected) */
-    IX_DEV_BAD_POSITION = 32    /* a RoPE position outside [0, max_pos): token skipped */
+    IX_DEV_BAD_POSITION = 32,   /* a RoPE position outside [0, max_pos): token skipped */
+    IX_DEV_BAD_HIST = 64        /* a top-k histogram did not match its row (workspace not zero before use) */
 };
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -196,6 +197,99 @@ IX_API int ix_topk_to_global(const float* logits, int64_t ld, int64_t rows,
                       const int32_t* block_table, int64_t bt_stride, int block_size,
                       int k, int32_t* out_local, int32_t* out_global,
                       ix_stream_t stream);
+
+/*
+ * Fused logits + top-k.  The two entry points below compute exactly what
+ * ix_paged_mqa_logits / ix_mqa_logits (with clean_logits = 0) followed by
+ * ix_topk_to_global compute -- the same logits, the same selection, the same
+ * remap -- for the rows those logits kernels produce, in one call that never
+ * re-reads a row from the start for the first radix pass: while the logits
+ * kernel writes a row with more than k visible keys, it also counts the first
+ * radix digit of each logit (the top 11 bits of its order key) into the row's
+ * histogram, and the selection that follows starts from the digit that holds
+ * the k-th largest key.  This is the clean_logits=False mode of vLLM PR #36250
+ * "[kernel] Fix FP8 paged MQA fallback for CUDA graph capture" (review thread:
+ * the logits past each row's end need no -inf fill, since the selection never
+ * reads them) feeding the 2-D top-k index buffer of ROCm/ATOM PR #1094
+ * "[Feat] Support DSv3.2 with sglang-ATOM plugin and sglang sparse MLA"
+ * (Technical Details: request-local top-k indices converted to global paged KV
+ * indices).
+ *
+ * Workspace: ix_topk_hist_workspace_size(rows) bytes (8448 per row: 64 coarse
+ * and 2048 fine u32 bins), 16-byte aligned, owned by the caller.  It must be
+ * ALL ZERO before its first use; every call that completes leaves it all zero
+ * again, so set it to zero once when it is allocated.  Calls that share a
+ * workspace must not overlap on the GPU.  If a call stops short (a pipeline
+ * wait gives up: IX_DEV_TIMEOUT), clear the workspace before reusing it.  A
+ * histogram that does not match its row (a workspace that was not zero) sets
+ * IX_DEV_BAD_HIST; that row's output is then incomplete and padded with -1.
+ * `logits` is written as by the unfused call (entries past each row's length
+ * are left untouched) and is read back by the selection.
+ */
+IX_API size_t ix_topk_hist_workspace_size(int64_t rows);
+
+/*
+ * ix_paged_mqa_logits_topk -- ix_paged_mqa_logits (clean_logits = 0) and then
+ * ix_topk_to_global over its rows: row r = b*next_n + j has length
+ * L = clamp(context_lens[b] - next_n + 1 + j, 0, ld) and request b; its indices
+ * are remapped through block_table[b, :] with block_size (64).  Arguments as
+ * in those two calls; out_local may be NULL.  Errors, before any launch: those
+ * of ix_paged_mqa_logits; IX_ERR_UNSUPPORTED for k < 1 or ld > 262144;
+ * IX_ERR_WORKSPACE for a missing or small workspace; IX_ERR_ALIGN for a
+ * workspace that is not 16-byte aligned; IX_ERR_NULL for out_global.
+ */
+IX_API int ix_paged_mqa_logits_topk(const uint8_t* q_fp8, const float* w, const uint8_t* cache,
+                        int64_t num_blocks, int block_size, const int32_t* context_lens,
+                        const int32_t* block_table, int64_t bt_stride, int batch, int next_n,
+                        int heads, int head_dim, float* logits, int64_t ld, int k,
+                        int32_t* out_local, int32_t* out_global, void* workspace,
+                        size_t workspace_bytes, ix_stream_t stream);
+
+/*
+ * ix_mqa_logits_topk -- ix_mqa_logits (clean_logits = 0) and then
+ * ix_topk_to_global over its rows: row t has length L = ke[t] - ks[t] (clamped
+ * as ix_mqa_logits clamps it, and to ld) and request row_req[t]; column j is
+ * remapped through block_table[row_req[t], j / block_size] (j is the
+ * request-local key index when ks[t] is the request's first gathered row).
+ * Arguments as in those two calls; row_req int32 [tq]; out_local may be NULL.
+ * Errors, before any launch: those of ix_mqa_logits; the k / ld / workspace
+ * errors of ix_paged_mqa_logits_topk; IX_ERR_SHAPE for bt_stride < 0;
+ * IX_ERR_UNSUPPORTED for block_size < 1; IX_ERR_NULL for row_req, block_table
+ * or out_global.
+ */
+IX_API int ix_mqa_logits_topk(const uint8_t* q_fp8, const float* w, const uint8_t* k_fp8,
+                        const float* k_scale, const int32_t* ks, const int32_t* ke, int64_t tq,
+                        int64_t tk, int heads, int head_dim, float* logits, int64_t ld,
+                        const int32_t* row_req, const int32_t* block_table, int64_t bt_stride,
+                        int block_size, int k, int32_t* out_local, int32_t* out_global,
+                        void* workspace, size_t workspace_bytes, ix_stream_t stream);
+
+/*
+ * The two halves of the fused calls, for callers that place the selection
+ * themselves (another stream, a later point of a graph) or time the halves:
+ * ix_*_logits_hist runs the logits kernel of the fused call (logits as
+ * ix_*_logits with clean_logits = 0, plus the histograms of the rows with
+ * more than k keys), ix_topk_from_hist the selection.  Between them the
+ * workspace holds the histograms: ix_topk_from_hist must follow on the same
+ * rows, with row_len[r] equal to the length the logits call gave row r (the
+ * clamped L above) and the same k, and it leaves the workspace zero again.
+ * Errors as in the fused calls (ix_topk_from_hist: those of
+ * ix_topk_to_global, then the workspace errors).
+ */
+IX_API int ix_paged_mqa_logits_hist(const uint8_t* q_fp8, const float* w, const uint8_t* cache,
+                        int64_t num_blocks, int block_size, const int32_t* context_lens,
+                        const int32_t* block_table, int64_t bt_stride, int batch, int next_n,
+                        int heads, int head_dim, float* logits, int64_t ld, int k,
+                        void* workspace, size_t workspace_bytes, ix_stream_t stream);
+IX_API int ix_mqa_logits_hist(const uint8_t* q_fp8, const float* w, const uint8_t* k_fp8,
+                        const float* k_scale, const int32_t* ks, const int32_t* ke, int64_t tq,
+                        int64_t tk, int heads, int head_dim, float* logits, int64_t ld, int k,
+                        void* workspace, size_t workspace_bytes, ix_stream_t stream);
+IX_API int ix_topk_from_hist(const float* logits, int64_t ld, int64_t rows,
+                        const int32_t* row_len, const int32_t* row_req,
+                        const int32_t* block_table, int64_t bt_stride, int block_size, int k,
+                        int32_t* out_local, int32_t* out_global, void* workspace,
+                        size_t workspace_bytes, ix_stream_t stream);
 
 /*
  * dsmla_quant_write -- the fp8_ds_mla cache write (vLLM PR #47090, prhub

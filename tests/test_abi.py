@@ -38,7 +38,7 @@ def _declared():
 
 def test_exports_match_header(lib):
     names = _declared()
-    assert len(names) == 12
+    assert len(names) == 18
     for n in names:
         assert hasattr(lib, n), n
     out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True,
@@ -119,6 +119,68 @@ def test_topk_host_checks(lib):
     assert f(*args(out=None)) == IX_ERR_NULL
     assert f(*args(lg=A1)) == IX_ERR_ALIGN
     assert f(*args(rows=0)) == IX_OK
+
+
+def test_fused_topk_host_checks(lib):
+    """The fused logits + top-k calls and their halves check every argument on
+    the host (the logits call's checks first, then k / ld / workspace, then the
+    top-k outputs) before any CUDA call."""
+    ws = lib.ix_topk_hist_workspace_size
+    assert ws(3) == 3 * (64 + 2048) * 4 and ws(0) == 0 and ws(-1) == 0
+    need = ws(2)
+    f = lib.ix_paged_mqa_logits_topk
+
+    def pargs(**kw):
+        return [kw.get("q", A16), A16, A16, 8, 64, A16, A16, 4, kw.get("batch", 2), 1, kw.get("heads", 64), 128,
+                A16, kw.get("ld", 64), kw.get("k", 16), None, kw.get("out", A16), kw.get("ws", A16),
+                kw.get("ws_bytes", need), None]
+
+    assert f(*pargs(heads=32)) == IX_ERR_UNSUPPORTED        # the logits checks come first
+    assert f(*pargs(q=None, ws=None)) == IX_ERR_NULL
+    assert f(*pargs(k=0)) == IX_ERR_UNSUPPORTED
+    assert f(*pargs(ld=262148)) == IX_ERR_UNSUPPORTED
+    assert f(*pargs(ws=None)) == IX_ERR_WORKSPACE
+    assert f(*pargs(ws_bytes=need - 1)) == IX_ERR_WORKSPACE
+    assert f(*pargs(ws=A1)) == IX_ERR_ALIGN
+    assert f(*pargs(out=None)) == IX_ERR_NULL
+    assert f(*pargs(batch=0, q=None, ws=None, out=None)) == IX_OK
+    h = lib.ix_paged_mqa_logits_hist
+    hargs = lambda **kw: pargs(**kw)[:15] + [kw.get("ws", A16), kw.get("ws_bytes", need), None]
+    assert h(*hargs(k=0)) == IX_ERR_UNSUPPORTED
+    assert h(*hargs(ws=None)) == IX_ERR_WORKSPACE
+    assert h(*hargs(batch=0, q=None)) == IX_OK
+
+    g = lib.ix_mqa_logits_topk
+    need16 = ws(16)
+
+    def cargs(**kw):
+        return [kw.get("q", A16), A16, A16, A16, A16, A16, kw.get("tq", 16), 16, 64, 128, A16, kw.get("ld", 16),
+                kw.get("req", A16), kw.get("bt", A16), kw.get("bts", 8), kw.get("bs", 64), kw.get("k", 4), None,
+                kw.get("out", A16), kw.get("ws", A16), kw.get("ws_bytes", need16), None]
+
+    assert g(*cargs(ld=18)) == IX_ERR_UNSUPPORTED
+    assert g(*cargs(k=0)) == IX_ERR_UNSUPPORTED
+    assert g(*cargs(ws_bytes=need16 - 4)) == IX_ERR_WORKSPACE
+    assert g(*cargs(bts=-1)) == IX_ERR_SHAPE
+    assert g(*cargs(bs=0)) == IX_ERR_UNSUPPORTED
+    assert g(*cargs(req=None)) == IX_ERR_NULL
+    assert g(*cargs(bt=None)) == IX_ERR_NULL
+    assert g(*cargs(out=None)) == IX_ERR_NULL
+    assert g(*cargs(tq=0)) == IX_OK
+    c = lib.ix_mqa_logits_hist
+    assert c(A16, A16, A16, A16, A16, A16, 16, 16, 64, 128, A16, 16, 0, A16, need16, None) == IX_ERR_UNSUPPORTED
+    assert c(A16, A16, A16, A16, A16, A16, 16, 16, 64, 128, A16, 16, 4, None, need16, None) == IX_ERR_WORKSPACE
+
+    t = lib.ix_topk_from_hist
+    targs = lambda **kw: [A16, kw.get("ld", 64), kw.get("rows", 2), A16, A16, A16, 8, 64, kw.get("k", 16), None,
+                          kw.get("out", A16), kw.get("ws", A16), kw.get("ws_bytes", need), None]
+    assert t(*targs(k=0)) == IX_ERR_UNSUPPORTED
+    assert t(*targs(ld=62)) == IX_ERR_UNSUPPORTED
+    assert t(*targs(rows=-1)) == IX_ERR_SHAPE
+    assert t(*targs(out=None)) == IX_ERR_NULL
+    assert t(*targs(ws=None)) == IX_ERR_WORKSPACE
+    assert t(*targs(ws=A1)) == IX_ERR_ALIGN
+    assert t(*targs(rows=0)) == IX_OK
 
 
 def test_dsmla_host_checks(lib):

@@ -91,10 +91,28 @@ def test_mixed_long_pipeline_sampled(dsix):
     assert dsix.ix_device_status() == 0
 
 
-def test_graph_capture_replays_identically(dsix):
+@pytest.mark.parametrize("name", ["decode_b32", "mixed_long"])
+def test_fused_step_matches_unfused_step(dsix, name):
+    """The benchmark's step with the fused calls selects exactly what the step
+    with the unfused pairs selects."""
+    wl = W.NAMED[name]()
+    a = make_step(wl, "cuda", with_local=True)
+    b = make_step(wl, "cuda", with_local=True, fused=True)
+    a.run()
+    b.run()
+    b.run()  # a second step on the same workspaces
+    torch.cuda.synchronize()
+    assert dsix.ix_device_status() == 0
+    assert torch.equal(a.dec_global, b.dec_global) and torch.equal(a.dec_local, b.dec_local)
+    if wl.prefill_req:
+        assert torch.equal(a.pf_global, b.pf_global) and torch.equal(a.pf_local, b.pf_local)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_graph_capture_replays_identically(dsix, fused):
     wl = W.build("graph", decode_ctx=[300, 5000, 77], next_n=2, prefill=[(1000, 300)],
                  topk=256, seed=9, dsmla=True)
-    step = make_step(wl, "cuda", clean=True, with_local=True)
+    step = make_step(wl, "cuda", clean=not fused, with_local=True, fused=fused)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -118,3 +136,5 @@ def test_graph_capture_replays_identically(dsix):
     for a, b in zip(eager, again):
         assert torch.equal(a, b)
     assert dsix.ix_device_status() == 0
+    if fused:  # each replay left the histogram workspaces zero
+        assert int(step.dec_ws.count_nonzero()) == 0 and int(step.pf_ws.count_nonzero()) == 0

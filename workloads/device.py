@@ -17,7 +17,7 @@ def _ld(max_len: int) -> int:
 
 
 def make_step(wl: Workload, device="cuda", clean: bool = False, with_local: bool = False,
-              write_history: bool = True):
+              write_history: bool = True, fused: bool = False):
     from deepseek_v3_sparse_gb300.step import DecodePart, IndexerStep, PrefillPart
 
     dev = torch.device(device)
@@ -42,7 +42,7 @@ def make_step(wl: Workload, device="cuda", clean: bool = False, with_local: bool
                        decode=decode, prefill=prefill,
                        nope=None if wl.nope_bf16 is None else wl.nope_bf16.to(dev),
                        rope=None if wl.rope_bf16 is None else wl.rope_bf16.to(dev),
-                       clean_logits=clean, with_local=with_local)
+                       clean_logits=clean, with_local=with_local, fused=fused)
     if write_history and (~wl.is_new).any():
         step.write_history(wl.hist_k.to(dev), torch.from_numpy(wl.hist_slot.copy()).to(dev))
     return step
