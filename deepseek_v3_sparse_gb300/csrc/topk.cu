@@ -786,7 +786,7 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
 //   1. hist_pick: the digit d that holds the k-th largest key, the keys above
 //      it (all selected) and the count c of keys in it.
 //   2. If not all c keys of d are taken: the keys of digit d (read from the
-//      logits row once, in index order) go to shared memory when c <= kSelCap,
+//      logits row once) go to shared memory when c <= kSelCap,
 //      and 7-bit radix levels over them settle the remaining 21 bits; past
 //      kSelCap the levels re-read the row instead.  The result is a prefix of
 //      the key (of `sh` bits below the top) above which everything is taken,
@@ -860,11 +860,9 @@ __device__ __forceinline__ int warp_excl_scan(int x, int& total) {
 
 __global__ void __launch_bounds__(kSelWarps * 32) select_warp_kernel(const TopkArgs a) {
     __shared__ uint32_t s_key[kSelWarps][kSelCap];
-    __shared__ int32_t s_idx[kSelWarps][kSelCap];
     __shared__ uint32_t s_h[kSelWarps][1 << kSelBits];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint32_t* ck = s_key[warp];
-    int32_t* ci = s_idx[warp];
     uint32_t* wh = s_h[warp];
     const int64_t nw = static_cast<int64_t>(gridDim.x) * kSelWarps;
     for (int64_t r = static_cast<int64_t>(blockIdx.x) * kSelWarps + warp; r < a.rows; r += nw) {
@@ -896,10 +894,7 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_warp_kernel(const TopkA
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         if ((eq >> j) & 1u) {
-                            if (pos < kSelCap) {
-                                ck[pos] = key[j];
-                                ci[pos] = c0 + 4 * lane + j;
-                            }
+                            if (pos < kSelCap) ck[pos] = key[j];
                             ++pos;
                         }
                     }
