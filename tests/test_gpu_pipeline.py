@@ -133,8 +133,13 @@ def test_graph_capture_replays_identically(dsix, fused):
     torch.cuda.synchronize()
     again = (step.dec_logits, step.dec_global, step.pf_logits, step.pf_global, step.dec_local,
              step.pf_local)
-    for a, b in zip(eager, again):
-        assert torch.equal(a, b)
+    for i, (a, b) in enumerate(zip(eager, again)):
+        if fused and i in (0, 2):  # the fused calls leave the logits past each row's end untouched
+            lens = (step.decode if i == 0 else step.prefill).row_len.cpu().tolist()
+            for r, L in enumerate(lens):
+                assert torch.equal(a[r, :L], b[r, :L])
+        else:
+            assert torch.equal(a, b)
     assert dsix.ix_device_status() == 0
     if fused:  # each replay left the histogram workspaces zero
         assert int(step.dec_ws.count_nonzero()) == 0 and int(step.pf_ws.count_nonzero()) == 0
