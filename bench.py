@@ -359,7 +359,8 @@ def gpu_arm(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = W.NAMED[args.workload](seed=rank)
-    step = make_step(wl, dev, fused=not args.unfused)
+    fused = () if args.unfused else tuple(args.fused.split(","))
+    step = make_step(wl, dev, fused=fused)
     stream = torch.cuda.current_stream(dev)
     names = []
     if wl.prefill_req:
@@ -473,7 +474,7 @@ def gpu_arm(args, world, rank, local):
     # each buffer's reuse (a set's inputs are rewritten only after the step that
     # read them ran, its indices only after they were copied out).
     e2e_steps = min(args.steps, 200)
-    steps = [step, make_step(wl, dev, fused=not args.unfused)]
+    steps = [step, make_step(wl, dev, fused=fused)]
     host_src = {
         "new_k": wl.new_k.pin_memory(),
         "new_slot": torch.from_numpy(wl.new_slot.copy()).pin_memory(),
@@ -746,7 +747,11 @@ def main():
     ap.add_argument("--impl", default="dsix", choices=["dsix", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused", action="store_true",
-                    help="run each logits call and its top-k as separate calls (default: the fused calls)")
+                    help="run every logits call and its top-k as separate calls")
+    ap.add_argument("--fused", default="decode",
+                    help="parts whose logits and top-k run as one fused call: decode, prefill or decode,prefill "
+                         "(default decode: for the prefill rows the histogram costs the logits kernel more than "
+                         "it saves the selection)")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-configuration timing of the decode, MTP and prefill kernels")
     ap.add_argument("--workload", default="mixed_long",
@@ -814,7 +819,7 @@ def main():
             "dtype": "fp8_e4m3 x fp8_e4m3 -> f32 (logits); u8/bf16 cache writes",
             "data": "synthetic (seeded; random-init inputs of the indexer shapes; no dataset)",
             "config": {**workload_config(wl), "parallelism": f"replicas x{world}",
-                       "fused_logits_topk": not args.unfused},
+                       "fused_logits_topk": [] if args.unfused else args.fused.split(",")},
             "roofline": roofline, "kernels": kernels,
             "prefill_tflops": pf_tflops, "decode_hbm_gbs": dec_gbs,
             "e2e": {"value": job_throughput(world, r["rows"], r["e2e_steps"], e2e_ms), "unit": UNIT,

@@ -10,10 +10,11 @@ Order of a step (the new tokens' caches are written before anything reads them):
   6. ix_topk_to_global    top-k + remap, once for the decode rows and once for the
                           prefill rows (they live in logits buffers of different ld)
 
-With ``fused=True`` each logits call and its top-k are one call
-(ix_paged_mqa_logits_topk, ix_mqa_logits_topk): the logits kernel also builds
-each row's first-digit histogram and the selection starts from it.  Each
-fused call keeps a histogram workspace of its own, zeroed once here.
+``fused`` names the parts ("decode", "prefill"; True = both) whose logits call
+and top-k run as one call (ix_paged_mqa_logits_topk, ix_mqa_logits_topk): the
+logits kernel also builds each row's first-digit histogram and the selection
+starts from it.  Each fused call keeps a histogram workspace of its own,
+zeroed once here.
 
 All buffers are allocated once here (torch, on the device); ``run`` allocates
 nothing and never synchronises, so it can be captured in a CUDA graph.
@@ -64,7 +65,10 @@ class IndexerStep:
                  new_k: torch.Tensor, new_slot: torch.Tensor,
                  decode: Optional[DecodePart] = None, prefill: Optional[PrefillPart] = None,
                  nope: Optional[torch.Tensor] = None, rope: Optional[torch.Tensor] = None,
-                 clean_logits: bool = False, with_local: bool = False, fused: bool = False):
+                 clean_logits: bool = False, with_local: bool = False, fused=False):
+        if fused is True:
+            fused = ("decode", "prefill")
+        fused = set(fused or ())
         if fused and clean_logits:
             raise ValueError("the fused calls leave the logits past each row's end untouched (no clean_logits)")
         dev = block_table.device
@@ -78,7 +82,8 @@ class IndexerStep:
         self.nope = nope
         self.rope = rope
         self.clean = clean_logits
-        self.fused = fused
+        self.fused_dec = "decode" in fused
+        self.fused_pf = "prefill" in fused
         self.cache = torch.zeros(num_blocks, INDEXER_BLOCK_BYTES, dtype=torch.uint8, device=dev)
         self.dsmla_cache = None
         if nope is not None:
@@ -91,7 +96,7 @@ class IndexerStep:
             self.dec_global = torch.empty(R, topk, **i32)
             self.dec_local = torch.empty(R, topk, **i32) if with_local else None
             self.dec_ws = (torch.zeros(ix_topk_hist_workspace_size(R), dtype=torch.uint8, device=dev)
-                           if fused else None)
+                           if self.fused_dec else None)
         if prefill is not None:
             T = prefill.w.shape[0]
             self.k_fp8 = torch.empty(max(prefill.gathered, 1), HEAD_DIM, dtype=torch.uint8,
@@ -102,7 +107,7 @@ class IndexerStep:
             self.pf_global = torch.empty(T, topk, **i32)
             self.pf_local = torch.empty(T, topk, **i32) if with_local else None
             self.pf_ws = (torch.zeros(ix_topk_hist_workspace_size(T), dtype=torch.uint8, device=dev)
-                          if fused else None)
+                          if self.fused_pf else None)
 
     def write_history(self, k_bf16: torch.Tensor, slots: torch.Tensor, chunk: int = 1 << 20):
         """Fill the indexer-K cache with already-cached positions (set-up, not a step)."""
@@ -144,11 +149,11 @@ class IndexerStep:
             dsmla_quant_write(self.nope, self.rope, self.new_slot, self.dsmla_cache, stream=s)
         if self.decode is not None:
             d = self.decode
-            if self.fused and not split:
+            if self.fused_dec and not split:
                 timed("paged_mqa_logits_topk", lambda: ix_paged_mqa_logits_topk(
                     d.q, d.w, self.cache, d.context_lens, self.block_table, self.dec_logits, self.topk,
                     self.dec_global, self.dec_ws, out_local=self.dec_local, stream=s))
-            elif self.fused:
+            elif self.fused_dec:
                 timed("paged_mqa_logits", lambda: ix_paged_mqa_logits_hist(
                     d.q, d.w, self.cache, d.context_lens, self.block_table, self.dec_logits, self.topk,
                     self.dec_ws, stream=s))
@@ -165,12 +170,12 @@ class IndexerStep:
         if self.prefill is not None:
             p = self.prefill
             ix_gather_k(self.cache, self.pf_bt, p.cu_seq_lens, self.k_fp8, self.k_scale, stream=s)
-            if self.fused and not split:
+            if self.fused_pf and not split:
                 timed("mqa_logits_topk", lambda: ix_mqa_logits_topk(
                     p.q, p.w, self.k_fp8, self.k_scale, p.ks, p.ke, self.pf_logits, p.row_req,
                     self.block_table, self.topk, self.pf_global, self.pf_ws, out_local=self.pf_local,
                     stream=s))
-            elif self.fused:
+            elif self.fused_pf:
                 timed("mqa_logits", lambda: ix_mqa_logits_hist(
                     p.q, p.w, self.k_fp8, self.k_scale, p.ks, p.ke, self.pf_logits, self.topk, self.pf_ws,
                     stream=s))

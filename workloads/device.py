@@ -17,7 +17,7 @@ def _ld(max_len: int) -> int:
 
 
 def make_step(wl: Workload, device="cuda", clean: bool = False, with_local: bool = False,
-              write_history: bool = True, fused: bool = False):
+              write_history: bool = True, fused=False):
     from deepseek_v3_sparse_gb300.step import DecodePart, IndexerStep, PrefillPart
 
     dev = torch.device(device)
