@@ -29,6 +29,12 @@ passage it follows; the definitions are:
   rounded once to f32, reciprocal root and scaling in f32), rotation of the
   interleaved RoPE pairs from a cos/sin table (f32, no fused multiply-add, bf16
   nearest-even), then the same 656-byte entry.
+* ``fused_q``: the query side of the sparse MLA attention -- q_pe rotated as the
+  cache's RoPE values are, then either the bf16 pair or (quantize_mqa) the
+  576-wide MQA query coded to fp8 with one amax/448 scale per (token, head)
+  (vLLM PR #47090 prhub summary: fused_q's quantize_mqa flag).
+* ``quant_q``: the indexer's fp8 query, one amax/448 scale per (token, head),
+  folded into the head weight (a positive scale commutes with the ReLU).
 * ``dsmla_sparse_decode``: the consumer of the global top-k indices -- softmax
   attention of the bf16 query (ql_nope, q_pe) over the dequantised 656-byte
   entries each token's index row names (fp8 NoPE times its tile scale, bf16
@@ -91,7 +97,10 @@ def _load():
                                                      I64, I32, I64, I64]
         lib.oracle_dsmla_sparse_decode.argtypes = [P, P, P, I64, I32, I64, I64, P, I64, I32, I32,
                                                    ctypes.c_double, P, P]
-        for name in ("oracle_dsmla_sparse_decode", "oracle_quant_write_k", "oracle_gather_k", "oracle_paged_mqa_logits",
+        lib.oracle_fused_q.argtypes = [P, P, P, P, I64, I64, I32, I32, P, P, P]
+        lib.oracle_quant_q.argtypes = [P, P, I64, I32, I32, P, P]
+        for name in ("oracle_fused_q", "oracle_quant_q",
+                     "oracle_dsmla_sparse_decode", "oracle_quant_write_k", "oracle_gather_k", "oracle_paged_mqa_logits",
                      "oracle_mqa_logits", "oracle_topk_to_global",
                      "oracle_dsmla_quant_write", "oracle_dsmla_norm_rope_write",
                      "oracle_num_threads"):
@@ -295,3 +304,43 @@ def dsmla_sparse_decode(q_nope_bf16: np.ndarray, q_pe_bf16: np.ndarray, cache: n
                                             entry_stride, _p(idx), T, H, topk, float(sm_scale),
                                             _p(out), _p(lse))
     return out, lse, rc == 0
+
+
+def fused_q(ql_nope_bf16: np.ndarray, q_pe_bf16: np.ndarray, positions: np.ndarray, cos_sin: np.ndarray,
+            quantize_mqa: bool):
+    """ql_nope uint16 [T, H, 512], q_pe uint16 [T, H, 64] (bf16 bits); positions
+    int64 [T]; cos_sin f32 [max_pos, 64].  Returns (out_pe uint16 [T, H, 64] or
+    None, out_mqa uint8 [T, H, 576] or None, out_scale f32 [T, H] or None, ok)."""
+    qn = _c(ql_nope_bf16, np.uint16)
+    qp = _c(q_pe_bf16, np.uint16)
+    pos = _c(positions, np.int64)
+    cs = _c(cos_sin, np.float32)
+    assert qn.ndim == 3 and qn.shape[2] == 512 and qp.shape == qn.shape[:2] + (64,)
+    T, H = qn.shape[:2]
+    assert pos.shape == (T,) and cs.ndim == 2 and cs.shape[1] == 64
+    out_pe = out_mqa = out_scale = None
+    if quantize_mqa:
+        out_mqa = np.zeros((T, H, 576), np.uint8)
+        out_scale = np.zeros((T, H), np.float32)
+    else:
+        out_pe = np.zeros((T, H, 64), np.uint16)
+    dummy8, dummyf, dummy16 = np.zeros(1, np.uint8), np.zeros(1, np.float32), np.zeros(1, np.uint16)
+    rc = _load().oracle_fused_q(_p(qn), _p(qp), _p(pos), _p(cs), cs.shape[0], T, H, int(bool(quantize_mqa)),
+                                _p(dummy16 if out_pe is None else out_pe),
+                                _p(dummy8 if out_mqa is None else out_mqa),
+                                _p(dummyf if out_scale is None else out_scale))
+    return out_pe, out_mqa, out_scale, rc == 0
+
+
+def quant_q(q_bf16: np.ndarray, w: np.ndarray):
+    """q uint16 [T, H, D] (bf16 bits), w f32 [T, H].  Returns (q_fp8 uint8
+    [T, H, D], w_out f32 [T, H])."""
+    q = _c(q_bf16, np.uint16)
+    ww = _c(w, np.float32)
+    assert q.ndim == 3 and ww.shape == q.shape[:2]
+    T, H, D = q.shape
+    out_q = np.zeros((T, H, D), np.uint8)
+    out_w = np.zeros((T, H), np.float32)
+    rc = _load().oracle_quant_q(_p(q), _p(ww), T, H, D, _p(out_q), _p(out_w))
+    _check(rc, "quant_q")
+    return out_q, out_w

@@ -536,6 +536,97 @@ int oracle_dsmla_norm_rope_write(const uint16_t* kv, const uint16_t* pe, const u
 }
 
 /* ------------------------------------------------------------------------- */
+/* Query side: fused_q with quantize_mqa [DSMLA]; the indexer query and head  */
+/* weights [SCORE]; the readings sit with each function                       */
+/* ------------------------------------------------------------------------- */
+
+/* n f32 values coded with one scale: s = max(amax / 448, FLT_MIN) (IEEE f32
+ * division, the indexer-K rule of [SCORE]), codes = enc(x / s) (IEEE f32
+ * division).  Returns s. */
+static float code_vector_div448(const float* x, int n, uint8_t* codes)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    float s = amax / 448.0f;
+    if (!(s >= FLT_MIN)) s = FLT_MIN;
+    for (int i = 0; i < n; ++i) codes[i] = oracle_e4m3_encode(x[i] / s);
+    return s;
+}
+
+/* The MQA query of the sparse MLA attention ([DSMLA]: fused_q's quantize_mqa
+ * flag selects an FP8 MQA query or the BF16 pair (ql_nope, q_pe)).  Readings of
+ * what the page leaves open: per token t and head h,
+ *   q_pe is rotated as the cache's RoPE values are (interleaved pairs; with
+ *   p = positions[t], c = cos_sin[p*64 + i], s = cos_sin[p*64 + 32 + i]:
+ *   r1 = x0*c - x1*s, r2 = x0*s + x1*c in f32, products rounded, then the sum,
+ *   each stored as bf16, nearest with ties to even);
+ *   quantize_mqa == 0: out_pe[t,h] = the 64 rotated bf16 values (ql_nope is
+ *   returned as it came in);
+ *   quantize_mqa != 0: the 576 values [ql_nope (512) | rotated q_pe (64)]
+ *   (each bf16, exact in f32) coded with one scale per (token, head),
+ *   s = max(amax / 448, FLT_MIN), codes = enc(v / s): out_mqa[t,h,576] and
+ *   out_scale[t,h] = s.
+ * A position outside [0, max_pos) skips the token and makes the call return -1. */
+int oracle_fused_q(const uint16_t* ql_nope, const uint16_t* q_pe, const int64_t* positions,
+                   const float* cos_sin, int64_t max_pos, int64_t tokens, int heads, int quantize_mqa,
+                   uint16_t* out_pe, uint8_t* out_mqa, float* out_scale)
+{
+    codec_init();
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int64_t t = 0; t < tokens; ++t) {
+        int64_t p = positions[t];
+        if (p < 0 || p >= max_pos) { bad = 1; continue; }
+        const float* cs = cos_sin + p * 64;
+        for (int h = 0; h < heads; ++h) {
+            const int64_t th = t * heads + h;
+            const uint16_t* x = q_pe + th * 64;
+            uint16_t rot[64];
+            for (int i = 0; i < 32; ++i) {
+                float x0 = bf16_to_f32(x[2 * i]), x1 = bf16_to_f32(x[2 * i + 1]);
+                float c = cs[i], s = cs[32 + i];
+                float a = x0 * c, b = x1 * s, u = x0 * s, w = x1 * c;
+                rot[2 * i] = f32_to_bf16(a - b);
+                rot[2 * i + 1] = f32_to_bf16(u + w);
+            }
+            if (!quantize_mqa) {
+                memcpy(out_pe + th * 64, rot, 128);
+                continue;
+            }
+            float v[576];
+            for (int i = 0; i < 512; ++i) v[i] = bf16_to_f32(ql_nope[th * 512 + i]);
+            for (int i = 0; i < 64; ++i) v[512 + i] = bf16_to_f32(rot[i]);
+            out_scale[th] = code_vector_div448(v, 576, out_mqa + th * 576);
+        }
+    }
+    return bad ? -1 : 0;
+}
+
+/* The indexer's FP8 query and head weights [SCORE]: per token t and head h of
+ * the bf16 query q[t,h,:] (head_dim values), s = max(amax / 448, FLT_MIN),
+ * q_fp8[t,h,:] = enc(q / s), w_out[t,h] = w[t,h] * s (f32 product).  Reading:
+ * the score is sum_h w_h * ReLU((s_h * q_fp8_h) . k); as s_h > 0,
+ * ReLU(s_h * x) = s_h * ReLU(x), so folding s_h into the weight lets the
+ * logits take the fp8 codes as they are. */
+int oracle_quant_q(const uint16_t* q, const float* w, int64_t tokens, int heads, int head_dim,
+                   uint8_t* q_fp8, float* w_out)
+{
+    codec_init();
+    if (head_dim > 1024) return -2;
+#pragma omp parallel for schedule(static)
+    for (int64_t th = 0; th < tokens * heads; ++th) {
+        float v[1024];
+        for (int d = 0; d < head_dim; ++d) v[d] = bf16_to_f32(q[th * head_dim + d]);
+        float s = code_vector_div448(v, head_dim, q_fp8 + th * head_dim);
+        w_out[th] = w[th] * s;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Sparse MLA decode attention over the fp8_ds_mla cache [DSMLA] [ATOM]       */
 /* ------------------------------------------------------------------------- */
 
