@@ -37,6 +37,14 @@ DECODE_BYTES_PER_KEY = 132        # 128 fp8 values + one fp32 scale
 PREFILL_FLOP_PER_PAIR = 2 * 64 * 128
 NORM_ROPE_BYTES_PER_TOKEN = 1024 + 128 + 8 + 8 + 256 + 656  # fused norm/RoPE ds_mla write
 SPARSE_DECODE_ENTRY = 656  # bytes of one fp8_ds_mla entry read by the sparse MLA decode
+# the query side, per query token: dsmla_fused_q with quantize_mqa over 128 heads
+# (1024 + 128 B read, 576 + 4 B written per head; 8 B position + 256 B table row
+# per token) and ix_quant_q over 64 heads (256 + 4 B read, 128 + 4 B written)
+QUERY_BYTES_PER_TOKEN = {
+    "dsmla_fused_q": (128 * (1024 + 128 + 576 + 4) + 8 + 256,
+                      "128 heads x (1152 B bf16 in + 580 B fp8 query and scale out) + 264 B position and table row"),
+    "ix_quant_q": (64 * (256 + 4 + 128 + 4), "64 heads x (260 B in + 132 B out)"),
+}
 
 
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "traffic_mixed_long.txt")
@@ -431,6 +439,42 @@ def gpu_arm(args, world, rank, local):
         if dsix.ix_device_status() != 0:
             raise RuntimeError("device status set by the fused norm/rope write")
 
+    # ---- the query side of the step's query tokens (decode and prefill rows):
+    # dsmla_fused_q with quantize_mqa (128 heads: RoPE, 576-wide fp8 MQA query)
+    # and ix_quant_q (64 indexer heads: fp8 query, folded head weights), each
+    # timed launch by launch with L2 flushed in between.
+    if wl.nope_bf16 is not None:
+        pos = torch.from_numpy(wl.new_positions()).to(dev)
+        T = int(pos.numel())
+        _, table = W.norm_rope_params(int(pos.max()) + 1)
+        qi = W.query_inputs(T, seed=rank)
+        qd = dict(qn=qi.ql_nope.to(dev), qp=qi.q_pe.to(dev), iq=qi.index_q.to(dev), iw=qi.index_w.to(dev),
+                  table=table.to(dev), mqa=torch.empty(T, 128, 576, dtype=torch.uint8, device=dev),
+                  sc=torch.empty(T, 128, dtype=torch.float32, device=dev),
+                  qf=torch.empty(T, 64, 128, dtype=torch.uint8, device=dev),
+                  wo=torch.empty(T, 64, dtype=torch.float32, device=dev))
+        flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+        sink = torch.empty((), dtype=torch.float32, device=dev)
+        calls = {
+            "dsmla_fused_q": lambda: dsix.dsmla_fused_q(qd["qp"], pos, qd["table"], True, ql_nope_bf16=qd["qn"],
+                                                        out_mqa=qd["mqa"], out_scale=qd["sc"], stream=stream),
+            "ix_quant_q": lambda: dsix.ix_quant_q(qd["iq"], qd["iw"], qd["qf"], qd["wo"], stream=stream)}
+        for name, fn in calls.items():
+            for _ in range(3):
+                fn()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+            for a, b in evs:
+                torch.sum(flush, 0, out=sink)
+                a.record(stream)
+                fn()
+                b.record(stream)
+            torch.cuda.synchronize()
+            ms_list = [a.elapsed_time(b) for a, b in evs]
+            next_rows[name] = dict(ms=float(np.mean(ms_list)), spread=spread(ms_list), units=T)
+        del flush, qd
+        if dsix.ix_device_status() != 0:
+            raise RuntimeError("device status set by the query side")
+
     # ---- the consumer of the decode indices: sparse MLA decode attention of the
     # decode tokens (128 heads) over top-k entries of the fp8_ds_mla cache, each
     # token's indices drawn from its own 131072-position context; entries written
@@ -689,6 +733,23 @@ def next_row_cpu_baselines(wl, rows):
         out["dsmla_norm_rope_write"] = {
             "value": n / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"all {n} new tokens into a compact pool, timed whole ({dt:.3f} s)"}
+    if ("dsmla_fused_q" in rows or "ix_quant_q" in rows) and wl.nope_bf16 is not None:
+        pos = wl.new_positions()
+        _, table = W.norm_rope_params(int(pos.max()) + 1)
+        n = 512  # a bounded sample of the step's query tokens
+        qi = W.query_inputs(n, seed=0)
+        t = time.perf_counter()
+        oracle.fused_q(W.bf16_bits(qi.ql_nope), W.bf16_bits(qi.q_pe), pos[:n], table.numpy(), True)
+        dt = time.perf_counter() - t
+        out["dsmla_fused_q"] = {
+            "value": n / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} of the step's {len(pos)} query tokens x 128 heads, quantize_mqa, timed whole ({dt:.3f} s)"}
+        t = time.perf_counter()
+        oracle.quant_q(W.bf16_bits(qi.index_q), qi.index_w.numpy())
+        dt = time.perf_counter() - t
+        out["ix_quant_q"] = {
+            "value": n / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} of the step's {len(pos)} query tokens x 64 heads, timed whole ({dt:.3f} s)"}
     if "dsmla_sparse_decode" in rows and wl.n_decode > 0:
         T = wl.n_decode * wl.next_n
         x = W.sparse_decode_inputs(T, wl.topk, int(wl.context_lens.max()), seed=17)
@@ -831,6 +892,15 @@ def main():
     for n, d in r["next_rows"].items():  # rows beyond the step, timed on their own
         if n == "dsmla_sparse_decode":
             line.setdefault("next_rows", {})[n] = sparse_decode_line(d, pk)
+            continue
+        if n in QUERY_BYTES_PER_TOKEN:
+            per, what = QUERY_BYTES_PER_TOKEN[n]
+            gbs = d["units"] * per / (d["ms"] / 1e3) / 1e9
+            line.setdefault("next_rows", {})[n] = {
+                "ms": d["ms"], **{f"ms_{k}": v for k, v in d["spread"].items()}, "achieved": gbs, "unit": "GB/s",
+                "peak": pk["hbm_gbs"], "frac": gbs / pk["hbm_gbs"], "units": d["units"],
+                "per_unit": f"{per} B per query token ({what})", "bound": "hbm",
+                "l2": "flushed between launches (256 MB read)"}
             continue
         gbs = d["units"] * NORM_ROPE_BYTES_PER_TOKEN / (d["ms"] / 1e3) / 1e9
         line.setdefault("next_rows", {})[n] = {

@@ -24,7 +24,7 @@ __all__ = [
     "DsixError", "load", "ix_status_string", "ix_device_status", "ix_quant_write_k",
     "ix_gather_k", "ix_paged_mqa_logits", "ix_mqa_logits", "ix_topk_to_global",
     "ix_topk_hist_workspace_size", "ix_paged_mqa_logits_topk", "ix_mqa_logits_topk",
-    "ix_paged_mqa_logits_hist", "ix_mqa_logits_hist", "ix_topk_from_hist",
+    "ix_paged_mqa_logits_hist", "ix_mqa_logits_hist", "ix_topk_from_hist", "dsmla_fused_q", "ix_quant_q",
     "dsmla_quant_write", "dsmla_norm_rope_write", "dsmla_sparse_decode",
     "dsmla_sparse_decode_workspace_size", "dsmla_sparse_decode_noalloc", "MLA_HEADS", "LIB_PATH", "HEADS", "HEAD_DIM", "BLOCK_SIZE",
 ]
@@ -67,6 +67,8 @@ _SIGNATURES = {
                                   _I32, _P, ctypes.c_size_t, _P], _I32),
     "ix_mqa_logits_hist": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _P, _I64, _I32, _P,
                             ctypes.c_size_t, _P], _I32),
+    "dsmla_fused_q": ([_P, _P, _P, _P, _I64, _I64, _I32, _I32, _P, _P, _P, _P], _I32),
+    "ix_quant_q": ([_P, _P, _I64, _I32, _I32, _P, _P, _P], _I32),
     "ix_topk_from_hist": ([_P, _I64, _I64, _P, _P, _P, _I64, _I32, _I32, _P, _P, _P, ctypes.c_size_t, _P],
                           _I32),
     "dsmla_quant_write": ([_P, _P, _I64, _P, _P, _I64, _I32, _I64, _I64, _P], _I32),
@@ -401,6 +403,48 @@ def ix_topk_from_hist(logits: torch.Tensor, row_len: torch.Tensor, row_req: torc
         block_table.stride(0), block_size, int(k), _opt(out_local, "out_local", _I32T),
         _dev(out_global, "out_global", _I32T), wp, wb, _stream(stream))
     _check(rc, "ix_topk_from_hist")
+
+
+def dsmla_fused_q(q_pe_bf16: torch.Tensor, positions: torch.Tensor, cos_sin: torch.Tensor,
+                  quantize_mqa: bool, ql_nope_bf16: Optional[torch.Tensor] = None,
+                  out_pe: Optional[torch.Tensor] = None, out_mqa: Optional[torch.Tensor] = None,
+                  out_scale: Optional[torch.Tensor] = None, stream=None) -> None:
+    """q_pe [T, H, 64] bf16; positions [T] int64; cos_sin [max_pos, 64] f32.
+    quantize_mqa: ql_nope [T, H, 512] bf16 -> out_mqa [T, H, 576] fp8/u8 and
+    out_scale [T, H] f32; else out_pe [T, H, 64] bf16 (the rotated q_pe)."""
+    _rows(q_pe_bf16, 0, "q_pe", 64, dim=3)
+    T, H, _ = q_pe_bf16.shape
+    _len(positions, T, "positions")
+    _rows(cos_sin, 0, "cos_sin", 64)
+    if quantize_mqa:
+        _need(ql_nope_bf16 is not None and out_mqa is not None and out_scale is not None,
+              "quantize_mqa: ql_nope, out_mqa and out_scale are required")
+        _need(tuple(ql_nope_bf16.shape) == (T, H, 512), f"ql_nope: shape {tuple(ql_nope_bf16.shape)}")
+        _len(out_mqa, T * H * 576, "out_mqa")
+        _len(out_scale, T * H, "out_scale")
+    else:
+        _need(out_pe is not None, "out_pe is required when quantize_mqa is False")
+        _len(out_pe, T * H * 64, "out_pe")
+    rc = load().dsmla_fused_q(
+        _opt(ql_nope_bf16, "ql_nope", _BF16) if quantize_mqa else None, _dev(q_pe_bf16, "q_pe", _BF16),
+        _dev(positions, "positions", _I64T), _dev(cos_sin, "cos_sin", _F32), cos_sin.shape[0], T, H,
+        int(bool(quantize_mqa)), None if quantize_mqa else _dev(out_pe, "out_pe", _BF16),
+        _dev(out_mqa, "out_mqa", _U8) if quantize_mqa else None,
+        _dev(out_scale, "out_scale", _F32) if quantize_mqa else None, _stream(stream))
+    _check(rc, "dsmla_fused_q")
+
+
+def ix_quant_q(q_bf16: torch.Tensor, w: torch.Tensor, q_fp8: torch.Tensor, w_out: torch.Tensor,
+               stream=None) -> None:
+    """q [T, H, 128] bf16; w [T, H] f32 -> q_fp8 [T, H, 128] fp8/u8, w_out [T, H] f32."""
+    _rows(q_bf16, 0, "q", dim=3)
+    T, H, D = q_bf16.shape
+    _rows(w, T, "w", H)
+    _len(q_fp8, T * H * D, "q_fp8")
+    _len(w_out, T * H, "w_out")
+    rc = load().ix_quant_q(_dev(q_bf16, "q", _BF16), _dev(w, "w", _F32), T, H, D, _dev(q_fp8, "q_fp8", _U8),
+                           _dev(w_out, "w_out", _F32), _stream(stream))
+    _check(rc, "ix_quant_q")
 
 
 def dsmla_quant_write(nope_bf16: torch.Tensor, rope_bf16: torch.Tensor,

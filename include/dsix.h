@@ -428,6 +428,52 @@ IX_API int dsmla_sparse_decode_noalloc(const void* q_nope_bf16, const void* q_pe
                     int heads, int topk, float sm_scale, void* out_bf16, float* lse,
                     ix_stream_t stream);
 
+/*
+ * dsmla_fused_q -- the MQA query of the sparse MLA attention (vLLM PR #47090,
+ * prhub summary: fused_q gains a quantize_mqa flag that selects an FP8 MQA
+ * query or returns the BF16 pair (ql_nope, q_pe)).  The page prints no formula;
+ * this entry point computes, for token t and head h (tokens x heads rows):
+ *   q_pe rotated as dsmla_norm_rope_write rotates the cache's RoPE values
+ *   (interleaved pairs; p = positions[t], c = cos_sin[p*64 + i],
+ *   s = cos_sin[p*64 + 32 + i]; r1 = x0*c - x1*s, r2 = x0*s + x1*c in f32,
+ *   products rounded, then the sum; bf16 nearest-even);
+ *   quantize_mqa == 0: out_pe[t,h,:] = the 64 rotated bf16 values (the pair
+ *   handed on is (ql_nope, out_pe); ql_nope is not read);
+ *   quantize_mqa != 0: the 576 values v = [ql_nope[t,h,:] | rotated q_pe],
+ *   coded with one scale per (token, head): sc = max(amax(|v|) / 448, FLT_MIN)
+ *   (IEEE f32 division), out_mqa[t,h,i] = fp8(v[i] / sc) (IEEE f32 division,
+ *   RNE, satfinite), out_scale[t,h] = sc (out_pe is not written).
+ * A position outside [0, max_pos) sets IX_DEV_BAD_POSITION and the token is
+ * skipped.
+ *   ql_nope_bf16  bf16 [tokens, heads, 512], 16-byte aligned (quantize_mqa only)
+ *   q_pe_bf16     bf16 [tokens, heads, 64], 4-byte aligned
+ *   positions     int64 [tokens];  cos_sin  f32 [max_pos, 64] (32 cosines, then 32 sines)
+ *   out_pe_bf16   bf16 [tokens, heads, 64], 4-byte aligned (quantize_mqa == 0)
+ *   out_mqa_fp8   fp8 [tokens, heads, 576], 16-byte aligned; out_mqa_scale f32
+ *                 [tokens, heads] (quantize_mqa != 0)
+ * heads >= 1 (128 for DeepSeek-V3.2); IX_ERR_NULL / IX_ERR_ALIGN for the
+ * buffers the chosen mode reads or writes.
+ */
+IX_API int dsmla_fused_q(const void* ql_nope_bf16, const void* q_pe_bf16, const int64_t* positions,
+                    const float* cos_sin, int64_t max_pos, int64_t tokens, int heads, int quantize_mqa,
+                    void* out_pe_bf16, uint8_t* out_mqa_fp8, float* out_mqa_scale, ix_stream_t stream);
+
+/*
+ * ix_quant_q -- the indexer's FP8 query and head weights, as the logits entry
+ * points consume them (the indexer score sums w[t,h] * ReLU(q[t,h] . k) with an
+ * fp8 q).  For token t and head h of the bf16 query (head_dim 128):
+ *   sc = max(amax(|q[t,h,:]|) / 448, FLT_MIN) (IEEE f32 division),
+ *   q_fp8[t,h,d] = fp8(q[t,h,d] / sc) (IEEE f32 division, RNE, satfinite),
+ *   w_out[t,h] = w[t,h] * sc (f32 product).
+ * Because sc > 0, ReLU(sc * x) = sc * ReLU(x): the logits of (q_fp8, w_out) are
+ * the logits of the dequantised query sc * q_fp8 with the weight w.
+ *   q_bf16  bf16 [tokens, heads, 128], 16-byte aligned;  w, w_out f32 [tokens, heads]
+ *   q_fp8   fp8 [tokens, heads, 128], 8-byte aligned
+ * heads >= 1 (64 for the indexer); head_dim != 128 returns IX_ERR_UNSUPPORTED.
+ */
+IX_API int ix_quant_q(const void* q_bf16, const float* w, int64_t tokens, int heads, int head_dim,
+                 uint8_t* q_fp8, float* w_out, ix_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

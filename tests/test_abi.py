@@ -38,7 +38,7 @@ def _declared():
 
 def test_exports_match_header(lib):
     names = _declared()
-    assert len(names) == 18
+    assert len(names) == 20
     for n in names:
         assert hasattr(lib, n), n
     out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True,
@@ -181,6 +181,33 @@ def test_fused_topk_host_checks(lib):
     assert t(*targs(ws=None)) == IX_ERR_WORKSPACE
     assert t(*targs(ws=A1)) == IX_ERR_ALIGN
     assert t(*targs(rows=0)) == IX_OK
+
+
+def test_query_side_host_checks(lib):
+    f = lib.dsmla_fused_q
+    args = lambda **kw: [kw.get("qn", A16), kw.get("qp", A16), kw.get("pos", A16), A16, kw.get("max_pos", 8),
+                         kw.get("T", 4), kw.get("H", 128), kw.get("quant", 1), kw.get("pe", A16),
+                         kw.get("mqa", A16), kw.get("sc", A16), None]
+    assert f(*args(T=-1)) == IX_ERR_SHAPE
+    assert f(*args(max_pos=-1)) == IX_ERR_SHAPE
+    assert f(*args(H=0)) == IX_ERR_UNSUPPORTED
+    assert f(*args(qp=None)) == IX_ERR_NULL
+    assert f(*args(qn=None)) == IX_ERR_NULL                 # read when quantising
+    assert f(*args(pe=None, quant=0)) == IX_ERR_NULL
+    assert f(*args(mqa=P(0x10004))) == IX_ERR_ALIGN
+    assert f(*args(qp=P(0x10002))) == IX_ERR_ALIGN
+    assert f(*args(pos=P(0x10004))) == IX_ERR_ALIGN
+    assert f(*args(T=0, qn=None, qp=None, pos=None)) == IX_OK
+    g = lib.ix_quant_q
+    gargs = lambda **kw: [kw.get("q", A16), A16, kw.get("T", 4), kw.get("H", 64), kw.get("D", 128),
+                          kw.get("out", A16), A16, None]
+    assert g(*gargs(T=-1)) == IX_ERR_SHAPE
+    assert g(*gargs(D=64)) == IX_ERR_UNSUPPORTED
+    assert g(*gargs(H=0)) == IX_ERR_UNSUPPORTED
+    assert g(*gargs(q=None)) == IX_ERR_NULL
+    assert g(*gargs(q=P(0x10008))) == IX_ERR_ALIGN
+    assert g(*gargs(out=P(0x10004))) == IX_ERR_ALIGN
+    assert g(*gargs(T=0)) == IX_OK
 
 
 def test_dsmla_host_checks(lib):

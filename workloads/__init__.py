@@ -348,3 +348,31 @@ def sparse_decode_inputs(tokens: int, topk: int, ctx: int, *, seed: int = 0, q_s
     rope = _bf16(torch.randn(n, ROPE_DIM, generator=g))
     return SparseDecodeInputs(q_nope, q_pe, nope, rope, slots.astype(np.int64), indices, num_blocks,
                               1.0 / math.sqrt(192.0))
+
+
+@dataclass
+class QueryInputs:
+    """Inputs of the query side of a step for `tokens` query tokens: the MLA
+    query pair before RoPE (ql_nope, q_pe; 128 heads) and the indexer's bf16
+    query and head weights (64 heads x 128).  Drawn like the cache inputs:
+    N(0,1) with each element scaled by 20 with probability 0.001, in bf16;
+    weights N(0,1)/8 in f32."""
+    ql_nope: torch.Tensor   # bf16 [T, 128, 512]
+    q_pe: torch.Tensor      # bf16 [T, 128, 64]
+    index_q: torch.Tensor   # bf16 [T, 64, 128]
+    index_w: torch.Tensor   # f32 [T, 64]
+
+
+def query_inputs(tokens: int, seed: int = 0) -> QueryInputs:
+    g = torch.Generator().manual_seed(seed + 104729)
+
+    def draw(*shape):
+        x = torch.randn(*shape, generator=g)
+        out = torch.rand(*shape, generator=g) < 0.001
+        return _bf16(torch.where(out, x * 20, x))
+
+    qn = draw(tokens, MLA_HEADS, NOPE_DIM)
+    qp = draw(tokens, MLA_HEADS, ROPE_DIM)
+    iq = draw(tokens, HEADS, HEAD_DIM)
+    iw = torch.randn(tokens, HEADS, generator=g) / 8
+    return QueryInputs(qn, qp, iq, iw)
