@@ -241,14 +241,14 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) 
     return r;
 }
 
-// Walks the flattened (group, tile) units of this CTA.  Groups below `cap`
+// Walks the flattened (group, tile) units of this CTA.  Groups below CAP
 // have their tile counts cached in shared memory.
-template <bool P>
+template <bool P, int CAP>
 struct Cursor {
-    int g, t, ntiles, left, cap;
+    int g, t, ntiles, left;
     __device__ __forceinline__ int tiles_of(const LogitsArgs& a, const int* s_tiles, int gg) const {
         if (gg >= a.num_groups) return 0;
-        return gg < cap ? s_tiles[gg] : group_tiles<P>(a, gg, false);
+        return gg < CAP ? s_tiles[gg] : group_tiles<P>(a, gg, false);
     }
     // Returns true when the next unit starts a new group.  Never walks past
     // the last group: if the unit count and the groups disagree, it stops.
@@ -528,11 +528,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     if (units > 0) {
-        Cursor<P> cur;
+        Cursor<P, C::kSmemGroups> cur;
         cur.g = misc[2];
         cur.t = misc[3];
         cur.left = units;
-        cur.cap = C::kSmemGroups;
         cur.ntiles = cur.tiles_of(a, s_tiles, cur.g);
 
         if (warp == kProducerWarp) {

@@ -46,21 +46,8 @@ struct TopkArgs {
     const float* logits;
     int64_t ld;
     int64_t rows;
-    // row geometry: kRowsGiven (row_len / row_req arrays), kRowsDecode (the
-    // paged logits' rows: context_lens, next_n) or kRowsPrefill (ks / ke, tk;
-    // row_req), each clamped exactly as the logits kernels clamp them
-    int geom;
     const int32_t* row_len;
     const int32_t* row_req;
-    const int32_t* context_lens;
-    int next_n;
-    const int32_t* ks;
-    const int32_t* ke;
-    int64_t tk;
-    // fused path: the rows' first-digit histograms written by the logits kernel
-    // (read and cleared here); nullptr otherwise
-    uint32_t* hist;
-    int* status;
     const int32_t* bt;
     int64_t bt_stride;
     int block_size;
@@ -73,17 +60,35 @@ struct TopkArgs {
 
 enum { kRowsGiven = 0, kRowsDecode = 1, kRowsPrefill = 2 };
 
+// The rows of the selection that follows a histogram logits kernel (a second
+// kernel argument, so the plain top-k kernels keep their own).
+struct RowsArgs {
+    // row geometry: kRowsGiven (row_len / row_req of TopkArgs), kRowsDecode (the
+    // paged logits' rows: context_lens, next_n) or kRowsPrefill (ks / ke, tk;
+    // row_req), each clamped exactly as the logits kernels clamp them
+    int geom;
+    const int32_t* context_lens;
+    int next_n;
+    const int32_t* ks;
+    const int32_t* ke;
+    int64_t tk;
+    // the rows' first-digit histograms written by the logits kernel (read and
+    // cleared here); nullptr for the plain top-k
+    uint32_t* hist;
+    int* status;
+};
+
 // Visible length L (clamped to [0, ld]) and request b of row r.
-__device__ __forceinline__ void row_geom(const TopkArgs& a, int64_t r, int64_t& L, int& b) {
-    if (a.geom == kRowsDecode) {
-        b = static_cast<int>(r / a.next_n);
-        L = static_cast<int64_t>(__ldg(a.context_lens + b)) - a.next_n + 1 + r % a.next_n;
-    } else if (a.geom == kRowsPrefill) {
+__device__ __forceinline__ void row_geom(const TopkArgs& a, const RowsArgs& f, int64_t r, int64_t& L, int& b) {
+    if (f.geom == kRowsDecode) {
+        b = static_cast<int>(r / f.next_n);
+        L = static_cast<int64_t>(__ldg(f.context_lens + b)) - f.next_n + 1 + r % f.next_n;
+    } else if (f.geom == kRowsPrefill) {
         b = __ldg(a.row_req + r);
-        int64_t x0 = __ldg(a.ks + r), x1 = __ldg(a.ke + r);
-        if (x0 < 0 || x1 > a.tk || x1 < x0) {
+        int64_t x0 = __ldg(f.ks + r), x1 = __ldg(f.ke + r);
+        if (x0 < 0 || x1 > f.tk || x1 < x0) {
             x0 = x0 < 0 ? 0 : x0;
-            x1 = x1 > a.tk ? a.tk : x1;
+            x1 = x1 > f.tk ? f.tk : x1;
             if (x1 < x0) x1 = x0;
         }
         L = x1 - x0;
@@ -239,7 +244,7 @@ __device__ __forceinline__ void block_pick(int* h, int nb, int k_rem, int* out, 
 // key min / max and the first histogram pass over all keys are skipped.
 template <int PER, bool HIST>
 __global__ void __launch_bounds__(kThreads, PER <= 4 ? 3 : (PER <= 32 ? 2 : 1))
-    topk_kernel(const TopkArgs a) {
+    topk_kernel(const TopkArgs a, const RowsArgs f) {
     cg::cluster_group cluster = cg::this_cluster();
     const int C = static_cast<int>(cluster.num_blocks());
     const int rank = static_cast<int>(cluster.block_rank());
@@ -268,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, PER <= 4 ? 3 : (PER <= 32 ? 2 : 1))
     for (int64_t r = cid; r < a.rows; r += nclusters) {
         int64_t L;
         int b;
-        row_geom(a, r, L, b);
+        row_geom(a, f, r, L, b);
         if (L <= a.k) {
             for (int i = rank * kThreads + tid; i < a.k; i += C * kThreads)
                 emit(a, r, b, i, i < L ? i : -1);
@@ -312,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, PER <= 4 ? 3 : (PER <= 32 ? 2 : 1))
             // reads (and clears) it and hands the result to every CTA
             if (rank == 0 && warp == 0) {
                 int hr[3];
-                if (!hist_pick(a.hist + r * kHistRowWords, a.k, L, hr) && tid == 0) flag(a.status, IX_DEV_BAD_HIST);
+                if (!hist_pick(f.hist + r * kHistRowWords, a.k, L, hr) && tid == 0) flag(f.status, IX_DEV_BAD_HIST);
                 if ((tid & 31) < 3)
                     for (int j = 0; j < C; ++j) cluster.map_shared_rank(res, j)[tid & 31] = hr[tid & 31];
             }
@@ -858,7 +863,7 @@ __device__ __forceinline__ int warp_excl_scan(int x, int& total) {
     return incl - x;
 }
 
-__global__ void __launch_bounds__(kSelWarps * 32) select_warp_kernel(const TopkArgs a) {
+__global__ void __launch_bounds__(kSelWarps * 32) select_warp_kernel(const TopkArgs a, const RowsArgs f) {
     __shared__ uint32_t s_key[kSelWarps][kSelCap];
     __shared__ uint32_t s_h[kSelWarps][1 << kSelBits];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -868,14 +873,14 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_warp_kernel(const TopkA
     for (int64_t r = static_cast<int64_t>(blockIdx.x) * kSelWarps + warp; r < a.rows; r += nw) {
         int64_t L64;
         int b;
-        row_geom(a, r, L64, b);
+        row_geom(a, f, r, L64, b);
         const int L = static_cast<int>(L64);
         if (L <= a.k) {
             for (int i = lane; i < a.k; i += 32) emit(a, r, b, i, i < L ? i : -1);
             continue;
         }
         int hr[3];
-        if (!hist_pick(a.hist + r * kHistRowWords, a.k, L, hr) && lane == 0) flag(a.status, IX_DEV_BAD_HIST);
+        if (!hist_pick(f.hist + r * kHistRowWords, a.k, L, hr) && lane == 0) flag(f.status, IX_DEV_BAD_HIST);
         uint32_t prefix = static_cast<uint32_t>(hr[0]);
         int take = a.k - hr[1], cnt = hr[2], sh = kDigitShift;
         const float* row = a.logits + r * a.ld;
@@ -969,7 +974,7 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_warp_kernel(const TopkA
             eq0 += eq_tot;
         }
         if (pos0 != a.k) {  // the histogram did not match the row: workspace not cleared before use
-            if (lane == 0) flag(a.status, IX_DEV_BAD_HIST);
+            if (lane == 0) flag(f.status, IX_DEV_BAD_HIST);
             for (int i = pos0 + lane; i < a.k; i += 32) emit(a, r, b, i, -1);
         }
     }
@@ -993,7 +998,7 @@ int cluster_setup() {  // the carve-out attribute, once per device
 }
 
 template <int PER, bool HIST>
-int launch_per(const TopkArgs& a, int C, int64_t clusters, cudaStream_t stream) {
+int launch_per(const TopkArgs& a, const RowsArgs& f, int C, int64_t clusters, cudaStream_t stream) {
     const int st = cluster_setup<PER, HIST>();
     if (st != IX_OK) return st;
     cudaLaunchConfig_t cfg = {};
@@ -1008,7 +1013,7 @@ int launch_per(const TopkArgs& a, int C, int64_t clusters, cudaStream_t stream) 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, topk_kernel<PER, HIST>, a) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, topk_kernel<PER, HIST>, a, f) != cudaSuccess) {
         cudaGetLastError();
         return IX_ERR_CUDA;
     }
@@ -1028,16 +1033,16 @@ int cluster_size(int64_t ld, int64_t rows, int sms, int* slice) {
 }
 
 template <bool HIST>
-int launch_cluster(TopkArgs a, int sms, cudaStream_t s) {
+int launch_cluster(TopkArgs a, const RowsArgs& f, int sms, cudaStream_t s) {
     const int C = cluster_size(a.ld, a.rows, sms, &a.slice);
     const int64_t max_clusters = static_cast<int64_t>(sms) * 3 / C;
     const int64_t clusters = a.rows < max_clusters ? a.rows : max_clusters;
     const int per_needed = (a.slice + kThreads - 1) / kThreads;
-    if (per_needed <= 4) return launch_per<4, HIST>(a, C, clusters, s);
-    if (per_needed <= 8) return launch_per<8, HIST>(a, C, clusters, s);
-    if (per_needed <= 16) return launch_per<16, HIST>(a, C, clusters, s);
-    if (per_needed <= 32) return launch_per<32, HIST>(a, C, clusters, s);
-    return launch_per<64, HIST>(a, C, clusters, s);
+    if (per_needed <= 4) return launch_per<4, HIST>(a, f, C, clusters, s);
+    if (per_needed <= 8) return launch_per<8, HIST>(a, f, C, clusters, s);
+    if (per_needed <= 16) return launch_per<16, HIST>(a, f, C, clusters, s);
+    if (per_needed <= 32) return launch_per<32, HIST>(a, f, C, clusters, s);
+    return launch_per<64, HIST>(a, f, C, clusters, s);
 }
 
 void set_block_size(TopkArgs& a, int block_size) {
@@ -1052,16 +1057,17 @@ int select_after_logits(const SelectRows& q, cudaStream_t s) {
     const int sms = num_sms();
     if (sms <= 0) return IX_ERR_CUDA;
     TopkArgs a{};
+    RowsArgs f{};
     a.logits = q.logits;
     a.ld = q.ld;
     a.rows = q.rows;
-    a.geom = q.row_len ? kRowsGiven : (q.context_lens ? kRowsDecode : kRowsPrefill);
+    f.geom = q.row_len ? kRowsGiven : (q.context_lens ? kRowsDecode : kRowsPrefill);
     a.row_len = q.row_len;
-    a.context_lens = q.context_lens;
-    a.next_n = q.next_n;
-    a.ks = q.ks;
-    a.ke = q.ke;
-    a.tk = q.tk;
+    f.context_lens = q.context_lens;
+    f.next_n = q.next_n;
+    f.ks = q.ks;
+    f.ke = q.ke;
+    f.tk = q.tk;
     a.row_req = q.row_req;
     a.bt = q.block_table;
     a.bt_stride = q.bt_stride;
@@ -1069,18 +1075,18 @@ int select_after_logits(const SelectRows& q, cudaStream_t s) {
     a.k = q.k;
     a.out_local = q.out_local;
     a.out_global = q.out_global;
-    a.hist = q.hist;
-    a.status = q.status;
+    f.hist = q.hist;
+    f.status = q.status;
     if (a.rows == 0) return IX_OK;
     if (a.ld <= kSelMaxLd && a.rows >= 2 * static_cast<int64_t>(sms)) {
         const int64_t cap = static_cast<int64_t>(sms) * 6;  // 6 CTAs of 8 warps per SM
         const unsigned grid = static_cast<unsigned>((a.rows + kSelWarps - 1) / kSelWarps < cap
                                                         ? (a.rows + kSelWarps - 1) / kSelWarps
                                                         : cap);
-        select_warp_kernel<<<grid, kSelWarps * 32, 0, s>>>(a);
+        select_warp_kernel<<<grid, kSelWarps * 32, 0, s>>>(a, f);
         return launch_status();
     }
-    return launch_cluster<true>(a, sms, s);
+    return launch_cluster<true>(a, f, sms, s);
 }
 
 }  // namespace dsix
@@ -1105,7 +1111,6 @@ extern "C" int ix_topk_to_global(const float* logits, int64_t ld, int64_t rows,
     a.logits = logits;
     a.ld = ld;
     a.rows = rows;
-    a.geom = kRowsGiven;
     a.row_len = row_len;
     a.row_req = row_req;
     a.bt = block_table;
@@ -1125,7 +1130,9 @@ extern "C" int ix_topk_to_global(const float* logits, int64_t ld, int64_t rows,
             topk_block_kernel<64><<<grid, kBlkThreads, 0, s>>>(a);
         return launch_status();
     }
-    return launch_cluster<false>(a, sms, s);
+    RowsArgs f{};
+    f.geom = kRowsGiven;
+    return launch_cluster<false>(a, f, sms, s);
 }
 
 extern "C" int ix_topk_from_hist(const float* logits, int64_t ld, int64_t rows, const int32_t* row_len,
