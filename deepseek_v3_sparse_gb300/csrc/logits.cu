@@ -143,8 +143,12 @@ struct LogitsArgs {
     const int32_t* ke;
     int64_t tq;
     int64_t tk;
-    // histogram variant: rows with more than k visible keys add the first radix
-    // digit of each of their logits to hist[row * kHistRowWords ...]
+};
+
+// Histogram variant: rows with more than k visible keys add the first radix
+// digit of each of their logits to hist[row * kHistRowWords ...].  A kernel
+// argument of its own: widening LogitsArgs costs the plain kernels registers.
+struct HistArgs {
     uint32_t* hist;
     int k;
 };
@@ -416,7 +420,7 @@ __device__ __forceinline__ float head_sums_16x256b(uint32_t tbase, const uint64_
 template <bool P, int NN, bool TK>
 __global__ void __launch_bounds__(kThreads, 1)
     logits_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
-                  const LogitsArgs a) {
+                  const LogitsArgs a, const HistArgs hk) {
     using C = Cfg<P, TK>;
     using S = Smem<P, TK>;
     extern __shared__ uint8_t smem_raw[];
@@ -723,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     src[i] = make_uint4(0u, 0u, 0u, 0u);
                 }
                 if (hh ? hw1 : hw0) {
-                    uint32_t* G = a.hist + (hh ? hr1 : hr0) * kHistRowWords;
+                    uint32_t* G = hk.hist + (hh ? hr1 : hr0) * kHistRowWords;
                     uint32_t csum = 0;
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -779,8 +783,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (TK) {
                         hr0 = static_cast<int64_t>(g) * C::kRows + wg;
                         hr1 = hr0 + 4;
-                        hw0 = hr0 < a.tq && rs1[0] - rs0[0] > a.k;
-                        hw1 = hr1 < a.tq && rs1[1] - rs0[1] > a.k;
+                        hw0 = hr0 < a.tq && rs1[0] - rs0[0] > hk.k;
+                        hw1 = hr1 < a.tq && rs1[1] - rs0[1] > hk.k;
                     }
                 }
                 const int s = kbeg + cur.t * kTile + m;  // key index
@@ -860,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint4 v = *src;
                     *src = make_uint4(0u, 0u, 0u, 0u);
                     if (hw[j]) {  // uniform over the CTA
-                        uint32_t* G = a.hist + (hrow0 + j) * kHistRowWords;
+                        uint32_t* G = hk.hist + (hrow0 + j) * kHistRowWords;
                         if (v.x) atomicAdd(G + kHistCoarse + 4 * et, v.x);
                         if (v.y) atomicAdd(G + kHistCoarse + 4 * et + 1, v.y);
                         if (v.z) atomicAdd(G + kHistCoarse + 4 * et + 2, v.z);
@@ -904,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (TK) {
                         hrow0 = static_cast<int64_t>(g) * NN;
 #pragma unroll
-                        for (int j = 0; j < NN; ++j) hw[j] = rs1[j] > a.k;
+                        for (int j = 0; j < NN; ++j) hw[j] = rs1[j] > hk.k;
                     }
                 }
                 const float* wq = sW + ((qi - 1) & 1) * C::kWFloats;
@@ -1020,7 +1024,7 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
 
 template <bool P, int NN, bool TK = false>
 int launch(const CUtensorMap& tmK, const CUtensorMap& tmQ,
-           const LogitsArgs& a, int64_t rows, int clean, cudaStream_t stream) {
+           const LogitsArgs& a, int64_t rows, int clean, cudaStream_t stream, const HistArgs& hk = HistArgs{}) {
     static std::mutex mu;
     static std::vector<char> ready;
     int dev = 0;
@@ -1038,7 +1042,7 @@ int launch(const CUtensorMap& tmK, const CUtensorMap& tmQ,
     const int sms = num_sms();
     if (sms <= 0) return IX_ERR_CUDA;
     if (a.num_groups > 0) {
-        logits_kernel<P, NN, TK><<<sms, kThreads, Smem<P, TK>::kAlloc, stream>>>(tmK, tmQ, a);
+        logits_kernel<P, NN, TK><<<sms, kThreads, Smem<P, TK>::kAlloc, stream>>>(tmK, tmQ, a, hk);
         if (launch_status() != IX_OK) return IX_ERR_CUDA;
     }
     if (clean && rows > 0) {
@@ -1244,10 +1248,9 @@ extern "C" int ix_paged_mqa_logits_hist(const uint8_t* q_fp8, const float* w, co
     chk = paged_prepare(q_fp8, w, cache, num_blocks, context_lens, block_table, bt_stride, batch, next_n, logits,
                         ld, &tmK, &tmQ, &a);
     if (chk != IX_OK) return chk;
-    a.hist = static_cast<uint32_t*>(workspace);
-    a.k = k;
+    const HistArgs hk{static_cast<uint32_t*>(workspace), k};
     cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
-    return next_n == 1 ? launch<true, 1, true>(tmK, tmQ, a, rows, 0, st_) : launch<true, 2, true>(tmK, tmQ, a, rows, 0, st_);
+    return next_n == 1 ? launch<true, 1, true>(tmK, tmQ, a, rows, 0, st_, hk) : launch<true, 2, true>(tmK, tmQ, a, rows, 0, st_, hk);
 }
 
 extern "C" int ix_mqa_logits_hist(const uint8_t* q_fp8, const float* w, const uint8_t* k_fp8,
@@ -1263,9 +1266,8 @@ extern "C" int ix_mqa_logits_hist(const uint8_t* q_fp8, const float* w, const ui
     if (chk != IX_OK) return chk;
     chk = contiguous_prepare(q_fp8, w, k_fp8, k_scale, ks, ke, tq, tk, logits, ld, &tmK, &tmQ, &a);
     if (chk != IX_OK) return chk;
-    a.hist = static_cast<uint32_t*>(workspace);
-    a.k = k;
-    return launch<false, 1, true>(tmK, tmQ, a, tq, 0, reinterpret_cast<cudaStream_t>(stream));
+    const HistArgs hk{static_cast<uint32_t*>(workspace), k};
+    return launch<false, 1, true>(tmK, tmQ, a, tq, 0, reinterpret_cast<cudaStream_t>(stream), hk);
 }
 
 extern "C" int ix_paged_mqa_logits_topk(const uint8_t* q_fp8, const float* w, const uint8_t* cache,
@@ -1288,10 +1290,9 @@ extern "C" int ix_paged_mqa_logits_topk(const uint8_t* q_fp8, const float* w, co
     chk = paged_prepare(q_fp8, w, cache, num_blocks, context_lens, block_table, bt_stride, batch, next_n, logits,
                         ld, &tmK, &tmQ, &a);
     if (chk != IX_OK) return chk;
-    a.hist = static_cast<uint32_t*>(workspace);
-    a.k = k;
+    const HistArgs hk{static_cast<uint32_t*>(workspace), k};
     cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
-    chk = next_n == 1 ? launch<true, 1, true>(tmK, tmQ, a, rows, 0, st_) : launch<true, 2, true>(tmK, tmQ, a, rows, 0, st_);
+    chk = next_n == 1 ? launch<true, 1, true>(tmK, tmQ, a, rows, 0, st_, hk) : launch<true, 2, true>(tmK, tmQ, a, rows, 0, st_, hk);
     if (chk != IX_OK) return chk;
     SelectRows q{};
     q.logits = logits;
@@ -1305,7 +1306,7 @@ extern "C" int ix_paged_mqa_logits_topk(const uint8_t* q_fp8, const float* w, co
     q.k = k;
     q.out_local = out_local;
     q.out_global = out_global;
-    q.hist = a.hist;
+    q.hist = hk.hist;
     q.status = a.status;
     return select_after_logits(q, st_);
 }
@@ -1328,10 +1329,9 @@ extern "C" int ix_mqa_logits_topk(const uint8_t* q_fp8, const float* w, const ui
     if (!row_req || !block_table || !out_global) return IX_ERR_NULL;
     chk = contiguous_prepare(q_fp8, w, k_fp8, k_scale, ks, ke, tq, tk, logits, ld, &tmK, &tmQ, &a);
     if (chk != IX_OK) return chk;
-    a.hist = static_cast<uint32_t*>(workspace);
-    a.k = k;
+    const HistArgs hk{static_cast<uint32_t*>(workspace), k};
     cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
-    chk = launch<false, 1, true>(tmK, tmQ, a, tq, 0, st_);
+    chk = launch<false, 1, true>(tmK, tmQ, a, tq, 0, st_, hk);
     if (chk != IX_OK) return chk;
     SelectRows q{};
     q.logits = logits;
@@ -1347,7 +1347,7 @@ extern "C" int ix_mqa_logits_topk(const uint8_t* q_fp8, const float* w, const ui
     q.k = k;
     q.out_local = out_local;
     q.out_global = out_global;
-    q.hist = a.hist;
+    q.hist = hk.hist;
     q.status = a.status;
     return select_after_logits(q, st_);
 }
