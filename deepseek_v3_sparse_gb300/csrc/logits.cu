@@ -145,13 +145,24 @@ struct LogitsArgs {
     int64_t tk;
 };
 
-// Histogram variant: rows with more than k visible keys add the first radix
-// digit of each of their logits to hist[row * kHistRowWords ...].  A kernel
-// argument of its own: widening LogitsArgs costs the plain kernels registers.
+// Kernel arguments beyond LogitsArgs (an argument of their own: widening
+// LogitsArgs costs the plain kernels registers).
+//   hist, k     histogram variant: rows with more than k visible keys add the
+//               first radix digit of each of their logits to
+//               hist[row * kHistRowWords ...]
+//   group_cost  the schedule's cost of a group beyond its tiles, in tiles: the
+//               work of each CTA is (tiles + group_cost per group started)
+//               split evenly, so CTAs that meet many short groups (the first
+//               rows of a causal chunk) get fewer tiles
 struct HistArgs {
     uint32_t* hist;
     int k;
+    int group_cost;
 };
+
+// Group costs of the schedule (tiles), measured per kernel kind.
+constexpr int kGroupCostPrefill = 2;
+constexpr int kGroupCostDecode = 0;
 
 // ---------------------------------------------------------------------------
 // per-row visible ranges (clamped; report=true records why)
@@ -489,10 +500,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         local += n;
     }
+    // Weighted split: group g costs n(g) + gc tiles of work (gc for a group
+    // with tiles), CTA c takes the weighted range [c W / grid, (c+1) W / grid),
+    // and a weighted position x inside group g maps to its real tile
+    // min(n(g), max(0, x - ws(g) - gc)) (the group's overhead comes first).
+    // u0 / u1 are the CTA's real tile range in the flattened tile list.
+    const int gc = hk.group_cost;
     int U;
     const int excl0 = block_excl_scan(local, scan, &U);
-    const int64_t u0 = static_cast<int64_t>(blockIdx.x) * U / gridDim.x;
-    const int64_t u1 = static_cast<int64_t>(blockIdx.x + 1) * U / gridDim.x;
+    int64_t u0, u1;
+    if (gc == 0) {
+        u0 = static_cast<int64_t>(blockIdx.x) * U / gridDim.x;
+        u1 = static_cast<int64_t>(blockIdx.x + 1) * U / gridDim.x;
+    } else {
+        // weighted costs of this thread's groups, and their total
+        int wlocal = 0;
+        for (int g = threadIdx.x; g < G; g += kThreads) {
+            const int n = g < C::kSmemGroups ? s_tiles[g] : group_tiles<P>(a, g, false);
+            wlocal += n > 0 ? n + gc : 0;
+        }
+        int W;
+        block_excl_scan(wlocal, scan, &W);
+        const int64_t w0 = static_cast<int64_t>(blockIdx.x) * W / gridDim.x;
+        const int64_t w1 = static_cast<int64_t>(blockIdx.x + 1) * W / gridDim.x;
+        if (threadIdx.x == 0) {
+            misc[6] = U;  // real positions of w0 / w1; W maps to U
+            misc[7] = U;
+        }
+        __syncthreads();
+        int wrun = 0, rrun = 0;
+        for (int base = 0; base < G && (wrun <= w0 || wrun <= w1); base += kThreads) {
+            const int g = base + threadIdx.x;
+            const int n = g < G ? (g < C::kSmemGroups ? s_tiles[g] : group_tiles<P>(a, g, false)) : 0;
+            const int wc = n > 0 ? n + gc : 0;
+            int wchunk, rchunk;
+            const int ws = block_excl_scan(wc, scan, &wchunk) + wrun;
+            const int rs = block_excl_scan(n, scan, &rchunk) + rrun;
+            if (wc > 0 && ws <= w0 && w0 < ws + wc) {
+                const int64_t x = w0 - ws - gc;
+                misc[6] = rs + static_cast<int>(x < 0 ? 0 : (x > n ? n : x));
+            }
+            if (wc > 0 && ws <= w1 && w1 < ws + wc) {
+                const int64_t x = w1 - ws - gc;
+                misc[7] = rs + static_cast<int>(x < 0 ? 0 : (x > n ? n : x));
+            }
+            wrun += wchunk;
+            rrun += rchunk;
+        }
+        __syncthreads();
+        u0 = misc[6];
+        u1 = misc[7];
+        __syncthreads();  // misc[6..7] are not rewritten, but misc[2..4] are written below
+    }
     if (G <= kThreads) {
         // one group per thread: the scan above already placed every group
         if (u1 > u0 && local > 0 && excl0 <= u0 && u0 < excl0 + local) {
@@ -1024,7 +1083,8 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
 
 template <bool P, int NN, bool TK = false>
 int launch(const CUtensorMap& tmK, const CUtensorMap& tmQ,
-           const LogitsArgs& a, int64_t rows, int clean, cudaStream_t stream, const HistArgs& hk = HistArgs{}) {
+           const LogitsArgs& a, int64_t rows, int clean, cudaStream_t stream, HistArgs hk = HistArgs{}) {
+    hk.group_cost = P ? kGroupCostDecode : kGroupCostPrefill;
     static std::mutex mu;
     static std::vector<char> ready;
     int dev = 0;
@@ -1248,7 +1308,7 @@ extern "C" int ix_paged_mqa_logits_hist(const uint8_t* q_fp8, const float* w, co
     chk = paged_prepare(q_fp8, w, cache, num_blocks, context_lens, block_table, bt_stride, batch, next_n, logits,
                         ld, &tmK, &tmQ, &a);
     if (chk != IX_OK) return chk;
-    const HistArgs hk{static_cast<uint32_t*>(workspace), k};
+    const HistArgs hk{static_cast<uint32_t*>(workspace), k, 0};
     cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
     return next_n == 1 ? launch<true, 1, true>(tmK, tmQ, a, rows, 0, st_, hk) : launch<true, 2, true>(tmK, tmQ, a, rows, 0, st_, hk);
 }
@@ -1266,7 +1326,7 @@ extern "C" int ix_mqa_logits_hist(const uint8_t* q_fp8, const float* w, const ui
     if (chk != IX_OK) return chk;
     chk = contiguous_prepare(q_fp8, w, k_fp8, k_scale, ks, ke, tq, tk, logits, ld, &tmK, &tmQ, &a);
     if (chk != IX_OK) return chk;
-    const HistArgs hk{static_cast<uint32_t*>(workspace), k};
+    const HistArgs hk{static_cast<uint32_t*>(workspace), k, 0};
     return launch<false, 1, true>(tmK, tmQ, a, tq, 0, reinterpret_cast<cudaStream_t>(stream), hk);
 }
 
@@ -1290,7 +1350,7 @@ extern "C" int ix_paged_mqa_logits_topk(const uint8_t* q_fp8, const float* w, co
     chk = paged_prepare(q_fp8, w, cache, num_blocks, context_lens, block_table, bt_stride, batch, next_n, logits,
                         ld, &tmK, &tmQ, &a);
     if (chk != IX_OK) return chk;
-    const HistArgs hk{static_cast<uint32_t*>(workspace), k};
+    const HistArgs hk{static_cast<uint32_t*>(workspace), k, 0};
     cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
     chk = next_n == 1 ? launch<true, 1, true>(tmK, tmQ, a, rows, 0, st_, hk) : launch<true, 2, true>(tmK, tmQ, a, rows, 0, st_, hk);
     if (chk != IX_OK) return chk;
@@ -1329,7 +1389,7 @@ extern "C" int ix_mqa_logits_topk(const uint8_t* q_fp8, const float* w, const ui
     if (!row_req || !block_table || !out_global) return IX_ERR_NULL;
     chk = contiguous_prepare(q_fp8, w, k_fp8, k_scale, ks, ke, tq, tk, logits, ld, &tmK, &tmQ, &a);
     if (chk != IX_OK) return chk;
-    const HistArgs hk{static_cast<uint32_t*>(workspace), k};
+    const HistArgs hk{static_cast<uint32_t*>(workspace), k, 0};
     cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
     chk = launch<false, 1, true>(tmK, tmQ, a, tq, 0, st_, hk);
     if (chk != IX_OK) return chk;
