@@ -141,3 +141,30 @@ def test_norm_rope_other_block_sizes_and_edge_positions(dsix, bs, entry, extra):
     assert ok
     assert np.array_equal(got, ref), np.argwhere(got != ref)[:5]
     assert dsix.ix_device_status() == 0
+
+
+def test_wide_dynamic_range_tokens_match(dsix):
+    """Tokens whose values span 2^0 down to 2^-60 (squares more than 2^38 apart):
+    the kernel's fixed-point sum of squares cuts squares below 2^-38 of the
+    largest one's binade, the oracle's double sum keeps them while it can; the
+    difference stays far inside one rounding of t = f32(S/512 + eps), so the
+    bytes agree."""
+    n = 64
+    g = torch.Generator().manual_seed(3)
+    exps = torch.arange(512) % 61                       # 2^0 .. 2^-60 across each token
+    mant = 1 + torch.rand(n, 512, generator=g)
+    sign = torch.where(torch.rand(n, 512, generator=g) < 0.5, -1.0, 1.0)
+    kv = (sign * mant * torch.pow(2.0, -exps.float())).to(torch.bfloat16)
+    kv[1] = 0.0
+    kv[1, 0] = 1.0
+    kv[1, 1:] = torch.pow(2.0, -torch.arange(40, 40 + 511).float().clamp(max=120)).to(torch.bfloat16)
+    kv[2] = (torch.pow(2.0, -torch.arange(512).float() % 100) * 3).to(torch.bfloat16)
+    pe = torch.randn(n, 64, generator=g).to(torch.bfloat16)
+    gamma, table = W.norm_rope_params(256, seed=3)
+    pos = np.arange(n, dtype=np.int64)
+    slots = np.arange(n, dtype=np.int64)
+    for eps in (1e-6, 0.0):
+        ok, got, ref = _run_both(dsix, kv, pe, gamma, eps, pos, table, slots, 2, 64, 656, 0)
+        assert ok
+        assert np.array_equal(got, ref), np.argwhere(got != ref)[:5]
+    assert dsix.ix_device_status() == 0
