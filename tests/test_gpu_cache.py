@@ -179,3 +179,51 @@ def test_dsmla_mixed_long_new_tokens(dsix):
     oracle.dsmla_quant_write(W.bf16_bits(wl.nope_bf16), W.bf16_bits(wl.rope_bf16),
                              np.arange(n, dtype=np.int64), dense, 64)
     assert np.array_equal(got, dense.reshape(-1, 656)[:n])
+
+
+def _near_midpoint_tokens(n, seed):
+    """Tokens whose quotients x / scale sit on or next to e4m3 rounding
+    boundaries (midpoints between neighbouring codes, ties to even): token t
+    has amax 448 * s_t, and its other values are bf16 roundings of
+    (midpoint +- a few f32 ulps) * s_t for every normal e4m3 binade."""
+    rng = np.random.default_rng(seed)
+    mids = []
+    for e in range(-6, 9):              # e4m3 normal binades
+        for m in range(8):
+            mids.append((1 + (2 * m + 1) / 16.0) * 2.0 ** e)
+    mids = np.array([v for v in mids if v < 448], np.float64)
+    k = np.zeros((n, 128), np.float32)
+    for t in range(n):
+        # t % 3 == 0: scale exactly 1; == 1: a power of two (quotients land exactly on
+        # midpoints: ties to even); == 2: any scale
+        s = 1.0 if t % 3 == 0 else 2.0 ** rng.integers(-8, 4) * (1.0 if t % 3 == 1 else 1 + rng.random())
+        vals = mids[rng.integers(0, len(mids), 127)] * s * (1 + (rng.integers(-3, 4, 127) * 2.0 ** -24))
+        vals *= np.where(rng.random(127) < 0.5, -1, 1)
+        k[t, 0] = 448.0 * s
+        k[t, 1:] = vals
+    return torch.from_numpy(k).to(torch.bfloat16)
+
+
+def test_quant_write_k_near_rounding_boundaries(dsix):
+    """The codes of quotients on and beside e4m3 midpoints match the oracle's
+    correctly rounded division (the kernels divide by multiplying with the
+    reciprocal except near such boundaries)."""
+    n = 600
+    k = _near_midpoint_tokens(n, 5)
+    slots = np.arange(n, dtype=np.int64)
+    nb = -(-n // 64)
+    cache = torch.zeros(nb, 64 * 132, dtype=torch.uint8, device="cuda")
+    dsix.ix_quant_write_k(k.cuda(), torch.from_numpy(slots).cuda(), cache)
+    torch.cuda.synchronize()
+    ref = np.zeros((nb, 64 * 132), np.uint8)
+    oracle.quant_write_k(W.bf16_bits(k), slots, ref, 64)
+    assert np.array_equal(cache.cpu().numpy(), ref)
+    # the same values through the indexer-query coding (one scale per 128 values)
+    w = torch.ones(n, 1)
+    qf = torch.empty(n, 1, 128, dtype=torch.uint8, device="cuda")
+    wo = torch.empty(n, 1, device="cuda")
+    dsix.ix_quant_q(k.view(n, 1, 128).cuda(), w.cuda(), qf, wo)
+    torch.cuda.synchronize()
+    rq, rw = oracle.quant_q(W.bf16_bits(k.view(n, 1, 128)), w.numpy())
+    assert np.array_equal(qf.cpu().numpy(), rq) and np.array_equal(wo.cpu().numpy(), rw)
+    assert dsix.ix_device_status() == 0
