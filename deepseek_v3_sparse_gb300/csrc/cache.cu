@@ -32,15 +32,13 @@ __device__ __forceinline__ float amax8(const float (&x)[8]) {
     return a;
 }
 
-// The e4m3 codes (RNE, satfinite) of x[i] / scale, the quotient correctly
-// rounded (quot_for_e4m3 gives the same codes); 8 codes packed little-endian
-// into two words.
+// x[i] / scale, correctly rounded, then e4m3 (RNE, satfinite); 8 codes packed
+// little-endian into two words.
 __device__ __forceinline__ uint2 quant8(const float (&x)[8], float scale) {
-    const float r = __frcp_rn(scale);
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-        w[i] = cvt_e4m3x2(quot_for_e4m3(x[2 * i], scale, r), quot_for_e4m3(x[2 * i + 1], scale, r));
+        w[i] = cvt_e4m3x2(__fdiv_rn(x[2 * i], scale), __fdiv_rn(x[2 * i + 1], scale));
     return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }
 

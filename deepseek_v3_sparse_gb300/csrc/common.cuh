@@ -354,23 +354,6 @@ struct SelectRows {
 };
 int select_after_logits(const SelectRows& q, cudaStream_t stream);
 
-// x / s for coding to e4m3: a value whose e4m3 code (round to nearest even,
-// saturating) equals the code of the correctly rounded quotient x / s, given
-// r = 1/s correctly rounded.  The product q = x * r (rounded) lies within 2 f32
-// ulps of the exact quotient, so it codes like the rounded quotient unless one
-// of the two sits on or near an e4m3 rounding boundary: for |q| >= 2^-5 (e4m3
-// normals) the boundaries are the f32 values whose 20 mantissa bits below the 3
-// kept ones read exactly 0x80000.  Within 4 ulps of such a value, and below
-// 2^-5 (the subnormal steps), the correctly rounded division is taken instead.
-__device__ __forceinline__ float quot_for_e4m3(float x, float s, float r) {
-    const float q = __fmul_rn(x, r);
-    const uint32_t b = __float_as_uint(q);
-    const uint32_t m = b & 0xFFFFFu;
-    const uint32_t d = m > 0x80000u ? m - 0x80000u : 0x80000u - m;
-    const bool small = (b & 0x7F800000u) < (122u << 23);
-    return (d <= 4u || small) ? __fdiv_rn(x, s) : q;
-}
-
 __device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xFFFF0000u); }
 

@@ -15,10 +15,7 @@
 // (token, head) for the indexer query (lane holds 8 of the 128 values), 16-byte
 // loads and stores, a shuffle max for amax.  Arithmetic: IEEE f32 products,
 // sums and divisions (no fused multiply-add), bf16 and e4m3 conversions round
-// to nearest even, e4m3 saturates; each value's division by the scale goes
-// through quot_for_e4m3 (a product by the reciprocal, the division itself only
-// near an e4m3 rounding boundary), which gives the codes of the correctly
-// rounded quotient.
+// to nearest even, e4m3 saturates.
 #include <math.h>
 
 #include "common.cuh"
@@ -105,16 +102,15 @@ __global__ void __launch_bounds__(kQThreads) fused_q_kernel(const FusedQArgs a) 
 #pragma unroll
         for (int i = 0; i < 18; ++i) amax = fmaxf(amax, fabsf(x[i]));
         const float sc = scale_of(warp_max(amax));
-        const float rc = __frcp_rn(sc);
         uint32_t code[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            code[i] = cvt_e4m3x2(quot_for_e4m3(x[4 * i], sc, rc), quot_for_e4m3(x[4 * i + 1], sc, rc)) |
-                      (cvt_e4m3x2(quot_for_e4m3(x[4 * i + 2], sc, rc), quot_for_e4m3(x[4 * i + 3], sc, rc)) << 16);
+            code[i] = cvt_e4m3x2(__fdiv_rn(x[4 * i], sc), __fdiv_rn(x[4 * i + 1], sc)) |
+                      (cvt_e4m3x2(__fdiv_rn(x[4 * i + 2], sc), __fdiv_rn(x[4 * i + 3], sc)) << 16);
         uint8_t* dst = a.out_mqa + th * kMqa;
         *reinterpret_cast<uint4*>(dst + 16 * lane) = make_uint4(code[0], code[1], code[2], code[3]);
         *reinterpret_cast<uint16_t*>(dst + kNope + 2 * lane) =
-            static_cast<uint16_t>(cvt_e4m3x2(quot_for_e4m3(x[16], sc, rc), quot_for_e4m3(x[17], sc, rc)));
+            static_cast<uint16_t>(cvt_e4m3x2(__fdiv_rn(x[16], sc), __fdiv_rn(x[17], sc)));
         if (lane == 0) a.out_scale[th] = sc;
     }
 }
@@ -143,12 +139,11 @@ __global__ void __launch_bounds__(kQThreads) quant_q_kernel(const uint4* __restr
 #pragma unroll
         for (int o = 1; o < 16; o <<= 1) u = max(u, __shfl_xor_sync(0xffffffffu, u, o));
         const float sc = scale_of(__uint_as_float(u));
-        const float rc = __frcp_rn(sc);
         if (live) {
-            const uint32_t c0 = cvt_e4m3x2(quot_for_e4m3(x[0], sc, rc), quot_for_e4m3(x[1], sc, rc)) |
-                                (cvt_e4m3x2(quot_for_e4m3(x[2], sc, rc), quot_for_e4m3(x[3], sc, rc)) << 16);
-            const uint32_t c1 = cvt_e4m3x2(quot_for_e4m3(x[4], sc, rc), quot_for_e4m3(x[5], sc, rc)) |
-                                (cvt_e4m3x2(quot_for_e4m3(x[6], sc, rc), quot_for_e4m3(x[7], sc, rc)) << 16);
+            const uint32_t c0 = cvt_e4m3x2(__fdiv_rn(x[0], sc), __fdiv_rn(x[1], sc)) |
+                                (cvt_e4m3x2(__fdiv_rn(x[2], sc), __fdiv_rn(x[3], sc)) << 16);
+            const uint32_t c1 = cvt_e4m3x2(__fdiv_rn(x[4], sc), __fdiv_rn(x[5], sc)) |
+                                (cvt_e4m3x2(__fdiv_rn(x[6], sc), __fdiv_rn(x[7], sc)) << 16);
             q_fp8[th * 16 + hl] = make_uint2(c0, c1);
             if (hl == 0) w_out[th] = __fmul_rn(wt, sc);
         }
