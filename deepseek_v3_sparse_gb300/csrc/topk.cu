@@ -533,11 +533,8 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
     __shared__ uint32_t mm[2][kBlkWarps];
     __shared__ int res[4];
     __shared__ __align__(16) int32_t stage[kBlkStage];
-    __shared__ uint32_t fin[3];  // prefix, shift, k_rem settled over the candidates
-    __shared__ int ccount;       // candidates appended to the stage
     const int tid = threadIdx.x;
     for (int i = tid; i < kBlkBins; i += kBlkThreads) hist[i] = 0;
-    if (tid == 0) ccount = 0;
     __syncthreads();
     int sc = 0;  // alternates the scan scratch so back-to-back scans need no extra barrier
     // A row's length and request are read one row ahead, and its block-table
@@ -714,92 +711,6 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
             prefix = (shift >= 32 ? 0u : (prefix << nbits)) | static_cast<uint32_t>(res[0]);
             shift = sh;
             done = shift == 0 || res[2] == k_rem;
-            if (!done && p == 0 && res[2] <= kBlkStage) {
-                // The first pass left few keys in the threshold digit: they go to
-                // shared memory (the stage is free until the write-out) and one
-                // warp settles the remaining bits over them, 8 at a time, in
-                // place of further block-wide passes.
-                const int lane = tid & 31;
-                uint32_t* cand = reinterpret_cast<uint32_t*>(stage);
-#pragma unroll
-                for (int j = 0; j < PER; ++j) {
-                    const bool m = j < nv && (key[j] >> shift) == prefix;
-                    const unsigned bal = __ballot_sync(0xffffffffu, m);
-                    if (bal) {
-                        const int leader = __ffs(bal) - 1;
-                        int at = 0;
-                        if (lane == leader) at = atomicAdd(&ccount, __popc(bal));
-                        at = __shfl_sync(0xffffffffu, at, leader);
-                        if (m) cand[at + __popc(bal & ((1u << lane) - 1u))] = key[j];
-                    }
-                }
-                __syncthreads();
-                if (tid < 32) {
-                    const int n = min(ccount, kBlkStage);  // the digit's count, res[2]
-                    int cnt = n, kr = k_rem, sh2 = shift;
-                    uint32_t pf = prefix;
-                    while (cnt != kr && sh2 > 0) {
-                        const int nb2 = sh2 < 8 ? sh2 : 8, ns = sh2 - nb2;
-                        const uint32_t msk = (1u << nb2) - 1u;
-                        for (int i = lane; i < n; i += 32) {
-                            const uint32_t kk = cand[i];
-                            if ((kk >> sh2) == pf) atomicAdd(hist + ((kk >> ns) & msk), 1);
-                        }
-                        __syncwarp();
-                        // lane l owns bins 2^nb2 - 1 - 8l - q, q = 0..7 (the top first); the
-                        // crossing lane reads its bins again rather than keep them in registers
-                        const int top = static_cast<int>(msk) - 8 * lane;
-                        int s8 = 0;
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) s8 += top - q >= 0 ? hist[top - q] : 0;
-                        int incl = s8;
-#pragma unroll
-                        for (int o = 1; o < 32; o <<= 1) {
-                            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                            if (lane >= o) incl += y;
-                        }
-                        const unsigned hit = __ballot_sync(0xffffffffu, incl >= kr);
-                        const int f = hit ? __ffs(hit) - 1 : 31;
-                        int dd = 0, ab = 0, cd = 0;
-                        if (lane == f) {
-                            int acc = incl - s8;
-                            for (int q = 0; q < 8; ++q) {
-                                const int cq = top - q >= 0 ? hist[top - q] : 0;
-                                if (acc + cq >= kr || q == 7) {
-                                    dd = top - q;
-                                    ab = acc;
-                                    cd = cq;
-                                    break;
-                                }
-                                acc += cq;
-                            }
-                        }
-                        dd = __shfl_sync(0xffffffffu, dd, f);
-                        ab = __shfl_sync(0xffffffffu, ab, f);
-                        cd = __shfl_sync(0xffffffffu, cd, f);
-                        __syncwarp();
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            if (top - q >= 0) hist[top - q] = 0;
-                        __syncwarp();
-                        pf = (pf << nb2) | static_cast<uint32_t>(dd < 0 ? 0 : dd);
-                        kr -= ab;
-                        cnt = cd;
-                        sh2 = ns;
-                    }
-                    if (lane == 0) {
-                        fin[0] = pf;
-                        fin[1] = static_cast<uint32_t>(sh2);
-                        fin[2] = static_cast<uint32_t>(kr);
-                        ccount = 0;
-                    }
-                }
-                __syncthreads();
-                prefix = fin[0];
-                shift = static_cast<int>(fin[1]);
-                k_rem = static_cast<int>(fin[2]);
-                done = true;
-            }
         }
         // Keys above the threshold bin are all taken; of the keys in it, the
         // first k_rem in index order (all of them when the bin holds exactly k_rem).
