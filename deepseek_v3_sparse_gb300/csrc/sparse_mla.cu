@@ -26,9 +26,8 @@
 // Phase 3  O[128 x 512] = P V into TMEM columns [0, 512) (S has been read by
 //          then): four chunks of 64 keys, V^T tiles [512 dims x 64 keys]
 //          written by the dequantisers, two N = 256 halves per K step.
-// Epilogue O / sum (rounded to bf16) and the split's lse go to the caller's
-//          workspace; a second kernel merges the splits of each (token, head)
-//          into bf16 output.
+// Epilogue O / sum and the split's lse go to the caller's workspace; a second
+//          kernel merges the splits of each (token, head) into bf16 output.
 // Every wait is bounded (IX_DEV_TIMEOUT, then all roles leave; in-flight
 // copies and MMAs are drained before the CTA frees its TMEM and exits).
 #include <cudaTypedefs.h>
@@ -87,7 +86,7 @@ struct SmlaArgs {
     int topk;
     int splits;
     float scale_log2;  // sm_scale * log2(e)
-    uint16_t* ws_o;    // [tokens * splits * 128, 512] bf16: O / row sum of each split
+    float* ws_o;       // [tokens * splits * 128, 512]: O / row sum of each split
     float* ws_lse;     // [tokens * splits * 128]: natural-log sum of exponentials
     int* status;
 };
@@ -500,37 +499,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv = l_used > 0.0f ? 1.0f / l_used : 0.0f;
             const int64_t prow_idx = (t * a.splits + split) * kH + h;
             // Rows leave through shared memory (the V^T region is free once O is
-            // complete) in bf16: each warp stages 32 heads x 64 columns (rows of
-            // 128 bytes padded to 144) and writes them as full 128-byte lines,
-            // 4 rows per store.
-            uint32_t* tile = reinterpret_cast<uint32_t*>(sm) + q4 * (32 * 36);
-            uint16_t* wrow0 = a.ws_o + (prow_idx - lane) * kNope;  // row of this warp's first head
-            for (int cc = 0; cc < kNope / 64; ++cc) {
-                uint32_t r0[32], r1[32];
-                tmem_ld32(trow + cc * 64, r0);
-                tmem_ld32(trow + cc * 64 + 32, r1);
-                tmem_wait_ld(r0);
-                tmem_wait_ld(r1);
-                uint32_t* trow_s = tile + lane * 36;
+            // complete): each warp stages 32 heads x 32 columns (rows padded to
+            // 36 floats) and writes them as full 128-byte lines, 4 rows per store.
+            float* tile = reinterpret_cast<float*>(sm) + q4 * (32 * 36);
+            float* wrow0 = a.ws_o + (prow_idx - lane) * kNope;  // row of this warp's first head
+            for (int cc = 0; cc < kNope / 32; ++cc) {
+                uint32_t r[32];
+                tmem_ld32(trow + cc * 32, r);
+                tmem_wait_ld(r);
 #pragma unroll
-                for (int k = 0; k < 32; k += 8) {
-                    *reinterpret_cast<uint4*>(trow_s + k / 2) =
-                        make_uint4(pack_bf16(__uint_as_float(r0[k]) * inv, __uint_as_float(r0[k + 1]) * inv),
-                                   pack_bf16(__uint_as_float(r0[k + 2]) * inv, __uint_as_float(r0[k + 3]) * inv),
-                                   pack_bf16(__uint_as_float(r0[k + 4]) * inv, __uint_as_float(r0[k + 5]) * inv),
-                                   pack_bf16(__uint_as_float(r0[k + 6]) * inv, __uint_as_float(r0[k + 7]) * inv));
-                    *reinterpret_cast<uint4*>(trow_s + 16 + k / 2) =
-                        make_uint4(pack_bf16(__uint_as_float(r1[k]) * inv, __uint_as_float(r1[k + 1]) * inv),
-                                   pack_bf16(__uint_as_float(r1[k + 2]) * inv, __uint_as_float(r1[k + 3]) * inv),
-                                   pack_bf16(__uint_as_float(r1[k + 4]) * inv, __uint_as_float(r1[k + 5]) * inv),
-                                   pack_bf16(__uint_as_float(r1[k + 6]) * inv, __uint_as_float(r1[k + 7]) * inv));
-                }
+                for (int k = 0; k < 32; k += 4)
+                    *reinterpret_cast<float4*>(tile + lane * 36 + k) =
+                        make_float4(__uint_as_float(r[k]) * inv, __uint_as_float(r[k + 1]) * inv,
+                                    __uint_as_float(r[k + 2]) * inv, __uint_as_float(r[k + 3]) * inv);
                 __syncwarp();
 #pragma unroll
                 for (int it = 0; it < 8; ++it) {
                     const int row = it * 4 + (lane >> 3), j = lane & 7;
-                    *reinterpret_cast<uint4*>(wrow0 + static_cast<int64_t>(row) * kNope + cc * 64 + 8 * j) =
-                        *reinterpret_cast<const uint4*>(tile + row * 36 + 4 * j);
+                    *reinterpret_cast<float4*>(wrow0 + static_cast<int64_t>(row) * kNope + cc * 32 + 4 * j) =
+                        *reinterpret_cast<const float4*>(tile + row * 36 + 4 * j);
                 }
                 __syncwarp();
             }
@@ -556,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kCombineWarps = 8;
 
 __global__ void __launch_bounds__(kCombineWarps * 32)
-    smla_combine_kernel(const uint16_t* __restrict__ ws_o, const float* __restrict__ ws_lse, int64_t rows,
+    smla_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse, int64_t rows,
                         int splits, uint16_t* __restrict__ out, float* __restrict__ lse) {
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -587,12 +574,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
                     const int64_t pr = (t * splits + s) * kH + h;
                     const float ls = __ldg(ws_lse + pr);
                     w[j] = ls == -INFINITY ? 0.0f : expf(ls - M);
-                    const uint2* src = reinterpret_cast<const uint2*>(ws_o + pr * kNope);
+                    const float4* src = reinterpret_cast<const float4*>(ws_o + pr * kNope);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint2 u = __ldg(src + lane + 32 * q);
-                        v[j][q] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
-                    }
+                    for (int q = 0; q < 4; ++q) v[j][q] = __ldg(src + lane + 32 * q);
                 }
             }
 #pragma unroll
@@ -619,10 +603,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 
 // File-scope scratch of dsmla_sparse_decode_noalloc: room for the split
 // outputs of kStaticSplits (token, split) pairs -- a decode batch of 16 tokens
-// at top-2048 -- 16.8 MB of device memory (bf16 outputs, f32 lse), placed
-// when this module loads.
+// at top-2048 -- 33.6 MB of device memory, placed when this module loads.
 constexpr int64_t kStaticSplits = 128;
-static __device__ __align__(256) uint8_t g_smla_scratch[kStaticSplits * kH * (kNope * 2 + 4)];
+static __device__ __align__(256) float g_smla_scratch[kStaticSplits * kH * (kNope + 1)];
 
 // ---------------------------------------------------------------------------
 // host side
@@ -680,7 +663,7 @@ using namespace dsix;
 extern "C" size_t dsmla_sparse_decode_workspace_size(int64_t tokens, int heads, int topk) {
     if (tokens <= 0 || heads <= 0 || topk <= 0) return 0;
     const int64_t splits = (static_cast<int64_t>(topk) + kSplit - 1) / kSplit;
-    return static_cast<size_t>(tokens * splits * heads) * (kNope * sizeof(uint16_t) + sizeof(float));
+    return static_cast<size_t>(tokens * splits * heads) * (kNope + 1) * sizeof(float);
 }
 
 namespace dsix {
@@ -747,8 +730,8 @@ extern "C" int dsmla_sparse_decode(const void* q_nope_bf16, const void* q_pe_bf1
     a.topk = topk;
     a.splits = splits;
     a.scale_log2 = sm_scale * 1.4426950408889634f;
-    a.ws_o = static_cast<uint16_t*>(workspace);
-    a.ws_lse = reinterpret_cast<float*>(a.ws_o + prow * kNope);
+    a.ws_o = static_cast<float*>(workspace);
+    a.ws_lse = a.ws_o + prow * kNope;
     a.status = status;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     smla_decode_kernel<<<static_cast<unsigned>(tokens * splits), kThreads, kSmemAlloc, s>>>(tmQn, tmQp, a);

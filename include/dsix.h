@@ -365,9 +365,7 @@ IX_API int dsmla_norm_rope_write(const void* kv_bf16, const void* pe_bf16, const
  * none.  Duplicate indices count once each.
  * Arithmetic: keys and values are dequantised to bf16 (f32 product, then
  * nearest-even), both products run on the tensor cores in bf16 with f32
- * accumulation, the softmax weights are rounded to bf16, each split's
- * normalised output (256 indices per split) to bf16 before the splits are
- * merged in f32, and the output to bf16.
+ * accumulation, the softmax weights are rounded to bf16, the output to bf16.
  *   q_nope_bf16  bf16 [tokens, heads, 512], contiguous, 16-byte aligned
  *   q_pe_bf16    bf16 [tokens, heads, 64], contiguous, 16-byte aligned
  *   cache        fp8_ds_mla entries (see dsmla_quant_write), 16-byte aligned;
@@ -380,7 +378,7 @@ IX_API int dsmla_norm_rope_write(const void* kv_bf16, const void* pe_bf16, const
  *   lse          f32 [tokens, heads] (written)
  *   workspace    16-byte aligned device scratch of at least
  *                dsmla_sparse_decode_workspace_size(tokens, heads, topk) bytes
- *                (per split of 256 indices: its normalised bf16 output and f32 lse);
+ *                (per split of 256 indices: its normalised output and lse);
  *                IX_ERR_WORKSPACE if missing or smaller.  Owned by the caller,
  *                in use until the call's work on `stream` completes.
  * Errors, checked on the host in this order before anything is launched:
