@@ -231,3 +231,26 @@ def test_decode_mtp2(dsix):
 def test_decode_mixed_long(dsix):
     wl = W.mixed_long()
     _decode_both(dsix, wl, [0, 9, 15])
+
+
+def test_prefill_long_rows_cluster_path_and_periodic_handoff(dsix):
+    """Prefill rows longer than 32768 keys: the histogram variant hands each
+    row's shared-memory counts off every 256 tiles (so no 16-bit counter
+    overflows), and with few rows the selection runs the cluster kernel from
+    the histograms.  A row of equal logits (zero query) holds all its keys in
+    one digit."""
+    tq, tk, topk = 24, 70000, 2048
+    q, k, ksc, w = _prefill_inputs(tq, tk, seed=101, zero_q_rows=(3,), dup_keys=5)
+    rng = np.random.default_rng(7)
+    ks = np.zeros(tq, np.int32)
+    ke = rng.integers(30000, tk + 1, tq).astype(np.int32)
+    ke[0] = tk                           # the longest row (70000 keys: 547 tiles, two hand-offs)
+    ke[1] = topk                         # L = k: no histogram
+    ke[2] = topk + 1
+    ke[3] = tk
+    ld = 70000
+    req = np.zeros(tq, np.int32)
+    bt = np.random.default_rng(3).permutation(1100).reshape(1, 1100).astype(np.int32)
+    o = _run_prefill_both(dsix, q, k, ksc, w, ks, ke, req, bt, topk, ld)
+    _oracle_exact(o["lg_f"], o["lens"], req, bt, topk, o["loc_f"], o["glb_f"], np.arange(tq))
+    assert np.array_equal(o["loc_f"][3], np.arange(topk))
