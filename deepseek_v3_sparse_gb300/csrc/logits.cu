@@ -600,7 +600,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == kProducerWarp) {
             // ------------------------------------------------------------ producer
             // The whole warp walks the loop; one lane, elected once, issues the copies.
+            // Paged K tiles are read once per launch: they go through L2 as
+            // evict-first lines, so the stream does not force out (and write back)
+            // lines that earlier work left dirty there.
             const bool leader = elect_one();
+            const uint64_t stream_policy = P ? l2_evict_first_policy() : 0;
             int it = 0, qi = 0;
             int kbeg = 0, kend = 0;
             // decode: lane l holds the block-table entry of block 2 * bt_base + l (16
@@ -662,8 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool two = (2 * cur.t + 1) * kBlk < kend;
                     if (leader) {
                         mbar_arrive_expect_tx(full + stage, two ? kTileBytes : kTileBytes / 2);
-                        tma_load_3d(kdst, &tmK, full + stage, 0, 0, blk0);
-                        if (two) tma_load_3d(kdst + kTileBytes / 2, &tmK, full + stage, 0, 0, blk1);
+                        tma_load_3d_hint(kdst, &tmK, full + stage, 0, 0, blk0, stream_policy);
+                        if (two) tma_load_3d_hint(kdst + kTileBytes / 2, &tmK, full + stage, 0, 0, blk1, stream_policy);
                     }
                 } else {
                     const int start = kbeg + cur.t * kTile;
