@@ -19,7 +19,9 @@
 //   warps 10-13 softmax and epilogue, one thread per head (= TMEM lane)
 // Phase 1  S[128 heads x 256 keys] = Q K^T (tcgen05 kind::f16, M 128, N 256)
 //          into TMEM columns [0, 256), over nine 64-dim chunks (the RoPE
-//          chunk, then eight NoPE chunks), two stages.
+//          chunk, then eight NoPE chunks), two stages; the gathered codes
+//          run ahead by cp.async into a ring in the space of the V^T
+//          tiles and P, both free until S is complete.
 // Phase 2  the softmax threads read their row of S twice (max, then
 //          exponentials), write P in bf16 as the A operand of the next product
 //          and keep the row sums.
@@ -61,18 +63,21 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s
 constexpr int kQBytes = kH * 128;                 // one 64-dim query chunk (16 KB)
 constexpr int kKBytes = kSplit * 128;             // one 64-dim key chunk (32 KB)
 constexpr int kStage1 = kQBytes + kKBytes;        // phase-1 stage (48 KB)
+constexpr int kP1Stages = 2;                      // phase-1 stages (query chunk + bf16 key chunk)
+constexpr int kRing = 6;                          // phase-1 chunks of gathered codes in flight
+constexpr int kRingOff = kP1Stages * kStage1;     // [kRing][256 keys x 64 codes], in the V^T and P space
 constexpr int kVtBytes = kNope * 128;             // V^T tile: 512 rows x 64 keys (64 KB)
-constexpr int kRegion = 2 * kVtBytes;             // both phase-1 stages, later both V^T stages
+constexpr int kRegion = 2 * kVtBytes;             // phase-1 stages 0-1, later both V^T stages
 constexpr int kPOff = kRegion;                    // P: 4 tiles of 128 rows x 64 keys
 constexpr int kPAtom = kH * 128;
 constexpr int kOffOff = kPOff + kKeyChunks * kPAtom;  // int64 entry offset per key (-1: none)
 constexpr int kMaskOff = kOffOff + kSplit * 8;        // validity bits of the 256 keys
 constexpr int kBarOff = kMaskOff + 64;
-constexpr int kNumBars = 12;
+constexpr int kNumBars = 2 * kP1Stages + 8;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;      // tmem base, abort flag, never-raised flag
 constexpr int kSmemUsed = kMiscOff + 64;
 constexpr int kSmemAlloc = kSmemUsed + 1024;
-static_assert(2 * kStage1 <= kRegion, "phase-1 stages fit the shared region");
+static_assert(kRingOff + kRing * kSplit * 64 <= kOffOff, "phase-1 stages and code ring fit the V^T region and P");
 static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
 
 struct SmlaArgs {
@@ -128,6 +133,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return r;
 }
 
+// 2^x by the hardware's approximate exponential; results below 2^-126 are
+// flushed to zero.
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 // Two e4m3 codes (low byte = first) -> their exact values as f32.
 __device__ __forceinline__ void e4m3x2_to_f32(uint32_t two, float& lo, float& hi) {
     uint32_t h2;
@@ -167,14 +180,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t* koff = reinterpret_cast<int64_t*>(sm + kOffOff);
     uint32_t* vmask = reinterpret_cast<uint32_t*>(sm + kMaskOff);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBarOff);
-    uint64_t* full1 = bars;       // [2] query chunk landed + key chunk written
-    uint64_t* empty1 = bars + 2;  // [2] the MMAs of a phase-1 stage are done
-    uint64_t* s_full = bars + 4;  // all of S is in TMEM (phase-1 MMAs done)
-    uint64_t* p_full = bars + 5;  // P written, S read (128 softmax threads)
-    uint64_t* full3 = bars + 6;   // [2] V^T chunk written
-    uint64_t* empty3 = bars + 8;  // [2] the MMAs of a V^T stage are done
-    uint64_t* o_full = bars + 10; // O complete in TMEM
-    uint64_t* mma_done = bars + 11;
+    uint64_t* full1 = bars;                   // [kP1Stages] query chunk landed + key chunk written
+    uint64_t* empty1 = bars + kP1Stages;      // [kP1Stages] the MMAs of a phase-1 stage are done
+    uint64_t* s_full = empty1 + kP1Stages;    // all of S is in TMEM (phase-1 MMAs done)
+    uint64_t* p_full = s_full + 1;            // P written, S read (128 softmax threads)
+    uint64_t* full3 = s_full + 2;             // [2] V^T chunk written
+    uint64_t* empty3 = s_full + 4;            // [2] the MMAs of a V^T stage are done
+    uint64_t* o_full = s_full + 6;            // O complete in TMEM
+    uint64_t* mma_done = s_full + 7;
     int* misc = reinterpret_cast<int*>(sm + kMiscOff);
     volatile int* abort_flag = misc + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -182,9 +195,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int split = static_cast<int>(blockIdx.x % a.splits);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kP1Stages; ++i) {
             mbar_init(full1 + i, 1 + kDeqThreads);
             mbar_init(empty1 + i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(full3 + i, kDeqThreads);
             mbar_init(empty3 + i, 1);
         }
@@ -235,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool leader = elect_one();
         int c = 0;
         for (; c < kChunks; ++c) {
-            const int stage = c & 1, use = c >> 1;
+            const int stage = c % kP1Stages, use = c / kP1Stages;
             if (use > 0 && !wait_warp(empty1 + stage, (use - 1) & 1, abort_flag, a.status)) break;
             if (leader) {
                 uint8_t* qdst = sm + stage * kStage1;
@@ -249,7 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // drain: the last copies issued must land before the CTA exits
         if (leader)
-            for (int i = c > 2 ? c - 2 : 0; i < c; ++i) drain_wait(full1 + (i & 1), (i >> 1) & 1, misc + 2, a.status);
+            for (int i = c > kP1Stages ? c - kP1Stages : 0; i < c; ++i)
+                drain_wait(full1 + i % kP1Stages, (i / kP1Stages) & 1, misc + 2, a.status);
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
@@ -257,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t kId = idesc_bf16_f32(kH, 256);
         bool ok = true, issued = false;
         for (int c = 0; c < kChunks; ++c) {
-            const int stage = c & 1;
-            if (!wait_warp(full1 + stage, (c >> 1) & 1, abort_flag, a.status)) {
+            const int stage = c % kP1Stages;
+            if (!wait_warp(full1 + stage, (c / kP1Stages) & 1, abort_flag, a.status)) {
                 ok = false;
                 break;
             }
@@ -316,11 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
             // phase 1: four threads per key -- thread i covers keys 64 p + i / 4
             // (p = 0..3) and, of each 64-dim chunk, the 16 dims 16 (i % 4) ..,
-            // i.e. two 16-byte pieces of the key's 128-byte operand row.  A warp
-            // load then reads 8 keys x 64 contiguous bytes.  Chunk 0 is the RoPE
-            // part (a plain copy), chunks 1-8 the NoPE codes times their tile
-            // scale.  The NoPE loads run two chunks ahead of the conversion.  A
-            // key without an entry keeps zero codes and a zero scale.
+            // i.e. two 16-byte pieces of the key's 128-byte operand row.  The
+            // codes travel by cp.async (16 bytes per key and chunk, no register
+            // round trip) into a ring of kRing chunks, so up to kRing chunks of
+            // gathered codes are in flight per CTA; a thread converts only the
+            // bytes it copied itself.  Chunk 0 is the RoPE part, copied as stored
+            // straight into its place in stage 0's tile; chunks 1-8 are the NoPE
+            // codes times their tile scale.  A key without an entry gives zeros.
             const int qtr = i & 3, kb = i >> 2;
             const uint8_t* ent[4];
             bool valid[4];
@@ -330,24 +348,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 valid[p] = off >= 0;
                 ent[p] = a.cache + (valid[p] ? off : 0);
             }
-            uint4 o[8], ra[4], rb[4];
-            float sa[4], sb[4];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) o[q] = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                ra[p] = rb[p] = make_uint4(0u, 0u, 0u, 0u);
-                sa[p] = sb[p] = 0.0f;
-            }
-            auto load_nope = [&](int n, uint4(&r)[4], float(&sc)[4]) {  // NoPE dims 64 n + 16 qtr ..
+            uint4* ring = reinterpret_cast<uint4*>(sm + kRingOff);  // [kRing][4 keys][256 threads]
+            {
+                uint8_t* kt = sm + kQBytes;  // stage 0, first use
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
+                    const int row = p * 64 + kb;
+                    uint8_t* d0 = kt + row * 128 + (((2 * qtr) ^ (row & 7)) << 4);
+                    uint8_t* d1 = kt + row * 128 + (((2 * qtr + 1) ^ (row & 7)) << 4);
                     if (valid[p]) {
-                        r[p] = __ldg(reinterpret_cast<const uint4*>(ent[p] + n * 64 + qtr * 16));
-                        sc[p] = __ldg(reinterpret_cast<const float*>(ent[p] + kNope) + (n >> 1));
+                        const uint8_t* rope = ent[p] + kNope + 16 + qtr * 32;
+                        cp_async16(d0, rope);
+                        cp_async16(d1, rope + 16);
+                    } else {
+                        *reinterpret_cast<uint4*>(d0) = make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4*>(d1) = make_uint4(0u, 0u, 0u, 0u);
                     }
                 }
+                cp_async_commit();
+            }
+            auto fetch = [&](int n) {  // NoPE chunk n's codes -> ring slot n % kRing (one group, maybe empty)
+                if (n < 8) {
+#pragma unroll
+                    for (int p = 0; p < 4; ++p)
+                        if (valid[p]) cp_async16(ring + ((n % kRing) * 4 + p) * 256 + i, ent[p] + n * 64 + qtr * 16);
+                }
+                cp_async_commit();
             };
+#pragma unroll
+            for (int n = 0; n < kRing; ++n) fetch(n);
+            float4 sc[4];  // the four tile scales of each key
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+                sc[p] = valid[p] ? __ldg(reinterpret_cast<const float4*>(ent[p] + kNope)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            uint4 o[8];
             auto put_rows = [&](int stage) {
                 uint8_t* kt = sm + stage * kStage1 + kQBytes;
 #pragma unroll
@@ -360,36 +394,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async();
                 mbar_arrive(full1 + stage);
             };
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                if (valid[p]) {
-                    const uint4* rope = reinterpret_cast<const uint4*>(ent[p] + kNope + 16 + qtr * 32);
-                    o[2 * p] = __ldg(rope);
-                    o[2 * p + 1] = __ldg(rope + 1);
-                }
-            }
-            load_nope(0, ra, sa);
-            load_nope(1, rb, sb);
-            put_rows(0);  // chunk 0: stage 0, first use
-            auto nope_step = [&](uint4(&r)[4], float(&sc)[4], int n) -> bool {
-                const int c = n + 1, stage = c & 1, use = c >> 1;
+            // chunk 0: its copies are the oldest group
+            cp_async_wait<kRing>();
+            fence_proxy_async();
+            mbar_arrive(full1 + 0);
+            for (int n = 0; n < 8 && ok; ++n) {
+                const int c = n + 1, stage = c % kP1Stages, use = c / kP1Stages;
+                cp_async_wait<kRing - 1>();  // this thread's copies of chunk n have landed
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
-                    const uint2 a0 = deq4(r[p].x, sc[p]), a1 = deq4(r[p].y, sc[p]), a2 = deq4(r[p].z, sc[p]),
-                                a3 = deq4(r[p].w, sc[p]);
+                    const float s4 = (n >> 1) == 0 ? sc[p].x : (n >> 1) == 1 ? sc[p].y : (n >> 1) == 2 ? sc[p].z : sc[p].w;
+                    uint4 r = make_uint4(0u, 0u, 0u, 0u);
+                    if (valid[p]) r = ring[((n % kRing) * 4 + p) * 256 + i];
+                    const uint2 a0 = deq4(r.x, s4), a1 = deq4(r.y, s4), a2 = deq4(r.z, s4), a3 = deq4(r.w, s4);
                     o[2 * p] = make_uint4(a0.x, a0.y, a1.x, a1.y);
                     o[2 * p + 1] = make_uint4(a2.x, a2.y, a3.x, a3.y);
                 }
-                if (n + 2 < 8) load_nope(n + 2, r, sc);
-                if (use > 0 && !wait_warp(empty1 + stage, (use - 1) & 1, abort_flag, a.status)) return false;
+                // the slot's codes are in registers (the dependency below orders the
+                // shared loads before the refill's copies)
+                asm volatile("" ::"r"(o[0].x), "r"(o[2].x), "r"(o[4].x), "r"(o[6].x) : "memory");
+                fetch(n + kRing);
+                if (use > 0 && !wait_warp(empty1 + stage, (use - 1) & 1, abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
                 put_rows(stage);
-                return true;
-            };
-#pragma unroll
-            for (int n = 0; n < 8; n += 2) {
-                if (ok) ok = nope_step(ra, sa, n);
-                if (ok) ok = nope_step(rb, sb, n + 1);
             }
+            cp_async_wait_all();  // nothing of phase 1 lands in shared memory after this point
         }
         // phase 3: V^T tiles; thread i covers 8 keys (g) x 16 dims (e) of a
         // 64-key chunk.  Chunk 0's codes are loaded before the wait for S, and
@@ -399,12 +430,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // phase-1 MMA has read it (s_full).
         const int g = i & 7, e = i >> 3;
         uint32_t wa[8][4];
+        float sc[8];  // tile scales of the 8 keys, loaded with their codes
         auto load_v = [&](int kc, uint32_t(&w)[8][4]) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const int64_t ko = koff[kc * 64 + g * 8 + kk];
                 uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (ko >= 0) v = __ldg(reinterpret_cast<const uint4*>(a.cache + ko + e * 16));
+                sc[kk] = 0.0f;
+                if (ko >= 0) {
+                    v = __ldg(reinterpret_cast<const uint4*>(a.cache + ko + e * 16));
+                    sc[kk] = __ldg(reinterpret_cast<const float*>(a.cache + ko + kNope) + (e >> 3));
+                }
                 w[kk][0] = v.x;
                 w[kk][1] = v.y;
                 w[kk][2] = v.z;
@@ -413,12 +449,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         auto put_v = [&](int kc, const uint32_t(&w)[8][4]) -> bool {
             const int stage = kc & 1, use = kc >> 1;
-            float sc[8];  // tile scales of the 8 keys (same entries as the codes: L1/L2 hits)
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const int64_t ko = koff[kc * 64 + g * 8 + kk];
-                sc[kk] = ko >= 0 ? __ldg(reinterpret_cast<const float*>(a.cache + ko + kNope) + (e >> 3)) : 0.0f;
-            }
             if (use > 0 && !wait_warp(empty3 + stage, (use - 1) & 1, abort_flag, a.status)) return false;
             uint8_t* vt = sm + stage * kVtBytes;
 #pragma unroll
@@ -453,18 +483,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = wait_warp(s_full, 0, abort_flag, a.status);
         if (ok) {
             tc_fence_after();
-            for (int cc = 0; cc < kSplit / 32; ++cc) {
-                uint32_t r[32];
-                tmem_ld32(trow + cc * 32, r);
-                tmem_wait_ld(r);
-                const uint32_t vm = vmask[cc];
+            // pass 1: row max over the keys with an entry, two TMEM chunks per wait
+            for (int cc = 0; cc < kSplit / 32; cc += 2) {
+                uint32_t r0[32], r1[32];
+                tmem_ld32(trow + cc * 32, r0);
+                tmem_ld32(trow + (cc + 1) * 32, r1);
+                tmem_wait_ld(r0);
+                tmem_wait_ld(r1);
+                const uint32_t v0 = vmask[cc], v1 = vmask[cc + 1];
+                if ((v0 & v1) == 0xffffffffu) {
+                    float m0 = m, m1 = -INFINITY;
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    if ((vm >> k) & 1u) m = fmaxf(m, __uint_as_float(r[k]));
+                    for (int k = 0; k < 32; k += 2) {
+                        m0 = fmaxf(m0, fmaxf(__uint_as_float(r0[k]), __uint_as_float(r0[k + 1])));
+                        m1 = fmaxf(m1, fmaxf(__uint_as_float(r1[k]), __uint_as_float(r1[k + 1])));
+                    }
+                    m = fmaxf(m0, m1);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        if ((v0 >> k) & 1u) m = fmaxf(m, __uint_as_float(r0[k]));
+                        if ((v1 >> k) & 1u) m = fmaxf(m, __uint_as_float(r1[k]));
+                    }
+                }
             }
             // sm_scale > 0, so the max of the scaled scores is the scaled max
             mc = m == -INFINITY ? 0.0f : m * a.scale_log2;
             uint8_t* prow = sm + kPOff + h * 128;
+            // pass 2: P = 2^(s scale_log2 - mc) in bf16 (exponentials below 2^-126
+            // flush to zero: far below the row's largest term, which is 1), the
+            // row sums of the exact and of the rounded values in two partial sums each
+            float le[2] = {0.0f, 0.0f}, lu[2] = {0.0f, 0.0f};
             for (int cc = 0; cc < kSplit / 32; ++cc) {
                 uint32_t r[32];
                 tmem_ld32(trow + cc * 32, r);
@@ -473,12 +522,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t pk[16];
 #pragma unroll
                 for (int k = 0; k < 32; k += 2) {
-                    const float p0 = ((vm >> k) & 1u) ? exp2f(fmaf(__uint_as_float(r[k]), a.scale_log2, -mc)) : 0.0f;
-                    const float p1 =
-                        ((vm >> (k + 1)) & 1u) ? exp2f(fmaf(__uint_as_float(r[k + 1]), a.scale_log2, -mc)) : 0.0f;
-                    l_exact += p0 + p1;
+                    float p0 = ex2_ftz(fmaf(__uint_as_float(r[k]), a.scale_log2, -mc));
+                    float p1 = ex2_ftz(fmaf(__uint_as_float(r[k + 1]), a.scale_log2, -mc));
+                    if (vm != 0xffffffffu) {
+                        p0 = ((vm >> k) & 1u) ? p0 : 0.0f;
+                        p1 = ((vm >> (k + 1)) & 1u) ? p1 : 0.0f;
+                    }
+                    le[(k >> 1) & 1] += p0 + p1;
                     const uint32_t b = pack_bf16(p0, p1);
-                    l_used += __uint_as_float(b << 16) + __uint_as_float(b & 0xFFFF0000u);
+                    lu[(k >> 1) & 1] += __uint_as_float(b << 16) + __uint_as_float(b & 0xFFFF0000u);
                     pk[k >> 1] = b;
                 }
                 uint8_t* atom = prow + (cc >> 1) * kPAtom;
@@ -489,6 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                 }
             }
+            l_exact = le[0] + le[1];
+            l_used = lu[0] + lu[1];
             tc_fence_before();
             fence_proxy_async();
             mbar_arrive(p_full);
