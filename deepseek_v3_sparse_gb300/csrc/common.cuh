@@ -182,6 +182,14 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
 
 // Plain (non-tensor) bulk copy global -> shared.  dst, src 16-byte aligned,
 // bytes a multiple of 16.
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream serialization attribute may start while the kernel before it runs;
+// pdl_wait() returns once that kernel has completed and its writes are
+// visible (at once when there is no such dependency).  pdl_trigger() lets the
+// dependent kernel be scheduled before this one ends.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // 16-byte asynchronous global -> shared copy (L2 only), and its groups.
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");

@@ -244,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = static_cast<uint32_t>(misc[0]);
+    pdl_trigger();  // the merge kernel may be scheduled now; it waits for this grid's end
 
     if (warp == kTmaWarp) {
         // ------------------------------------------------------------ query chunks
@@ -601,6 +602,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
                         int splits, uint16_t* __restrict__ out, float* __restrict__ lse) {
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    pdl_wait();  // launched as the main kernel's dependent: its split outputs are complete here
     if (row >= rows) return;
     const int64_t t = row / kH;
     const int h = static_cast<int>(row % kH);
@@ -791,8 +793,22 @@ extern "C" int dsmla_sparse_decode(const void* q_nope_bf16, const void* q_pe_bf1
     smla_decode_kernel<<<static_cast<unsigned>(tokens * splits), kThreads, kSmemAlloc, s>>>(tmQn, tmQp, a);
     if (cudaGetLastError() != cudaSuccess) return IX_ERR_CUDA;
     const int64_t rows = tokens * kH;
-    smla_combine_kernel<<<static_cast<unsigned>((rows + kCombineWarps - 1) / kCombineWarps), kCombineWarps * 32, 0,
-                          s>>>(a.ws_o, a.ws_lse, rows, splits, static_cast<uint16_t*>(out_bf16), lse);
+    // the merge is the main kernel's programmatic dependent: its launch overlaps
+    // the main kernel's last CTAs, and it reads the splits after pdl_wait()
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + kCombineWarps - 1) / kCombineWarps));
+    cfg.blockDim = dim3(kCombineWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, smla_combine_kernel, static_cast<const float*>(a.ws_o),
+                           static_cast<const float*>(a.ws_lse), rows, splits, static_cast<uint16_t*>(out_bf16),
+                           lse) != cudaSuccess)
+        return IX_ERR_CUDA;
     return launch_status();
 }
 

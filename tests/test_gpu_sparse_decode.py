@@ -178,3 +178,40 @@ def test_sparse_decode_binding_checks_workspace(dsix):
     ref_o, ref_l, ok = _oracle(x, dense, 64)
     _compare(out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ref_o, ref_l,
              _vmax(dense, x.indices, 64))
+
+
+def test_sparse_decode_graph_capture_replays_identically(dsix):
+    """Both kernels (the merge is launched as the main kernel's programmatic
+    dependent) captured in a CUDA graph: replays give the eager call's bits,
+    and a replay after the inputs change follows them."""
+    x = W.sparse_decode_inputs(5, 700, 2000, seed=41)
+    dense, _, _, _ = _cache_bytes(x, 64)
+    cache = torch.from_numpy(dense).cuda()
+    qn, qp, idx = x.q_nope.cuda(), x.q_pe.cuda(), torch.from_numpy(x.indices).cuda()
+    ws = torch.empty(dsix.dsmla_sparse_decode_workspace_size(5, 128, 700), dtype=torch.uint8, device="cuda")
+    out_e = torch.empty(5, 128, 512, dtype=torch.bfloat16, device="cuda")
+    lse_e = torch.empty(5, 128, dtype=torch.float32, device="cuda")
+    dsix.dsmla_sparse_decode(qn, qp, cache, idx, x.sm_scale, out_e, lse_e, ws)
+    out_g, lse_g = torch.full_like(out_e, 7.0), torch.full_like(lse_e, 7.0)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            dsix.dsmla_sparse_decode(qn, qp, cache, idx, x.sm_scale, out_g, lse_g, ws,
+                                     stream=torch.cuda.current_stream())
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert dsix.ix_device_status() == 0
+    assert torch.equal(out_g.view(torch.int16), out_e.view(torch.int16))
+    assert torch.equal(lse_g, lse_e)
+    # new query values in the captured buffers: the replay follows them
+    qn.copy_(torch.flip(qn, dims=[0]))
+    qp.copy_(torch.flip(qp, dims=[0]))
+    g.replay()
+    dsix.dsmla_sparse_decode(qn, qp, cache, idx, x.sm_scale, out_e, lse_e, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_g.view(torch.int16), out_e.view(torch.int16))
+    assert torch.equal(lse_g, lse_e)
