@@ -182,6 +182,22 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
 
 // Plain (non-tensor) bulk copy global -> shared.  dst, src 16-byte aligned,
 // bytes a multiple of 16.
+// 2-D tiled TMA store shared -> global (a bulk group of the issuing thread).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// At most N of this thread's bulk groups still reading their shared source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// All of this thread's bulk groups complete (their writes done).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Programmatic dependent launch: a kernel launched with the programmatic
 // stream serialization attribute may start while the kernel before it runs;
 // pdl_wait() returns once that kernel has completed and its writes are

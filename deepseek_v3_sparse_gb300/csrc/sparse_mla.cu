@@ -174,7 +174,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, volat
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1)
     smla_decode_kernel(const __grid_constant__ CUtensorMap tmQn, const __grid_constant__ CUtensorMap tmQp,
-                       const SmlaArgs a) {
+                       const __grid_constant__ CUtensorMap tmO, const SmlaArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     int64_t* koff = reinterpret_cast<int64_t*>(sm + kOffOff);
@@ -553,29 +553,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const float inv = l_used > 0.0f ? 1.0f / l_used : 0.0f;
             const int64_t prow_idx = (t * a.splits + split) * kH + h;
-            // Rows leave through shared memory (the V^T region is free once O is
-            // complete): each warp stages 32 heads x 32 columns (rows padded to
-            // 36 floats) and writes them as full 128-byte lines, 4 rows per store.
-            float* tile = reinterpret_cast<float*>(sm) + q4 * (32 * 36);
-            float* wrow0 = a.ws_o + (prow_idx - lane) * kNope;  // row of this warp's first head
-            for (int cc = 0; cc < kNope / 32; ++cc) {
-                uint32_t r[32];
-                tmem_ld32(trow + cc * 32, r);
-                tmem_wait_ld(r);
-#pragma unroll
-                for (int k = 0; k < 32; k += 4)
-                    *reinterpret_cast<float4*>(tile + lane * 36 + k) =
-                        make_float4(__uint_as_float(r[k]) * inv, __uint_as_float(r[k + 1]) * inv,
-                                    __uint_as_float(r[k + 2]) * inv, __uint_as_float(r[k + 3]) * inv);
-                __syncwarp();
-#pragma unroll
-                for (int it = 0; it < 8; ++it) {
-                    const int row = it * 4 + (lane >> 3), j = lane & 7;
-                    *reinterpret_cast<float4*>(wrow0 + static_cast<int64_t>(row) * kNope + cc * 32 + 4 * j) =
-                        *reinterpret_cast<const float4*>(tile + row * 36 + 4 * j);
+            // Rows leave by TMA (the V^T region is free once O is complete): a warp
+            // writes 32 heads x 32 columns of O / sum into a 4 KB tile in the
+            // 128-byte-swizzled layout of the split-output map, and one lane
+            // stores it as a box; four tiles per warp rotate, a pair per step.
+            uint8_t* tiles = sm + q4 * (4 * 4096);
+            const int row0 = static_cast<int>(prow_idx - lane);  // the warp's first head row
+            for (int cc = 0; cc < kNope / 32; cc += 2) {
+                uint32_t r0[32], r1[32];
+                tmem_ld32(trow + cc * 32, r0);
+                tmem_ld32(trow + (cc + 1) * 32, r1);
+                tmem_wait_ld(r0);
+                tmem_wait_ld(r1);
+                uint8_t* t0 = tiles + ((cc >> 1) & 1) * 8192;
+                if (cc >= 4) {  // the pair stored from these tiles two steps ago has been read
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
                 }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int pos = ((j ^ (lane & 7)) << 4);
+                    *reinterpret_cast<float4*>(t0 + lane * 128 + pos) =
+                        make_float4(__uint_as_float(r0[4 * j]) * inv, __uint_as_float(r0[4 * j + 1]) * inv,
+                                    __uint_as_float(r0[4 * j + 2]) * inv, __uint_as_float(r0[4 * j + 3]) * inv);
+                    *reinterpret_cast<float4*>(t0 + 4096 + lane * 128 + pos) =
+                        make_float4(__uint_as_float(r1[4 * j]) * inv, __uint_as_float(r1[4 * j + 1]) * inv,
+                                    __uint_as_float(r1[4 * j + 2]) * inv, __uint_as_float(r1[4 * j + 3]) * inv);
+                }
+                fence_proxy_async();
                 __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmO, t0, cc * 32, row0);
+                    tma_store_2d(&tmO, t0 + 4096, (cc + 1) * 32, row0);
+                    bulk_commit();
+                }
             }
+            if (lane == 0) bulk_wait_all();  // the splits are written before the CTA ends
+            __syncwarp();
             a.ws_lse[prow_idx] = m == -INFINITY ? -INFINITY : (mc + log2f(l_exact)) * 0.69314718055994531f;
         } else {
             // a wait gave up: this split's output was not written, so its lse is
@@ -695,6 +709,19 @@ bool make_query_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t ro
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The split outputs [rows, 512] f32 as boxes of 32 rows x 32 columns (128-byte rows).
+bool make_split_map(CUtensorMap* m, float* base, uint64_t rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t d[2] = {static_cast<cuuint64_t>(kNope), rows};
+    cuuint64_t s[1] = {static_cast<cuuint64_t>(kNope) * 4};
+    cuuint32_t b[2] = {32, 32};
+    cuuint32_t e[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int smem_setup() {  // the dynamic shared memory limit, once per device
     static std::mutex mu;
     static std::vector<char> ready;
@@ -790,7 +817,9 @@ extern "C" int dsmla_sparse_decode(const void* q_nope_bf16, const void* q_pe_bf1
     a.ws_lse = a.ws_o + prow * kNope;
     a.status = status;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    smla_decode_kernel<<<static_cast<unsigned>(tokens * splits), kThreads, kSmemAlloc, s>>>(tmQn, tmQp, a);
+    CUtensorMap tmO{};
+    if (!make_split_map(&tmO, a.ws_o, static_cast<uint64_t>(prow))) return IX_ERR_CUDA;
+    smla_decode_kernel<<<static_cast<unsigned>(tokens * splits), kThreads, kSmemAlloc, s>>>(tmQn, tmQp, tmO, a);
     if (cudaGetLastError() != cudaSuccess) return IX_ERR_CUDA;
     const int64_t rows = tokens * kH;
     // the merge is the main kernel's programmatic dependent: its launch overlaps
