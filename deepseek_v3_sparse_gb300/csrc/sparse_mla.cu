@@ -19,9 +19,10 @@
 //   warps 10-13 softmax and epilogue, one thread per head (= TMEM lane)
 // Phase 1  S[128 heads x 256 keys] = Q K^T (tcgen05 kind::f16, M 128, N 256)
 //          into TMEM columns [0, 256), over nine 64-dim chunks (the RoPE
-//          chunk, then eight NoPE chunks), two stages; the gathered codes
-//          run ahead by cp.async into a ring in the space of the V^T
-//          tiles and P, both free until S is complete.
+//          chunk, then eight NoPE chunks): query chunks in a ring of four
+//          (TMA), bf16 key chunks in two stages, the gathered codes ahead
+//          by cp.async in a ring of four, all in the space of the V^T tiles
+//          and P (both free until S is complete).
 // Phase 2  the softmax threads read their row of S twice (max, then
 //          exponentials), write P in bf16 as the A operand of the next product
 //          and keep the row sums.
@@ -62,18 +63,20 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s
 // shared memory map (offsets from a 1024-byte-aligned base)
 constexpr int kQBytes = kH * 128;                 // one 64-dim query chunk (16 KB)
 constexpr int kKBytes = kSplit * 128;             // one 64-dim key chunk (32 KB)
-constexpr int kStage1 = kQBytes + kKBytes;        // phase-1 stage (48 KB)
-constexpr int kP1Stages = 2;                      // phase-1 stages (query chunk + bf16 key chunk)
-constexpr int kRing = 6;                          // phase-1 chunks of gathered codes in flight
-constexpr int kRingOff = kP1Stages * kStage1;     // [kRing][256 keys x 64 codes], in the V^T and P space
+// Phase 1 uses the V^T region and the P tiles (both free until S is complete):
+constexpr int kQStages = 4;                       // query chunks in flight (TMA)
+constexpr int kP1Stages = 2;                      // bf16 key chunk stages (written by the dequantisers)
+constexpr int kRing = 4;                          // chunks of gathered codes in flight (cp.async)
+constexpr int kKStageOff = kQStages * kQBytes;    // after the query ring
+constexpr int kRingOff = kKStageOff + kP1Stages * kKBytes;  // [kRing][256 keys x 64 codes]
 constexpr int kVtBytes = kNope * 128;             // V^T tile: 512 rows x 64 keys (64 KB)
-constexpr int kRegion = 2 * kVtBytes;             // phase-1 stages 0-1, later both V^T stages
+constexpr int kRegion = 2 * kVtBytes;             // both V^T stages (phase 1: query ring, key stages)
 constexpr int kPOff = kRegion;                    // P: 4 tiles of 128 rows x 64 keys
 constexpr int kPAtom = kH * 128;
 constexpr int kOffOff = kPOff + kKeyChunks * kPAtom;  // int64 entry offset per key (-1: none)
 constexpr int kMaskOff = kOffOff + kSplit * 8;        // validity bits of the 256 keys
 constexpr int kBarOff = kMaskOff + 64;
-constexpr int kNumBars = 2 * kP1Stages + 8;
+constexpr int kNumBars = 2 * kQStages + 2 * kP1Stages + 8;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;      // tmem base, abort flag, never-raised flag
 constexpr int kSmemUsed = kMiscOff + 64;
 constexpr int kSmemAlloc = kSmemUsed + 1024;
@@ -180,8 +183,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t* koff = reinterpret_cast<int64_t*>(sm + kOffOff);
     uint32_t* vmask = reinterpret_cast<uint32_t*>(sm + kMaskOff);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBarOff);
-    uint64_t* full1 = bars;                   // [kP1Stages] query chunk landed + key chunk written
-    uint64_t* empty1 = bars + kP1Stages;      // [kP1Stages] the MMAs of a phase-1 stage are done
+    uint64_t* qfull = bars;                   // [kQStages] query chunk landed
+    uint64_t* qempty = qfull + kQStages;      // [kQStages] the MMAs reading a query chunk are done
+    uint64_t* full1 = qempty + kQStages;      // [kP1Stages] key chunk written
+    uint64_t* empty1 = full1 + kP1Stages;     // [kP1Stages] the MMAs of a key stage are done
     uint64_t* s_full = empty1 + kP1Stages;    // all of S is in TMEM (phase-1 MMAs done)
     uint64_t* p_full = s_full + 1;            // P written, S read (128 softmax threads)
     uint64_t* full3 = s_full + 2;             // [2] V^T chunk written
@@ -195,8 +200,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int split = static_cast<int>(blockIdx.x % a.splits);
 
     if (threadIdx.x == 0) {
+        for (int i = 0; i < kQStages; ++i) {
+            mbar_init(qfull + i, 1);
+            mbar_init(qempty + i, 1);
+        }
         for (int i = 0; i < kP1Stages; ++i) {
-            mbar_init(full1 + i, 1 + kDeqThreads);
+            mbar_init(full1 + i, kDeqThreads);
             mbar_init(empty1 + i, 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -251,22 +260,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool leader = elect_one();
         int c = 0;
         for (; c < kChunks; ++c) {
-            const int stage = c % kP1Stages, use = c / kP1Stages;
-            if (use > 0 && !wait_warp(empty1 + stage, (use - 1) & 1, abort_flag, a.status)) break;
+            const int stage = c % kQStages, use = c / kQStages;
+            if (use > 0 && !wait_warp(qempty + stage, (use - 1) & 1, abort_flag, a.status)) break;
             if (leader) {
-                uint8_t* qdst = sm + stage * kStage1;
-                mbar_arrive_expect_tx(full1 + stage, kQBytes);
+                uint8_t* qdst = sm + stage * kQBytes;
+                mbar_arrive_expect_tx(qfull + stage, kQBytes);
                 if (c == 0)  // chunk 0: the RoPE part; chunks 1-8: NoPE dims 64 (c - 1) ..
-                    tma_load_2d(qdst, &tmQp, full1 + stage, 0, static_cast<int>(t * kH));
+                    tma_load_2d(qdst, &tmQp, qfull + stage, 0, static_cast<int>(t * kH));
                 else
-                    tma_load_2d(qdst, &tmQn, full1 + stage, (c - 1) * 64, static_cast<int>(t * kH));
+                    tma_load_2d(qdst, &tmQn, qfull + stage, (c - 1) * 64, static_cast<int>(t * kH));
             }
             __syncwarp();
         }
         // drain: the last copies issued must land before the CTA exits
         if (leader)
-            for (int i = c > kP1Stages ? c - kP1Stages : 0; i < c; ++i)
-                drain_wait(full1 + i % kP1Stages, (i / kP1Stages) & 1, misc + 2, a.status);
+            for (int i = c > kQStages ? c - kQStages : 0; i < c; ++i)
+                drain_wait(qfull + i % kQStages, (i / kQStages) & 1, misc + 2, a.status);
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
@@ -274,18 +283,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t kId = idesc_bf16_f32(kH, 256);
         bool ok = true, issued = false;
         for (int c = 0; c < kChunks; ++c) {
-            const int stage = c % kP1Stages;
-            if (!wait_warp(full1 + stage, (c / kP1Stages) & 1, abort_flag, a.status)) {
+            const int stage = c % kP1Stages, qs = c % kQStages;
+            if (!wait_warp(qfull + qs, (c / kQStages) & 1, abort_flag, a.status) ||
+                !wait_warp(full1 + stage, (c / kP1Stages) & 1, abort_flag, a.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             if (leader) {
-                const uint32_t qa = smem_u32(sm + stage * kStage1), kb = qa + kQBytes;
+                const uint32_t qa = smem_u32(sm + qs * kQBytes), kb = smem_u32(sm + kKStageOff + stage * kKBytes);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tmem_base, sdesc_k_sw128(qa + 32 * kk), sdesc_k_sw128(kb + 32 * kk), kId,
                              (c | kk) != 0);
+                mma_commit(qempty + qs);
                 mma_commit(empty1 + stage);
             }
             issued = true;
@@ -351,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             uint4* ring = reinterpret_cast<uint4*>(sm + kRingOff);  // [kRing][4 keys][256 threads]
             {
-                uint8_t* kt = sm + kQBytes;  // stage 0, first use
+                uint8_t* kt = sm + kKStageOff;  // key stage 0, first use
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     const int row = p * 64 + kb;
@@ -384,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sc[p] = valid[p] ? __ldg(reinterpret_cast<const float4*>(ent[p] + kNope)) : make_float4(0.f, 0.f, 0.f, 0.f);
             uint4 o[8];
             auto put_rows = [&](int stage) {
-                uint8_t* kt = sm + stage * kStage1 + kQBytes;
+                uint8_t* kt = sm + kKStageOff + stage * kKBytes;
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     const int row = p * 64 + kb;
