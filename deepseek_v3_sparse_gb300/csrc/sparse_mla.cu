@@ -410,7 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             cp_async_wait<kRing>();
             fence_proxy_async();
             mbar_arrive(full1 + 0);
-            for (int n = 0; n < 8 && ok; ++n) {
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {  // unrolled: slots, scales and stages are constants
+                if (!ok) break;
                 const int c = n + 1, stage = c % kP1Stages, use = c / kP1Stages;
                 cp_async_wait<kRing - 1>();  // this thread's copies of chunk n have landed
 #pragma unroll
