@@ -84,6 +84,7 @@ class IndexerStep:
         self.clean = clean_logits
         self.fused_dec = "decode" in fused
         self.fused_pf = "prefill" in fused
+        self._graph = None
         self.cache = torch.zeros(num_blocks, INDEXER_BLOCK_BYTES, dtype=torch.uint8, device=dev)
         self.dsmla_cache = None
         if nope is not None:
@@ -108,6 +109,23 @@ class IndexerStep:
             self.pf_local = torch.empty(T, topk, **i32) if with_local else None
             self.pf_ws = (torch.zeros(ix_topk_hist_workspace_size(T), dtype=torch.uint8, device=dev)
                           if self.fused_pf else None)
+
+    def graph(self) -> "torch.cuda.CUDAGraph":
+        """The step as one CUDA graph (captured on first use, on a side stream,
+        after at least one eager run() has done the library's one-time set-up):
+        replaying it issues the same kernels as run() with less launch overhead.
+        The graph reads and writes this step's buffers in place."""
+        if self._graph is None:
+            dev = self.block_table.device
+            side = torch.cuda.Stream(device=dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g, stream=side):
+                    self.run(stream=side)
+            torch.cuda.current_stream(dev).wait_stream(side)
+            self._graph = g
+        return self._graph
 
     def write_history(self, k_bf16: torch.Tensor, slots: torch.Tensor, chunk: int = 1 << 20):
         """Fill the indexer-K cache with already-cached positions (set-up, not a step)."""
