@@ -351,20 +351,20 @@ def config_entries(dev, stream, n_launch=60):
             n_b2b = 40
             sus = {}
             for kind in ("plain", "hist"):
-                def one(c):
+                def one(c, strm):
                     if kind == "plain":
                         dsix.ix_paged_mqa_logits(d.q, d.w, c, d.context_lens, st.block_table, st.dec_logits,
-                                                 stream=stream)
+                                                 stream=strm)
                     else:
                         dsix.ix_paged_mqa_logits_hist(d.q, d.w, c, d.context_lens, st.block_table, st.dec_logits,
-                                                      wl.topk, st.dec_ws, stream=stream)
+                                                      wl.topk, st.dec_ws, stream=strm)
                 side = torch.cuda.Stream(device=dev)
                 side.wait_stream(stream)
                 graph = torch.cuda.CUDAGraph()
                 with torch.cuda.stream(side):
                     with torch.cuda.graph(graph, stream=side):
                         for j in range(n_b2b):
-                            one(caches[j % copies])
+                            one(caches[j % copies], side)
                 stream.wait_stream(side)
                 times = []
                 for rep in range(4):
@@ -404,6 +404,41 @@ def config_entries(dev, stream, n_launch=60):
         del st
         torch.cuda.empty_cache()
     return out
+
+
+def kernel_event_pass(step, names, n_ev, stream, graph):
+    """Per-kernel times of `n_ev` steps: events around each logits / top-k
+    launch (a fused call issued as its two halves).  With `graph` the step and
+    its events are one CUDA graph, replayed n_ev times as the timed steps are;
+    otherwise the kernels are launched one by one.  Returns name -> list of ms."""
+    if graph:
+        try:
+            ev = {n: (torch.cuda.Event(enable_timing=True, external=True),
+                      torch.cuda.Event(enable_timing=True, external=True)) for n in names}
+        except TypeError:  # no event nodes in graphs in this torch: launch one by one
+            graph = False
+    if graph:
+        side = torch.cuda.Stream(device=stream.device)
+        side.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                step.run(stream=side, events=ev, split=True)
+        stream.wait_stream(side)
+        out = {n: [] for n in names}
+        for _ in range(n_ev):
+            g.replay()
+            torch.cuda.synchronize()
+            for n in names:
+                out[n].append(ev[n][0].elapsed_time(ev[n][1]))
+        del g
+        return out, "events inside one CUDA graph of the step, replayed per sample"
+    evl = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_ev)] for n in names}
+    for i in range(n_ev):
+        step.run(stream=stream, events={n: evl[n][i] for n in names}, split=True)
+    torch.cuda.synchronize()
+    return {n: [a.elapsed_time(b) for a, b in evl[n]] for n in names}, "events around eager launches"
 
 
 def gpu_arm(args, world, rank, local):
@@ -451,13 +486,9 @@ def gpu_arm(args, world, rank, local):
     elapsed_ms = t0.elapsed_time(t1)
     clk = clocks.summary()
     n_ev = min(args.steps, 200)
-    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(n_ev)] for n in names}
-    for i in range(n_ev):  # a fused step issues its fused calls as their two halves here
-        step.run(stream=stream, events={n: ev[n][i] for n in names}, split=True)
-    torch.cuda.synchronize()
-    kern_ms = {n: float(np.mean([a.elapsed_time(b) for a, b in ev[n]])) for n in names}
-    kern_spread = {n: spread([a.elapsed_time(b) for a, b in ev[n]]) for n in names}
+    samples, kern_mode = kernel_event_pass(step, names, n_ev, stream, graph=not args.eager)
+    kern_ms = {n: float(np.mean(samples[n])) for n in names}
+    kern_spread = {n: spread(samples[n]) for n in names}
     status = dsix.ix_device_status()
 
     # ---- the next row beyond the step: fused RMSNorm + RoPE + fp8_ds_mla write of
@@ -654,6 +685,7 @@ def gpu_arm(args, world, rank, local):
     rows = int(wl.n_decode * wl.next_n + wl.n_prefill_rows)
     configs = {} if args.no_configs else config_entries(dev, stream)
     return dict(wl=wl, step=step, elapsed_ms=elapsed_ms, kern_ms=kern_ms, kern_spread=kern_spread,
+                kern_mode=kern_mode,
                 configs=configs, clocks=clk,
                 status=status, e2e_ms=e2e_ms, e2e_steps=e2e_steps, h2d=h2d, d2h=d2h,
                 dec_keys=dec_keys, pairs=pairs, rows=rows, next_rows=next_rows)
@@ -946,6 +978,7 @@ def main():
             "e2e": {"value": job_throughput(world, r["rows"], r["e2e_steps"], e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
             "gpu_launches": step.kernels_per_step() * args.steps,
+            "kernel_timing": r["kern_mode"],
             "clocks": r["clocks"], "device_status": r["status"]}
     if r["configs"]:
         line["configs"] = r["configs"]
