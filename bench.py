@@ -247,14 +247,16 @@ NOMINAL_HBM_GBS = 8000.0     # HBM3e, the round figure the targets are stated ag
 L2_BYTES = 129 << 20  # GB300 L2 (129 MB; about 126 MB usable)
 
 
-def config_entries(dev, stream, n_launch=60):
+def config_entries(dev, stream, n_launch=60, n_graph=20, replays=8):
     """The three single-kernel configurations (batch-32 decode, next_n=2 MTP
-    decode over 128 requests, 8192-token causal prefill), each timed launch by
-    launch with L2 flushed before every launch (a 256 MB read), logits kernel
-    and top-k back to back as the step runs them.  Per configuration: per-kernel
-    mean and min/median/max over the launches, the algorithmic rate (132 B per
-    key, keys read once per request; 16384 flop per visible (query, key) pair)
-    and its fraction of the measured and of the nominal peak."""
+    decode over 128 requests, 8192-token causal prefill), the fused call's two
+    kernels and the unfused pair.  Main figures: CUDA-graph replays of n_graph
+    back-to-back launches with L2-cold operands (copies in rotation); also, under
+    `single_launch`, one launch at a time after an L2 flush with events around
+    each kernel.  Per configuration: per-kernel mean and min/median/max, the
+    algorithmic rate (132 B per key, keys read once per request; 16384 flop per
+    visible (query, key) pair) and its fraction of the measured and of the
+    nominal peak; query tokens per second of logits + top-k."""
     import deepseek_v3_sparse_gb300 as dsix
     import workloads as W
     from workloads.device import make_step
@@ -268,29 +270,38 @@ def config_entries(dev, stream, n_launch=60):
         wl = fn(seed=0)
         st = make_step(wl, dev, fused=True)
         st.run(stream=stream)
-        R = st.decode.w.shape[0] if wl.n_decode else st.prefill.w.shape[0]
+        # each call takes the copy of its streamed operand (the cache for decode,
+        # the query rows and weights for prefill) and the stream to issue on
         if wl.n_decode:
             d = st.decode
             rows = wl.n_decode * wl.next_n
-            hist = lambda: dsix.ix_paged_mqa_logits_hist(d.q, d.w, st.cache, d.context_lens, st.block_table,
-                                                         st.dec_logits, wl.topk, st.dec_ws, stream=stream)
-            sel = lambda: dsix.ix_topk_from_hist(st.dec_logits, d.row_len, d.row_req, st.block_table, wl.topk,
-                                                 st.dec_global, st.dec_ws, stream=stream)
-            logits = lambda: dsix.ix_paged_mqa_logits(d.q, d.w, st.cache, d.context_lens, st.block_table,
-                                                      st.dec_logits, stream=stream)
-            topk = lambda: dsix.ix_topk_to_global(st.dec_logits, d.row_len, d.row_req, st.block_table,
-                                                  wl.topk, st.dec_global, None, stream=stream)
+            ws = st.dec_ws
+            operand = st.cache
+            hist_c = lambda c, s_: dsix.ix_paged_mqa_logits_hist(d.q, d.w, c, d.context_lens, st.block_table,
+                                                                 st.dec_logits, wl.topk, ws, stream=s_)
+            sel_c = lambda s_: dsix.ix_topk_from_hist(st.dec_logits, d.row_len, d.row_req, st.block_table, wl.topk,
+                                                      st.dec_global, ws, stream=s_)
+            logits_c = lambda c, s_: dsix.ix_paged_mqa_logits(d.q, d.w, c, d.context_lens, st.block_table,
+                                                              st.dec_logits, stream=s_)
+            topk_c = lambda s_: dsix.ix_topk_to_global(st.dec_logits, d.row_len, d.row_req, st.block_table,
+                                                       wl.topk, st.dec_global, None, stream=s_)
         else:
             p = st.prefill
             rows = wl.n_prefill_rows
-            hist = lambda: dsix.ix_mqa_logits_hist(p.q, p.w, st.k_fp8, st.k_scale, p.ks, p.ke, st.pf_logits,
-                                                   wl.topk, st.pf_ws, stream=stream)
-            sel = lambda: dsix.ix_topk_from_hist(st.pf_logits, p.row_len, p.row_req, st.block_table, wl.topk,
-                                                 st.pf_global, st.pf_ws, stream=stream)
-            logits = lambda: dsix.ix_mqa_logits(p.q, p.w, st.k_fp8, st.k_scale, p.ks, p.ke, st.pf_logits,
-                                                stream=stream)
-            topk = lambda: dsix.ix_topk_to_global(st.pf_logits, p.row_len, p.row_req, st.block_table,
-                                                  wl.topk, st.pf_global, None, stream=stream)
+            ws = st.pf_ws
+            operand = (p.q, p.w)
+            hist_c = lambda c, s_: dsix.ix_mqa_logits_hist(c[0], c[1], st.k_fp8, st.k_scale, p.ks, p.ke,
+                                                           st.pf_logits, wl.topk, ws, stream=s_)
+            sel_c = lambda s_: dsix.ix_topk_from_hist(st.pf_logits, p.row_len, p.row_req, st.block_table, wl.topk,
+                                                      st.pf_global, ws, stream=s_)
+            logits_c = lambda c, s_: dsix.ix_mqa_logits(c[0], c[1], st.k_fp8, st.k_scale, p.ks, p.ke, st.pf_logits,
+                                                        stream=s_)
+            topk_c = lambda s_: dsix.ix_topk_to_global(st.pf_logits, p.row_len, p.row_req, st.block_table,
+                                                       wl.topk, st.pf_global, None, stream=s_)
+        hist = lambda: hist_c(operand, stream)
+        sel = lambda: sel_c(stream)
+        logits = lambda: logits_c(operand, stream)
+        topk = lambda: topk_c(stream)
         for _ in range(3):
             hist()
             sel()
@@ -339,67 +350,77 @@ def config_entries(dev, stream, n_launch=60):
                           frac_of_nominal_fp8=tfs / NOMINAL_FP8_TFLOPS, target=0.50)
             return kd
 
-        sustained = None
-        if wl.n_decode:
-            # back-to-back launches of each decode logits kernel over copies of the
-            # cache whose total is more than twice L2 (each launch reads a copy the
-            # previous ones have pushed out of L2), issued as one CUDA graph of
-            # n_b2b launches (as a serving loop would replay them); events bracket
-            # each replay of the graph.
-            copies = max(2, int(np.ceil(2 * L2_BYTES / st.cache.numel())))
-            caches = [st.cache] + [st.cache.clone() for _ in range(copies - 1)]
-            n_b2b = 40
-            sus = {}
-            for kind in ("plain", "hist"):
-                def one(c, strm):
-                    if kind == "plain":
-                        dsix.ix_paged_mqa_logits(d.q, d.w, c, d.context_lens, st.block_table, st.dec_logits,
-                                                 stream=strm)
-                    else:
-                        dsix.ix_paged_mqa_logits_hist(d.q, d.w, c, d.context_lens, st.block_table, st.dec_logits,
-                                                      wl.topk, st.dec_ws, stream=strm)
-                side = torch.cuda.Stream(device=dev)
-                side.wait_stream(stream)
-                graph = torch.cuda.CUDAGraph()
-                with torch.cuda.stream(side):
-                    with torch.cuda.graph(graph, stream=side):
-                        for j in range(n_b2b):
-                            one(caches[j % copies], side)
-                stream.wait_stream(side)
-                times = []
-                for rep in range(4):
-                    torch.sum(flush, 0, out=sink)
-                    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    b0.record(stream)
-                    graph.replay()
-                    b1.record(stream)
-                    torch.cuda.synchronize()
-                    if kind == "hist":
-                        st.dec_ws.zero_()  # the hist kernel alone leaves its counts for a selection
-                    if rep > 0:
-                        times.append(b0.elapsed_time(b1) / n_b2b)
-                sus[kind] = rate(kern(times))
-                del graph
-            sus.update(launches_per_graph=n_b2b, replays=3, cache_copies=copies,
-                       l2="back to back in one CUDA graph, cycling through cache copies totalling more "
-                          "than twice L2")
-            sustained = sus
-            del caches
+        # ---- graph timing: each call sequence as one CUDA graph of n_graph back-to-back
+        # launches (the way the step is replayed), cycling through copies of the
+        # streamed operand that total more than twice L2, so no launch finds it in
+        # L2; per launch = replay time / n_graph, over `replays` replays (L2
+        # flushed before each).  A top-k's time is its pair's minus its logits'.
+        op_bytes = (operand.numel() * operand.element_size() if wl.n_decode
+                    else sum(x.numel() * x.element_size() for x in operand))
+        n_copies = max(2, int(np.ceil(2 * L2_BYTES / op_bytes)))
+        copies = [operand] + [operand.clone() if wl.n_decode else tuple(x.clone() for x in operand)
+                              for _ in range(n_copies - 1)]
+
+        def graph_ms(body, clears_ws):
+            side = torch.cuda.Stream(device=dev)
+            side.wait_stream(stream)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g, stream=side):
+                    for j in range(n_graph):
+                        body(copies[j % n_copies], side)
+            stream.wait_stream(side)
+            times = []
+            for rep in range(replays + 1):
+                torch.sum(flush, 0, out=sink)
+                b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                b0.record(stream)
+                g.replay()
+                b1.record(stream)
+                torch.cuda.synchronize()
+                if not clears_ws:
+                    ws.zero_()  # histogram kernels alone leave their counts behind
+                if rep > 0:  # the first replay is a warm-up
+                    times.append(b0.elapsed_time(b1) / n_graph)
+            del g
+            return times
+
+        g_hist = graph_ms(lambda c, s_: hist_c(c, s_), False)
+        g_fpair = graph_ms(lambda c, s_: (hist_c(c, s_), sel_c(s_)), True)
+        g_plain = graph_ms(lambda c, s_: logits_c(c, s_), True)
+        g_upair = graph_ms(lambda c, s_: (logits_c(c, s_), topk_c(s_)), True)
+        if dsix.ix_device_status() != 0:
+            raise RuntimeError(f"device status set in the {name} graph timing")
+        del copies
+
+        def pair_entry(ms_list):
+            ms = float(np.mean(ms_list))
+            return {"ms": ms, **{f"ms_{k}": v for k, v in spread(ms_list).items()},
+                    "query_tokens_per_s": rows / (ms / 1e3),
+                    "query_tokens_per_s_at_median": rows / (float(np.median(ms_list)) / 1e3)}
+
         fused_pair = [a + b for a, b in zip(t(0, 1), t(1, 2))]
         unfused_pair = [a + b for a, b in zip(t(3, 4), t(4, 5))]
         e = {"workload": wl.name, "rows": rows, "top_k": wl.topk,
-             "l2": "flushed before each logits launch (256 MB read); the top-k follows its logits",
-             "logits": rate(kern(t(0, 1))),
-             "topk": kern(t(1, 2)),
-             "logits_plus_topk": {"ms": float(np.mean(fused_pair)),
-                                  "query_tokens_per_s": rows / (float(np.mean(fused_pair)) / 1e3)},
-             "unfused": {"logits": rate(kern(t(3, 4))), "topk": kern(t(4, 5)),
-                         "logits_plus_topk": {"ms": float(np.mean(unfused_pair)),
-                                              "query_tokens_per_s": rows / (float(np.mean(unfused_pair)) / 1e3)}},
+             "timing": f"CUDA graph of {n_graph} back-to-back launches, {replays} replays, L2 flushed before "
+                       f"each replay, {n_copies} copies of the streamed operand in rotation (more than twice L2)",
+             "logits": rate(kern(g_hist)),
+             "topk": kern([b - a for a, b in zip(g_hist, g_fpair)]),
+             "logits_plus_topk": pair_entry(g_fpair),
+             "unfused": {"logits": rate(kern(g_plain)),
+                         "topk": kern([b - a for a, b in zip(g_plain, g_upair)]),
+                         "logits_plus_topk": pair_entry(g_upair)},
+             "single_launch": {
+                 "timing": f"{n_launch} launches one at a time, L2 flushed (256 MB read) before each logits "
+                           "launch, events around each kernel (launch and completion latency included)",
+                 "logits": rate(kern(t(0, 1))), "topk": kern(t(1, 2)),
+                 "logits_plus_topk": {"ms": float(np.mean(fused_pair)),
+                                      "query_tokens_per_s": rows / (float(np.mean(fused_pair)) / 1e3)},
+                 "unfused": {"logits": rate(kern(t(3, 4))), "topk": kern(t(4, 5)),
+                             "logits_plus_topk": {"ms": float(np.mean(unfused_pair)),
+                                                  "query_tokens_per_s": rows / (float(np.mean(unfused_pair)) / 1e3)}}},
              "note": "logits / topk: the two kernels of the fused call (histogram logits kernel, selection "
                      "from the histograms); unfused: the standalone logits kernel and top-k"}
-        if sustained is not None:
-            e["sustained"] = sustained
         out[name] = e
         del st
         torch.cuda.empty_cache()
