@@ -143,3 +143,34 @@ def test_graph_capture_replays_identically(dsix, fused):
     assert dsix.ix_device_status() == 0
     if fused:  # each replay left the histogram workspaces zero
         assert int(step.dec_ws.count_nonzero()) == 0 and int(step.pf_ws.count_nonzero()) == 0
+
+
+def test_step_graph_method_matches_eager(dsix):
+    """IndexerStep.graph() (the benchmark's timed step): captured after an eager
+    run, its replays give the eager step's indices and visible logits, also after
+    the cache is rewritten between replays (the graph reads it in place)."""
+    wl = W.build("graph_method", decode_ctx=[4100, 70], next_n=1, prefill=[(600, 200)],
+                 topk=128, seed=17, dsmla=True)
+    step = make_step(wl, "cuda", fused=("decode",))
+    step.run()
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (step.dec_global, step.pf_global)]
+    g = step.graph()
+    assert step.graph() is g  # captured once
+    for t in (step.dec_global, step.pf_global):
+        t.fill_(-9)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(step.dec_global, eager[0]) and torch.equal(step.pf_global, eager[1])
+    # new cache contents: the replay follows them, as the eager step does
+    step.cache.copy_(torch.roll(step.cache, shifts=1, dims=0))
+    g.replay()
+    torch.cuda.synchronize()
+    replayed = [t.clone() for t in (step.dec_global, step.pf_global, step.dec_logits)]
+    step.run()
+    torch.cuda.synchronize()
+    assert torch.equal(replayed[0], step.dec_global) and torch.equal(replayed[1], step.pf_global)
+    for r, L in enumerate(step.decode.row_len.cpu().tolist()):
+        assert torch.equal(replayed[2][r, :L], step.dec_logits[r, :L])
+    assert dsix.ix_device_status() == 0
+    assert int(step.dec_ws.count_nonzero()) == 0
