@@ -24,13 +24,15 @@
 //          by cp.async in a ring of four, all in the space of the V^T tiles
 //          and P (both free until S is complete).
 // Phase 2  the softmax threads read their row of S twice (max, then
-//          exponentials), write P in bf16 as the A operand of the next product
-//          and keep the row sums.
+//          exponentials by the hardware approximation), write P in bf16 as the
+//          A operand of the next product and keep the row sums.
 // Phase 3  O[128 x 512] = P V into TMEM columns [0, 512) (S has been read by
 //          then): four chunks of 64 keys, V^T tiles [512 dims x 64 keys]
 //          written by the dequantisers, two N = 256 halves per K step.
-// Epilogue O / sum and the split's lse go to the caller's workspace; a second
-//          kernel merges the splits of each (token, head) into bf16 output.
+// Epilogue O / sum (32 x 32 tiles, 128-byte swizzled, stored by TMA) and the
+//          split's lse go to the caller's workspace; a second kernel, launched
+//          as this one's programmatic dependent, merges the splits of each
+//          (token, head) into bf16 output.
 // Every wait is bounded (IX_DEV_TIMEOUT, then all roles leave; in-flight
 // copies and MMAs are drained before the CTA frees its TMEM and exits).
 #include <cudaTypedefs.h>
