@@ -628,14 +628,10 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
                     }
                 }
             } else {
-                // few keys are left in the bin: a warp with none of them skips the atomic
+                // few keys are left in the bin: one predicated atomic per key in it
 #pragma unroll
-                for (int j = 0; j < PER; ++j) {
-                    const bool m = j < nv && (key[j] >> shift) == prefix;
-                    if (__any_sync(0xffffffffu, m)) {
-                        if (m) atomicAdd(hist + ((key[j] >> sh) & (nb - 1)), 1);
-                    }
-                }
+                for (int j = 0; j < PER; ++j)
+                    if (j < nv && (key[j] >> shift) == prefix) atomicAdd(hist + ((key[j] >> sh) & (nb - 1)), 1);
             }
             __syncthreads();
             // Block-wide pick: thread t owns max(nb / 256, 1) consecutive bins
