@@ -78,7 +78,8 @@ template <bool TK>
 struct Cfg<true, TK> {  // decode over the paged cache
     static constexpr int kStages = 8;
     static constexpr int kSmemGroups = 2048;
-    static constexpr int kHistWords = TK ? 2 * 2048 : 0;  // next_n <= 2 rows, one u32 per bin
+    // one u32 per bin: two one-row buffers for next_n = 1, one two-row buffer for next_n = 2
+    static constexpr int kHistWords = TK ? 2 * 2048 : 0;
     static constexpr int kQBytes = 2 * kHeads * kDim;  // next_n <= 2
     static constexpr int kWFloats = 2 * kHeads;
     static constexpr int kSlots = 4;
@@ -449,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* acc_full = qw_empty + 2;
     uint64_t* acc_empty = acc_full + C::kSlots;
     uint64_t* mma_done = acc_empty + C::kSlots;
-    uint64_t* hbar = mma_done + 1;  // histogram hand-offs (TK): one per warpgroup (prefill), [0] (decode)
+    uint64_t* hbar = mma_done + 1;  // histogram hand-offs (TK): one per warpgroup (prefill); decode: filled [0..1], cleared [2..3]
     uint32_t* s_hist = reinterpret_cast<uint32_t*>(sm + S::kHist);
     int* misc = reinterpret_cast<int*>(sm + S::kMisc);  // tmem base, abort, g0, t0, units
     int* scan = reinterpret_cast<int*>(sm + S::kScan);
@@ -911,23 +912,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool new_group = true, have_group = false, live = true;
             // TK: the group's rows keep one u32 digit histogram each in shared
             // memory, shared by all 16 epilogue warps (jobs rotate over the
-            // warpgroups); when the group ends every warp hands off its share.
-            bool hw[NN];          // the row has more than k visible keys
-            int64_t hrow0 = 0;    // first row of the group
-            uint32_t hsync = 0;   // waits done on the hand-off barrier
-            auto hflush = [&]() -> bool {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(hbar);
-                if (!wait_warp(hbar, hsync & 1, abort_flag, a.status)) return false;
-                ++hsync;
+            // warpgroups).  A warp leaving a group arrives on its buffer's
+            // "filled" barrier; once all 16 have, each warp adds its share of the
+            // buffer to the rows' global histograms, clears it and arrives on the
+            // buffer's "cleared" barrier, which a warp waits on before it counts
+            // into that buffer for a later group.  One-row groups alternate
+            // between two buffers and defer the flush (a warp runs it as soon as
+            // it finds the filled barrier complete at a later unit, at the latest
+            // when it leaves the next group), so with groups of more than a few
+            // tiles no warp stops at a group change.  Two-row groups fill the one
+            // buffer the space holds and flush it when they leave the group
+            // (measured faster there than a second buffer would be).
+            constexpr int kHB = NN == 1 ? 2 : 1;  // histogram buffers
+            uint64_t* hfill = hbar;     // [2]
+            uint64_t* hclr = hbar + 2;  // [2]
+            uint32_t hwm0 = 0, hwm1 = 0;  // per buffer: bit j set when row j has more than k keys
+            int hr0 = 0, hr1 = 0;         // per buffer: first row of its group
+            int huse0 = 0, huse1 = 0;     // per buffer: groups that have counted into it
+            int hb = 0;                   // buffer of the current group
+            int pend = -1;                // buffer all warps have filled, not yet flushed by this warp
+            auto flush_share = [&](int b) {
                 const int et = threadIdx.x - kFirstEpiWarp * 32;  // 0..511: fine bins 4 et .. 4 et + 3
+                const uint32_t wm = b ? hwm1 : hwm0;
+                const int64_t row0 = b ? hr1 : hr0;  // rows fit in int: a row's logits start at row * ld
 #pragma unroll
                 for (int j = 0; j < NN; ++j) {
-                    uint4* src = reinterpret_cast<uint4*>(s_hist + j * kHistFine + 4 * et);
+                    uint4* src = reinterpret_cast<uint4*>(s_hist + (NN * b + j) * kHistFine + 4 * et);
                     const uint4 v = *src;
                     *src = make_uint4(0u, 0u, 0u, 0u);
-                    if (hw[j]) {  // uniform over the CTA
-                        uint32_t* G = hk.hist + (hrow0 + j) * kHistRowWords;
+                    if ((wm >> j) & 1u) {  // uniform over the CTA
+                        uint32_t* G = hk.hist + (row0 + j) * kHistRowWords;
                         if (v.x) atomicAdd(G + kHistCoarse + 4 * et, v.x);
                         if (v.y) atomicAdd(G + kHistCoarse + 4 * et + 1, v.y);
                         if (v.z) atomicAdd(G + kHistCoarse + 4 * et + 2, v.z);
@@ -940,19 +954,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(hbar);
-                if (!wait_warp(hbar, hsync & 1, abort_flag, a.status)) return false;
-                ++hsync;
+                if (lane == 0) mbar_arrive(hclr + b);
+            };
+            // the pending buffer's flush; `block` waits for its filled barrier,
+            // otherwise the flush runs only if that barrier is already complete
+            auto flush_pending = [&](bool block) -> bool {
+                if (pend < 0) return true;
+                const uint32_t ph = static_cast<uint32_t>((pend ? huse1 : huse0) - 1) & 1u;
+                if (block) {
+                    if (!wait_warp(hfill + pend, ph, abort_flag, a.status)) return false;
+                } else if (!__all_sync(0xffffffffu, mbar_try_wait(hfill + pend, ph))) {
+                    return true;
+                }
+                flush_share(pend);
+                pend = -1;
                 return true;
             };
             while (cur.left > 0) {
                 const int g = cur.g;
                 if (new_group) {
                     if constexpr (TK) {
-                        if (have_group && !hflush()) {
+                        if (have_group) {
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(hfill + hb);  // this warp's counts of the group are in
+                            if (!flush_pending(true)) {  // the buffer before, if this warp has not flushed it yet
+                                live = false;
+                                break;
+                            }
+                            pend = hb;
+                            if constexpr (kHB == 2) hb ^= 1;
+                            if (kHB == 1 && !flush_pending(true)) {
+                                live = false;
+                                break;
+                            }
+                        }
+                        const int used = hb ? huse1 : huse0;
+                        if (used > 0 && !wait_warp(hclr + hb, static_cast<uint32_t>(used - 1) & 1u, abort_flag, a.status)) {
                             live = false;
                             break;
                         }
+                        if (hb) ++huse1; else ++huse0;
                     }
                     if (have_group) {
                         __syncwarp();
@@ -969,9 +1010,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < NN; ++j) rs1[j] = decode_row_len(a, ctx, j, false);
                     if constexpr (TK) {
-                        hrow0 = static_cast<int64_t>(g) * NN;
+                        uint32_t wm = 0;
 #pragma unroll
-                        for (int j = 0; j < NN; ++j) hw[j] = rs1[j] > hk.k;
+                        for (int j = 0; j < NN; ++j) wm |= (rs1[j] > hk.k ? 1u : 0u) << j;
+                        if (hb) {
+                            hwm1 = wm;
+                            hr1 = g * NN;
+                        } else {
+                            hwm0 = wm;
+                            hr0 = g * NN;
+                        }
+                    }
+                } else if constexpr (TK) {
+                    if (pend >= 0 && !flush_pending(false)) {
+                        live = false;
+                        break;
                     }
                 }
                 const float* wq = sW + ((qi - 1) & 1) * C::kWFloats;
@@ -1007,7 +1060,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const float v = sums[i] * ksc;
                                 a.logits[(static_cast<int64_t>(g) * NN + i) * a.ld + s] = v;
                                 if constexpr (TK) {
-                                    if (hw[i]) atomicAdd(s_hist + i * kHistFine + (order_key(v) >> kDigitShift), 1u);
+                                    if (((hb ? hwm1 : hwm0) >> i) & 1u)
+                                        atomicAdd(s_hist + (NN * hb + i) * kHistFine + (order_key(v) >> kDigitShift), 1u);
                                 }
                             }
                         }
@@ -1021,7 +1075,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 new_group = cur.advance(a, s_tiles);
             }
             if constexpr (TK) {
-                if (live && have_group) hflush();
+                if (live && have_group) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(hfill + hb);
+                    if (flush_pending(true)) {  // the buffer before, then the last group's
+                        pend = hb;
+                        flush_pending(true);
+                    }
+                }
             }
         }
     }
