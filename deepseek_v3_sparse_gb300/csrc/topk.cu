@@ -476,6 +476,7 @@ static_assert(kBlkBt == kBlkThreads, "one staged block-table entry per thread");
 constexpr int kBlkBits = 12;  // radix digit width: 12 + 12 + 8 bits cover a 32-bit key
 constexpr int kBlkBins = 1 << kBlkBits;
 constexpr int kBlkFewKeys = 1024;  // threshold-bin size below which later passes take 10-bit digits
+constexpr int kBlkRankKeys = 128;  // threshold-bin size up to which its keys are ranked directly
 
 __device__ __forceinline__ uint32_t blk_scan_excl(uint32_t v, uint32_t* scratch) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -532,6 +533,7 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
     __shared__ uint32_t scratch[2][kBlkWarps];
     __shared__ uint32_t mm[2][kBlkWarps];
     __shared__ int res[4];
+    __shared__ uint32_t taken[kBlkWarps];  // ranked bin: bit i of word w = candidate 32 w + i is taken
     __shared__ __align__(16) int32_t stage[kBlkStage];
     const int tid = threadIdx.x;
     for (int i = tid; i < kBlkBins; i += kBlkThreads) hist[i] = 0;
@@ -607,7 +609,7 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
         int shift = 32 - __clz(kmin ^ kmax);  // bits below the common prefix; 0 when all keys are equal
         uint32_t prefix = shift >= 32 ? 0u : (kmin >> shift);
         int k_rem = a.k;
-        bool done = shift == 0;
+        bool done = shift == 0, ranked = false;
         for (int p = 0; !done; ++p) {
             // after the first pass few keys remain in the threshold bin: a 10-bit
             // digit (four bins per thread in the pick) usually settles them
@@ -707,6 +709,10 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
             prefix = (shift >= 32 ? 0u : (prefix << nbits)) | static_cast<uint32_t>(res[0]);
             shift = sh;
             done = shift == 0 || res[2] == k_rem;
+            if (!done && res[2] <= kBlkRankKeys) {  // few keys left in the bin: rank them below
+                done = true;
+                ranked = true;
+            }
         }
         // Keys above the threshold bin are all taken; of the keys in it, the
         // first k_rem in index order (all of them when the bin holds exactly k_rem).
@@ -724,14 +730,64 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
                                           scratch[sc]);  // both fields stay below 2^16
         sc ^= 1;
         const int bg = static_cast<int>(ex >> 16), be = static_cast<int>(ex & 0xFFFFu);
-        const int take = max(0, min(pe, k_rem - be));
         mask_t sel = gm;
-        if (take == pe) {
-            sel |= em;
-        } else if (take > 0) {
-            mask_t rest = em;
-            for (int i = 0; i < take; ++i) rest &= rest - 1;
-            sel |= em ^ rest;
+        int pos;
+        if (ranked) {
+            // The bin's n <= kBlkRankKeys keys, numbered in index order (this
+            // thread's are be .., its keys re-read from L1/L2), go to shared
+            // memory; candidate i is taken when fewer than k_rem candidates
+            // rank above it (a larger key, or an equal key at a lower index).
+            const int n = res[2];
+            uint32_t* cand = reinterpret_cast<uint32_t*>(stage);  // stage is written only after the next barrier
+            // only keys before the row end count (a bin at key 0 would also hold the
+            // padding slots), and no index leaves [0, n)
+            em &= nv >= PER ? ~mask_t(0) : ((mask_t(1) << nv) - 1);
+            const int b0 = min(be, n);
+            {
+                mask_t e = em;
+                int c = b0;
+                while (e && c < n) {
+                    cand[c++] = order_key(__ldg(src + mask_low(e)));
+                    e &= e - 1;
+                }
+            }
+            __syncthreads();
+            bool tk = false;
+            if (tid < n) {
+                const uint32_t kt = cand[tid];
+                int above = 0;
+                for (int u = 0; u < n; ++u) {
+                    const uint32_t ku = cand[u];
+                    above += (ku > kt || (ku == kt && u < tid)) ? 1 : 0;
+                }
+                tk = above < k_rem;
+            }
+            const uint32_t bal = __ballot_sync(0xffffffffu, tk);
+            if ((tid & 31) == 0) taken[tid >> 5] = bal;
+            __syncthreads();
+            // this thread's candidates be .. be + pe - 1, and the taken ones before them
+            int before = 0;
+            for (int w = 0; w < (b0 >> 5); ++w) before += __popc(taken[w]);
+            if (b0 & 31) before += __popc(taken[b0 >> 5] & ((1u << (b0 & 31)) - 1u));
+            mask_t e = em;
+            int c = b0;
+            while (e && c < n) {
+                const mask_t low = e & (~e + 1);
+                if ((taken[c >> 5] >> (c & 31)) & 1u) sel |= low;
+                ++c;
+                e &= e - 1;
+            }
+            pos = bg + before;
+        } else {
+            const int take = max(0, min(pe, k_rem - be));
+            if (take == pe) {
+                sel |= em;
+            } else if (take > 0) {
+                mask_t rest = em;
+                for (int i = 0; i < take; ++i) rest &= rest - 1;
+                sel |= em ^ rest;
+            }
+            pos = bg + min(be, k_rem);
         }
         // The winners of one thread are consecutive positions, so lanes write
         // far-apart runs; for k <= kBlkStage the local indices are placed in
@@ -740,7 +796,6 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
         const bool staged = a.k <= kBlkStage;
         int32_t* __restrict__ og = a.out_global + r * a.k;
         int32_t* __restrict__ ol = a.out_local ? a.out_local + r * a.k : nullptr;
-        int pos = bg + min(be, k_rem);
         while (sel) {
             const int s = mine + mask_low(sel);
             sel &= sel - 1;
