@@ -151,3 +151,28 @@ def test_exact_other_block_sizes(dsix, bs, R):
     logits = (rng.standard_normal((R, ld)) * 2).astype(np.float32)
     row_len = rng.integers(k + 1, ld + 1, R).astype(np.int32)
     _exact(dsix, logits, row_len, k, bs=bs, seed=bs)
+
+
+@pytest.mark.parametrize("R", [12, 400])
+def test_exact_ties_in_a_small_threshold_bin(dsix, R):
+    # The row's k-th largest value repeated m times, spread over the row or in
+    # one run: the bin that holds the k-th key has about m keys (ranked directly
+    # up to 128, by a further digit pass above), and the k_rem that are taken
+    # must be the lowest-index copies.
+    rng = np.random.default_rng(13)
+    ld, k = 8192, 2048
+    logits = (rng.standard_normal((R, ld)) * 8).astype(np.float32)
+    row_len = rng.integers(k + 200, ld + 1, R).astype(np.int32)
+    row_len[0] = ld
+    copies = [2, 5, 20, 60, 100, 126, 127, 128, 129, 140, 300]
+    for r in range(R):
+        L = int(row_len[r])
+        v = np.sort(logits[r, :L])[::-1][k - 1]
+        m = copies[r % len(copies)]
+        if r % 3 == 2:  # one run of consecutive positions (one or two threads' keys)
+            s0 = int(rng.integers(0, L - m))
+            pos = np.arange(s0, s0 + m)
+        else:
+            pos = rng.choice(L, m, replace=False)
+        logits[r, pos] = v
+    _exact(dsix, logits, row_len, k, seed=13)
