@@ -14,8 +14,10 @@
 // holds ql_nope values 16l .. 16l + 15 and RoPE pair l), half a warp per
 // (token, head) for the indexer query (lane holds 8 of the 128 values), 16-byte
 // loads and stores, a shuffle max for amax.  Arithmetic: IEEE f32 products,
-// sums and divisions (no fused multiply-add), bf16 and e4m3 conversions round
-// to nearest even, e4m3 saturates.
+// sums and divisions (no fused multiply-add in the RoPE), bf16 and e4m3
+// conversions round to nearest even, e4m3 saturates.  The divisions by the
+// scale are correctly rounded quotients obtained from one correctly rounded
+// reciprocal per (token, head) and two FMAs per value (div_by_rcp).
 #include <math.h>
 
 #include "common.cuh"
@@ -45,6 +47,39 @@ __device__ __forceinline__ float warp_max(float v) {
 __device__ __forceinline__ float scale_of(float amax) {
     const float s = __fdiv_rn(amax, 448.0f);
     return s >= 1.17549435e-38f ? s : 1.17549435e-38f;
+}
+
+// x / b rounded to nearest even, given y = RN(1/b).  Markstein's theorem for
+// division with an FMA (P. Markstein, "Computation of elementary functions on
+// the IBM RISC System/6000 processor", IBM J. Res. Develop. 34(1), 1990; see
+// also Muller et al., Handbook of Floating-Point Arithmetic, the chapter on
+// FMA-based division): q0 = RN(x y) is within one ulp of x / b, the residual
+// x - b q0 is exact in one FMA, and RN(q0 + r y) is RN(x / b), as long as
+// nothing underflows.  Used for b >= 2^-90 and |x / b| <= 448: then the
+// residual is exact for every quotient of 2^-11 or more, and smaller quotients
+// code to an e4m3 zero of the right sign whichever faithful value they get.  A
+// zero product keeps its sign (the FMAs would return +0 for x = -0).
+__device__ __forceinline__ float div_by_rcp(float x, float b, float y) {
+    const float q0 = __fmul_rn(x, y);
+    const float r = __fmaf_rn(-q0, b, x);
+    const float q = __fmaf_rn(r, y, q0);
+    return q0 == 0.0f ? q0 : q;
+}
+
+// Divisions by one per-(token, head) scale: the reciprocal path above for
+// scales of 2^-90 or more (every realistic scale), IEEE division below that.
+struct ScaleDiv {
+    float sc, y;
+    bool fast;
+    __device__ __forceinline__ float operator()(float x) const { return fast ? div_by_rcp(x, sc, y) : __fdiv_rn(x, sc); }
+};
+
+__device__ __forceinline__ ScaleDiv scale_div(float s) {
+    ScaleDiv d;
+    d.sc = s;
+    d.y = __frcp_rn(s);
+    d.fast = s >= 0x1p-90f;
+    return d;
 }
 
 struct FusedQArgs {
@@ -102,15 +137,14 @@ __global__ void __launch_bounds__(kQThreads) fused_q_kernel(const FusedQArgs a) 
 #pragma unroll
         for (int i = 0; i < 18; ++i) amax = fmaxf(amax, fabsf(x[i]));
         const float sc = scale_of(warp_max(amax));
+        const ScaleDiv dv = scale_div(sc);
         uint32_t code[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            code[i] = cvt_e4m3x2(__fdiv_rn(x[4 * i], sc), __fdiv_rn(x[4 * i + 1], sc)) |
-                      (cvt_e4m3x2(__fdiv_rn(x[4 * i + 2], sc), __fdiv_rn(x[4 * i + 3], sc)) << 16);
+            code[i] = cvt_e4m3x2(dv(x[4 * i]), dv(x[4 * i + 1])) | (cvt_e4m3x2(dv(x[4 * i + 2]), dv(x[4 * i + 3])) << 16);
         uint8_t* dst = a.out_mqa + th * kMqa;
         *reinterpret_cast<uint4*>(dst + 16 * lane) = make_uint4(code[0], code[1], code[2], code[3]);
-        *reinterpret_cast<uint16_t*>(dst + kNope + 2 * lane) =
-            static_cast<uint16_t>(cvt_e4m3x2(__fdiv_rn(x[16], sc), __fdiv_rn(x[17], sc)));
+        *reinterpret_cast<uint16_t*>(dst + kNope + 2 * lane) = static_cast<uint16_t>(cvt_e4m3x2(dv(x[16]), dv(x[17])));
         if (lane == 0) a.out_scale[th] = sc;
     }
 }
@@ -140,10 +174,9 @@ __global__ void __launch_bounds__(kQThreads) quant_q_kernel(const uint4* __restr
         for (int o = 1; o < 16; o <<= 1) u = max(u, __shfl_xor_sync(0xffffffffu, u, o));
         const float sc = scale_of(__uint_as_float(u));
         if (live) {
-            const uint32_t c0 = cvt_e4m3x2(__fdiv_rn(x[0], sc), __fdiv_rn(x[1], sc)) |
-                                (cvt_e4m3x2(__fdiv_rn(x[2], sc), __fdiv_rn(x[3], sc)) << 16);
-            const uint32_t c1 = cvt_e4m3x2(__fdiv_rn(x[4], sc), __fdiv_rn(x[5], sc)) |
-                                (cvt_e4m3x2(__fdiv_rn(x[6], sc), __fdiv_rn(x[7], sc)) << 16);
+            const ScaleDiv dv = scale_div(sc);
+            const uint32_t c0 = cvt_e4m3x2(dv(x[0]), dv(x[1])) | (cvt_e4m3x2(dv(x[2]), dv(x[3])) << 16);
+            const uint32_t c1 = cvt_e4m3x2(dv(x[4]), dv(x[5])) | (cvt_e4m3x2(dv(x[6]), dv(x[7])) << 16);
             q_fp8[th * 16 + hl] = make_uint2(c0, c1);
             if (hl == 0) w_out[th] = __fmul_rn(wt, sc);
         }

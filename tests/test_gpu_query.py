@@ -163,3 +163,71 @@ def test_quant_q_prefill_chunk_sampled_and_logits(dsix):
     tol = 1e-3 * np.abs(ref).max(axis=1, keepdims=True) + 1e-4
     assert np.all(np.abs(got - ref) <= tol)
     assert dsix.ix_device_status() == 0
+
+
+def _bf16_from_fields(sign, exp, man):
+    bits = (np.asarray(sign, np.uint16) << 15) | (np.asarray(exp, np.uint16) << 7) | np.asarray(man, np.uint16)
+    return torch.from_numpy(bits.astype(np.uint16).view(np.int16)).view(torch.bfloat16)
+
+
+# Exponents of the largest value of a (token, head): ordinary, near the smallest
+# scale that takes the reciprocal path (2^-90), below it, and large.
+_AMAX_EXPS = [3, -80, -100, 100]
+
+
+def test_fused_q_every_significand_pair(dsix):
+    """The codes are quotients x / scale with scale = RN(amax / 448); their
+    rounding depends only on the significands of x and amax (no quantity here
+    under- or overflows).  Head h of each token holds amax = (1 + h/128) 2^E in
+    slot 0 and, in the other 511 NoPE slots, all 128 bf16 significands at
+    2^(E-1) .. 2^(E-4) with both signs, so the 128 heads cover every
+    (x, amax) significand pair; E runs over both division paths."""
+    T, H = len(_AMAX_EXPS), 128
+    sign = np.zeros((T, H, 512), np.uint16)
+    exp = np.zeros((T, H, 512), np.uint16)
+    man = np.zeros((T, H, 512), np.uint16)
+    s = np.arange(512)
+    for t, E in enumerate(_AMAX_EXPS):
+        off = np.where(s == 0, 0, 1 + s // 128)
+        exp[t] = (E + 127 - off)[None, :]
+        man[t] = np.where(s == 0, np.arange(H)[:, None], (s % 128)[None, :])
+        sign[t] = np.where(s == 0, 0, (s // 128) & 1)[None, :]
+    qn = _bf16_from_fields(sign, exp, man)
+    qp = torch.zeros(T, H, 64, dtype=torch.bfloat16)
+    pos = torch.arange(T, dtype=torch.int64)
+    _, table = W.norm_rope_params(16, seed=1)
+    got, gsc = _fused_gpu(dsix, qn, qp, pos, table, True)
+    torch.cuda.synchronize()
+    assert dsix.ix_device_status() == 0
+    _, ref_mqa, ref_sc, ok = oracle.fused_q(_bits(qn), _bits(qp), pos.numpy(), table.numpy(), True)
+    assert ok
+    assert np.array_equal(gsc.view(np.uint32), ref_sc.view(np.uint32))
+    bad = np.argwhere(got != ref_mqa)
+    assert bad.size == 0, f"{len(bad)} codes differ, first (token, head, slot) {bad[:4].tolist()}"
+
+
+def test_quant_q_every_significand_pair(dsix):
+    """As above for the indexer query (128 values per head): amax significand
+    (64 g + h) in slot 0 of head h of token group g, the other 127 slots all
+    significands but one at 2^(E-1-v) with sign (-1)^v, for v = 0, 1."""
+    H = 64
+    rows = []
+    for E in _AMAX_EXPS:
+        for g in range(2):
+            for v in range(2):
+                s = np.arange(128)
+                man = np.where(s == 0, (64 * g + np.arange(H))[:, None], s[None, :])
+                exp = np.where(s == 0, E + 127, E + 126 - v)[None, :].repeat(H, 0)
+                sign = np.where(s == 0, 0, v)[None, :].repeat(H, 0)
+                rows.append((sign, exp, man))
+    sign = np.stack([r[0] for r in rows])
+    exp = np.stack([r[1] for r in rows])
+    man = np.stack([r[2] for r in rows])
+    q = _bf16_from_fields(sign, exp, man)
+    w = torch.linspace(-1, 1, q.shape[0] * H).view(q.shape[0], H)
+    gq, gw = _quant_gpu(dsix, q, w)
+    assert dsix.ix_device_status() == 0
+    rq, rw = oracle.quant_q(_bits(q), w.numpy())
+    assert np.array_equal(gw.view(np.uint32), rw.view(np.uint32))
+    bad = np.argwhere(gq != rq)
+    assert bad.size == 0, f"{len(bad)} codes differ, first (token, head, slot) {bad[:4].tolist()}"
