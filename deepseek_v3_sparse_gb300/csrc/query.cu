@@ -12,8 +12,9 @@
 //
 // Both are HBM-streaming: one warp per (token, head) for the MLA query (lane l
 // holds ql_nope values 16l .. 16l + 15 and RoPE pair l), half a warp per
-// (token, head) for the indexer query (lane holds 8 of the 128 values), 16-byte
-// loads and stores, a shuffle max for amax.  Arithmetic: IEEE f32 products,
+// (token, head) for the indexer query (lane holds 8 of the 128 values; four
+// units' loads in flight per half-warp), 16-byte loads and stores, a shuffle
+// max for amax.  Arithmetic: IEEE f32 products,
 // sums and divisions (no fused multiply-add in the RoPE), bf16 and e4m3
 // conversions round to nearest even, e4m3 saturates.  The divisions by the
 // scale are correctly rounded quotients obtained from one correctly rounded
@@ -29,6 +30,7 @@ constexpr int kNope = 512;
 constexpr int kRope = 64;
 constexpr int kMqa = kNope + kRope;
 constexpr int kQThreads = 256;
+constexpr int kQUnroll = 4;  // indexer-query units per half-warp and iteration
 
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
     uint32_t r;
@@ -57,33 +59,31 @@ __device__ __forceinline__ float scale_of(float amax) {
 // x - b q0 is exact in one FMA, and RN(q0 + r y) is RN(x / b), as long as
 // nothing underflows.  Used for b >= 2^-90 and |x / b| <= 448: then the
 // residual is exact for every quotient of 2^-11 or more, and smaller quotients
-// code to an e4m3 zero of the right sign whichever faithful value they get.  A
-// zero product keeps its sign (the FMAs would return +0 for x = -0).
+// code to an e4m3 zero of the right sign whichever faithful value they get.
+// The residual is formed as -(q0 b - x) so that x = -0 gives q0 = -0, a +0
+// residual and the quotient -0 (x - q0 b would give +0 + -0 = +0).
 __device__ __forceinline__ float div_by_rcp(float x, float b, float y) {
     const float q0 = __fmul_rn(x, y);
-    const float r = __fmaf_rn(-q0, b, x);
-    const float q = __fmaf_rn(r, y, q0);
-    return q0 == 0.0f ? q0 : q;
+    const float rn = __fmaf_rn(q0, b, -x);  // -(x - b q0), exact
+    return __fmaf_rn(-rn, y, q0);
 }
 
-// Divisions by one per-(token, head) scale: the reciprocal path above for
-// scales of 2^-90 or more (every realistic scale), IEEE division below that.
-struct ScaleDiv {
+// Divisions by one per-(token, head) scale, chosen once per (token, head): the
+// reciprocal path above for scales of 2^-90 or more (every realistic scale),
+// IEEE division below that.
+struct RcpDiv {
     float sc, y;
-    bool fast;
-    __device__ __forceinline__ float operator()(float x) const { return fast ? div_by_rcp(x, sc, y) : __fdiv_rn(x, sc); }
+    __device__ __forceinline__ float operator()(float x) const { return div_by_rcp(x, sc, y); }
 };
-
-__device__ __forceinline__ ScaleDiv scale_div(float s) {
-    ScaleDiv d;
-    d.sc = s;
-    d.y = __frcp_rn(s);
-    d.fast = s >= 0x1p-90f;
-    return d;
-}
+struct IeeeDiv {
+    float sc;
+    __device__ __forceinline__ float operator()(float x) const { return __fdiv_rn(x, sc); }
+};
+constexpr float kRcpMinScale = 0x1p-90f;
 
 struct FusedQArgs {
     const uint4* ql_nope;   // [T*H][64] uint4 (8 bf16 each)
+    int heads_shift;        // log2(heads) when heads is a power of two, else -1
     const uint32_t* q_pe;   // [T*H][32] bf16 pairs
     const int64_t* positions;
     const float* cos_sin;
@@ -97,12 +97,28 @@ struct FusedQArgs {
     int* status;
 };
 
+// e4m3 codes of a lane's 18 values: four words of the NoPE part, the RoPE pair
+template <class Div>
+__device__ __forceinline__ void mqa_codes(const float (&x)[18], const Div& dv, uint32_t (&code)[5]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        code[i] = cvt_e4m3x2(dv(x[4 * i]), dv(x[4 * i + 1])) | (cvt_e4m3x2(dv(x[4 * i + 2]), dv(x[4 * i + 3])) << 16);
+    code[4] = cvt_e4m3x2(dv(x[16]), dv(x[17]));
+}
+
+// e4m3 codes of a half-warp lane's 8 values (indexer query)
+template <class Div>
+__device__ __forceinline__ uint2 q_codes(const float (&x)[8], const Div& dv) {
+    return make_uint2(cvt_e4m3x2(dv(x[0]), dv(x[1])) | (cvt_e4m3x2(dv(x[2]), dv(x[3])) << 16),
+                      cvt_e4m3x2(dv(x[4]), dv(x[5])) | (cvt_e4m3x2(dv(x[6]), dv(x[7])) << 16));
+}
+
 __global__ void __launch_bounds__(kQThreads) fused_q_kernel(const FusedQArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t n = a.tokens * a.heads;
     const int64_t nw = static_cast<int64_t>(gridDim.x) * (kQThreads / 32);
     for (int64_t th = static_cast<int64_t>(blockIdx.x) * (kQThreads / 32) + (threadIdx.x >> 5); th < n; th += nw) {
-        const int64_t t = th / a.heads;
+        const int64_t t = a.heads_shift >= 0 ? th >> a.heads_shift : th / a.heads;
         // loads first: the position, this lane's RoPE pair and NoPE values
         const int64_t p = __ldg(a.positions + t);
         const uint32_t pe = __ldg(a.q_pe + th * 32 + lane);
@@ -137,14 +153,14 @@ __global__ void __launch_bounds__(kQThreads) fused_q_kernel(const FusedQArgs a) 
 #pragma unroll
         for (int i = 0; i < 18; ++i) amax = fmaxf(amax, fabsf(x[i]));
         const float sc = scale_of(warp_max(amax));
-        const ScaleDiv dv = scale_div(sc);
-        uint32_t code[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            code[i] = cvt_e4m3x2(dv(x[4 * i]), dv(x[4 * i + 1])) | (cvt_e4m3x2(dv(x[4 * i + 2]), dv(x[4 * i + 3])) << 16);
+        uint32_t code[5];
+        if (sc >= kRcpMinScale)  // uniform over the warp
+            mqa_codes(x, RcpDiv{sc, __frcp_rn(sc)}, code);
+        else
+            mqa_codes(x, IeeeDiv{sc}, code);
         uint8_t* dst = a.out_mqa + th * kMqa;
         *reinterpret_cast<uint4*>(dst + 16 * lane) = make_uint4(code[0], code[1], code[2], code[3]);
-        *reinterpret_cast<uint16_t*>(dst + kNope + 2 * lane) = static_cast<uint16_t>(cvt_e4m3x2(dv(x[16]), dv(x[17])));
+        *reinterpret_cast<uint16_t*>(dst + kNope + 2 * lane) = static_cast<uint16_t>(code[4]);
         if (lane == 0) a.out_scale[th] = sc;
     }
 }
@@ -155,30 +171,39 @@ __global__ void __launch_bounds__(kQThreads) quant_q_kernel(const uint4* __restr
                                                             float* __restrict__ w_out) {
     const int lane = threadIdx.x & 31, hl = lane & 15;
     const int64_t nh = static_cast<int64_t>(gridDim.x) * (kQThreads / 16);
-    // the loop test uses the warp's first (token, head), so both halves of a
-    // warp walk it together
-    for (int64_t th = static_cast<int64_t>(blockIdx.x) * (kQThreads / 16) + (threadIdx.x >> 4);
-         th - (lane >> 4) < n; th += nh) {
-        // both halves of a warp walk the loop together (the shuffles below span
-        // the whole warp); a half past the end computes on zeros and stores nothing
-        const bool live = th < n;
-        const uint4 v = live ? __ldg(q + th * 16 + hl) : make_uint4(0u, 0u, 0u, 0u);
-        const float wt = live ? __ldg(w + th) : 0.0f;
-        const float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                            bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-        float amax = 0.0f;
+    // Each half-warp takes kQUnroll (token, head) units per iteration, nh apart,
+    // and issues all their loads before any arithmetic.  The loop test uses the
+    // warp's first unit, so both halves of a warp walk it together (the shuffles
+    // span the whole warp); a unit past the end computes on zeros and stores nothing.
+    for (int64_t th0 = static_cast<int64_t>(blockIdx.x) * (kQThreads / 16) + (threadIdx.x >> 4);
+         th0 - (lane >> 4) < n; th0 += kQUnroll * nh) {
+        uint4 v[kQUnroll];
+        float wt[kQUnroll];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
-        uint32_t u = __float_as_uint(amax);  // max over the 16 lanes of this half
+        for (int u = 0; u < kQUnroll; ++u) {
+            const int64_t th = th0 + u * nh;
+            const bool live = th < n;
+            v[u] = live ? __ldg(q + th * 16 + hl) : make_uint4(0u, 0u, 0u, 0u);
+            wt[u] = live ? __ldg(w + th) : 0.0f;
+        }
 #pragma unroll
-        for (int o = 1; o < 16; o <<= 1) u = max(u, __shfl_xor_sync(0xffffffffu, u, o));
-        const float sc = scale_of(__uint_as_float(u));
-        if (live) {
-            const ScaleDiv dv = scale_div(sc);
-            const uint32_t c0 = cvt_e4m3x2(dv(x[0]), dv(x[1])) | (cvt_e4m3x2(dv(x[2]), dv(x[3])) << 16);
-            const uint32_t c1 = cvt_e4m3x2(dv(x[4]), dv(x[5])) | (cvt_e4m3x2(dv(x[6]), dv(x[7])) << 16);
-            q_fp8[th * 16 + hl] = make_uint2(c0, c1);
-            if (hl == 0) w_out[th] = __fmul_rn(wt, sc);
+        for (int u = 0; u < kQUnroll; ++u) {
+            const int64_t th = th0 + u * nh;
+            const float x[8] = {bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y),
+                                bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w)};
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+            uint32_t m = __float_as_uint(amax);  // max over the 16 lanes of this half
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+            const float sc = scale_of(__uint_as_float(m));
+            if (th < n) {
+                // the scale is uniform over the half-warp
+                q_fp8[th * 16 + hl] =
+                    sc >= kRcpMinScale ? q_codes(x, RcpDiv{sc, __frcp_rn(sc)}) : q_codes(x, IeeeDiv{sc});
+                if (hl == 0) w_out[th] = __fmul_rn(wt[u], sc);
+            }
         }
     }
 }
@@ -220,6 +245,7 @@ extern "C" int dsmla_fused_q(const void* ql_nope_bf16, const void* q_pe_bf16, co
     a.max_pos = max_pos;
     a.tokens = tokens;
     a.heads = heads;
+    a.heads_shift = (heads & (heads - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(heads)) : -1;
     a.quantize = quantize_mqa ? 1 : 0;
     a.out_pe = static_cast<uint32_t*>(out_pe_bf16);
     a.out_mqa = out_mqa_fp8;

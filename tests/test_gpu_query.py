@@ -181,7 +181,8 @@ def test_fused_q_every_significand_pair(dsix):
     under- or overflows).  Head h of each token holds amax = (1 + h/128) 2^E in
     slot 0 and, in the other 511 NoPE slots, all 128 bf16 significands at
     2^(E-1) .. 2^(E-4) with both signs, so the 128 heads cover every
-    (x, amax) significand pair; E runs over both division paths."""
+    (x, amax) significand pair; E runs over both division paths.  Slot 1 holds
+    -0 or +0 (codes 0x80 / 0x00)."""
     T, H = len(_AMAX_EXPS), 128
     sign = np.zeros((T, H, 512), np.uint16)
     exp = np.zeros((T, H, 512), np.uint16)
@@ -192,6 +193,7 @@ def test_fused_q_every_significand_pair(dsix):
         exp[t] = (E + 127 - off)[None, :]
         man[t] = np.where(s == 0, np.arange(H)[:, None], (s % 128)[None, :])
         sign[t] = np.where(s == 0, 0, (s // 128) & 1)[None, :]
+    exp[:, :, 1], man[:, :, 1], sign[:, :, 1] = 0, 0, np.arange(H) & 1  # zeros of both signs
     qn = _bf16_from_fields(sign, exp, man)
     qp = torch.zeros(T, H, 64, dtype=torch.bfloat16)
     pos = torch.arange(T, dtype=torch.int64)
@@ -223,6 +225,7 @@ def test_quant_q_every_significand_pair(dsix):
     sign = np.stack([r[0] for r in rows])
     exp = np.stack([r[1] for r in rows])
     man = np.stack([r[2] for r in rows])
+    exp[:, :, 1], man[:, :, 1], sign[:, :, 1] = 0, 0, np.arange(H) & 1  # zeros of both signs
     q = _bf16_from_fields(sign, exp, man)
     w = torch.linspace(-1, 1, q.shape[0] * H).view(q.shape[0], H)
     gq, gw = _quant_gpu(dsix, q, w)
