@@ -567,27 +567,34 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
         const float* src = a.logits + r * a.ld + mine;  // 16-byte aligned
         uint32_t key[PER];
         uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+        // Threads past the row end (whole warps of a short row) skip every loop
+        // over their key slots; their slots hold 0 and count nowhere.
+        if (nv > 0) {
 #pragma unroll
-        for (int j = 0; j < PER; j += 4) {
-            if (j + 4 <= nv) {
-                const float4 v = __ldg(reinterpret_cast<const float4*>(src + j));
-                key[j] = order_key(v.x);
-                key[j + 1] = order_key(v.y);
-                key[j + 2] = order_key(v.z);
-                key[j + 3] = order_key(v.w);
-                kmin = min(kmin, min(min(key[j], key[j + 1]), min(key[j + 2], key[j + 3])));
-                kmax = max(kmax, max(max(key[j], key[j + 1]), max(key[j + 2], key[j + 3])));
-            } else {
+            for (int j = 0; j < PER; j += 4) {
+                if (j + 4 <= nv) {
+                    const float4 v = __ldg(reinterpret_cast<const float4*>(src + j));
+                    key[j] = order_key(v.x);
+                    key[j + 1] = order_key(v.y);
+                    key[j + 2] = order_key(v.z);
+                    key[j + 3] = order_key(v.w);
+                    kmin = min(kmin, min(min(key[j], key[j + 1]), min(key[j + 2], key[j + 3])));
+                    kmax = max(kmax, max(max(key[j], key[j + 1]), max(key[j + 2], key[j + 3])));
+                } else {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    key[j + q] = 0u;
-                    if (j + q < nv) {
-                        key[j + q] = order_key(__ldg(src + j + q));
-                        kmin = min(kmin, key[j + q]);
-                        kmax = max(kmax, key[j + q]);
+                    for (int q = 0; q < 4; ++q) {
+                        key[j + q] = 0u;
+                        if (j + q < nv) {
+                            key[j + q] = order_key(__ldg(src + j + q));
+                            kmin = min(kmin, key[j + q]);
+                            kmax = max(kmax, key[j + q]);
+                        }
                     }
                 }
             }
+        } else {
+#pragma unroll
+            for (int j = 0; j < PER; ++j) key[j] = 0u;
         }
         // Bits every key of the row shares need no histogram.  A row of logits
         // often spans one or two binades, so a first digit taken from the sign
@@ -617,7 +624,8 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
             const int nbits = shift < width ? shift : width;
             const int nb = 1 << nbits;
             const int sh = shift - nbits;
-            if (p == 0) {
+            if (nv == 0) {
+            } else if (p == 0) {
 #pragma unroll
                 for (int j = 0; j < PER; j += 4) {
                     if (j + 4 <= nv) {
@@ -719,12 +727,14 @@ __global__ void __launch_bounds__(kBlkThreads, PER <= 32 ? 4 : 2) topk_block_ker
         const uint32_t thr_lo = prefix << shift;
         const uint32_t thr_hi = thr_lo | ((1u << shift) - 1u);
         mask_t gm = 0, em = 0;
+        if (nv > 0) {
 #pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            gm |= key[j] > thr_hi ? (mask_t(1) << j) : mask_t(0);
-            em |= key[j] >= thr_lo ? (mask_t(1) << j) : mask_t(0);
+            for (int j = 0; j < PER; ++j) {
+                gm |= key[j] > thr_hi ? (mask_t(1) << j) : mask_t(0);
+                em |= key[j] >= thr_lo ? (mask_t(1) << j) : mask_t(0);
+            }
+            em &= ~gm;
         }
-        em &= ~gm;
         const int pg = mask_popc(gm), pe = mask_popc(em);
         const uint32_t ex = blk_scan_excl((static_cast<uint32_t>(pg) << 16) | static_cast<uint32_t>(pe),
                                           scratch[sc]);  // both fields stay below 2^16
