@@ -14,11 +14,11 @@
 // holds ql_nope values 16l .. 16l + 15 and RoPE pair l), half a warp per
 // (token, head) for the indexer query (lane holds 8 of the 128 values; four
 // units' loads in flight per half-warp), 16-byte loads and stores, a shuffle
-// max for amax.  Arithmetic: IEEE f32 products,
-// sums and divisions (no fused multiply-add in the RoPE), bf16 and e4m3
-// conversions round to nearest even, e4m3 saturates.  The divisions by the
-// scale are correctly rounded quotients obtained from one correctly rounded
-// reciprocal per (token, head) and two FMAs per value (div_by_rcp).
+// max for amax.  Arithmetic: IEEE f32 products, sums and divisions (no fused
+// multiply-add in the RoPE), bf16 and e4m3 conversions round to nearest even,
+// e4m3 saturates.  The divisions by the scale are correctly rounded quotients
+// obtained from one correctly rounded reciprocal per (token, head) and two
+// FMAs per value (div_by_rcp).
 #include <math.h>
 
 #include "common.cuh"
